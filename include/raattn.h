@@ -1,0 +1,180 @@
+/*
+ * libraattn -- rational-softmax (Ra-family) attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only.  Every device pointer is memory the
+ * caller owns (for example from torch, cudaMalloc or a pool); the library keeps
+ * no allocation of its own across calls and never frees caller memory.
+ *
+ * Source of the method: page "Ra-Family: Rational Neural Architecture"
+ * (LuminaV-Optimizer docs/nn/README.md), section 3 "Rational Attention &
+ * Softmax":
+ *   ra_softmax of a row x:  Delta_i = x_max - x_i,  u_i = Delta_i / 16,
+ *   q_i = (1 - u_i) / (1 + u_i),  phi_i = q_i^8 for u_i < 1 and exactly 0
+ *   otherwise,  p_i = phi_i / sum_j phi_j  (sum_j phi_j >= 1 because the
+ *   maximum has phi = 1);  closed-form backward d phi/du = -16 phi / (1 - u^2).
+ *   ra_attention:  O = ra_softmax(scale * Q K^T [causal]) V, a drop-in for
+ *   scaled_dot_product_attention, computed tile by tile without storing the
+ *   [B, H, N_Q, N_K] matrix.
+ *
+ * Conventions shared by every entry point:
+ *   - stream: a cudaStream_t passed as void*; NULL means the legacy default
+ *     stream.  Work is enqueued on it and the call returns without waiting.
+ *   - Validation happens on the host before anything is launched.  A call
+ *     that returns an error status has launched nothing and written nothing.
+ *   - Device-side faults are not possible by design; the one device-side
+ *     failure is a bounded wait that gave up (RA_ERR_TIMEOUT), which the
+ *     kernels record in a library-owned status word and which
+ *     ra_device_status() reports.
+ *   - No entry point prints, throws or exits.
+ *   - Tensors are dense, row-major, contiguous, with every base pointer
+ *     16-byte aligned.
+ */
+#ifndef RAATTN_H
+#define RAATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_F32 = 0,   /* IEEE binary32 */
+  RA_BF16 = 1   /* bfloat16 */
+} ra_dtype_t;
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_ARG = 1,          /* null pointer, size < 1, overflow, misalignment, bad enum */
+  RA_ERR_UNSUPPORTED = 2,  /* valid request outside what this build implements */
+  RA_ERR_LAUNCH = 3,       /* the CUDA runtime refused the launch or the set-up */
+  RA_ERR_TIMEOUT = 4       /* a device-side wait exceeded its limit (see ra_device_status) */
+} ra_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ra_status_string(ra_status_t status);
+
+/*
+ * ra_softmax_fwd -- y = ra_softmax(x) along the last dimension.
+ * Page "Ra-Family: Rational Neural Architecture", section 3, ra_softmax
+ * (shift, rational numerator, exact zero for Delta >= 16, normalisation).
+ *   x, y     device pointers to rows*cols elements of `dtype`, row-major.  y may
+ *            equal x (in place); partial overlap is an error the call cannot see.
+ *   rows     >= 1; cols >= 1 (cols == 1 gives p = 1).
+ *   dtype    RA_F32 (RA_BF16 returns RA_ERR_UNSUPPORTED in this build).
+ * Errors: RA_ERR_ARG for null pointers, rows/cols < 1, rows*cols overflowing
+ * int64; RA_ERR_UNSUPPORTED for dtype != RA_F32; RA_ERR_LAUNCH on launch failure.
+ */
+ra_status_t ra_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols,
+                           ra_dtype_t dtype, void* stream);
+
+/*
+ * ra_softmax_bwd -- dx = d/dx sum(dy * ra_softmax(x)) along the last dimension.
+ * Page "Ra-Family: Rational Neural Architecture", section 3, ra_softmax,
+ * "Closed-Form Backward Pass": from the saved probabilities p = ra_softmax(x)
+ * and the shift u = (x_max - x)/16 (recomputed from x), with
+ * d phi/du = -16 phi/(1-u^2) and the chain rule through x_max:
+ *   dx_j = p_j (dy_j - sum_k p_k dy_k) / (1 - u_j^2)   for j != argmax, u_j < 1
+ *   dx_j = 0                                           for u_j >= 1
+ *   dx_argmax = -(sum of the other dx_j)               (lowest index among ties)
+ *   x, p, dy, dx   device pointers to rows*cols elements of `dtype`; dx may equal dy.
+ *   dtype          RA_F32.
+ * Errors as ra_softmax_fwd.
+ */
+ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* dx,
+                           int64_t rows, int64_t cols, ra_dtype_t dtype, void* stream);
+
+/*
+ * ra_attention_fwd -- O = ra_softmax(scale * Q K^T [causal]) V, two passes per query tile.
+ * Page "Ra-Family: Rational Neural Architecture", section 3, ra_attention
+ * (functional form, drop-in for scaled_dot_product_attention; two-pass tiled
+ * kernel that skips the V tile whenever every entry of a tile has u >= 1).
+ *   q            [B, H, N_Q, D] of in_dtype.
+ *   k, v         [B, H, N_K, D] of in_dtype.
+ *   o            [B, H, N_Q, D] of out_dtype (written).
+ *   row_m        [B, H, N_Q] float: max over allowed keys of the scaled score (written).
+ *   row_s        [B, H, N_Q] float: sum of phi over the row, >= 1 (written).
+ *   row_arg      [B, H, N_Q] int32: lowest key index attaining the max (written).
+ *                row_m, row_s and row_arg are what ra_attention_bwd needs; each may
+ *                be NULL when no backward follows.
+ *   tile_counts  optional (NULL allowed) int64[2] in device memory, zeroed then written:
+ *                [0] = (query tile, key tile) pairs visited by the second pass,
+ *                [1] = pairs whose V tile and P*V product were skipped because every
+ *                      entry of the pair lies outside the compact support.
+ *                Tiles are 128 x 128 on the tensor-core path.
+ *   scale        score scale; <= 0 means 1/sqrt(D).
+ *   causal       0: every key visible; nonzero: key j visible to query i iff j <= i
+ *                (top-left alignment, as scaled_dot_product_attention's is_causal).
+ *   in_dtype     RA_BF16: tensor-core path, D in {64, 128}.
+ *                RA_F32: CUDA-core fp32 path (no TF32), D in {16, 32, 64, 128}.
+ *   out_dtype    RA_F32 or RA_BF16 for o.
+ * Errors: RA_ERR_ARG for null q/k/v/o, B, H, N_Q, N_K, D < 1, element counts
+ * overflowing int32 indexing per head, a pointer not 16-byte aligned or a bad
+ * enum; RA_ERR_UNSUPPORTED for D outside the sets above; RA_ERR_LAUNCH on
+ * launch or tensor-map set-up failure.
+ */
+ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* o,
+                             float* row_m, float* row_s, int32_t* row_arg,
+                             int64_t* tile_counts,
+                             int B, int H, int N_Q, int N_K, int D, float scale, int causal,
+                             ra_dtype_t in_dtype, ra_dtype_t out_dtype, void* stream);
+
+/*
+ * ra_attention_bwd_workspace_size -- bytes of device workspace ra_attention_bwd needs
+ * for these sizes (per query row: D_i = dO_i . O_i and the argmax correction R_i,
+ * both float).  Returns 0 for invalid sizes.
+ */
+size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
+
+/*
+ * ra_attention_bwd -- gradients of sum(dout * O) with respect to q, k and v.
+ * Page "Ra-Family: Rational Neural Architecture", section 3, ra_softmax
+ * "Closed-Form Backward Pass" (d phi/du = -16 phi/(1-u^2), evaluated from p and
+ * u without saved powers of q) and ra_attention ("tiled forward and backward",
+ * saved state O(B H N_Q D)).  With P = phi / row_s, dP = dout V^T,
+ * D_i = sum_d dout_id O_id and, for allowed j != row_arg_i with u_ij < 1,
+ * E_ij = P_ij (dP_ij - D_i) / (1 - u_ij^2), R_i = sum_j E_ij:
+ *   dS_ij = E_ij,  dS_{i,row_arg_i} = -R_i,  0 elsewhere;
+ *   dq = scale dS K,  dk = scale dS^T Q,  dv = P^T dout.
+ *   q, k, v, o, dout   as in ra_attention_fwd (o and dout use in_dtype... o may be
+ *                      float: see o_dtype below).  Same shapes.
+ *   row_m, row_s, row_arg   the statistics ra_attention_fwd wrote for these inputs
+ *                      (all three required).
+ *   dq, dk, dv         [B,H,N_Q,D], [B,H,N_K,D], [B,H,N_K,D] of grad_dtype (written).
+ *   workspace          device memory of at least ra_attention_bwd_workspace_size()
+ *                      bytes, 16-byte aligned; contents on entry do not matter.
+ *   o_dtype            dtype of o (RA_F32 or RA_BF16); dout has in_dtype.
+ *   grad_dtype         RA_F32 or RA_BF16.
+ * Supported combinations and errors as ra_attention_fwd.
+ */
+ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* row_m, const float* row_s,
+                             const int32_t* row_arg, void* dq, void* dk, void* dv,
+                             void* workspace,
+                             int B, int H, int N_Q, int N_K, int D, float scale, int causal,
+                             ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype,
+                             void* stream);
+
+/*
+ * ra_device_status -- synchronise `stream`, then report and clear the device-side
+ * status word of the current device: RA_OK, or RA_ERR_TIMEOUT if any kernel of
+ * this library gave up a bounded wait since the last call.  RA_ERR_LAUNCH if the
+ * synchronisation itself failed.
+ */
+ra_status_t ra_device_status(void* stream);
+
+/*
+ * ra_set_wait_limit_ns -- limit, in nanoseconds of %globaltimer, on every
+ * device-side wait of later launches (default 2e9).  0 restores the default.
+ * A wait that runs out sets RA_ERR_TIMEOUT and makes the kernel wind down
+ * cleanly (in-flight copies drained, tensor memory freed); results are then
+ * undefined but the context stays usable.
+ */
+void ra_set_wait_limit_ns(uint64_t limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RAATTN_H */

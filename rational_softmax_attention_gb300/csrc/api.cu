@@ -1,0 +1,250 @@
+// The C ABI of libraattn (declared in include/raattn.h): argument validation,
+// TMA tensor-map construction, the device status word, and dispatch to the
+// kernels.  Nothing here allocates device memory.
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace raattn {
+namespace {
+
+// One status word per device, read and cleared by ra_device_status().
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+
+ra_status_t status_ptr_for_current_device(unsigned int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return RA_ERR_LAUNCH;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return RA_OK;
+}
+
+ra_status_t make_ctx(LaunchCtx* ctx) {
+  unsigned int* p = nullptr;
+  const ra_status_t st = status_ptr_for_current_device(&p);
+  if (st != RA_OK) return st;
+  ctx->status = p;
+  ctx->wait_limit_ns = g_wait_limit_ns.load();
+  return RA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dtype_ok(ra_dtype_t t) { return t == RA_F32 || t == RA_BF16; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a [BH, N, D] bf16 tensor: box {64, 128, 1}, 128-byte swizzle, zero fill
+// out of bounds (rows past N of a head read as zeros, never the next head's rows).
+bool make_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int D) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+ra_status_t check_attn_sizes(int B, int H, int NQ, int NK, int D) {
+  if (B < 1 || H < 1 || NQ < 1 || NK < 1 || D < 1) return RA_ERR_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > INT_MAX) return RA_ERR_ARG;
+  // every per-tensor element index must fit comfortably in 64-bit arithmetic and
+  // the per-head row counts in 32-bit
+  if (bh * NQ > INT_MAX || bh * NK > INT_MAX) return RA_ERR_ARG;
+  return RA_OK;
+}
+
+}  // namespace
+}  // namespace raattn
+
+using namespace raattn;
+
+extern "C" {
+
+const char* ra_status_string(ra_status_t status) {
+  switch (status) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_ARG: return "RA_ERR_ARG: invalid argument";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED: not implemented for these arguments";
+    case RA_ERR_LAUNCH: return "RA_ERR_LAUNCH: CUDA launch or set-up failed";
+    case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT: a device-side wait exceeded its limit";
+    default: return "unknown ra_status_t";
+  }
+}
+
+void ra_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns == 0 ? 2000000000ull : static_cast<unsigned long long>(limit_ns));
+}
+
+ra_status_t ra_device_status(void* stream) {
+  unsigned int* p = nullptr;
+  if (status_ptr_for_current_device(&p) != RA_OK) return RA_ERR_LAUNCH;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return RA_ERR_LAUNCH;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return RA_ERR_LAUNCH;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return RA_ERR_LAUNCH;
+  return (v & kStatusTimeout) ? RA_ERR_TIMEOUT : RA_OK;
+}
+
+ra_status_t ra_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, ra_dtype_t dtype, void* stream) {
+  if (!x || !y || rows < 1 || cols < 1 || !dtype_ok(dtype)) return RA_ERR_ARG;
+  if (rows > INT_MAX || cols > (INT64_MAX / rows)) return RA_ERR_ARG;
+  if (dtype != RA_F32) return RA_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_ra_softmax_fwd_f32(static_cast<const float*>(x), static_cast<float*>(y), rows, cols,
+                                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* dx, int64_t rows, int64_t cols,
+                           ra_dtype_t dtype, void* stream) {
+  if (!x || !p || !dy || !dx || rows < 1 || cols < 1 || !dtype_ok(dtype)) return RA_ERR_ARG;
+  if (rows > INT_MAX || cols > (INT64_MAX / rows)) return RA_ERR_ARG;
+  if (dtype != RA_F32) return RA_ERR_UNSUPPORTED;
+  const cudaError_t e =
+      launch_ra_softmax_bwd_f32(static_cast<const float*>(x), static_cast<const float*>(p),
+                                static_cast<const float*>(dy), static_cast<float*>(dx), rows, cols,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* o, float* row_m, float* row_s,
+                             int32_t* row_arg, int64_t* tile_counts, int B, int H, int N_Q, int N_K, int D,
+                             float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t out_dtype, void* stream) {
+  if (!q || !k || !v || !o || !dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return RA_ERR_ARG;
+  if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return RA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RA_ERR_ARG;
+  if ((row_m && !aligned16(row_m)) || (row_s && !aligned16(row_s)) || (row_arg && !aligned16(row_arg)) ||
+      (tile_counts && !aligned16(tile_counts)))
+    return RA_ERR_ARG;
+  if (!(scale > 0.0f)) scale = 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(scale)) return RA_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const AttnShape s{B, H, N_Q, N_K, D, scale, causal ? 1 : 0};
+
+  if (in_dtype == RA_F32) {
+    if (!(D == 16 || D == 32 || D == 64 || D == 128)) return RA_ERR_UNSUPPORTED;
+    if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
+    const cudaError_t e = launch_attn_fwd_simt(s, static_cast<const float*>(q), static_cast<const float*>(k),
+                                               static_cast<const float*>(v), o, out_dtype == RA_BF16, row_m, row_s,
+                                               row_arg, st);
+    return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+  }
+  // bf16: tensor-core path
+  if (!(D == 64 || D == 128)) return RA_ERR_UNSUPPORTED;
+  LaunchCtx ctx;
+  if (make_ctx(&ctx) != RA_OK) return RA_ERR_LAUNCH;
+  FwdTcArgs a;
+  const int BH = B * H;
+  if (!make_map_bf16(&a.tm_q, q, BH, N_Q, D) || !make_map_bf16(&a.tm_k, k, BH, N_K, D) ||
+      !make_map_bf16(&a.tm_v, v, BH, N_K, D))
+    return RA_ERR_LAUNCH;
+  a.o = o;
+  a.row_m = row_m;
+  a.row_s = row_s;
+  a.row_arg = row_arg;
+  a.tile_counts = reinterpret_cast<unsigned long long*>(tile_counts);
+  a.out_bf16 = out_dtype == RA_BF16 ? 1 : 0;
+  if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
+  const cudaError_t e = launch_attn_fwd_tc(s, a, ctx, st);
+  return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D) {
+  if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N_Q;
+  const size_t per = ((rows * sizeof(float)) + 255) & ~static_cast<size_t>(255);
+  return 2 * per;
+}
+
+ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                             const float* row_m, const float* row_s, const int32_t* row_arg, void* dq, void* dk,
+                             void* dv, void* workspace, int B, int H, int N_Q, int N_K, int D, float scale,
+                             int causal, ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype,
+                             void* stream) {
+  if (!q || !k || !v || !o || !dout || !row_m || !row_s || !row_arg || !dq || !dk || !dv || !workspace)
+    return RA_ERR_ARG;
+  if (!dtype_ok(in_dtype) || !dtype_ok(o_dtype) || !dtype_ok(grad_dtype)) return RA_ERR_ARG;
+  if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return RA_ERR_ARG;
+  const void* ptrs[] = {q, k, v, o, dout, row_m, row_s, row_arg, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RA_ERR_ARG;
+  if (!(scale > 0.0f)) scale = 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(scale)) return RA_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const AttnShape s{B, H, N_Q, N_K, D, scale, causal ? 1 : 0};
+  const size_t rows = static_cast<size_t>(B) * H * N_Q;
+  const size_t per = ((rows * sizeof(float)) + 255) & ~static_cast<size_t>(255);
+  float* ws_d = static_cast<float*>(workspace);
+  float* ws_r = reinterpret_cast<float*>(static_cast<char*>(workspace) + per);
+
+  if (in_dtype == RA_F32) {
+    if (!(D == 16 || D == 32 || D == 64 || D == 128)) return RA_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_attn_bwd_simt(
+        s, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), o,
+        o_dtype == RA_BF16, static_cast<const float*>(dout), row_m, row_s, row_arg, dq, dk, dv,
+        grad_dtype == RA_BF16, ws_d, ws_r, st);
+    return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+  }
+  if (!(D == 64 || D == 128)) return RA_ERR_UNSUPPORTED;
+  LaunchCtx ctx;
+  if (make_ctx(&ctx) != RA_OK) return RA_ERR_LAUNCH;
+  BwdTcArgs a;
+  const int BH = B * H;
+  if (!make_map_bf16(&a.tm_q, q, BH, N_Q, D) || !make_map_bf16(&a.tm_k, k, BH, N_K, D) ||
+      !make_map_bf16(&a.tm_v, v, BH, N_K, D) || !make_map_bf16(&a.tm_do, dout, BH, N_Q, D))
+    return RA_ERR_LAUNCH;
+  a.o = o;
+  a.o_bf16 = o_dtype == RA_BF16 ? 1 : 0;
+  a.dout = dout;
+  a.row_m = row_m;
+  a.row_s = row_s;
+  a.row_arg = row_arg;
+  a.k_raw = k;
+  a.q_raw = q;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.grad_bf16 = grad_dtype == RA_BF16 ? 1 : 0;
+  a.ws_d = ws_d;
+  a.ws_r = ws_r;
+  const cudaError_t e = launch_attn_bwd_tc(s, a, ctx, st);
+  return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+}  // extern "C"

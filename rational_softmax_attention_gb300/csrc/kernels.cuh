@@ -1,0 +1,61 @@
+// Launchers exported by each kernel translation unit to the C-ABI layer (api.cu).
+#pragma once
+
+#include <cuda.h>
+#include "common.cuh"
+
+namespace raattn {
+
+// ra_softmax (ra_softmax.cu)
+cudaError_t launch_ra_softmax_fwd_f32(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t st);
+cudaError_t launch_ra_softmax_bwd_f32(const float* x, const float* p, const float* dy, float* dx, int64_t rows,
+                                      int64_t cols, cudaStream_t st);
+
+// Problem description shared by the attention launchers.
+struct AttnShape {
+  int B, H, NQ, NK, D;
+  float scale;   // > 0 (the C-ABI layer resolves the default)
+  int causal;
+};
+
+// fp32 CUDA-core attention (attn_simt.cu).  out_bf16 selects the output dtype.
+cudaError_t launch_attn_fwd_simt(const AttnShape& s, const float* q, const float* k, const float* v, void* o,
+                                 bool out_bf16, float* row_m, float* row_s, int32_t* row_arg, cudaStream_t st);
+cudaError_t launch_attn_bwd_simt(const AttnShape& s, const float* q, const float* k, const float* v,
+                                 const void* o, bool o_bf16, const float* dout, const float* row_m,
+                                 const float* row_s, const int32_t* row_arg, void* dq, void* dk, void* dv,
+                                 bool grad_bf16, float* ws_d, float* ws_r, cudaStream_t st);
+
+// bf16 tensor-core attention forward (attn_fwd_tc.cu).  Tensor maps are built by the caller.
+struct FwdTcArgs {
+  CUtensorMap tm_q, tm_k, tm_v;   // 3-D maps {D, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+  void* o;
+  float* row_m;
+  float* row_s;
+  int32_t* row_arg;
+  unsigned long long* tile_counts;   // may be null
+  int out_bf16;
+};
+cudaError_t launch_attn_fwd_tc(const AttnShape& s, const FwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st);
+
+// bf16 tensor-core attention backward (attn_bwd_tc.cu).
+struct BwdTcArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // same geometry as the forward maps
+  const void* o;
+  int o_bf16;
+  const void* dout;
+  const float* row_m;
+  const float* row_s;
+  const int32_t* row_arg;
+  const void* k_raw;   // K in global memory (bf16), for the argmax correction
+  const void* q_raw;   // Q in global memory (bf16)
+  void* dq;
+  void* dk;
+  void* dv;
+  int grad_bf16;
+  float* ws_d;   // [B*H*NQ]  D_i = dO_i . O_i
+  float* ws_r;   // [B*H*NQ]  R_i = sum_j E_ij (argmax excluded)
+};
+cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st);
+
+}  // namespace raattn

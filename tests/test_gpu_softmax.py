@@ -1,0 +1,84 @@
+"""GPU parity of the ra_softmax row kernels against the float64 oracle (fp32: max-abs 2e-5)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+import rational_softmax_attention_gb300 as ra
+from rational_softmax_attention_gb300.inputs import RA_SOFTMAX_LONG_ROWS, softmax_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(x_cpu):
+    y = ra.ra_softmax(x_cpu.cuda())
+    torch.cuda.synchronize()
+    assert ra.device_status() == "RA_OK"
+    return parity.f64(y)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 3), (5, 4), (7, 100), (9, 256), (4, 257), (2, 1000),
+                                       (3, 1024), (2, 2048), (2, 4096), (3, 8192), (2, 8191), (2, 12288),
+                                       (2, 16384), (2, 16388), (1, 40000)])
+def test_ra_softmax_matches_oracle(rows, cols):
+    x = softmax_inputs(rows, cols, seed=rows * 7 + cols, sigma=4.0)
+    got = _run(x)
+    want, *_ = oracle.ra_softmax(x.double().numpy())
+    parity.assert_close_fp32(got, want, f"ra_softmax[{rows}x{cols}]")
+    xd = x.double().numpy()
+    dead = (xd.max(-1, keepdims=True) - xd) >= 16.0
+    assert np.all(got[dead] == 0.0), "entries at Delta >= 16 must be exactly 0"
+    np.testing.assert_allclose(got.sum(-1), 1.0, atol=1e-5)
+
+
+def test_ra_softmax_worked_example():
+    # the page's worked logits; exact rationals are pinned on the oracle side
+    x = torch.tensor([[2.0, 1.0, 0.0], [5.0, 1.0, -10.0]])
+    got = _run(x)
+    want, *_ = oracle.ra_softmax(x.double().numpy())
+    parity.assert_close_fp32(got, want, "worked example")
+
+
+def test_ra_softmax_full_workload():
+    w = RA_SOFTMAX_LONG_ROWS
+    x = softmax_inputs(w.rows, w.cols, seed=w.seed, sigma=w.sigma)
+    got = _run(x)
+    want, *_ = oracle.ra_softmax(x.double().numpy())
+    parity.assert_close_fp32(got, want, w.name)
+    xd = x.double().numpy()
+    dead = (xd.max(-1, keepdims=True) - xd) >= 16.0
+    assert dead.mean() > 0.3          # the workload really exercises the compact support
+    assert np.all(got[dead] == 0.0)
+
+
+def test_ra_softmax_in_place_and_misaligned_rows():
+    x = softmax_inputs(6, 130, seed=3, sigma=3.0)
+    want, *_ = oracle.ra_softmax(x.double().numpy())
+    xg = x.cuda()
+    L = ra.lib()
+    st = torch.cuda.current_stream().cuda_stream
+    import ctypes
+    assert L.ra_softmax_fwd(ctypes.c_void_p(xg.data_ptr()), ctypes.c_void_p(xg.data_ptr()), 6, 130, 0,
+                            ctypes.c_void_p(st)) == 0
+    torch.cuda.synchronize()
+    parity.assert_close_fp32(parity.f64(xg), want, "in place, cols % 4 != 0")
+    # a row view starting 4 bytes off a 16-byte boundary takes the generic kernel
+    buf = softmax_inputs(1, 4 * 64 + 1, seed=4, sigma=3.0).cuda()
+    view = buf[0, 1:].reshape(4, 64)
+    got = parity.f64(ra.ra_softmax(view.contiguous()))
+    want2, *_ = oracle.ra_softmax(view.double().cpu().numpy())
+    parity.assert_close_fp32(got, want2, "offset rows")
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 5), (4, 64), (2, 1000), (2, 8192)])
+def test_ra_softmax_backward_matches_oracle(rows, cols):
+    g = torch.Generator().manual_seed(cols)
+    x = torch.randn(rows, cols, generator=g) * 4.0
+    dy = torch.randn(rows, cols, generator=g)
+    xg = x.cuda()
+    p = ra.ra_softmax(xg)
+    dx = ra.ra_softmax_backward(xg, p, dy.cuda())
+    torch.cuda.synchronize()
+    want = oracle.ra_softmax_bwd(x.double().numpy(), dy.double().numpy())
+    parity.assert_close_fp32(parity.f64(dx), want, f"ra_softmax_bwd[{rows}x{cols}]")
