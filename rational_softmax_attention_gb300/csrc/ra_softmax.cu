@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(THREADS) ra_softmax_bwd_kernel(const float* x,
     if (c != amin) dr[c] = e;
   }
   rsum = block_sum<THREADS>(rsum, red);
-  if (threadIdx.x == 0) dr[amin] = -rsum;
+  if (threadIdx.x == 0 && amin >= 0 && amin < cols) dr[amin] = -rsum;
 }
 
 // ----------------------------------------------------------------------------
