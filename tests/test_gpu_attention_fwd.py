@@ -148,8 +148,10 @@ def test_single_key_gives_V(dtype):
     want = v.float().expand(2, 3, 150, D)
     if dtype == torch.float32:
         assert torch.equal(o.cpu(), want)          # phi_max = 1 exactly on the fp32 path
-    else:                                          # approximate reciprocal: phi_max = 1 to ~1e-7
-        torch.testing.assert_close(o.cpu(), want, rtol=1e-6, atol=0)
+    else:
+        # tensor-core path: phi_max comes from an approximate reciprocal (a few ulp), and
+        # q ~ 1 raised to the 8th power multiplies that by 8, so phi_max = 1 to ~2e-6
+        torch.testing.assert_close(o.cpu(), want, rtol=1e-5, atol=0)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
@@ -160,7 +162,7 @@ def test_causal_first_row_and_causality_probe(dtype):
     if dtype == torch.float32:
         assert torch.equal(o1[:, :, 0].cpu(), v[:, :, 0].float())
     else:
-        torch.testing.assert_close(o1[:, :, 0].cpu(), v[:, :, 0].float(), rtol=1e-6, atol=0)
+        torch.testing.assert_close(o1[:, :, 0].cpu(), v[:, :, 0].float(), rtol=1e-5, atol=0)
     t = 140
     k2, v2 = k.clone(), v.clone()
     k2[:, :, t + 1:] = k2[:, :, t + 1:] * -2
