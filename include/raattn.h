@@ -122,8 +122,9 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
 
 /*
  * ra_attention_bwd_workspace_size -- bytes of device workspace ra_attention_bwd needs
- * for these sizes (per query row: D_i = dO_i . O_i and the argmax correction R_i,
- * both float).  Returns 0 for invalid sizes.
+ * for these sizes: four float arrays of B*H*N_Q entries (D_i = dO_i . O_i, the argmax
+ * correction R_i, and two per-row constants of the recomputed weights), each padded
+ * to 256 bytes.  Returns 0 for invalid sizes.
  */
 size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 
@@ -137,8 +138,8 @@ size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
  * E_ij = P_ij (dP_ij - D_i) / (1 - u_ij^2), R_i = sum_j E_ij:
  *   dS_ij = E_ij,  dS_{i,row_arg_i} = -R_i,  0 elsewhere;
  *   dq = scale dS K,  dk = scale dS^T Q,  dv = P^T dout.
- *   q, k, v, o, dout   as in ra_attention_fwd (o and dout use in_dtype... o may be
- *                      float: see o_dtype below).  Same shapes.
+ *   q, k, v, dout      [B,H,N_Q,D], [B,H,N_K,D], [B,H,N_K,D], [B,H,N_Q,D] of in_dtype.
+ *   o                  [B,H,N_Q,D] of o_dtype: the output of ra_attention_fwd.
  *   row_m, row_s, row_arg   the statistics ra_attention_fwd wrote for these inputs
  *                      (all three required).
  *   dq, dk, dv         [B,H,N_Q,D], [B,H,N_K,D], [B,H,N_K,D] of grad_dtype (written).

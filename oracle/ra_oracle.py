@@ -90,7 +90,7 @@ def ra_softmax(x, allowed=None):
     return p, m, s, a
 
 
-def ra_softmax_bwd(x, dy, allowed=None):
+def ra_softmax_bwd(x, dy, allowed=None, argmax=None):
     """Gradient of sum(dy * ra_softmax(x)) with respect to x, last axis.
 
     Built from the page's closed form d phi/du = -16 phi/(1-u^2) on u < 1
@@ -99,12 +99,24 @@ def ra_softmax_bwd(x, dy, allowed=None):
       u_j = (x_max - x_j)/16  ->  du_j/dx_j = -1/16 (j != argmax), du_j/dx_max = 1/16
     so for j != a (a = argmax): dx_j = p_j (dy_j - D) / (1 - u_j^2), zero if
     u_j >= 1 or j is masked, and dx_a = -sum_{j != a} dx_j.
+
+    `argmax` (optional, int array of the row shape) names the entry treated as
+    x_max.  The max is not differentiable at a tie, and two entries whose values
+    differ by less than rounding are both valid choices; passing the index a
+    fixed-precision implementation chose reproduces its branch of the gradient
+    (x_max is then x[argmax], the value that implementation's weights used).
     """
     x = np.asarray(x, dtype=np.float64)
     dy = np.asarray(dy, dtype=np.float64)
     if allowed is None:
         allowed = np.ones(x.shape, dtype=bool)
-    p, m, s, a = ra_softmax(x, allowed)
+    if argmax is None:
+        p, m, s, a = ra_softmax(x, allowed)
+    else:
+        a = np.asarray(argmax, dtype=np.int64)
+        m = np.take_along_axis(x, a[..., None], axis=-1)[..., 0]
+        phi = np.where(allowed, ra_phi(np.where(allowed, m[..., None] - x, SUPPORT)), 0.0)
+        p = phi / phi.sum(axis=-1, keepdims=True)
     D = (p * dy).sum(axis=-1, keepdims=True)
     u = (m[..., None] - x) / SUPPORT
     live = allowed & (u < 1.0)
@@ -143,18 +155,25 @@ def ra_attention_head_fwd(q, k, v, scale, causal):
     return O, m, s, a
 
 
-def ra_attention_head_bwd(q, k, v, do, scale, causal):
+def ra_attention_head_bwd(q, k, v, do, scale, causal, argmax=None):
     """One (batch, head): gradients of sum(do * O) with respect to q, k, v.
 
     The score gradient dS is ra_softmax_bwd applied to the materialised scores
     with upstream gradient dP = do v^T; then dq = scale dS k, dk = scale dS^T q,
     dv = P^T do (the plain chain rule through S = scale q k^T and O = P v).
+    `argmax` (optional, per query row) is passed on to ra_softmax_bwd, and P is
+    then formed with x_max = S[i, argmax_i] as well.
     """
     S = scale * (q @ k.T)
     allowed = _causal_allowed(q.shape[0], k.shape[0]) if causal else np.ones(S.shape, dtype=bool)
-    P, _, _, _ = ra_softmax(S, allowed)
+    if argmax is None:
+        P, _, _, _ = ra_softmax(S, allowed)
+    else:
+        m = np.take_along_axis(S, np.asarray(argmax, dtype=np.int64)[:, None], axis=-1)
+        phi = np.where(allowed, ra_phi(np.where(allowed, m - S, SUPPORT)), 0.0)
+        P = phi / phi.sum(axis=-1, keepdims=True)
     dP = do @ v.T
-    dS = ra_softmax_bwd(S, dP, allowed)
+    dS = ra_softmax_bwd(S, dP, allowed, argmax=argmax)
     dq = scale * (dS @ k)
     dk = scale * (dS.T @ q)
     dv = P.T @ do

@@ -119,6 +119,7 @@ ra_status_t ra_device_status(void* stream) {
   if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return RA_ERR_LAUNCH;
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return RA_ERR_LAUNCH;
+  if (v & kStatusBadSmem) return RA_ERR_LAUNCH;
   return (v & kStatusTimeout) ? RA_ERR_TIMEOUT : RA_OK;
 }
 
@@ -189,7 +190,7 @@ size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D) {
   if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return 0;
   const size_t rows = static_cast<size_t>(B) * H * N_Q;
   const size_t per = ((rows * sizeof(float)) + 255) & ~static_cast<size_t>(255);
-  return 2 * per;
+  return 4 * per;   // D_i, R_i, 0.5 + m_i/32, 1/s_i
 }
 
 ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -243,6 +244,8 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
   a.grad_bf16 = grad_dtype == RA_BF16 ? 1 : 0;
   a.ws_d = ws_d;
   a.ws_r = ws_r;
+  a.ws_base = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * per);
+  a.ws_invs = reinterpret_cast<float*>(static_cast<char*>(workspace) + 3 * per);
   const cudaError_t e = launch_attn_bwd_tc(s, a, ctx, st);
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }

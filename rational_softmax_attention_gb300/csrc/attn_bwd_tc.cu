@@ -1,10 +1,819 @@
-// bf16 ra_attention backward on the tensor cores (being written).
+// bf16 ra_attention backward on the tensor cores (tcgen05 + TMEM + TMA).
+//
+// Page "Ra-Family: Rational Neural Architecture", section 3, ra_softmax
+// "Closed-Form Backward Pass": d phi/du = -16 phi/(1-u^2), evaluated from the
+// recomputed u and p, with no saved powers of q; section 3, ra_attention:
+// "tiled forward and backward" keeping only O(B H N_Q D) saved state (O and the
+// per-row max, sum and argmax of the forward).
+//
+// Chain rule (the gradient of x_max goes to the lowest-index argmax a_i):
+//   P = phi / s_i,  dP = dO V^T,  D_i = dO_i . O_i,
+//   E_ij = P_ij (dP_ij - D_i) / (1 - u_ij^2)   for allowed j != a_i with u_ij < 1,
+//   R_i = sum_j E_ij,   dS = E with dS_{i,a_i} = -R_i,
+//   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+// With w = (1+u)/2 and q = 1/w - 1:  phi/(1-u^2) = q^7 / (4 w^2),  so
+//   E_ij = [q^7 (1/w)^2 / (4 s_i)] (dP_ij - D_i).
+//
+// Two kernels, no atomics:
+//   dQ kernel (one CTA per 128-row query tile, loop over key tiles): S = Q K^T and
+//     dP = dO V^T in TMEM; the softmax warpgroup (thread = query row) forms E,
+//     zeroes it at the argmax, sums R_i, and writes E (bf16) to shared memory;
+//     dQ += E K accumulates in TMEM; epilogue dq = scale (dQ - R_i K_{a_i}).  It
+//     also writes D_i, R_i and two per-row constants to the workspace.
+//   dK/dV kernel (one CTA per 128-key tile, loop over query tiles): S^T = K Q^T
+//     and dP^T = V dO^T in TMEM; the softmax warpgroup (thread = key row) forms
+//     P^T and dS^T (with -R_i at the argmax entries) in shared memory;
+//     dV += P^T dO and dK += dS^T Q accumulate in TMEM.
+// The second kernel reads what the first wrote, so they run in stream order.
 #include "kernels.cuh"
 
 namespace raattn {
+namespace {
 
-cudaError_t launch_attn_bwd_tc(const AttnShape&, const BwdTcArgs&, const LaunchCtx&, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int PRODUCER_WARP = 4;
+constexpr int MMA_WARP = 5;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int BOX_BYTES = 128 * 64 * 2;
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+// 16-byte chunk `chunk` (0..15) of row r of a 128 x 128 bf16 K-major operand tile,
+// stored as two 64-column halves in the 128-byte-swizzled layout TMA and tcgen05 use.
+__device__ __forceinline__ void st_tile16(uint8_t* tile, int r, int chunk, uint4 val) {
+  const int half = chunk >> 3, c = chunk & 7;
+  *reinterpret_cast<uint4*>(tile + half * BOX_BYTES + r * 128 + ((c ^ (r & 7)) << 4)) = val;
+}
+
+// 1/w0 and 1/w1 (w in [0.5, 1]) from one rcp.approx of w0 w1.
+__device__ __forceinline__ float2 rcp_pair(float w0, float w1) {
+  const float R = rcp_approx(w0 * w1);
+  return __fmul2_rn(make_float2(R, R), make_float2(w1, w0));
+}
+
+// Row of 8 bf16 from global memory as floats.
+__device__ __forceinline__ void load8_bf16(const void* p, float* out) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ void store_row32(void* base, size_t idx, const float* v, int bf16) {
+  if (bf16) {
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + idx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      dst[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+  } else {
+    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+// ============================================================================ dQ kernel
+template <int D>
+struct DqCfg {
+  static constexpr int TILE = BN * D * 2;
+  static constexpr int NKS = 3;                    // K stages: K_j lives from S_j to dQ_j
+  static constexpr int NVS = (D == 128) ? 1 : 2;   // V stages
+  static constexpr int E_BYTES = BM * BN * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = TILE;
+  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NKS * TILE;
+  static constexpr int OFF_E = OFF_V + NVS * TILE;
+  static constexpr int OFF_BAR = OFF_E + E_BYTES;
+  // qdo_full, k_full[NKS], k_empty[NKS], v_full[NVS], v_empty[NVS], s_full[2], s_free[2],
+  // dp_full, dp_free, e_full, e_free, dq_full, drain
+  static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 4 + 6;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+};
+constexpr uint32_t DQ_TM_S0 = 0, DQ_TM_S1 = 128, DQ_TM_DP = 256, DQ_TM_DQ = 384;
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_dq_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sDO = smem + C::OFF_DO;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sE = smem + C::OFF_E;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* qdo_full = bars;
+  uint64_t* k_full = qdo_full + 1;
+  uint64_t* k_empty = k_full + C::NKS;
+  uint64_t* v_full = k_empty + C::NKS;
+  uint64_t* v_empty = v_full + C::NVS;
+  uint64_t* s_full = v_empty + C::NVS;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* dp_full = s_free + 2;
+  uint64_t* dp_free = dp_full + 1;
+  uint64_t* e_full = dp_free + 1;
+  uint64_t* e_free = e_full + 1;
+  uint64_t* dq_full = e_free + 1;
+  uint64_t* drain = dq_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int BH = s.B * s.H;
+  const int nqt = (s.NQ + BM - 1) / BM;
+  const int item = blockIdx.x;
+  const int qt = s.causal ? (nqt - 1 - item / BH) : (item / BH);
+  const int bh = item % BH;
+  const int q0 = qt * BM;
+  const int last_key = s.causal ? min(s.NK - 1, min(s.NQ - 1, q0 + BM - 1)) : s.NK - 1;
+  const int nkt = last_key / BN + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qdo_full, 1);
+    for (int i = 0; i < C::NKS; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < C::NVS; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+    }
+    mbar_init(dp_full, 1);
+    mbar_init(dp_free, 4);
+    mbar_init(e_full, 4);
+    mbar_init(e_free, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      tma_prefetch_desc(&args.tm_q);
+      tma_prefetch_desc(&args.tm_k);
+      tma_prefetch_desc(&args.tm_v);
+      tma_prefetch_desc(&args.tm_do);
+      mbar_arrive_expect_tx(qdo_full, 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sQ + c * BOX_BYTES, &args.tm_q, qdo_full, c * 64, q0, bh);
+        tma_load_3d(sDO + c * BOX_BYTES, &args.tm_do, qdo_full, c * 64, q0, bh);
+      }
+      bool ok = true;
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int ks = j % C::NKS;
+        ok = mbar_wait(&k_empty[ks], ((j / C::NKS) & 1u) ^ 1u, abort_flag, ctx);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&k_full[ks], C::TILE);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sK + ks * C::TILE + c * BOX_BYTES, &args.tm_k, &k_full[ks], c * 64, j * BN, bh);
+        k_issued = j + 1;
+        const int vs = j % C::NVS;
+        ok = mbar_wait(&v_empty[vs], ((j / C::NVS) & 1u) ^ 1u, abort_flag, ctx);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&v_full[vs], C::TILE);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sV + vs * C::TILE + c * BOX_BYTES, &args.tm_v, &v_full[vs], c * 64, j * BN, bh);
+        v_issued = j + 1;
+      }
+      // drain every copy issued (the last fill of each stage)
+      drain_wait(qdo_full, 0, ctx);
+      for (int j = max(0, k_issued - C::NKS); j < k_issued; ++j)
+        drain_wait(&k_full[j % C::NKS], (j / C::NKS) & 1u, ctx);
+      for (int j = max(0, v_issued - C::NVS); j < v_issued; ++j)
+        drain_wait(&v_full[j % C::NVS], (j / C::NVS) & 1u, ctx);
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_ss = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t idesc_kmn = idesc_bf16_f32(BM, D, 0, 1);
+      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aK = smem_u32(sK), aV = smem_u32(sV),
+                     aE = smem_u32(sE);
+      auto do_dq = [&](int t) -> bool {   // dQ += E_t K_t
+        if (!mbar_wait(e_full, t & 1u, abort_flag, ctx)) return false;
+        tc_fence_after();
+        const uint32_t kaddr = aK + (t % C::NKS) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc_mma_f16(tmem + DQ_TM_DQ, smem_desc_sw128(aE + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024),
+                     smem_desc_sw128(kaddr + kk * 2048, BOX_BYTES, 1024), idesc_kmn, (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&k_empty[t % C::NKS]);
+        tc_commit(e_free);
+        return true;
+      };
+      bool ok = mbar_wait(qdo_full, 0, abort_flag, ctx);
+      for (int j = 0; j < nkt && ok; ++j) {
+        // S_j = Q K_j^T
+        const int ks = j % C::NKS, sb = j & 1;
+        ok = mbar_wait(&k_full[ks], (j / C::NKS) & 1u, abort_flag, ctx) &&
+             mbar_wait(&s_free[sb], ((j >> 1) & 1u) ^ 1u, abort_flag, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          tc_mma_f16(tmem + (sb ? DQ_TM_S1 : DQ_TM_S0), smem_desc_sw128(aQ + off, 16, 1024),
+                     smem_desc_sw128(aK + ks * C::TILE + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[sb]);
+        // dP_j = dO V_j^T
+        const int vs = j % C::NVS;
+        ok = mbar_wait(&v_full[vs], (j / C::NVS) & 1u, abort_flag, ctx) &&
+             mbar_wait(dp_free, (j & 1u) ^ 1u, abort_flag, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          tc_mma_f16(tmem + DQ_TM_DP, smem_desc_sw128(aDO + off, 16, 1024),
+                     smem_desc_sw128(aV + vs * C::TILE + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&v_empty[vs]);
+        tc_commit(dp_full);
+        if (j >= 1) ok = do_dq(j - 1);
+      }
+      if (ok) ok = do_dq(nkt - 1);
+      if (ok) tc_commit(dq_full);
+      tc_commit(drain);
+      drain_wait(drain, 0, ctx);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroup (row = query)
+    const int r = threadIdx.x;
+    const int i = q0 + r;
+    const bool i_ok = i < s.NQ;
+    const size_t ro = static_cast<size_t>(bh) * s.NQ + (i_ok ? i : s.NQ - 1);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
+      int okv = 1;
+      if (lane == 0) okv = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, okv, 0) != 0;
+    };
+    const float m_sc = args.row_m[ro];
+    const float inv_s = 1.0f / args.row_s[ro];
+    const int a = min(max(args.row_arg[ro], 0), s.NK - 1);
+    // D_i = dO_i . O_i
+    float Di = 0.0f;
+    {
+      const char* dorow = reinterpret_cast<const char*>(args.dout) + ro * D * 2;
+#pragma unroll 4
+      for (int d = 0; d < D; d += 8) {
+        float g[8], o[8];
+        load8_bf16(dorow + d * 2, g);
+        if (args.o_bf16) {
+          load8_bf16(reinterpret_cast<const char*>(args.o) + (ro * D + d) * 2, o);
+        } else {
+          const float4* op = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(args.o) + ro * D + d);
+          const float4 x0 = op[0], x1 = op[1];
+          o[0] = x0.x; o[1] = x0.y; o[2] = x0.z; o[3] = x0.w;
+          o[4] = x1.x; o[5] = x1.y; o[6] = x1.z; o[7] = x1.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Di = fmaf(g[e], o[e], Di);
+      }
+    }
+    // rows past N_Q read zero-filled Q rows (s = 0): base 2 saturates every w to 1, weight 0
+    const float base = i_ok ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
+    const float c2 = s.scale * (1.0f / 32.0f);
+    const float cE = 0.25f * inv_s;
+    const int lim = s.causal ? min(i, s.NK - 1) : s.NK - 1;
+    float R = 0.0f;
+    bool ok = true;
+    uint32_t sv[4][32];
+#define SV(c) sv[(c) >> 5][(c) & 31]
+    for (int j = 0; j < nkt && ok; ++j) {
+      const int sb = j & 1;
+      ok = warp_wait(&s_full[sb], (j >> 1) & 1u);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const uint32_t col = lane_addr + (sb ? DQ_TM_S1 : DQ_TM_S0);
+        tmem_ld32(col, sv[0]);
+        tmem_ld32(col + 32, sv[1]);
+        tmem_ld32(col + 64, sv[2]);
+        tmem_ld32(col + 96, sv[3]);
+        tc_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      const int col0 = j * BN;
+      const bool need_mask = col0 + BN - 1 > lim;
+      // coefficient q^7 (1/w)^2 / (4 s_i) per entry, in place
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        float s0 = u2f(SV(c)), s1 = u2f(SV(c + 1));
+        if (need_mask) {
+          if (col0 + c > lim) s0 = -INFINITY;
+          if (col0 + c + 1 > lim) s1 = -INFINITY;
+        }
+        const float2 rr = rcp_pair(fma_sat(s0, -c2, base), fma_sat(s1, -c2, base));
+        const float2 qq = __fadd2_rn(rr, make_float2(-1.0f, -1.0f));
+        const float2 q2 = __fmul2_rn(qq, qq);
+        const float2 q4 = __fmul2_rn(q2, q2);
+        const float2 q7 = __fmul2_rn(__fmul2_rn(q4, q2), qq);
+        const float2 coef = __fmul2_rn(__fmul2_rn(q7, __fmul2_rn(rr, rr)), make_float2(cE, cE));
+        SV(c) = __float_as_uint(coef.x);
+        SV(c + 1) = __float_as_uint(coef.y);
+      }
+      if (a >= col0 && a < col0 + BN) {   // the argmax entry takes -R_i, not E
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (col0 + c == a) SV(c) = 0u;
+      }
+      ok = warp_wait(e_free, (j & 1u) ^ 1u) && warp_wait(dp_full, j & 1u);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t dv[32];
+        tmem_ld32(lane_addr + DQ_TM_DP + cc * 32, dv);
+        tc_wait_ld();
+        if (cc == BN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dp_free);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int c = cc * 32 + e * 8 + 2 * t;
+            const float e0 = u2f(SV(c)) * (u2f(dv[e * 8 + 2 * t]) - Di);
+            const float e1 = u2f(SV(c + 1)) * (u2f(dv[e * 8 + 2 * t + 1]) - Di);
+            R += e0 + e1;
+            pk[t] = pack_bf16x2(e0, e1);
+          }
+          st_tile16(sE, r, cc * 4 + e, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(e_full);
+    }
+#undef SV
+    if (ok) ok = warp_wait(dq_full, 0);
+    if (ok) {
+      tc_fence_after();
+      if (i_ok) {
+        args.ws_d[ro] = Di;
+        args.ws_r[ro] = R;
+        args.ws_base[ro] = base;
+        args.ws_invs[ro] = inv_s;
+      }
+      const char* krow = reinterpret_cast<const char*>(args.k_raw) + (static_cast<size_t>(bh) * s.NK + a) * D * 2;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t acc[32];
+        tmem_ld32(lane_addr + DQ_TM_DQ + c0, acc);
+        tc_wait_ld();
+        if (i_ok) {
+          float out[32];
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            float kv[8];
+            load8_bf16(krow + (c0 + e) * 2, kv);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) out[e + t] = s.scale * fmaf(-R, kv[t], u2f(acc[e + t]));
+          }
+          store_row32(args.dq, ro * D + c0, out, args.grad_bf16);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ============================================================================ dK/dV kernel
+template <int D>
+struct DkvCfg {
+  static constexpr int TILE = BN * D * 2;
+  static constexpr int NQS = 2;                    // Q stages
+  static constexpr int NDS = (D == 128) ? 1 : 2;   // dO stages
+  static constexpr int A_BYTES = BN * BM * 2;      // P^T or dS^T tile (keys x queries, bf16)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;
+  static constexpr int OFF_DO = OFF_Q + NQS * TILE;
+  static constexpr int OFF_P = OFF_DO + NDS * TILE;
+  static constexpr int OFF_DS = OFF_P + A_BYTES;
+  static constexpr int OFF_ST = OFF_DS + A_BYTES;          // per-query constants of one tile
+  static constexpr int ST_BYTES = 5 * BM * 4;
+  static constexpr int OFF_BAR = OFF_ST + ST_BYTES;
+  // kv_full, q_full[NQS], q_empty[NQS], do_full[NDS], do_empty[NDS],
+  // st_full, st_free, dpt_full, dpt_free, p_full, p_free, acc_full, drain
+  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 8;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int USED = OFF_MISC + 16;
+  // alignment slack only where it fits; otherwise the kernel requires (and checks) a
+  // 1024-byte aligned dynamic shared-memory base
+  static constexpr int SLACK = (USED + 1024 <= 232448) ? 1024 : 0;
+  static constexpr int SMEM_BYTES = USED + SLACK;
+};
+constexpr uint32_t KV_TM_ST = 0, KV_TM_DPT = 128, KV_TM_DV = 256, KV_TM_DK = 384;
+
+__device__ __forceinline__ void softmax_group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_dkdv_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
+  using C = DkvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t mis = smem_u32(smem_raw) & 1023u;
+  if (C::SLACK == 0 && mis != 0) {   // uniform across the CTA: nothing launched yet
+    if (threadIdx.x == 0) atomicOr(ctx.status, kStatusBadSmem);
+    return;
+  }
+  uint8_t* smem = smem_raw + ((1024u - mis) & 1023u);
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sDO = smem + C::OFF_DO;
+  uint8_t* sP = smem + C::OFF_P;
+  uint8_t* sDS = smem + C::OFF_DS;
+  float* st_base = reinterpret_cast<float*>(smem + C::OFF_ST);
+  float* st_invs = st_base + BM;
+  float* st_d = st_base + 2 * BM;
+  float* st_r = st_base + 3 * BM;
+  int* st_a = reinterpret_cast<int*>(st_base + 4 * BM);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = kv_full + 1;
+  uint64_t* q_empty = q_full + C::NQS;
+  uint64_t* do_full = q_empty + C::NQS;
+  uint64_t* do_empty = do_full + C::NDS;
+  uint64_t* st_full = do_empty + C::NDS;
+  uint64_t* st_free = st_full + 1;
+  uint64_t* dpt_full = st_free + 1;
+  uint64_t* dpt_free = dpt_full + 1;
+  uint64_t* p_full = dpt_free + 1;
+  uint64_t* p_free = p_full + 1;
+  uint64_t* acc_full = p_free + 1;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int BH = s.B * s.H;
+  const int nqt = (s.NQ + BM - 1) / BM;
+  const int item = blockIdx.x;
+  const int kt = item / BH;   // ascending: under the causal mask the first key tiles see the most queries
+  const int bh = item % BH;
+  const int k0 = kt * BN;
+  const int qt0 = s.causal ? k0 / BM : 0;   // first query tile that can see key k0 (j <= i)
+  const int nq = max(0, nqt - qt0);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < C::NQS; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < C::NDS; ++i) {
+      mbar_init(&do_full[i], 1);
+      mbar_init(&do_empty[i], 1);
+    }
+    mbar_init(st_full, 1);
+    mbar_init(st_free, 4);
+    mbar_init(dpt_full, 1);
+    mbar_init(dpt_free, 4);
+    mbar_init(p_full, 4);
+    mbar_init(p_free, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      tma_prefetch_desc(&args.tm_q);
+      tma_prefetch_desc(&args.tm_k);
+      tma_prefetch_desc(&args.tm_v);
+      tma_prefetch_desc(&args.tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sK + c * BOX_BYTES, &args.tm_k, kv_full, c * 64, k0, bh);
+        tma_load_3d(sV + c * BOX_BYTES, &args.tm_v, kv_full, c * 64, k0, bh);
+      }
+      bool ok = true;
+      int q_issued = 0, d_issued = 0;
+      for (int it = 0; it < nq && ok; ++it) {
+        const int i0 = (qt0 + it) * BM;
+        const int qs = it % C::NQS;
+        ok = mbar_wait(&q_empty[qs], ((it / C::NQS) & 1u) ^ 1u, abort_flag, ctx);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&q_full[qs], C::TILE);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sQ + qs * C::TILE + c * BOX_BYTES, &args.tm_q, &q_full[qs], c * 64, i0, bh);
+        q_issued = it + 1;
+        const int ds = it % C::NDS;
+        ok = mbar_wait(&do_empty[ds], ((it / C::NDS) & 1u) ^ 1u, abort_flag, ctx);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&do_full[ds], C::TILE);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sDO + ds * C::TILE + c * BOX_BYTES, &args.tm_do, &do_full[ds], c * 64, i0, bh);
+        d_issued = it + 1;
+      }
+      drain_wait(kv_full, 0, ctx);
+      for (int it = max(0, q_issued - C::NQS); it < q_issued; ++it)
+        drain_wait(&q_full[it % C::NQS], (it / C::NQS) & 1u, ctx);
+      for (int it = max(0, d_issued - C::NDS); it < d_issued; ++it)
+        drain_wait(&do_full[it % C::NDS], (it / C::NDS) & 1u, ctx);
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_ss = idesc_bf16_f32(BN, BM, 0, 0);
+      constexpr uint32_t idesc_kmn = idesc_bf16_f32(BN, D, 0, 1);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
+                     aP = smem_u32(sP), aDS = smem_u32(sDS);
+      bool ok = mbar_wait(kv_full, 0, abort_flag, ctx);
+      for (int it = 0; it < nq && ok; ++it) {
+        const int qs = it % C::NQS, ds = it % C::NDS;
+        const uint32_t par = it & 1u;
+        // S^T = K Q_i^T
+        ok = mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
+             mbar_wait(st_free, par ^ 1u, abort_flag, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          tc_mma_f16(tmem + KV_TM_ST, smem_desc_sw128(aK + off, 16, 1024),
+                     smem_desc_sw128(aQ + qs * C::TILE + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(st_full);
+        // dP^T = V dO_i^T
+        ok = mbar_wait(&do_full[ds], (it / C::NDS) & 1u, abort_flag, ctx) &&
+             mbar_wait(dpt_free, par ^ 1u, abort_flag, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          tc_mma_f16(tmem + KV_TM_DPT, smem_desc_sw128(aV + off, 16, 1024),
+                     smem_desc_sw128(aDO + ds * C::TILE + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(dpt_full);
+        // dV += P^T dO_i, dK += dS^T Q_i
+        ok = mbar_wait(p_full, par, abort_flag, ctx);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_f16(tmem + KV_TM_DV, smem_desc_sw128(aP + aoff, 16, 1024),
+                     smem_desc_sw128(aDO + ds * C::TILE + kk * 2048, BOX_BYTES, 1024), idesc_kmn, acc);
+          tc_mma_f16(tmem + KV_TM_DK, smem_desc_sw128(aDS + aoff, 16, 1024),
+                     smem_desc_sw128(aQ + qs * C::TILE + kk * 2048, BOX_BYTES, 1024), idesc_kmn, acc);
+        }
+        tc_commit(&do_empty[ds]);
+        tc_commit(&q_empty[qs]);
+        tc_commit(p_free);
+      }
+      if (ok) tc_commit(acc_full);
+      tc_commit(drain);
+      drain_wait(drain, 0, ctx);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroup (row = key)
+    const int r = threadIdx.x;
+    const int j = k0 + r;
+    const bool j_ok = j < s.NK;
+    const size_t ko = static_cast<size_t>(bh) * s.NK + (j_ok ? j : s.NK - 1);
+    const size_t so = static_cast<size_t>(bh) * s.NQ;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c2 = s.scale * (1.0f / 32.0f);
+    bool ok = true;
+    // A wait that gives up sets ok = false; the loop still runs to the end without
+    // waiting (its named barriers must be reached by all four warps) and the
+    // epilogue is skipped.
+    auto warp_wait = [&](uint64_t* bar, uint32_t par) {
+      if (!ok) return;
+      int okv = 1;
+      if (lane == 0) okv = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, okv, 0) != 0;
+    };
+    uint32_t sv[4][32];
+#define SV(c) sv[(c) >> 5][(c) & 31]
+    for (int it = 0; it < nq; ++it) {
+      const int i0 = (qt0 + it) * BM;
+      const uint32_t par = it & 1u;
+      // per-query constants of this tile (queries past N_Q get base 2: zero weight)
+      softmax_group_sync();
+      {
+        const int ii = i0 + r;
+        const bool q_ok = ii < s.NQ;
+        const size_t qo = so + (q_ok ? ii : 0);
+        st_base[r] = q_ok ? args.ws_base[qo] : 2.0f;
+        st_invs[r] = q_ok ? args.ws_invs[qo] : 0.0f;
+        st_d[r] = q_ok ? args.ws_d[qo] : 0.0f;
+        st_r[r] = q_ok ? args.ws_r[qo] : 0.0f;
+        st_a[r] = q_ok ? args.row_arg[qo] : -1;
+      }
+      softmax_group_sync();
+      warp_wait(st_full, par);
+      tc_fence_after();
+      {
+        tmem_ld32(lane_addr + KV_TM_ST, sv[0]);
+        tmem_ld32(lane_addr + KV_TM_ST + 32, sv[1]);
+        tmem_ld32(lane_addr + KV_TM_ST + 64, sv[2]);
+        tmem_ld32(lane_addr + KV_TM_ST + 96, sv[3]);
+        tc_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(st_free);
+      // masked: key past N_K, or (causal) query i0 + c < j
+      const bool need_mask = !j_ok || (s.causal && i0 < j);
+      const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
+      warp_wait(p_free, par ^ 1u);
+      // P^T and the dS coefficient q^7 (1/w)^2 / (4 s_i), in place
+#pragma unroll
+      for (int c = 0; c < BM; c += 8) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cb = c + 4 * h;
+          const float4 b4 = *reinterpret_cast<const float4*>(st_base + cb);
+          const float4 i4 = *reinterpret_cast<const float4*>(st_invs + cb);
+          float x[4] = {u2f(SV(cb)), u2f(SV(cb + 1)), u2f(SV(cb + 2)), u2f(SV(cb + 3))};
+          if (need_mask) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if (cb + t < first_vis) x[t] = -INFINITY;
+          }
+          const float2 ra = rcp_pair(fma_sat(x[0], -c2, b4.x), fma_sat(x[1], -c2, b4.y));
+          const float2 rb = rcp_pair(fma_sat(x[2], -c2, b4.z), fma_sat(x[3], -c2, b4.w));
+          const float2 iva = make_float2(i4.x, i4.y), ivb = make_float2(i4.z, i4.w);
+          const float2 qa = __fadd2_rn(ra, make_float2(-1.0f, -1.0f));
+          const float2 qb = __fadd2_rn(rb, make_float2(-1.0f, -1.0f));
+          const float2 qa2 = __fmul2_rn(qa, qa), qb2 = __fmul2_rn(qb, qb);
+          const float2 qa4 = __fmul2_rn(qa2, qa2), qb4 = __fmul2_rn(qb2, qb2);
+          const float2 pa = __fmul2_rn(__fmul2_rn(qa4, qa4), iva);
+          const float2 pb = __fmul2_rn(__fmul2_rn(qb4, qb4), ivb);
+          const float2 ca = __fmul2_rn(__fmul2_rn(__fmul2_rn(qa4, qa2), qa),
+                                       __fmul2_rn(__fmul2_rn(ra, ra), __fmul2_rn(iva, make_float2(0.25f, 0.25f))));
+          const float2 cbv = __fmul2_rn(__fmul2_rn(__fmul2_rn(qb4, qb2), qb),
+                                        __fmul2_rn(__fmul2_rn(rb, rb), __fmul2_rn(ivb, make_float2(0.25f, 0.25f))));
+          SV(cb) = __float_as_uint(ca.x);
+          SV(cb + 1) = __float_as_uint(ca.y);
+          SV(cb + 2) = __float_as_uint(cbv.x);
+          SV(cb + 3) = __float_as_uint(cbv.y);
+          pk[2 * h] = pack_bf16x2(pa.x, pa.y);
+          pk[2 * h + 1] = pack_bf16x2(pb.x, pb.y);
+        }
+        st_tile16(sP, r, c >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+      }
+      // dS^T = coef (dP^T - D_i), with -R_i where this key is the query's argmax
+      warp_wait(dpt_full, par);
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < BM / 32; ++cc) {
+        uint32_t dv[32];
+        tmem_ld32(lane_addr + KV_TM_DPT + cc * 32, dv);
+        tc_wait_ld();
+        if (cc == BM / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dpt_free);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int cb = cc * 32 + e * 8;
+          float dsv[8];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float4 d4 = *reinterpret_cast<const float4*>(st_d + cb + 4 * h);
+            const float4 r4 = *reinterpret_cast<const float4*>(st_r + cb + 4 * h);
+            const int4 a4 = *reinterpret_cast<const int4*>(st_a + cb + 4 * h);
+            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+            const float rr4[4] = {r4.x, r4.y, r4.z, r4.w};
+            const int aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int c = cb + 4 * h + t;
+              const float v = u2f(SV(c)) * (u2f(dv[e * 8 + 4 * h + t]) - dd[t]);
+              dsv[4 * h + t] = (aa[t] == j) ? -rr4[t] : v;
+            }
+          }
+          st_tile16(sDS, r, cb >> 3,
+                    make_uint4(pack_bf16x2(dsv[0], dsv[1]), pack_bf16x2(dsv[2], dsv[3]),
+                               pack_bf16x2(dsv[4], dsv[5]), pack_bf16x2(dsv[6], dsv[7])));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+#undef SV
+    if (nq > 0) warp_wait(acc_full, 0);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t av[32], kv[32];
+        tmem_ld32(lane_addr + KV_TM_DV + c0, av);
+        tmem_ld32(lane_addr + KV_TM_DK + c0, kv);
+        tc_wait_ld();
+        if (j_ok) {
+          float ov[32], okv[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            ov[e] = nq > 0 ? u2f(av[e]) : 0.0f;
+            okv[e] = nq > 0 ? s.scale * u2f(kv[e]) : 0.0f;
+          }
+          store_row32(args.dv, ko * D + c0, ov, args.grad_bf16);
+          store_row32(args.dk, ko * D + c0, okv, args.grad_bf16);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <typename KernelFn>
+cudaError_t set_smem(KernelFn fn, int bytes) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
+  cudaError_t e = set_smem(attn_bwd_dq_tc_kernel<D>, DqCfg<D>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = set_smem(attn_bwd_dkdv_tc_kernel<D>, DkvCfg<D>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const unsigned BH = static_cast<unsigned>(s.B * s.H);
+  const unsigned nqt = static_cast<unsigned>((s.NQ + BM - 1) / BM);
+  const unsigned nkt = static_cast<unsigned>((s.NK + BN - 1) / BN);
+  attn_bwd_dq_tc_kernel<D><<<nqt * BH, THREADS, DqCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_bwd_dkdv_tc_kernel<D><<<nkt * BH, THREADS, DkvCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
+  if (s.D == 128) return launch_bwd_d<128>(s, a, ctx, st);
+  if (s.D == 64) return launch_bwd_d<64>(s, a, ctx, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace raattn

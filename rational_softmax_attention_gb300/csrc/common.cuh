@@ -13,6 +13,9 @@ namespace raattn {
 
 // Device-side status codes written into the library's status word.
 constexpr unsigned int kStatusTimeout = 1u;
+// A kernel whose shared-memory layout needs a 1024-byte aligned dynamic base found
+// another base and returned before doing anything.
+constexpr unsigned int kStatusBadSmem = 2u;
 
 // Passed by value to every kernel: where to report a timeout and how long a wait may last.
 struct LaunchCtx {

@@ -53,8 +53,10 @@ struct BwdTcArgs {
   void* dk;
   void* dv;
   int grad_bf16;
-  float* ws_d;   // [B*H*NQ]  D_i = dO_i . O_i
-  float* ws_r;   // [B*H*NQ]  R_i = sum_j E_ij (argmax excluded)
+  float* ws_d;      // [B*H*NQ]  D_i = dO_i . O_i
+  float* ws_r;      // [B*H*NQ]  R_i = sum_j E_ij (argmax excluded)
+  float* ws_base;   // [B*H*NQ]  0.5 + row_m_i / 32 (so w = (1+u)/2 = base - scale*s/32)
+  float* ws_invs;   // [B*H*NQ]  1 / row_s_i
 };
 cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st);
 

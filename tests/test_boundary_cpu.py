@@ -36,8 +36,8 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    assert lib.ra_attention_bwd_workspace_size(4, 16, 8192, 8192, 128) == 2 * 4 * 16 * 8192 * 4
-    assert lib.ra_attention_bwd_workspace_size(1, 1, 3, 3, 64) == 2 * 256
+    assert lib.ra_attention_bwd_workspace_size(4, 16, 8192, 8192, 128) == 4 * 4 * 16 * 8192 * 4
+    assert lib.ra_attention_bwd_workspace_size(1, 1, 3, 3, 64) == 4 * 256
     assert lib.ra_attention_bwd_workspace_size(0, 1, 3, 3, 64) == 0
     assert lib.ra_attention_bwd_workspace_size(1, 1, -3, 3, 64) == 0
 

@@ -149,3 +149,30 @@ def test_attention_score_gradient_rows_sum_to_zero():
     dq1, _, _ = oracle.ra_attention_head_bwd(q, k, v, do, 0.7, False)
     dq2, _, _ = oracle.ra_attention_head_bwd(q, k + 0.5, v, do, 0.7, False)
     np.testing.assert_allclose(dq1, dq2, rtol=1e-9, atol=1e-11)
+
+
+def test_argmax_override_is_the_branch_of_the_tied_entry():
+    # At an exact tie the max is not differentiable; routing the gradient to the second tied
+    # entry must give the gradient of the function in which that entry is (just) the maximum.
+    rng = np.random.default_rng(21)
+    x = rng.normal(0, 3.0, size=(1, 7))
+    x[0, 5] = x[0, 2] = x.max() + 0.5          # tie between columns 2 and 5
+    dy = rng.normal(size=x.shape)
+    default = oracle.ra_softmax_bwd(x, dy)                       # lowest index: column 2
+    routed = oracle.ra_softmax_bwd(x, dy, argmax=np.array([5]))
+    xp = x.copy()
+    xp[0, 5] += 1e-9                                              # column 5 strictly largest
+    np.testing.assert_allclose(routed, oracle.ra_softmax_bwd(xp, dy), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(default, oracle.ra_softmax_bwd(x, dy, argmax=np.array([2])), rtol=0, atol=0)
+    assert not np.allclose(default, routed)
+
+
+def test_argmax_override_with_the_true_argmax_changes_nothing():
+    rng = np.random.default_rng(22)
+    q, k, v, do = (rng.normal(size=(12, 4)) for _ in range(4))
+    S = 0.8 * q @ k.T
+    a = np.argmax(np.where(np.tril(np.ones((12, 12), bool)), S, -np.inf), axis=-1)
+    base = oracle.ra_attention_head_bwd(q, k, v, do, 0.8, True)
+    routed = oracle.ra_attention_head_bwd(q, k, v, do, 0.8, True, argmax=a)
+    for g0, g1 in zip(base, routed):
+        np.testing.assert_allclose(g1, g0, rtol=1e-13, atol=1e-14)
