@@ -1,0 +1,469 @@
+"""Benchmark of the rational-softmax attention hot path on GB300.
+
+One step = the whole hot path over one batch of seeded synthetic input:
+  ra_softmax      fp32 logits [16384, 8192] ~ N(0, 4^2)
+  ra_attention    forward + backward, B=4, H=16, N=8192, D=128, bf16, Q,K ~ N(0, 3^2),
+                  V, dO ~ N(0, 1), scale 1/sqrt(128), non-causal (fp32 outputs/gradients)
+value = counted attention FLOPs of the step / step time (standard-attention count:
+forward 4 B H N^2 D, backward 2.5x forward), in TFLOP/s.  ra_softmax's GB/s, the
+per-call times and a causal long-sequence forward (B=4, H=16, N=8192, D=128) are
+reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle (the only reference that exists
+for this method) on a bounded sample of the same workload.  Under torchrun each
+rank runs the full step on its own GPU (weak scaling; the path has no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ra_attention fwd/bwd TFLOP/s and % bf16 TC peak; ra_softmax GB/s vs HBM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def attn_flops(B, H, NQ, NK, D, causal, backward):
+    f = 4.0 * B * H * NQ * NK * D * (0.5 if causal else 1.0)
+    return f * (3.5 if backward else 1.0)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _ptr(t):
+    import ctypes
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class HotPath:
+    """Preallocated device buffers and the C-ABI calls of one step."""
+
+    def __init__(self, dev, host_inputs, w, sw):
+        import ctypes
+
+        import torch
+
+        import rational_softmax_attention_gb300 as ra
+        self.torch, self.ra, self.ctypes = torch, ra, ctypes
+        self.L = ra.lib()
+        self.w, self.sw = w, sw
+        self.host_in = host_inputs
+        self.dev_in = [t.to(dev) for t in host_inputs]
+        q, k, v, do, x = self.dev_in
+        B, H, N, D = q.shape
+        f32 = torch.float32
+        self.o = torch.empty((B, H, N, D), dtype=f32, device=dev)
+        self.rm = torch.empty((B, H, N), dtype=f32, device=dev)
+        self.rs = torch.empty((B, H, N), dtype=f32, device=dev)
+        self.ra_ = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+        self.dq = torch.empty((B, H, N, D), dtype=f32, device=dev)
+        self.dk = torch.empty_like(self.dq)
+        self.dv = torch.empty_like(self.dq)
+        self.y = torch.empty_like(x)
+        self.ws = torch.empty(self.L.ra_attention_bwd_workspace_size(B, H, N, N, D), dtype=torch.uint8, device=dev)
+        self.outs = [self.o, self.dq, self.dk, self.dv, self.y]
+        self.host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in self.outs]
+        self.shape = (B, H, N, D)
+
+    def _check(self, name, code):
+        if code != 0:
+            raise RuntimeError(f"{name}: {self.L.ra_status_string(code).decode()}")
+
+    def softmax(self, st):
+        x = self.dev_in[4]
+        self._check("ra_softmax_fwd", self.L.ra_softmax_fwd(_ptr(x), _ptr(self.y), x.shape[0], x.shape[1], 0, st))
+
+    def fwd(self, st, counts=None):
+        q, k, v, _, _ = self.dev_in
+        B, H, N, D = self.shape
+        self._check("ra_attention_fwd", self.L.ra_attention_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(self.o), _ptr(self.rm), _ptr(self.rs), _ptr(self.ra_), _ptr(counts),
+            B, H, N, N, D, float(self.w.scale), int(self.w.causal), 1, 0, st))
+
+    def bwd(self, st):
+        q, k, v, do, _ = self.dev_in
+        B, H, N, D = self.shape
+        self._check("ra_attention_bwd", self.L.ra_attention_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(self.o), _ptr(do), _ptr(self.rm), _ptr(self.rs), _ptr(self.ra_),
+            _ptr(self.dq), _ptr(self.dk), _ptr(self.dv), _ptr(self.ws), B, H, N, N, D, float(self.w.scale),
+            int(self.w.causal), 1, 0, 0, st))
+
+    def step(self, st, events=None):
+        if events:
+            events[0].record()
+        self.softmax(st)
+        if events:
+            events[1].record()
+        self.fwd(st)
+        if events:
+            events[2].record()
+        self.bwd(st)
+        if events:
+            events[3].record()
+
+    def step_e2e(self, st):
+        for d, h in zip(self.dev_in, self.host_in):
+            d.copy_(h, non_blocking=True)
+        self.step(st)
+        for h, d in zip(self.host_out, self.outs):
+            h.copy_(d, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host_in)
+
+    def d2h_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.outs)
+
+
+def traffic_from_profiles(kernel_tag):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/ (None when absent)."""
+    path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
+    try:
+        with open(path) as fh:
+            for ln in fh:
+                parts = ln.split()
+                if len(parts) >= 2 and parts[0] == kernel_tag:
+                    return float(parts[1])
+    except OSError:
+        pass
+    return None
+
+
+def cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=1024, softmax_rows=64):
+    """Bounded sample of the same workload through the float64 oracle (head 0, the first
+    `query_rows` queries against all keys, forward + backward; `softmax_rows` logit rows).
+    Returns (seconds, counted attention FLOPs, description)."""
+    import numpy as np
+
+    import oracle
+    qd = q[0, 0, :query_rows].double().numpy()
+    dod = do[0, 0, :query_rows].double().numpy()
+    kd, vd = k[0, 0].double().numpy(), v[0, 0].double().numpy()
+    xd = x[:softmax_rows].double().numpy()
+    t0 = time.perf_counter()
+    oracle.ra_attention_head_fwd(qd, kd, vd, w.scale, w.causal)
+    oracle.ra_attention_head_bwd(qd, kd, vd, dod, w.scale, w.causal)
+    oracle.ra_softmax(xd)
+    dt = time.perf_counter() - t0
+    flops = attn_flops(1, 1, query_rows, kd.shape[0], kd.shape[1], w.causal, True)
+    desc = (f"head (0,0), queries 0..{query_rows - 1} against all {kd.shape[0]} keys, forward+backward "
+            f"in float64, plus ra_softmax of {softmax_rows} logit rows")
+    del np
+    return dt, flops, desc
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return n
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def run_ours(args):
+    import torch
+
+    from rational_softmax_attention_gb300.inputs import (ATTN_LONG_CAUSAL, ATTN_LONG_WIDE, RA_SOFTMAX_LONG_ROWS,
+                                                         softmax_inputs, workload_inputs)
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w, sw = ATTN_LONG_WIDE, RA_SOFTMAX_LONG_ROWS
+    q, k, v, do = workload_inputs(w)
+    x = softmax_inputs(sw.rows, sw.cols, seed=sw.seed, sigma=sw.sigma)
+    host_in = [t.pin_memory() for t in (q, k, v, do, x)]
+    hp = HotPath(dev, host_in, w, sw)
+    stream = torch.cuda.current_stream(dev)
+    st = hp.ctypes.c_void_p(stream.cuda_stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # warm-up, then the timed region: exactly `steps` steps, device-resident inputs
+    for _ in range(args.warmup):
+        hp.step(st)
+    barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for i in range(args.steps):
+            hp.step(st, ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    status = hp.ra.device_status(stream)
+    if status != "RA_OK":
+        raise RuntimeError(f"device status after the timed region: {status}")
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    per_call = {"ra_softmax_ms": [], "ra_attention_fwd_ms": [], "ra_attention_bwd_ms": []}
+    for e in ev:
+        per_call["ra_softmax_ms"].append(e[0].elapsed_time(e[1]))
+        per_call["ra_attention_fwd_ms"].append(e[1].elapsed_time(e[2]))
+        per_call["ra_attention_bwd_ms"].append(e[2].elapsed_time(e[3]))
+    med = {kk: statistics.median(vv) for kk, vv in per_call.items()}
+
+    B, H, N, D = hp.shape
+    flops_step = attn_flops(B, H, N, N, D, w.causal, True)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
+    fwd_fl = attn_flops(B, H, N, N, D, w.causal, False)
+    bwd_fl = flops_step - fwd_fl
+    sm_bytes = 2.0 * x.numel() * 4
+
+    # end to end: pinned host inputs -> device, the step, results -> pinned host buffers
+    for _ in range(max(1, args.warmup)):
+        hp.step_e2e(st)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        hp.step_e2e(st)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12
+
+    # skipped-tile fraction of the forward (one untimed call with the counters)
+    counts = torch.zeros(2, dtype=torch.int64, device=dev)
+    hp.fwd(st, counts)
+    torch.cuda.synchronize(dev)
+    visited, skipped = (int(c) for c in counts.tolist())
+
+    # causal long-sequence forward (reported beside the step; its own timed loop)
+    wc = ATTN_LONG_CAUSAL
+    qc, kc, vc = (t.to(dev) for t in workload_inputs(wc)[:3])
+    oc = torch.empty(qc.shape, dtype=torch.float32, device=dev)
+    rmc = torch.empty(qc.shape[:3], dtype=torch.float32, device=dev)
+    rsc = torch.empty_like(rmc)
+    rac = torch.empty(qc.shape[:3], dtype=torch.int32, device=dev)
+
+    def fwd_causal():
+        code = hp.L.ra_attention_fwd(_ptr(qc), _ptr(kc), _ptr(vc), _ptr(oc), _ptr(rmc), _ptr(rsc), _ptr(rac), None,
+                                     wc.B, wc.H, wc.N, wc.N, wc.D, float(wc.scale), 1, 1, 0, st)
+        if code != 0:
+            raise RuntimeError("ra_attention_fwd (causal) failed")
+    for _ in range(3):
+        fwd_causal()
+    torch.cuda.synchronize(dev)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(args.steps):
+        fwd_causal()
+    c1.record(stream)
+    torch.cuda.synchronize(dev)
+    causal_ms = c0.elapsed_time(c1) / args.steps
+    causal_fl = attn_flops(wc.B, wc.H, wc.N, wc.N, wc.D, True, False)
+
+    peaks, peak_src = load_peaks()
+    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tc_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bwd_tflops = bwd_fl / (med["ra_attention_bwd_ms"] * 1e-3) / 1e12
+    fwd_tflops = fwd_fl / (med["ra_attention_fwd_ms"] * 1e-3) / 1e12
+    sm_gbs = sm_bytes / (med["ra_softmax_ms"] * 1e-3) / 1e9
+    dominant = max(("ra_attention_bwd", med["ra_attention_bwd_ms"]), ("ra_attention_fwd", med["ra_attention_fwd_ms"]),
+                   ("ra_softmax", med["ra_softmax_ms"]), key=lambda t: t[1])[0]
+    rl = {
+        "ra_attention_bwd": {"bound": "tensor", "achieved": bwd_tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                             "traffic": traffic_from_profiles("ra_attention_bwd"),
+                             "kernel": "ra_attention_bwd call: bf16_to_f16 + attn_bwd_dq_tc + attn_bwd_dkdv_tc",
+                             "algorithmic": f"{bwd_fl:.4e} FLOP per call (2.5 x 4 B H N^2 D)"},
+        "ra_attention_fwd": {"bound": "tensor", "achieved": fwd_tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                             "traffic": traffic_from_profiles("ra_attention_fwd"), "kernel": "attn_fwd_tc_kernel",
+                             "algorithmic": f"{fwd_fl:.4e} FLOP per launch (4 B H N^2 D)"},
+        "ra_softmax": {"bound": "hbm", "achieved": sm_gbs, "peak": hbm_peak, "unit": "GB/s",
+                       "traffic": traffic_from_profiles("ra_softmax"), "kernel": "ra_softmax_fwd_vec_kernel",
+                       "algorithmic": f"{sm_bytes:.4e} B per launch (4 B read + 4 B written per element)"},
+    }[dominant]
+    rl["frac"] = rl["achieved"] / rl["peak"]
+    rl["peak_source"] = f"{peak_src} ({'bf16 sustained' if rl['unit'] == 'TFLOP/s' else 'HBM copy'})"
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded torch.randn (CPU generator), no dataset",
+        "config": {
+            "workload": "ra_softmax fp32 [16384, 8192] sigma 4 + ra_attention fwd+bwd B4 H16 N8192 D128 bf16 "
+                        "Q,K sigma 3 scale 1/sqrt(128) non-causal (fp32 O and gradients)",
+            "ra_softmax": {"rows": sw.rows, "cols": sw.cols, "sigma": sw.sigma, "dtype": "f32"},
+            "attention": {"B": B, "H": H, "N": N, "D": D, "sigma_qk": w.sigma_qk, "causal": w.causal,
+                          "dtype": "bf16 in, fp32 accumulate, fp32 out"},
+            "l2": "no flush: each step reads > 1.5 GiB of inputs, above the 129 MB L2",
+            "per_gpu": "each rank runs the whole step on its own GPU (no exchange on this path)",
+        },
+        "components": {
+            "ra_softmax": {"ms": med["ra_softmax_ms"], "GB_per_s": sm_gbs, "frac_hbm": sm_gbs / hbm_peak,
+                           "frac_hbm_8000": sm_gbs / 8000.0},
+            "ra_attention_fwd": {"ms": med["ra_attention_fwd_ms"], "TFLOP_per_s": fwd_tflops,
+                                 "frac_bf16_burst": fwd_tflops / tc_burst,
+                                 "tiles_visited": visited, "tiles_skipped": skipped,
+                                 "skipped_fraction": (skipped / visited) if visited else None},
+            "ra_attention_bwd": {"ms": med["ra_attention_bwd_ms"], "TFLOP_per_s": bwd_tflops,
+                                 "frac_bf16_burst": bwd_tflops / tc_burst},
+            "ra_attention_fwd_causal_b4h16n8192d128": {"ms": causal_ms,
+                                                       "TFLOP_per_s": causal_fl / (causal_ms * 1e-3) / 1e12,
+                                                       "frac_bf16_burst": causal_fl / (causal_ms * 1e-3) / 1e12 / tc_burst},
+        },
+        "roofline": rl,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": hp.h2d_bytes(),
+                "d2h_bytes_per_step": hp.d2h_bytes(), "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": 5 * args.steps,
+        "gpu_launches_per_step": {"ra_softmax_fwd_vec_kernel": 1, "attn_fwd_tc_kernel": 1, "bf16_to_f16_kernel": 1,
+                                  "attn_bwd_dq_tc_kernel": 1, "attn_bwd_dkdv_tc_kernel": 1},
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, desc = cpu_oracle_sample(w, sw, q, k, v, do, x)
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+                                "kind": "oracle", "sample": desc, "seconds": dt}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The float64 CPU oracle on a bounded sample of the same workload, per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from rational_softmax_attention_gb300.inputs import ATTN_LONG_WIDE, RA_SOFTMAX_LONG_ROWS, softmax_inputs, workload_inputs
+    w, sw = ATTN_LONG_WIDE, RA_SOFTMAX_LONG_ROWS
+    q, k, v, do = workload_inputs(w)
+    x = softmax_inputs(sw.rows, sw.cols, seed=sw.seed, sigma=sw.sigma)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=256, softmax_rows=16)
+    total, flops, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        dt, fl, desc = cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=256, softmax_rows=16)
+        total += dt
+        flops += fl
+    value = flops / total / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+        "data": "synthetic: seeded torch.randn (CPU generator), no dataset",
+        "config": {"workload": "ra_softmax fp32 [16384, 8192] sigma 4 + ra_attention fwd+bwd B4 H16 N8192 D128 bf16 "
+                               "Q,K sigma 3 scale 1/sqrt(128) non-causal (fp32 O and gradients)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -122,9 +122,12 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
 
 /*
  * ra_attention_bwd_workspace_size -- bytes of device workspace ra_attention_bwd needs
- * for these sizes: four float arrays of B*H*N_Q entries (D_i = dO_i . O_i, the argmax
- * correction R_i, and two per-row constants of the recomputed weights), each padded
- * to 256 bytes.  Returns 0 for invalid sizes.
+ * for these sizes (either input dtype): four float arrays of B*H*N_Q entries
+ * (D_i = dO_i . O_i, the argmax correction R_i, and two per-row constants of the
+ * recomputed weights), then fp16 copies of q, dout, k and v, which the tensor-core
+ * path multiplies in fp16 (exact for bf16 values up to 65504; P, E and dS are then
+ * rounded to fp16 rather than bf16 before their products).  Each piece is padded to
+ * 256 bytes.  Returns 0 for invalid sizes.
  */
 size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 
@@ -159,9 +162,13 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
 
 /*
  * ra_device_status -- synchronise `stream`, then report and clear the device-side
- * status word of the current device: RA_OK, or RA_ERR_TIMEOUT if any kernel of
- * this library gave up a bounded wait since the last call.  RA_ERR_LAUNCH if the
- * synchronisation itself failed.
+ * status word of the current device, for everything launched since the last call:
+ *   RA_OK               nothing to report;
+ *   RA_ERR_TIMEOUT      a kernel gave up a bounded wait (its outputs are undefined);
+ *   RA_ERR_UNSUPPORTED  a tensor-core backward met an input beyond the fp16 range
+ *                       (|x| > 65504 or NaN); its gradients are undefined;
+ *   RA_ERR_LAUNCH       the synchronisation failed, or a kernel found its shared
+ *                       memory misaligned and returned without doing anything.
  */
 ra_status_t ra_device_status(void* stream);
 

@@ -63,9 +63,9 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 3-D map over a [BH, N, D] bf16 tensor: box {64, 128, 1}, 128-byte swizzle, zero fill
+// 3-D map over a [BH, N, D] 16-bit tensor: box {64, 128, 1}, 128-byte swizzle, zero fill
 // out of bounds (rows past N of a head read as zeros, never the next head's rows).
-bool make_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int D) {
+bool make_map_16bit(CUtensorMap* map, const void* base, int BH, int N, int D, CUtensorMapDataType type) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
@@ -73,10 +73,28 @@ bool make_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int D) {
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(map, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+bool make_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int D) {
+  return make_map_16bit(map, base, BH, N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+// Backward workspace: four per-row float arrays, then (tensor-core path only) fp16
+// copies of Q, K, V and dO; every piece starts on a 256-byte boundary.
+struct BwdLayout {
+  size_t per_row, q16, kv16, total_f32, total_tc;
+  BwdLayout(int B, int H, int NQ, int NK, int D) {
+    auto pad = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+    const size_t bh = static_cast<size_t>(B) * H;
+    per_row = pad(bh * NQ * sizeof(float));
+    q16 = pad(bh * NQ * D * 2);
+    kv16 = pad(bh * NK * D * 2);
+    total_f32 = 4 * per_row;
+    total_tc = total_f32 + 2 * q16 + 2 * kv16;
+  }
+};
 
 ra_status_t check_attn_sizes(int B, int H, int NQ, int NK, int D) {
   if (B < 1 || H < 1 || NQ < 1 || NK < 1 || D < 1) return RA_ERR_ARG;
@@ -120,7 +138,8 @@ ra_status_t ra_device_status(void* stream) {
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return RA_ERR_LAUNCH;
   if (v & kStatusBadSmem) return RA_ERR_LAUNCH;
-  return (v & kStatusTimeout) ? RA_ERR_TIMEOUT : RA_OK;
+  if (v & kStatusTimeout) return RA_ERR_TIMEOUT;
+  return (v & kStatusRange) ? RA_ERR_UNSUPPORTED : RA_OK;
 }
 
 ra_status_t ra_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, ra_dtype_t dtype, void* stream) {
@@ -188,9 +207,7 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
 
 size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D) {
   if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N_Q;
-  const size_t per = ((rows * sizeof(float)) + 255) & ~static_cast<size_t>(255);
-  return 4 * per;   // D_i, R_i, 0.5 + m_i/32, 1/s_i
+  return BwdLayout(B, H, N_Q, N_K, D).total_tc;   // enough for either path
 }
 
 ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -209,10 +226,11 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
   if (!std::isfinite(scale)) return RA_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const AttnShape s{B, H, N_Q, N_K, D, scale, causal ? 1 : 0};
-  const size_t rows = static_cast<size_t>(B) * H * N_Q;
-  const size_t per = ((rows * sizeof(float)) + 255) & ~static_cast<size_t>(255);
-  float* ws_d = static_cast<float*>(workspace);
-  float* ws_r = reinterpret_cast<float*>(static_cast<char*>(workspace) + per);
+  const BwdLayout lay(B, H, N_Q, N_K, D);
+  const size_t per = lay.per_row;
+  char* ws = static_cast<char*>(workspace);
+  float* ws_d = reinterpret_cast<float*>(ws);
+  float* ws_r = reinterpret_cast<float*>(ws + per);
 
   if (in_dtype == RA_F32) {
     if (!(D == 16 || D == 32 || D == 64 || D == 128)) return RA_ERR_UNSUPPORTED;
@@ -227,9 +245,15 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
   if (make_ctx(&ctx) != RA_OK) return RA_ERR_LAUNCH;
   BwdTcArgs a;
   const int BH = B * H;
-  if (!make_map_bf16(&a.tm_q, q, BH, N_Q, D) || !make_map_bf16(&a.tm_k, k, BH, N_K, D) ||
-      !make_map_bf16(&a.tm_v, v, BH, N_K, D) || !make_map_bf16(&a.tm_do, dout, BH, N_Q, D))
+  a.q16 = ws + lay.total_f32;
+  a.do16 = ws + lay.total_f32 + lay.q16;
+  a.k16 = ws + lay.total_f32 + 2 * lay.q16;
+  a.v16 = ws + lay.total_f32 + 2 * lay.q16 + lay.kv16;
+  const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!make_map_16bit(&a.tm_q, a.q16, BH, N_Q, D, f16) || !make_map_16bit(&a.tm_k, a.k16, BH, N_K, D, f16) ||
+      !make_map_16bit(&a.tm_v, a.v16, BH, N_K, D, f16) || !make_map_16bit(&a.tm_do, a.do16, BH, N_Q, D, f16))
     return RA_ERR_LAUNCH;
+  a.v_raw = v;
   a.o = o;
   a.o_bf16 = o_dtype == RA_BF16 ? 1 : 0;
   a.dout = dout;

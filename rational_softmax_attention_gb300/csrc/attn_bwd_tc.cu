@@ -25,6 +25,13 @@
 //     P^T and dS^T (with -R_i at the argmax entries) in shared memory;
 //     dV += P^T dO and dK += dS^T Q accumulate in TMEM.
 // The second kernel reads what the first wrote, so they run in stream order.
+//
+// Operand format: the MMAs of the backward take fp16 operands (fp32 accumulation).
+// A prologue converts Q, K, V and dO from bf16 to fp16 into the workspace; that is
+// exact for |x| <= 65504 (bf16 has 8 significant bits, fp16 11), so the recomputed
+// scores equal the forward's, while P, E and dS -- formed in fp32 -- are rounded to
+// fp16 (unit roundoff 2^-11) instead of bf16 (2^-8) before their products.  With
+// |E| up to ~10 at wide score spreads, bf16 rounding alone costs ~2e-2 in dQ.
 #include "kernels.cuh"
 
 namespace raattn {
@@ -212,8 +219,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
-      constexpr uint32_t idesc_ss = idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idesc_kmn = idesc_bf16_f32(BM, D, 0, 1);
+      constexpr uint32_t idesc_ss = idesc_fp16_f32(BM, BN, 0, 0);
+      constexpr uint32_t idesc_kmn = idesc_fp16_f32(BM, D, 0, 1);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aK = smem_u32(sK), aV = smem_u32(sV),
                      aE = smem_u32(sE);
       auto do_dq = [&](int t) -> bool {   // dQ += E_t K_t
@@ -370,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float e0 = u2f(SV(c)) * (u2f(dv[e * 8 + 2 * t]) - Di);
             const float e1 = u2f(SV(c + 1)) * (u2f(dv[e * 8 + 2 * t + 1]) - Di);
             R += e0 + e1;
-            pk[t] = pack_bf16x2(e0, e1);
+            pk[t] = pack_f16x2_sat(e0, e1);
           }
           st_tile16(sE, r, cc * 4 + e, make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
@@ -570,8 +577,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
-      constexpr uint32_t idesc_ss = idesc_bf16_f32(BN, BM, 0, 0);
-      constexpr uint32_t idesc_kmn = idesc_bf16_f32(BN, D, 0, 1);
+      constexpr uint32_t idesc_ss = idesc_fp16_f32(BN, BM, 0, 0);
+      constexpr uint32_t idesc_kmn = idesc_fp16_f32(BN, D, 0, 1);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
                      aP = smem_u32(sP), aDS = smem_u32(sDS);
       bool ok = mbar_wait(kv_full, 0, abort_flag, ctx);
@@ -708,8 +715,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           SV(cb + 1) = __float_as_uint(ca.y);
           SV(cb + 2) = __float_as_uint(cbv.x);
           SV(cb + 3) = __float_as_uint(cbv.y);
-          pk[2 * h] = pack_bf16x2(pa.x, pa.y);
-          pk[2 * h + 1] = pack_bf16x2(pb.x, pb.y);
+          pk[2 * h] = pack_f16x2_sat(pa.x, pa.y);
+          pk[2 * h + 1] = pack_f16x2_sat(pb.x, pb.y);
         }
         st_tile16(sP, r, c >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
       }
@@ -746,8 +753,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
           st_tile16(sDS, r, cb >> 3,
-                    make_uint4(pack_bf16x2(dsv[0], dsv[1]), pack_bf16x2(dsv[2], dsv[3]),
-                               pack_bf16x2(dsv[4], dsv[5]), pack_bf16x2(dsv[6], dsv[7])));
+                    make_uint4(pack_f16x2_sat(dsv[0], dsv[1]), pack_f16x2_sat(dsv[2], dsv[3]),
+                               pack_f16x2_sat(dsv[4], dsv[5]), pack_f16x2_sat(dsv[6], dsv[7])));
         }
       }
       fence_proxy_async_smem();
@@ -787,6 +794,36 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// bf16 -> fp16 copies of Q, K, V and dO (blockIdx.y selects the tensor), 8 values per
+// 16-byte access; any |x| > 65504 (or NaN) sets kStatusRange.
+struct ConvertJob {
+  const uint4* src[4];
+  uint4* dst[4];
+  size_t n8[4];
+};
+
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const ConvertJob job, unsigned int* status) {
+  const int t = blockIdx.y;
+  const uint4* __restrict__ src = job.src[t];
+  uint4* __restrict__ dst = job.dst[t];
+  const size_t n8 = job.n8[t];
+  bool bad = false;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 u = __ldcs(src + i);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      bad |= !(fabsf(f.x) <= 65504.0f) || !(fabsf(f.y) <= 65504.0f);
+      o[k] = pack_f16x2_sat(f.x, f.y);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusRange);
+}
+
 template <typename KernelFn>
 cudaError_t set_smem(KernelFn fn, int bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -801,6 +838,21 @@ cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx
   const unsigned BH = static_cast<unsigned>(s.B * s.H);
   const unsigned nqt = static_cast<unsigned>((s.NQ + BM - 1) / BM);
   const unsigned nkt = static_cast<unsigned>((s.NK + BN - 1) / BN);
+  ConvertJob job;
+  const size_t nq8 = static_cast<size_t>(BH) * s.NQ * D / 8, nk8 = static_cast<size_t>(BH) * s.NK * D / 8;
+  const void* srcs[4] = {a.q_raw, a.k_raw, a.v_raw, a.dout};
+  void* dsts[4] = {a.q16, a.k16, a.v16, a.do16};
+  const size_t ns[4] = {nq8, nk8, nk8, nq8};
+  for (int i = 0; i < 4; ++i) {
+    job.src[i] = static_cast<const uint4*>(srcs[i]);
+    job.dst[i] = static_cast<uint4*>(dsts[i]);
+    job.n8[i] = ns[i];
+  }
+  const size_t nmax = nq8 > nk8 ? nq8 : nk8;
+  const unsigned cblocks = static_cast<unsigned>(std::min<size_t>((nmax + 255) / 256, 152 * 8));
+  bf16_to_f16_kernel<<<dim3(cblocks, 4), 256, 0, st>>>(job, ctx.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   attn_bwd_dq_tc_kernel<D><<<nqt * BH, THREADS, DqCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

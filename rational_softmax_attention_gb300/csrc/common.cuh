@@ -16,6 +16,9 @@ constexpr unsigned int kStatusTimeout = 1u;
 // A kernel whose shared-memory layout needs a 1024-byte aligned dynamic base found
 // another base and returned before doing anything.
 constexpr unsigned int kStatusBadSmem = 2u;
+// An input of the tensor-core backward lies outside the fp16 range (|x| > 65504) that
+// its internal operand format covers; the gradients of that call are not valid.
+constexpr unsigned int kStatusRange = 4u;
 
 // Passed by value to every kernel: where to report a timeout and how long a wait may last.
 struct LaunchCtx {
@@ -197,14 +200,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B, fp32 accumulator.
+// Instruction descriptor for kind::f16 with fp32 accumulator; A and B share one
+// 16-bit format (ab_format 1 = bf16, 0 = fp16).
 // a_mn_major / b_mn_major: 0 = K-major operand, 1 = MN-major operand.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, int a_mn_major, int b_mn_major,
+                                                         uint32_t ab_format) {
   return (1u << 4)                                  // D format: f32
-         | (1u << 7)                                // A format: bf16
-         | (1u << 10)                               // B format: bf16
+         | (ab_format << 7)                         // A format
+         | (ab_format << 10)                        // B format
          | (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+  return idesc_f16kind_f32(M, N, a_mn_major, b_mn_major, 1u);
+}
+__host__ __device__ constexpr uint32_t idesc_fp16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+  return idesc_f16kind_f32(M, N, a_mn_major, b_mn_major, 0u);
 }
 
 // ----------------------------------------------------------------------------
@@ -232,6 +243,13 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two floats to fp16x2 (lo in the low half), round to nearest, saturating at +-65504.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 }  // namespace raattn

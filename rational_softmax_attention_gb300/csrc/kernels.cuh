@@ -49,6 +49,11 @@ struct BwdTcArgs {
   const int32_t* row_arg;
   const void* k_raw;   // K in global memory (bf16), for the argmax correction
   const void* q_raw;   // Q in global memory (bf16)
+  const void* v_raw;   // V in global memory (bf16)
+  void* q16;           // fp16 copies in the workspace, read through the tensor maps
+  void* k16;
+  void* v16;
+  void* do16;
   void* dq;
   void* dk;
   void* dv;

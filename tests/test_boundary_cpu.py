@@ -36,8 +36,10 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    assert lib.ra_attention_bwd_workspace_size(4, 16, 8192, 8192, 128) == 4 * 4 * 16 * 8192 * 4
-    assert lib.ra_attention_bwd_workspace_size(1, 1, 3, 3, 64) == 4 * 256
+    # four per-row float arrays + fp16 copies of Q, dO (N_Q rows) and K, V (N_K rows)
+    assert lib.ra_attention_bwd_workspace_size(4, 16, 8192, 8192, 128) == \
+        4 * (4 * 16 * 8192 * 4) + 4 * (4 * 16 * 8192 * 128 * 2)
+    assert lib.ra_attention_bwd_workspace_size(1, 1, 3, 3, 64) == 4 * 256 + 4 * 512
     assert lib.ra_attention_bwd_workspace_size(0, 1, 3, 3, 64) == 0
     assert lib.ra_attention_bwd_workspace_size(1, 1, -3, 3, 64) == 0
 
