@@ -23,9 +23,12 @@
 //   warps 0-3   softmax warpgroup, thread t owns query row t (TMEM lane t):
 //               pass 1 reads S and keeps the running max and lowest argmax;
 //               pass 2 reads S, forms phi on the FMA pipe (no exp), writes
-//               P = bf16(phi) into a 128-byte-swizzled shared-memory tile for the
+//               P = fp16(phi) into a 128-byte-swizzled shared-memory tile for the
 //               P V product, sums phi in fp32, and votes whether the tile is live.
 //               Epilogue: O = acc / sum(phi), row statistics for the backward.
+//   warps 6-7   convert each landed V tile from bf16 to fp16 in place, so the P V
+//               product runs in fp16 (P rounded to 2^-11, not 2^-8; bf16 V values
+//               up to 65504 convert exactly).  Q K^T stays in bf16.
 //
 // phi on the FMA pipe: w = (1+u)/2 = 0.5 + (m - s)/32 (scaled units) computed with
 // one saturating FMA, so every u >= 1 (and every masked entry, fed as -inf) gives
@@ -42,7 +45,8 @@ constexpr int BM = 128;   // query rows per CTA: the MMA M and the 128 TMEM lane
 constexpr int BN = 128;   // keys per tile: the N of Q K^T and the K of P V
 constexpr int PRODUCER_WARP = 4;
 constexpr int MMA_WARP = 5;
-constexpr int THREADS = 192;
+constexpr int CONVERT_WARP0 = 6;   // warps 6 and 7: bf16 -> fp16 conversion of V tiles
+constexpr int THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S0 = 0;
 constexpr uint32_t TMEM_S1 = 128;
@@ -58,8 +62,9 @@ struct FwdCfg {
   static constexpr int OFF_RING = OFF_Q + TILE_BYTES;
   static constexpr int OFF_P = OFF_RING + NSTAGE * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain
-  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2;
+  // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain,
+  // v_conv[NSTAGE]
+  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2 + NSTAGE;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int MISC_BYTES = 64;   // tmem base, abort flag, live votes [2][4]
   static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;   // + slack for 1024-byte alignment
@@ -88,6 +93,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* p_empty = p_full + 2;
   uint64_t* o_full = p_empty + 2;
   uint64_t* drain = o_full + 1;
+  uint64_t* v_conv = drain + 1;   // [NST]: the V tile in this ring slot has been converted to fp16
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);   // [2][4]
@@ -109,6 +115,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < NST; ++i) {
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
+      mbar_init(&v_conv[i], 2);    // one arrival per converter warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -172,13 +179,52 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < NST; ++i)
         if (issued[i]) drain_wait(&ring_full[i], last_par[i], ctx);
     }
+  } else if (warp >= CONVERT_WARP0) {
+    // ------------------------------------------------------------------ V converters (warps 6, 7)
+    // Each V tile is rewritten in place from bf16 to fp16 (same swizzled positions), so
+    // that the P V product takes fp16 P: P is then rounded to 2^-11 instead of 2^-8.
+    // The ring slot of V_t follows the producer's order: pass-2 position 2(t+1), and
+    // 2*nkt - 1 for the last tile.
+    const int half = warp - CONVERT_WARP0;
+    constexpr int CHUNKS = C::TILE_BYTES / 16;
+    constexpr int PER_LANE = CHUNKS / 2 / 32;
+    bool out_of_range = false;
+    for (int t = 0; t < nkt; ++t) {
+      const int itv = nkt + ((t < nkt - 1) ? 2 * (t + 1) : 2 * nkt - 1);
+      const int st = itv % NST;
+      const uint32_t par = (itv / NST) & 1u;
+      int okv = 1;
+      if (lane == 0) okv = mbar_wait(&ring_full[st], par, abort_flag, ctx) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, okv, 0)) break;
+      while (!mbar_try_wait(&ring_full[st], par)) {
+      }   // completed already: gives every lane the acquire of the TMA data
+      uint4* tile = reinterpret_cast<uint4*>(sRing + st * C::TILE_BYTES) + half * (CHUNKS / 2);
+#pragma unroll 4
+      for (int i = 0; i < PER_LANE; ++i) {
+        const uint4 u = tile[i * 32 + lane];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+          out_of_range |= !(fabsf(f.x) <= 65504.0f) || !(fabsf(f.y) <= 65504.0f);
+          o[e] = pack_f16x2_sat(f.x, f.y);
+        }
+        tile[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&v_conv[st]);
+    }
+    if (__any_sync(0xffffffffu, out_of_range) && lane == 0) atomicOr(ctx.status, kStatusRange);
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 0, 1);
+      constexpr uint32_t idesc_pv = idesc_fp16_f32(BM, D, 0, 1);   // P and V in fp16
       const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sRing), sPa = smem_u32(sP);
       uint32_t it = 0, sidx = 0;
+      uint32_t vconv_par = 0;   // bit st: parity of the next v_conv[st] phase to wait for
       unsigned long long visited = 0, skipped = 0;
       bool o_started = false;
       auto mma_s = [&]() -> bool {   // S[sidx & 1] = Q K^T, K from ring slot `it`
@@ -207,9 +253,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int pb = t & 1;
         const uint32_t ppar = (t >> 1) & 1u;
         const int st = it % NST;
-        const uint32_t par = (it / NST) & 1u;
         if (!mbar_wait(&p_full[pb], ppar, abort_flag, ctx)) return false;
-        if (!mbar_wait(&ring_full[st], par, abort_flag, ctx)) return false;
+        // the V tile landed (ring_full) and was converted to fp16 in place (v_conv)
+        if (!mbar_wait(&v_conv[st], (vconv_par >> st) & 1u, abort_flag, ctx)) return false;
+        vconv_par ^= 1u << st;
         tc_fence_after();
         const bool is_live = (live[pb * 4 + 0] | live[pb * 4 + 1] | live[pb * 4 + 2] | live[pb * 4 + 3]) != 0;
         ++visited;
@@ -362,7 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float2 q4 = __fmul2_rn(q2, q2);
           const float2 ph = __fmul2_rn(q4, q4);
           tsum2 = __fadd2_rn(tsum2, ph);
-          packed[e] = pack_bf16x2(ph.x, ph.y);
+          packed[e] = pack_f16x2_sat(ph.x, ph.y);
         }
         const int half = c8 >> 3, chunk = c8 & 7;
         *reinterpret_cast<uint4*>(prow + half * BOX_BYTES + ((chunk ^ (row_local & 7)) << 4)) =
