@@ -63,8 +63,8 @@ struct FwdCfg {
   static constexpr int OFF_P = OFF_RING + NSTAGE * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
   // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain,
-  // v_conv[NSTAGE]
-  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2 + NSTAGE;
+  // v_landed, v_conv
+  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int MISC_BYTES = 64;   // tmem base, abort flag, live votes [2][4]
   static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;   // + slack for 1024-byte alignment
@@ -93,7 +93,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* p_empty = p_full + 2;
   uint64_t* o_full = p_empty + 2;
   uint64_t* drain = o_full + 1;
-  uint64_t* v_conv = drain + 1;   // [NST]: the V tile in this ring slot has been converted to fp16
+  // V-tile hand-off, one phase per V tile t: the MMA thread, which consumes the ring in
+  // order, arrives on v_landed once V_t's fill has landed; the converter warps arrive on
+  // v_conv once V_t is fp16.  Each has in-order waiters that never skip a phase.
+  uint64_t* v_landed = drain + 1;
+  uint64_t* v_conv = drain + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);   // [2][4]
@@ -115,8 +119,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < NST; ++i) {
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
-      mbar_init(&v_conv[i], 2);    // one arrival per converter warp
     }
+    mbar_init(v_landed, 1);
+    mbar_init(v_conv, 2);          // one arrival per converter warp
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 4);   // one arrival per softmax warp
@@ -192,12 +197,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int t = 0; t < nkt; ++t) {
       const int itv = nkt + ((t < nkt - 1) ? 2 * (t + 1) : 2 * nkt - 1);
       const int st = itv % NST;
-      const uint32_t par = (itv / NST) & 1u;
-      int okv = 1;
-      if (lane == 0) okv = mbar_wait(&ring_full[st], par, abort_flag, ctx) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, okv, 0)) break;
-      while (!mbar_try_wait(&ring_full[st], par)) {
-      }   // completed already: gives every lane the acquire of the TMA data
+      // v_landed phase t: the MMA thread saw V_t land.  The slot cannot be refilled before
+      // this conversion is done, so ring_full[st] is now exactly at V_t's completed phase;
+      // every lane checks it too (bounded), which gives each lane the acquire of the data.
+      bool okw = mbar_wait(v_landed, static_cast<uint32_t>(t) & 1u, abort_flag, ctx);
+      if (okw) okw = mbar_wait(&ring_full[st], (itv / NST) & 1u, abort_flag, ctx);
+      if (!__all_sync(0xffffffffu, okw)) break;
       uint4* tile = reinterpret_cast<uint4*>(sRing + st * C::TILE_BYTES) + half * (CHUNKS / 2);
 #pragma unroll 4
       for (int i = 0; i < PER_LANE; ++i) {
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&v_conv[st]);
+      if (lane == 0) mbar_arrive(v_conv);
     }
     if (__any_sync(0xffffffffu, out_of_range) && lane == 0) atomicOr(ctx.status, kStatusRange);
   } else if (warp == MMA_WARP) {
@@ -224,7 +229,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc_pv = idesc_fp16_f32(BM, D, 0, 1);   // P and V in fp16
       const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sRing), sPa = smem_u32(sP);
       uint32_t it = 0, sidx = 0;
-      uint32_t vconv_par = 0;   // bit st: parity of the next v_conv[st] phase to wait for
       unsigned long long visited = 0, skipped = 0;
       bool o_started = false;
       auto mma_s = [&]() -> bool {   // S[sidx & 1] = Q K^T, K from ring slot `it`
@@ -253,10 +257,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int pb = t & 1;
         const uint32_t ppar = (t >> 1) & 1u;
         const int st = it % NST;
+        // V_t is the next fill in ring order: once it has landed, hand it to the converters
+        if (!mbar_wait(&ring_full[st], (it / NST) & 1u, abort_flag, ctx)) return false;
+        mbar_arrive(v_landed);
         if (!mbar_wait(&p_full[pb], ppar, abort_flag, ctx)) return false;
-        // the V tile landed (ring_full) and was converted to fp16 in place (v_conv)
-        if (!mbar_wait(&v_conv[st], (vconv_par >> st) & 1u, abort_flag, ctx)) return false;
-        vconv_par ^= 1u << st;
+        if (!mbar_wait(v_conv, static_cast<uint32_t>(t) & 1u, abort_flag, ctx)) return false;
         tc_fence_after();
         const bool is_live = (live[pb * 4 + 0] | live[pb * 4 + 1] | live[pb * 4 + 2] | live[pb * 4 + 3]) != 0;
         ++visited;
