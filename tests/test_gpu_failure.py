@@ -1,0 +1,66 @@
+"""Device-side failure handling without a GPU fault.
+
+The wait limit is shrunk to 1 ns, so every wait that is not already satisfied gives
+up at once: the kernel raises its abort flag, drains its in-flight copies and
+tensor-core work, frees its tensor memory and returns.  The status word must then
+read RA_ERR_TIMEOUT, and the context must stay usable: the next normal call is
+checked against the oracle.  One small CTA per kernel keeps the drain bounded.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+import rational_softmax_attention_gb300 as ra
+from rational_softmax_attention_gb300.inputs import attention_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _normal_forward_matches(q, k, v):
+    o, *_ = ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.125, causal=False,
+                                    out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert ra.device_status() == "RA_OK"
+    O, *_ = oracle.ra_attention_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), scale=0.125)
+    parity.assert_close_bf16(parity.f64(o), O, "O after a timed-out call")
+
+
+def test_forward_wait_timeout_is_reported_and_the_context_survives():
+    q, k, v = attention_inputs(1, 1, 128, 384, 64, seed=11, dtype=torch.bfloat16, with_dout=False)
+    assert ra.device_status() == "RA_OK"
+    ra.set_wait_limit_ns(1)
+    try:
+        ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.125, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        status = ra.device_status()
+    finally:
+        ra.set_wait_limit_ns(0)
+    assert status == "RA_ERR_TIMEOUT"
+    _normal_forward_matches(q, k, v)
+
+
+def test_backward_wait_timeout_is_reported_and_the_context_survives():
+    q, k, v, do = attention_inputs(1, 1, 128, 256, 64, seed=12, dtype=torch.bfloat16)
+    qg, kg, vg, dog = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, rm, rs, ra_, _ = ra.ra_attention_forward(qg, kg, vg, scale=0.125, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert ra.device_status() == "RA_OK"
+    ra.set_wait_limit_ns(1)
+    try:
+        ra.ra_attention_backward(qg, kg, vg, o, dog, rm, rs, ra_, scale=0.125)
+        torch.cuda.synchronize()
+        status = ra.device_status()
+    finally:
+        ra.set_wait_limit_ns(0)
+    assert status == "RA_ERR_TIMEOUT"
+    dq, dk, dv = ra.ra_attention_backward(qg, kg, vg, o, dog, rm, rs, ra_, scale=0.125)
+    torch.cuda.synchronize()
+    assert ra.device_status() == "RA_OK"
+    gq, gk, gv = oracle.ra_attention_head_bwd(q[0, 0].double().numpy(), k[0, 0].double().numpy(),
+                                              v[0, 0].double().numpy(), do[0, 0].double().numpy(), 0.125, False)
+    parity.assert_close_bf16(parity.f64(dq[0, 0]), gq, "dq after a timed-out call")
+    parity.assert_close_bf16(parity.f64(dk[0, 0]), gk, "dk after a timed-out call")
+    parity.assert_close_bf16(parity.f64(dv[0, 0]), gv, "dv after a timed-out call")
+    del np
