@@ -6,7 +6,6 @@ tensor-core work, frees its tensor memory and returns.  The status word must the
 read RA_ERR_TIMEOUT, and the context must stay usable: the next normal call is
 checked against the oracle.  One small CTA per kernel keeps the drain bounded.
 """
-import numpy as np
 import pytest
 import torch
 
@@ -63,4 +62,3 @@ def test_backward_wait_timeout_is_reported_and_the_context_survives():
     parity.assert_close_bf16(parity.f64(dq[0, 0]), gq, "dq after a timed-out call")
     parity.assert_close_bf16(parity.f64(dk[0, 0]), gk, "dk after a timed-out call")
     parity.assert_close_bf16(parity.f64(dv[0, 0]), gv, "dv after a timed-out call")
-    del np
