@@ -181,6 +181,33 @@ ra_status_t ra_device_status(void* stream);
  */
 void ra_set_wait_limit_ns(uint64_t limit_ns);
 
+/* Size of the device array behind ra_attention_bwd_noalloc (32 MiB). */
+#define RA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * ra_attention_bwd_noalloc -- ra_attention_bwd without a caller-supplied workspace.
+ * The pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory, such as code inside a framework that owns the allocator and
+ * offers no temporary buffers, or a host path where cudaMalloc (which may synchronise
+ * the device) is not allowed.  The workspace comes instead from a fixed array of
+ * RA_NOALLOC_SCRATCH_BYTES inside the library: every GPU that loads the library holds
+ * that memory until the process exits, and nothing is allocated per call.
+ *   Arguments, results and errors are those of ra_attention_bwd without `workspace`.
+ *   Sizes whose ra_attention_bwd_workspace_size() exceeds RA_NOALLOC_SCRATCH_BYTES are
+ *   rejected with RA_ERR_UNSUPPORTED before anything runs (use ra_attention_bwd then).
+ *   The first call on a device looks up the array's device address (once per device);
+ *   make that first call before any stream capture.
+ *   All calls share the one array and it keeps the previous call's contents (nothing in
+ *   it needs to start at zero).  Calls that overlap on the GPU -- on different streams,
+ *   or from different host threads without ordering -- race on it: serialise them.
+ */
+ra_status_t ra_attention_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                     const void* dout, const float* row_m, const float* row_s,
+                                     const int32_t* row_arg, void* dq, void* dk, void* dv,
+                                     int B, int H, int N_Q, int N_K, int D, float scale, int causal,
+                                     ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype,
+                                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif
