@@ -137,6 +137,7 @@ class HotPath:
         self.dv = torch.empty_like(self.dq)
         self.y = torch.empty_like(x)
         self.ws = torch.empty(self.L.ra_attention_bwd_workspace_size(B, H, N, N, D), dtype=torch.uint8, device=dev)
+        self.fws = torch.empty(self.L.ra_attention_fwd_workspace_size(B, H, N, N, D), dtype=torch.uint8, device=dev)
         self.outs = [self.o, self.dq, self.dk, self.dv, self.y]
         self.host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in self.outs]
         self.shape = (B, H, N, D)
@@ -154,7 +155,7 @@ class HotPath:
         B, H, N, D = self.shape
         self._check("ra_attention_fwd", self.L.ra_attention_fwd(
             _ptr(q), _ptr(k), _ptr(v), _ptr(self.o), _ptr(self.rm), _ptr(self.rs), _ptr(self.ra_), _ptr(counts),
-            B, H, N, N, D, float(self.w.scale), int(self.w.causal), 1, 0, st))
+            _ptr(self.fws), B, H, N, N, D, float(self.w.scale), int(self.w.causal), 1, 0, st))
 
     def bwd(self, st):
         q, k, v, do, _ = self.dev_in
@@ -334,7 +335,7 @@ def run_ours(args):
 
     def fwd_causal():
         code = hp.L.ra_attention_fwd(_ptr(qc), _ptr(kc), _ptr(vc), _ptr(oc), _ptr(rmc), _ptr(rsc), _ptr(rac), None,
-                                     wc.B, wc.H, wc.N, wc.N, wc.D, float(wc.scale), 1, 1, 0, st)
+                                     _ptr(hp.fws), wc.B, wc.H, wc.N, wc.N, wc.D, float(wc.scale), 1, 1, 0, st)
         if code != 0:
             raise RuntimeError("ra_attention_fwd (causal) failed")
     for _ in range(3):

@@ -103,22 +103,35 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
  *                [1] = pairs whose V tile and P*V product were skipped because every
  *                      entry of the pair lies outside the compact support.
  *                Tiles are 128 x 128 on the tensor-core path.
+ *   workspace    device memory of ra_attention_fwd_workspace_size() bytes, 16-byte
+ *                aligned, contents on entry irrelevant; required for RA_BF16 inputs
+ *                (NULL allowed for RA_F32).  The call writes an fp16 copy of v there
+ *                and forms P V in fp16: exact for bf16 values up to 65504, and P is
+ *                rounded to 2^-11 instead of 2^-8.  Larger |v| (or NaN) saturates and
+ *                is reported as RA_ERR_UNSUPPORTED by ra_device_status().
  *   scale        score scale; <= 0 means 1/sqrt(D).
  *   causal       0: every key visible; nonzero: key j visible to query i iff j <= i
  *                (top-left alignment, as scaled_dot_product_attention's is_causal).
  *   in_dtype     RA_BF16: tensor-core path, D in {64, 128}.
  *                RA_F32: CUDA-core fp32 path (no TF32), D in {16, 32, 64, 128}.
  *   out_dtype    RA_F32 or RA_BF16 for o.
- * Errors: RA_ERR_ARG for null q/k/v/o, B, H, N_Q, N_K, D < 1, element counts
- * overflowing int32 indexing per head, a pointer not 16-byte aligned or a bad
- * enum; RA_ERR_UNSUPPORTED for D outside the sets above; RA_ERR_LAUNCH on
- * launch or tensor-map set-up failure.
+ * Errors: RA_ERR_ARG for null q/k/v/o (or a null workspace with RA_BF16), B, H, N_Q,
+ * N_K, D < 1, element counts overflowing int32 indexing per head, a pointer not
+ * 16-byte aligned or a bad enum; RA_ERR_UNSUPPORTED for D outside the sets above;
+ * RA_ERR_LAUNCH on launch or tensor-map set-up failure.
  */
 ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* o,
                              float* row_m, float* row_s, int32_t* row_arg,
-                             int64_t* tile_counts,
+                             int64_t* tile_counts, void* workspace,
                              int B, int H, int N_Q, int N_K, int D, float scale, int causal,
                              ra_dtype_t in_dtype, ra_dtype_t out_dtype, void* stream);
+
+/*
+ * ra_attention_fwd_workspace_size -- bytes of device workspace ra_attention_fwd needs
+ * for these sizes: the fp16 copy of v (B*H*N_K*D*2 bytes, padded to 256).  Returns 0
+ * for invalid sizes.
+ */
+size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 
 /*
  * ra_attention_bwd_workspace_size -- bytes of device workspace ra_attention_bwd needs

@@ -47,8 +47,9 @@ _SIGNATURES = {
     "ra_status_string": ([_i32], ctypes.c_char_p),
     "ra_softmax_fwd": ([_vp, _vp, _i64, _i64, _i32, _vp], _i32),
     "ra_softmax_bwd": ([_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp], _i32),
-    "ra_attention_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
+    "ra_attention_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
                           _i32, _i32, _vp], _i32),
+    "ra_attention_fwd_workspace_size": ([_i32, _i32, _i32, _i32, _i32], ctypes.c_size_t),
     "ra_attention_bwd_workspace_size": ([_i32, _i32, _i32, _i32, _i32], ctypes.c_size_t),
     "ra_attention_bwd": ([_vp] * 12 + [_i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp], _i32),
     "ra_device_status": ([_vp], _i32),
@@ -148,8 +149,12 @@ def ra_attention_forward(q, k, v, *, scale=None, causal=False, out_dtype=None, w
                  torch.empty((B, H, NQ), dtype=torch.int32, device=q.device))
     counts = torch.empty(2, dtype=torch.int64, device=q.device) if tile_counts else None
     rm, rs, ra = stats if stats else (None, None, None)
-    _check("ra_attention_fwd", lib().ra_attention_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(rm), _ptr(rs), _ptr(ra), _ptr(counts),
+    L = lib()
+    ws = None
+    if q.dtype == torch.bfloat16:
+        ws = torch.empty(L.ra_attention_fwd_workspace_size(B, H, NQ, NK, D), dtype=torch.uint8, device=q.device)
+    _check("ra_attention_fwd", L.ra_attention_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(rm), _ptr(rs), _ptr(ra), _ptr(counts), _ptr(ws),
         B, H, NQ, NK, D, float(scale or 0.0), 1 if causal else 0, _dtype_code(q.dtype), _dtype_code(out_dtype),
         _stream(q.device)))
     return o, rm, rs, ra, counts

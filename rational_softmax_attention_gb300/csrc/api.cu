@@ -163,15 +163,22 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
 
+size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D) {
+  if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return 0;
+  return (static_cast<size_t>(B) * H * N_K * D * 2 + 255) & ~static_cast<size_t>(255);   // fp16 copy of V
+}
+
 ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* o, float* row_m, float* row_s,
-                             int32_t* row_arg, int64_t* tile_counts, int B, int H, int N_Q, int N_K, int D,
-                             float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t out_dtype, void* stream) {
+                             int32_t* row_arg, int64_t* tile_counts, void* workspace, int B, int H, int N_Q,
+                             int N_K, int D, float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t out_dtype,
+                             void* stream) {
   if (!q || !k || !v || !o || !dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return RA_ERR_ARG;
   if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return RA_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RA_ERR_ARG;
   if ((row_m && !aligned16(row_m)) || (row_s && !aligned16(row_s)) || (row_arg && !aligned16(row_arg)) ||
-      (tile_counts && !aligned16(tile_counts)))
+      (tile_counts && !aligned16(tile_counts)) || (workspace && !aligned16(workspace)))
     return RA_ERR_ARG;
+  if (in_dtype == RA_BF16 && !workspace) return RA_ERR_ARG;   // the tensor-core path needs the fp16 V copy
   if (!(scale > 0.0f)) scale = 1.0f / std::sqrt(static_cast<float>(D));
   if (!std::isfinite(scale)) return RA_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -192,8 +199,13 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
   FwdTcArgs a;
   const int BH = B * H;
   if (!make_map_bf16(&a.tm_q, q, BH, N_Q, D) || !make_map_bf16(&a.tm_k, k, BH, N_K, D) ||
-      !make_map_bf16(&a.tm_v, v, BH, N_K, D))
+      !make_map_16bit(&a.tm_v, workspace, BH, N_K, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return RA_ERR_LAUNCH;
+  ConvertJob job;
+  job.src[0] = static_cast<const uint4*>(v);
+  job.dst[0] = static_cast<uint4*>(workspace);
+  job.n8[0] = static_cast<size_t>(BH) * N_K * D / 8;
+  job.count = 1;
   a.o = o;
   a.row_m = row_m;
   a.row_s = row_s;
@@ -201,6 +213,7 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
   a.tile_counts = reinterpret_cast<unsigned long long*>(tile_counts);
   a.out_bf16 = out_dtype == RA_BF16 ? 1 : 0;
   if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
+  if (launch_bf16_to_f16(job, ctx.status, st) != cudaSuccess) return RA_ERR_LAUNCH;
   const cudaError_t e = launch_attn_fwd_tc(s, a, ctx, st);
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }

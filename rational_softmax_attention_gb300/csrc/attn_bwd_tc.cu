@@ -794,36 +794,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// bf16 -> fp16 copies of Q, K, V and dO (blockIdx.y selects the tensor), 8 values per
-// 16-byte access; any |x| > 65504 (or NaN) sets kStatusRange.
-struct ConvertJob {
-  const uint4* src[4];
-  uint4* dst[4];
-  size_t n8[4];
-};
-
-__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const ConvertJob job, unsigned int* status) {
-  const int t = blockIdx.y;
-  const uint4* __restrict__ src = job.src[t];
-  uint4* __restrict__ dst = job.dst[t];
-  const size_t n8 = job.n8[t];
-  bool bad = false;
-  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const uint4 u = __ldcs(src + i);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-    uint32_t o[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(h[k]);
-      bad |= !(fabsf(f.x) <= 65504.0f) || !(fabsf(f.y) <= 65504.0f);
-      o[k] = pack_f16x2_sat(f.x, f.y);
-    }
-    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusRange);
-}
-
 template <typename KernelFn>
 cudaError_t set_smem(KernelFn fn, int bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -848,10 +818,8 @@ cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx
     job.dst[i] = static_cast<uint4*>(dsts[i]);
     job.n8[i] = ns[i];
   }
-  const size_t nmax = nq8 > nk8 ? nq8 : nk8;
-  const unsigned cblocks = static_cast<unsigned>(std::min<size_t>((nmax + 255) / 256, 152 * 8));
-  bf16_to_f16_kernel<<<dim3(cblocks, 4), 256, 0, st>>>(job, ctx.status);
-  e = cudaGetLastError();
+  job.count = 4;
+  e = launch_bf16_to_f16(job, ctx.status, st);
   if (e != cudaSuccess) return e;
   attn_bwd_dq_tc_kernel<D><<<nqt * BH, THREADS, DqCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
   e = cudaGetLastError();

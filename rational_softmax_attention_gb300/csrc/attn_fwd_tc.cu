@@ -26,9 +26,9 @@
 //               P = fp16(phi) into a 128-byte-swizzled shared-memory tile for the
 //               P V product, sums phi in fp32, and votes whether the tile is live.
 //               Epilogue: O = acc / sum(phi), row statistics for the backward.
-//   warps 6-7   convert each landed V tile from bf16 to fp16 in place, so the P V
-//               product runs in fp16 (P rounded to 2^-11, not 2^-8; bf16 V values
-//               up to 65504 convert exactly).  Q K^T stays in bf16.
+//   V arrives as the fp16 copy the C-ABI layer made once per call (exact for bf16
+//   values up to 65504), so the P V product runs in fp16 and P is rounded to 2^-11
+//   rather than 2^-8.  Q K^T stays in bf16.
 //
 // phi on the FMA pipe: w = (1+u)/2 = 0.5 + (m - s)/32 (scaled units) computed with
 // one saturating FMA, so every u >= 1 (and every masked entry, fed as -inf) gives
@@ -45,8 +45,7 @@ constexpr int BM = 128;   // query rows per CTA: the MMA M and the 128 TMEM lane
 constexpr int BN = 128;   // keys per tile: the N of Q K^T and the K of P V
 constexpr int PRODUCER_WARP = 4;
 constexpr int MMA_WARP = 5;
-constexpr int CONVERT_WARP0 = 6;   // warps 6 and 7: bf16 -> fp16 conversion of V tiles
-constexpr int THREADS = 256;
+constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S0 = 0;
 constexpr uint32_t TMEM_S1 = 128;
@@ -62,9 +61,8 @@ struct FwdCfg {
   static constexpr int OFF_RING = OFF_Q + TILE_BYTES;
   static constexpr int OFF_P = OFF_RING + NSTAGE * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain,
-  // v_landed, v_conv
-  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2 + 2;
+  // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain
+  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int MISC_BYTES = 64;   // tmem base, abort flag, live votes [2][4]
   static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;   // + slack for 1024-byte alignment
@@ -93,11 +91,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* p_empty = p_full + 2;
   uint64_t* o_full = p_empty + 2;
   uint64_t* drain = o_full + 1;
-  // V-tile hand-off, one phase per V tile t: the MMA thread, which consumes the ring in
-  // order, arrives on v_landed once V_t's fill has landed; the converter warps arrive on
-  // v_conv once V_t is fp16.  Each has in-order waiters that never skip a phase.
-  uint64_t* v_landed = drain + 1;
-  uint64_t* v_conv = drain + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);   // [2][4]
@@ -120,8 +113,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
-    mbar_init(v_landed, 1);
-    mbar_init(v_conv, 2);          // one arrival per converter warp
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 4);   // one arrival per softmax warp
@@ -184,44 +175,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < NST; ++i)
         if (issued[i]) drain_wait(&ring_full[i], last_par[i], ctx);
     }
-  } else if (warp >= CONVERT_WARP0) {
-    // ------------------------------------------------------------------ V converters (warps 6, 7)
-    // Each V tile is rewritten in place from bf16 to fp16 (same swizzled positions), so
-    // that the P V product takes fp16 P: P is then rounded to 2^-11 instead of 2^-8.
-    // The ring slot of V_t follows the producer's order: pass-2 position 2(t+1), and
-    // 2*nkt - 1 for the last tile.
-    const int half = warp - CONVERT_WARP0;
-    constexpr int CHUNKS = C::TILE_BYTES / 16;
-    constexpr int PER_LANE = CHUNKS / 2 / 32;
-    bool out_of_range = false;
-    for (int t = 0; t < nkt; ++t) {
-      const int itv = nkt + ((t < nkt - 1) ? 2 * (t + 1) : 2 * nkt - 1);
-      const int st = itv % NST;
-      // v_landed phase t: the MMA thread saw V_t land.  The slot cannot be refilled before
-      // this conversion is done, so ring_full[st] is now exactly at V_t's completed phase;
-      // every lane checks it too (bounded), which gives each lane the acquire of the data.
-      bool okw = mbar_wait(v_landed, static_cast<uint32_t>(t) & 1u, abort_flag, ctx);
-      if (okw) okw = mbar_wait(&ring_full[st], (itv / NST) & 1u, abort_flag, ctx);
-      if (!__all_sync(0xffffffffu, okw)) break;
-      uint4* tile = reinterpret_cast<uint4*>(sRing + st * C::TILE_BYTES) + half * (CHUNKS / 2);
-#pragma unroll 4
-      for (int i = 0; i < PER_LANE; ++i) {
-        const uint4 u = tile[i * 32 + lane];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-          out_of_range |= !(fabsf(f.x) <= 65504.0f) || !(fabsf(f.y) <= 65504.0f);
-          o[e] = pack_f16x2_sat(f.x, f.y);
-        }
-        tile[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(v_conv);
-    }
-    if (__any_sync(0xffffffffu, out_of_range) && lane == 0) atomicOr(ctx.status, kStatusRange);
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -257,11 +210,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int pb = t & 1;
         const uint32_t ppar = (t >> 1) & 1u;
         const int st = it % NST;
-        // V_t is the next fill in ring order: once it has landed, hand it to the converters
-        if (!mbar_wait(&ring_full[st], (it / NST) & 1u, abort_flag, ctx)) return false;
-        mbar_arrive(v_landed);
         if (!mbar_wait(&p_full[pb], ppar, abort_flag, ctx)) return false;
-        if (!mbar_wait(v_conv, static_cast<uint32_t>(t) & 1u, abort_flag, ctx)) return false;
+        if (!mbar_wait(&ring_full[st], (it / NST) & 1u, abort_flag, ctx)) return false;
         tc_fence_after();
         const bool is_live = (live[pb * 4 + 0] | live[pb * 4 + 1] | live[pb * 4 + 2] | live[pb * 4 + 3]) != 0;
         ++visited;

@@ -26,9 +26,19 @@ cudaError_t launch_attn_bwd_simt(const AttnShape& s, const float* q, const float
                                  const float* row_s, const int32_t* row_arg, void* dq, void* dk, void* dv,
                                  bool grad_bf16, float* ws_d, float* ws_r, cudaStream_t st);
 
+// bf16 -> fp16 copies of up to four tensors in one launch (convert.cu).  n8 = elements / 8.
+struct ConvertJob {
+  const uint4* src[4];
+  uint4* dst[4];
+  size_t n8[4];
+  int count;
+};
+cudaError_t launch_bf16_to_f16(const ConvertJob& job, unsigned int* status, cudaStream_t st);
+
 // bf16 tensor-core attention forward (attn_fwd_tc.cu).  Tensor maps are built by the caller.
 struct FwdTcArgs {
-  CUtensorMap tm_q, tm_k, tm_v;   // 3-D maps {D, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_q, tm_k;   // bf16 Q and K: 3-D maps {D, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_v;         // fp16 copy of V (same geometry)
   void* o;
   float* row_m;
   float* row_s;

@@ -60,8 +60,8 @@ def test_softmax_validation(lib):
     assert lib.ra_softmax_bwd(FAKE, NULL, FAKE, FAKE, 4, 4, 0, S) == 1
 
 
-def _fwd(lib, q=FAKE, o=FAKE, B=1, H=1, NQ=8, NK=8, D=64, in_dt=1, out_dt=0, scale=0.0):
-    return lib.ra_attention_fwd(q, FAKE, FAKE, o, NULL, NULL, NULL, NULL, B, H, NQ, NK, D, scale, 0,
+def _fwd(lib, q=FAKE, o=FAKE, ws=FAKE, B=1, H=1, NQ=8, NK=8, D=64, in_dt=1, out_dt=0, scale=0.0):
+    return lib.ra_attention_fwd(q, FAKE, FAKE, o, NULL, NULL, NULL, NULL, ws, B, H, NQ, NK, D, scale, 0,
                                 in_dt, out_dt, S)
 
 
@@ -77,6 +77,11 @@ def test_attention_fwd_validation(lib):
     assert _fwd(lib, D=48) == 2                                       # bf16 tensor-core path: D in {64, 128}
     assert _fwd(lib, D=256) == 2
     assert _fwd(lib, D=48, in_dt=0) == 2                              # fp32 path: D in {16, 32, 64, 128}
+    assert _fwd(lib, ws=NULL) == 1                                    # bf16 needs the fp16 V workspace
+    assert _fwd(lib, ws=MISALIGNED) == 1
+    assert lib.ra_attention_fwd_workspace_size(4, 16, 8192, 8192, 128) == 4 * 16 * 8192 * 128 * 2
+    assert lib.ra_attention_fwd_workspace_size(1, 1, 3, 3, 64) == 512
+    assert lib.ra_attention_fwd_workspace_size(1, 1, 3, 0, 64) == 0
 
 
 def test_attention_bwd_validation(lib):
