@@ -103,12 +103,21 @@ struct DqCfg {
   // dp_full, dp_free, e_full, e_free, dq_full, drain
   static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 4 + 6;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_XCH = OFF_MISC + 16;   // [2][128] floats: per-half partials of D_i, then R_i
+  static constexpr int SMEM_BYTES = OFF_XCH + 2 * BM * 4 + 1024;
 };
 constexpr uint32_t DQ_TM_S0 = 0, DQ_TM_S1 = 128, DQ_TM_DP = 256, DQ_TM_DQ = 384;
+// 8 softmax warps: warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the same query
+// rows) and split each key tile's 128 columns 64 / 64, two warps per scheduler.
+constexpr int DQ_SOFTMAX_WARPS = 8;
+constexpr int DQ_PRODUCER_WARP = 8;
+constexpr int DQ_MMA_WARP = 9;
+constexpr int DQ_THREADS = 320;
+
+__device__ __forceinline__ void softmax8_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 template <int D>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -140,8 +149,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int BH = s.B * s.H;
   const int nqt = (s.NQ + BM - 1) / BM;
   const int item = blockIdx.x;
-  const int qt = s.causal ? (nqt - 1 - item / BH) : (item / BH);
-  const int bh = item % BH;
+  // head-major order (K/V of a head shared in L2), longest causal query tiles first
+  const int bh = item / nqt;
+  const int qt = s.causal ? (nqt - 1 - item % nqt) : (item % nqt);
   const int q0 = qt * BM;
   const int last_key = s.causal ? min(s.NK - 1, min(s.NQ - 1, q0 + BM - 1)) : s.NK - 1;
   const int nkt = last_key / BN + 1;
@@ -158,18 +168,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
+      mbar_init(&s_free[i], DQ_SOFTMAX_WARPS);
     }
     mbar_init(dp_full, 1);
-    mbar_init(dp_free, 4);
-    mbar_init(e_full, 4);
+    mbar_init(dp_free, DQ_SOFTMAX_WARPS);
+    mbar_init(e_full, DQ_SOFTMAX_WARPS);
     mbar_init(e_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == MMA_WARP) {
+  if (warp == DQ_MMA_WARP) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
@@ -178,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == PRODUCER_WARP) {
+  if (warp == DQ_PRODUCER_WARP) {
     if (lane == 0) {
       tma_prefetch_desc(&args.tm_q);
       tma_prefetch_desc(&args.tm_k);
@@ -217,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = max(0, v_issued - C::NVS); j < v_issued; ++j)
         drain_wait(&v_full[j % C::NVS], (j / C::NVS) & 1u, ctx);
     }
-  } else if (warp == MMA_WARP) {
+  } else if (warp == DQ_MMA_WARP) {
     if (lane == 0) {
       constexpr uint32_t idesc_ss = idesc_fp16_f32(BM, BN, 0, 0);
       constexpr uint32_t idesc_kmn = idesc_fp16_f32(BM, D, 0, 1);
@@ -272,12 +282,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       drain_wait(drain, 0, ctx);
     }
   } else {
-    // ------------------------------------------------------------------ softmax warpgroup (row = query)
-    const int r = threadIdx.x;
+    // ------------------------------------------------------------------ softmax warps (row = query)
+    // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key columns
+    // [64 (w / 4), 64 (w / 4) + 64) of every tile; D_i and R_i are combined across
+    // the two halves through shared memory.
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int cbase = half * 64;
+    const int r = quarter * 32 + lane;
     const int i = q0 + r;
     const bool i_ok = i < s.NQ;
     const size_t ro = static_cast<size_t>(bh) * s.NQ + (i_ok ? i : s.NQ - 1);
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);   // [2][BM]
     auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
       int okv = 1;
       if (lane == 0) okv = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
@@ -286,12 +303,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float m_sc = args.row_m[ro];
     const float inv_s = 1.0f / args.row_s[ro];
     const int a = min(max(args.row_arg[ro], 0), s.NK - 1);
-    // D_i = dO_i . O_i
-    float Di = 0.0f;
+    // D_i = dO_i . O_i: each half of the warps sums half of the D dimensions
     {
+      float part = 0.0f;
       const char* dorow = reinterpret_cast<const char*>(args.dout) + ro * D * 2;
 #pragma unroll 4
-      for (int d = 0; d < D; d += 8) {
+      for (int d = half * (D / 2); d < (half + 1) * (D / 2); d += 8) {
         float g[8], o[8];
         load8_bf16(dorow + d * 2, g);
         if (args.o_bf16) {
@@ -303,9 +320,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           o[4] = x1.x; o[5] = x1.y; o[6] = x1.z; o[7] = x1.w;
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) Di = fmaf(g[e], o[e], Di);
+        for (int e = 0; e < 8; ++e) part = fmaf(g[e], o[e], part);
       }
+      xch[half * BM + r] = part;
     }
+    softmax8_sync();
+    const float Di = xch[r] + xch[BM + r];
+    softmax8_sync();   // xch is reused for R_i after the loop
     // rows past N_Q read zero-filled Q rows (s = 0): base 2 saturates every w to 1, weight 0
     const float base = i_ok ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
     const float c2 = s.scale * (1.0f / 32.0f);
@@ -313,7 +334,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int lim = s.causal ? min(i, s.NK - 1) : s.NK - 1;
     float R = 0.0f;
     bool ok = true;
-    uint32_t sv[4][32];
+    uint32_t sv[2][32];
 #define SV(c) sv[(c) >> 5][(c) & 31]
     for (int j = 0; j < nkt && ok; ++j) {
       const int sb = j & 1;
@@ -321,21 +342,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       {
-        const uint32_t col = lane_addr + (sb ? DQ_TM_S1 : DQ_TM_S0);
+        const uint32_t col = lane_addr + (sb ? DQ_TM_S1 : DQ_TM_S0) + cbase;
         tmem_ld32(col, sv[0]);
         tmem_ld32(col + 32, sv[1]);
-        tmem_ld32(col + 64, sv[2]);
-        tmem_ld32(col + 96, sv[3]);
         tc_wait_ld();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
-      const int col0 = j * BN;
-      const bool need_mask = col0 + BN - 1 > lim;
+      const int col0 = j * BN + cbase;   // key index of local column 0
+      const bool need_mask = col0 + 63 > lim;
       // coefficient q^7 (1/w)^2 / (4 s_i) per entry, in place
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
+      for (int c = 0; c < 64; c += 2) {
         float s0 = u2f(SV(c)), s1 = u2f(SV(c + 1));
         if (need_mask) {
           if (col0 + c > lim) s0 = -INFINITY;
@@ -350,20 +369,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         SV(c) = __float_as_uint(coef.x);
         SV(c + 1) = __float_as_uint(coef.y);
       }
-      if (a >= col0 && a < col0 + BN) {   // the argmax entry takes -R_i, not E
+      if (a >= col0 && a < col0 + 64) {   // the argmax entry takes -R_i, not E
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
+        for (int c = 0; c < 64; ++c)
           if (col0 + c == a) SV(c) = 0u;
       }
       ok = warp_wait(e_free, (j & 1u) ^ 1u) && warp_wait(dp_full, j & 1u);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < BN / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dv[32];
-        tmem_ld32(lane_addr + DQ_TM_DP + cc * 32, dv);
+        tmem_ld32(lane_addr + DQ_TM_DP + cbase + cc * 32, dv);
         tc_wait_ld();
-        if (cc == BN / 32 - 1) {
+        if (cc == 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(dp_free);
@@ -379,7 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             R += e0 + e1;
             pk[t] = pack_f16x2_sat(e0, e1);
           }
-          st_tile16(sE, r, cc * 4 + e, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          st_tile16(sE, r, (cbase + cc * 32 + e * 8) >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
       }
       fence_proxy_async_smem();
@@ -387,18 +406,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(e_full);
     }
 #undef SV
+    // R_i over both halves (reached by all eight warps, also after a wait gave up)
+    xch[half * BM + r] = R;
+    softmax8_sync();
+    R = xch[r] + xch[BM + r];
     if (ok) ok = warp_wait(dq_full, 0);
     if (ok) {
       tc_fence_after();
-      if (i_ok) {
+      if (i_ok && half == 0) {
         args.ws_d[ro] = Di;
         args.ws_r[ro] = R;
         args.ws_base[ro] = base;
         args.ws_invs[ro] = inv_s;
       }
       const char* krow = reinterpret_cast<const char*>(args.k_raw) + (static_cast<size_t>(bh) * s.NK + a) * D * 2;
+      // each half of the warps stores half of the D columns of its rows
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
         uint32_t acc[32];
         tmem_ld32(lane_addr + DQ_TM_DQ + c0, acc);
         tc_wait_ld();
@@ -419,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == DQ_MMA_WARP) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -453,11 +477,17 @@ struct DkvCfg {
   static constexpr int SMEM_BYTES = USED + SLACK;
 };
 constexpr uint32_t KV_TM_ST = 0, KV_TM_DPT = 128, KV_TM_DV = 256, KV_TM_DK = 384;
+// 8 softmax warps: warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the same key rows)
+// and split each tile's 128 query columns 64 / 64, two warps per scheduler.
+constexpr int KV_SOFTMAX_WARPS = 8;
+constexpr int KV_PRODUCER_WARP = 8;
+constexpr int KV_MMA_WARP = 9;
+constexpr int KV_THREADS = 320;
 
-__device__ __forceinline__ void softmax_group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void softmax_group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 template <int D>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(KV_THREADS, 1)
     attn_bwd_dkdv_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
   using C = DkvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -500,8 +530,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int BH = s.B * s.H;
   const int nqt = (s.NQ + BM - 1) / BM;
   const int item = blockIdx.x;
-  const int kt = item / BH;   // ascending: under the causal mask the first key tiles see the most queries
-  const int bh = item % BH;
+  // head-major order (Q/dO of a head shared in L2); within a head ascending key tiles,
+  // which under the causal mask see the most queries
+  const int nkt_all = (s.NK + BN - 1) / BN;
+  const int bh = item / nkt_all;
+  const int kt = item % nkt_all;
   const int k0 = kt * BN;
   const int qt0 = s.causal ? k0 / BM : 0;   // first query tile that can see key k0 (j <= i)
   const int nq = max(0, nqt - qt0);
@@ -517,17 +550,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&do_empty[i], 1);
     }
     mbar_init(st_full, 1);
-    mbar_init(st_free, 4);
+    mbar_init(st_free, KV_SOFTMAX_WARPS);
     mbar_init(dpt_full, 1);
-    mbar_init(dpt_free, 4);
-    mbar_init(p_full, 4);
+    mbar_init(dpt_free, KV_SOFTMAX_WARPS);
+    mbar_init(p_full, KV_SOFTMAX_WARPS);
     mbar_init(p_free, 1);
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == MMA_WARP) {
+  if (warp == KV_MMA_WARP) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
@@ -536,7 +569,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == PRODUCER_WARP) {
+  if (warp == KV_PRODUCER_WARP) {
     if (lane == 0) {
       tma_prefetch_desc(&args.tm_q);
       tma_prefetch_desc(&args.tm_k);
@@ -575,7 +608,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int it = max(0, d_issued - C::NDS); it < d_issued; ++it)
         drain_wait(&do_full[it % C::NDS], (it / C::NDS) & 1u, ctx);
     }
-  } else if (warp == MMA_WARP) {
+  } else if (warp == KV_MMA_WARP) {
     if (lane == 0) {
       constexpr uint32_t idesc_ss = idesc_fp16_f32(BN, BM, 0, 0);
       constexpr uint32_t idesc_kmn = idesc_fp16_f32(BN, D, 0, 1);
@@ -631,17 +664,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       drain_wait(drain, 0, ctx);
     }
   } else {
-    // ------------------------------------------------------------------ softmax warpgroup (row = key)
-    const int r = threadIdx.x;
+    // ------------------------------------------------------------------ softmax warps (row = key)
+    // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (key rows) and query columns
+    // [64 (w / 4), 64 (w / 4) + 64) of every tile.
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int cbase = half * 64;
+    const int r = quarter * 32 + lane;
     const int j = k0 + r;
     const bool j_ok = j < s.NK;
     const size_t ko = static_cast<size_t>(bh) * s.NK + (j_ok ? j : s.NK - 1);
     const size_t so = static_cast<size_t>(bh) * s.NQ;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = s.scale * (1.0f / 32.0f);
     bool ok = true;
     // A wait that gives up sets ok = false; the loop still runs to the end without
-    // waiting (its named barriers must be reached by all four warps) and the
+    // waiting (its named barriers must be reached by all eight warps) and the
     // epilogue is skipped.
     auto warp_wait = [&](uint64_t* bar, uint32_t par) {
       if (!ok) return;
@@ -649,54 +687,51 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) okv = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, okv, 0) != 0;
     };
-    uint32_t sv[4][32];
+    uint32_t sv[2][32];
 #define SV(c) sv[(c) >> 5][(c) & 31]
     for (int it = 0; it < nq; ++it) {
       const int i0 = (qt0 + it) * BM;
       const uint32_t par = it & 1u;
       // per-query constants of this tile (queries past N_Q get base 2: zero weight)
       softmax_group_sync();
-      {
-        const int ii = i0 + r;
+      if (threadIdx.x < BM) {
+        const int ii = i0 + threadIdx.x;
         const bool q_ok = ii < s.NQ;
         const size_t qo = so + (q_ok ? ii : 0);
-        st_base[r] = q_ok ? args.ws_base[qo] : 2.0f;
-        st_invs[r] = q_ok ? args.ws_invs[qo] : 0.0f;
-        st_d[r] = q_ok ? args.ws_d[qo] : 0.0f;
-        st_r[r] = q_ok ? args.ws_r[qo] : 0.0f;
-        st_a[r] = q_ok ? args.row_arg[qo] : -1;
+        st_base[threadIdx.x] = q_ok ? args.ws_base[qo] : 2.0f;
+        st_invs[threadIdx.x] = q_ok ? args.ws_invs[qo] : 0.0f;
+        st_d[threadIdx.x] = q_ok ? args.ws_d[qo] : 0.0f;
+        st_r[threadIdx.x] = q_ok ? args.ws_r[qo] : 0.0f;
+        st_a[threadIdx.x] = q_ok ? args.row_arg[qo] : -1;
       }
       softmax_group_sync();
       warp_wait(st_full, par);
       tc_fence_after();
-      {
-        tmem_ld32(lane_addr + KV_TM_ST, sv[0]);
-        tmem_ld32(lane_addr + KV_TM_ST + 32, sv[1]);
-        tmem_ld32(lane_addr + KV_TM_ST + 64, sv[2]);
-        tmem_ld32(lane_addr + KV_TM_ST + 96, sv[3]);
-        tc_wait_ld();
-      }
+      tmem_ld32(lane_addr + KV_TM_ST + cbase, sv[0]);
+      tmem_ld32(lane_addr + KV_TM_ST + cbase + 32, sv[1]);
+      tc_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(st_free);
       // masked: key past N_K, or (causal) query i0 + c < j
-      const bool need_mask = !j_ok || (s.causal && i0 < j);
+      const bool need_mask = !j_ok || (s.causal && i0 + cbase < j);
       const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
       warp_wait(p_free, par ^ 1u);
       // P^T and the dS coefficient q^7 (1/w)^2 / (4 s_i), in place
 #pragma unroll
-      for (int c = 0; c < BM; c += 8) {
+      for (int c = 0; c < 64; c += 8) {
         uint32_t pk[4];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int cb = c + 4 * h;
-          const float4 b4 = *reinterpret_cast<const float4*>(st_base + cb);
-          const float4 i4 = *reinterpret_cast<const float4*>(st_invs + cb);
+          const int cb = c + 4 * h;        // local column
+          const int cg = cbase + cb;       // column in the tile
+          const float4 b4 = *reinterpret_cast<const float4*>(st_base + cg);
+          const float4 i4 = *reinterpret_cast<const float4*>(st_invs + cg);
           float x[4] = {u2f(SV(cb)), u2f(SV(cb + 1)), u2f(SV(cb + 2)), u2f(SV(cb + 3))};
           if (need_mask) {
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-              if (cb + t < first_vis) x[t] = -INFINITY;
+              if (cg + t < first_vis) x[t] = -INFINITY;
           }
           const float2 ra = rcp_pair(fma_sat(x[0], -c2, b4.x), fma_sat(x[1], -c2, b4.y));
           const float2 rb = rcp_pair(fma_sat(x[2], -c2, b4.z), fma_sat(x[3], -c2, b4.w));
@@ -718,17 +753,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           pk[2 * h] = pack_f16x2_sat(pa.x, pa.y);
           pk[2 * h + 1] = pack_f16x2_sat(pb.x, pb.y);
         }
-        st_tile16(sP, r, c >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        st_tile16(sP, r, (cbase + c) >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
       }
       // dS^T = coef (dP^T - D_i), with -R_i where this key is the query's argmax
       warp_wait(dpt_full, par);
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < BM / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dv[32];
-        tmem_ld32(lane_addr + KV_TM_DPT + cc * 32, dv);
+        tmem_ld32(lane_addr + KV_TM_DPT + cbase + cc * 32, dv);
         tc_wait_ld();
-        if (cc == BM / 32 - 1) {
+        if (cc == 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(dpt_free);
@@ -736,12 +771,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int cb = cc * 32 + e * 8;
+          const int cg = cbase + cb;
           float dsv[8];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float4 d4 = *reinterpret_cast<const float4*>(st_d + cb + 4 * h);
-            const float4 r4 = *reinterpret_cast<const float4*>(st_r + cb + 4 * h);
-            const int4 a4 = *reinterpret_cast<const int4*>(st_a + cb + 4 * h);
+            const float4 d4 = *reinterpret_cast<const float4*>(st_d + cg + 4 * h);
+            const float4 r4 = *reinterpret_cast<const float4*>(st_r + cg + 4 * h);
+            const int4 a4 = *reinterpret_cast<const int4*>(st_a + cg + 4 * h);
             const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
             const float rr4[4] = {r4.x, r4.y, r4.z, r4.w};
             const int aa[4] = {a4.x, a4.y, a4.z, a4.w};
@@ -752,7 +788,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               dsv[4 * h + t] = (aa[t] == j) ? -rr4[t] : v;
             }
           }
-          st_tile16(sDS, r, cb >> 3,
+          st_tile16(sDS, r, cg >> 3,
                     make_uint4(pack_f16x2_sat(dsv[0], dsv[1]), pack_f16x2_sat(dsv[2], dsv[3]),
                                pack_f16x2_sat(dsv[4], dsv[5]), pack_f16x2_sat(dsv[6], dsv[7])));
         }
@@ -765,8 +801,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (nq > 0) warp_wait(acc_full, 0);
     if (ok) {
       tc_fence_after();
+      // each half of the warps stores half of the D columns of its key rows
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
         uint32_t av[32], kv[32];
         tmem_ld32(lane_addr + KV_TM_DV + c0, av);
         tmem_ld32(lane_addr + KV_TM_DK + c0, kv);
@@ -787,7 +824,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == KV_MMA_WARP) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -821,10 +858,10 @@ cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx
   job.count = 4;
   e = launch_bf16_to_f16(job, ctx.status, st);
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_tc_kernel<D><<<nqt * BH, THREADS, DqCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
+  attn_bwd_dq_tc_kernel<D><<<nqt * BH, DQ_THREADS, DqCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_tc_kernel<D><<<nkt * BH, THREADS, DkvCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
+  attn_bwd_dkdv_tc_kernel<D><<<nkt * BH, KV_THREADS, DkvCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
   return cudaGetLastError();
 }
 

@@ -43,9 +43,12 @@ namespace {
 
 constexpr int BM = 128;   // query rows per CTA: the MMA M and the 128 TMEM lanes
 constexpr int BN = 128;   // keys per tile: the N of Q K^T and the K of P V
-constexpr int PRODUCER_WARP = 4;
-constexpr int MMA_WARP = 5;
-constexpr int THREADS = 192;
+// 8 softmax warps: warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the same query
+// rows) and split each tile's 128 key columns 64 / 64, two warps per scheduler.
+constexpr int SOFTMAX_WARPS = 8;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S0 = 0;
 constexpr uint32_t TMEM_S1 = 128;
@@ -64,8 +67,9 @@ struct FwdCfg {
   // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain
   static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int MISC_BYTES = 64;   // tmem base, abort flag, live votes [2][4]
-  static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;   // + slack for 1024-byte alignment
+  static constexpr int MISC_BYTES = 96;   // tmem base, abort flag, live votes [2][8]
+  static constexpr int OFF_XCH = OFF_MISC + MISC_BYTES;   // [2][128] floats + [2][128] ints: half partials
+  static constexpr int SMEM_BYTES = OFF_XCH + 4 * BM * 4 + 1024;   // + slack for 1024-byte alignment
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -93,16 +97,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = o_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);   // [2][4]
+  volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);   // [2][8]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int BH = s.B * s.H;
   const int nqt = (s.NQ + BM - 1) / BM;
   const int item = blockIdx.x;
-  // causal: the longest query tiles (largest index) are scheduled first
-  const int qt = s.causal ? (nqt - 1 - item / BH) : (item / BH);
-  const int bh = item % BH;
+  // Head-major order: the ~150 resident CTAs share a few heads, so each head's K and V
+  // (4 MB at N = 8192, D = 128) stay in L2 across its query tiles.  Causal: within a
+  // head the longest query tiles (largest index) go first.
+  const int bh = item / nqt;
+  const int qt = s.causal ? (nqt - 1 - item % nqt) : (item % nqt);
   const int q0 = qt * BM;
   const int last_key = s.causal ? min(s.NK - 1, min(s.NQ - 1, q0 + BM - 1)) : s.NK - 1;
   const int nkt = last_key / BN + 1;
@@ -115,8 +121,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);   // one arrival per softmax warp
-      mbar_init(&p_full[i], 4);
+      mbar_init(&s_empty[i], SOFTMAX_WARPS);   // one arrival per softmax warp
+      mbar_init(&p_full[i], SOFTMAX_WARPS);
       mbar_init(&p_empty[i], 1);
     }
     mbar_init(o_full, 1);
@@ -213,7 +219,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&p_full[pb], ppar, abort_flag, ctx)) return false;
         if (!mbar_wait(&ring_full[st], (it / NST) & 1u, abort_flag, ctx)) return false;
         tc_fence_after();
-        const bool is_live = (live[pb * 4 + 0] | live[pb * 4 + 1] | live[pb * 4 + 2] | live[pb * 4 + 3]) != 0;
+        int any = 0;
+#pragma unroll
+        for (int w = 0; w < SOFTMAX_WARPS; ++w) any |= live[pb * SOFTMAX_WARPS + w];
+        const bool is_live = any != 0;
         ++visited;
         if (is_live) {
           const uint32_t vaddr = sRa + st * C::TILE_BYTES;
@@ -252,23 +261,30 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------------ softmax warpgroup
-    const int row_local = threadIdx.x;   // 0..127 == TMEM lane
+    // ------------------------------------------------------------------ softmax warps
+    // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key columns
+    // [64 (w / 4), 64 (w / 4) + 64) of every tile; the row maximum, its argmax and the
+    // row sum are combined across the two halves through shared memory.
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int cbase = half * 64;
+    const int row_local = quarter * 32 + lane;   // TMEM lane
     const int row = q0 + row_local;
     const int lim = s.causal ? min(row, s.NK - 1) : s.NK - 1;   // last key this row may see
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float* xf = reinterpret_cast<float*>(smem + C::OFF_XCH);          // [2][BM]
+    int* xi = reinterpret_cast<int*>(smem + C::OFF_XCH + 2 * BM * 4);  // [2][BM]
+    auto group_sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
       int r = 1;
       if (lane == 0) r = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
-    uint32_t sv[4][32];
+    uint32_t sv[2][32];
     auto load_s = [&](int sb) {
-      const uint32_t col = lane_addr + (sb ? TMEM_S1 : TMEM_S0);
+      const uint32_t col = lane_addr + (sb ? TMEM_S1 : TMEM_S0) + cbase;
       tmem_ld32(col + 0, sv[0]);
       tmem_ld32(col + 32, sv[1]);
-      tmem_ld32(col + 64, sv[2]);
-      tmem_ld32(col + 96, sv[3]);
       tc_wait_ld();
     };
 #define SV(c) u2f(sv[(c) >> 5][(c) & 31])
@@ -277,7 +293,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t sidx = 0;
     float m = -INFINITY;
     int a = -1;
-    // pass 1: running maximum of the raw scores q.k (scale > 0 keeps the argmax)
+    // pass 1: running maximum of the raw scores q.k over this half's columns (scale > 0
+    // keeps the argmax)
     for (int j = 0; j < nkt && ok; ++j) {
       const int sb = sidx & 1;
       const uint32_t spar = (sidx >> 1) & 1u;
@@ -289,12 +306,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[sb]);
       ++sidx;
-      const int col0 = j * BN;
-      const bool need_mask = col0 + BN - 1 > lim;
+      const int col0 = j * BN + cbase;   // key index of local column 0
+      const bool need_mask = col0 + 63 > lim;
       float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
       if (!need_mask) {
 #pragma unroll
-        for (int c = 0; c < BN; c += 8) {
+        for (int c = 0; c < 64; c += 8) {
           t0 = max3f(t0, SV(c), SV(c + 1));
           t1 = max3f(t1, SV(c + 2), SV(c + 3));
           t2 = max3f(t2, SV(c + 4), SV(c + 5));
@@ -302,7 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
+        for (int c = 0; c < 64; ++c) {
           const float x = (col0 + c <= lim) ? SV(c) : -INFINITY;
           if ((c & 3) == 0) t0 = fmaxf(t0, x);
           if ((c & 3) == 1) t1 = fmaxf(t1, x);
@@ -312,14 +329,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const float tmax = fmaxf(fmaxf(t0, t1), fmaxf(t2, t3));
       if (tmax > m) {   // strictly greater: an earlier tile keeps ties (lowest index)
-        int idx = BN;
+        int idx = 64;
 #pragma unroll
-        for (int c = BN - 1; c >= 0; --c)
+        for (int c = 63; c >= 0; --c)
           if (SV(c) == tmax && col0 + c <= lim) idx = c;
         m = tmax;
         a = col0 + idx;
       }
     }
+    // combine the two halves (reached by all eight warps, also after a wait gave up)
+    xf[half * BM + row_local] = m;
+    xi[half * BM + row_local] = a;
+    group_sync();
+    {
+      const float m0 = xf[row_local], m1 = xf[BM + row_local];
+      const int a0 = xi[row_local], a1 = xi[BM + row_local];
+      m = fmaxf(m0, m1);
+      a = (m0 > m1) ? a0 : (m1 > m0) ? a1 : ((a0 >= 0 && (a1 < 0 || a0 < a1)) ? a0 : a1);
+    }
+    group_sync();   // xf is reused for the row sum
 
     // pass 2: phi, sum(phi), P tiles
     const float m_sc = m * s.scale;
@@ -337,15 +365,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[sb]);
       ++sidx;
-      const int col0 = j * BN;
-      const bool need_mask = col0 + BN - 1 > lim;
+      const int col0 = j * BN + cbase;
+      const bool need_mask = col0 + 63 > lim;
       const int pb = j & 1;
       ok = warp_wait(&p_empty[pb], ((j >> 1) & 1u) ^ 1u);
       if (!ok) break;
       uint8_t* prow = sP + pb * C::P_BYTES + row_local * 128;
       float2 tsum2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int c8 = 0; c8 < BN / 8; ++c8) {
+      for (int c8 = 0; c8 < 8; ++c8) {
         uint32_t packed[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -366,27 +394,31 @@ __global__ void __launch_bounds__(THREADS, 1)
           tsum2 = __fadd2_rn(tsum2, ph);
           packed[e] = pack_f16x2_sat(ph.x, ph.y);
         }
-        const int half = c8 >> 3, chunk = c8 & 7;
-        *reinterpret_cast<uint4*>(prow + half * BOX_BYTES + ((chunk ^ (row_local & 7)) << 4)) =
+        const int chunk = (cbase >> 3) + c8;   // 16-byte chunk of the 128-key row
+        *reinterpret_cast<uint4*>(prow + (chunk >> 3) * BOX_BYTES + (((chunk & 7) ^ (row_local & 7)) << 4)) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
       }
       fence_proxy_async_smem();
       const float tsum = tsum2.x + tsum2.y;
       const unsigned any_live = __any_sync(0xffffffffu, tsum > 0.0f);
-      if (lane == 0) live[pb * 4 + warp] = any_live ? 1 : 0;
+      if (lane == 0) live[pb * SOFTMAX_WARPS + warp] = any_live ? 1 : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
       rowsum += tsum;
     }
 #undef SV
+    xf[half * BM + row_local] = rowsum;
+    group_sync();
+    rowsum = xf[row_local] + xf[BM + row_local];
     if (ok) ok = warp_wait(o_full, 0);
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < s.NQ;
       const float inv = 1.0f / rowsum;
       const size_t ro = static_cast<size_t>(bh) * s.NQ + (row_ok ? row : 0);
+      // each half of the warps stores half of the D columns of its rows
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
         uint32_t ov[32];
         tmem_ld32(lane_addr + TMEM_O + c0, ov);
         tc_wait_ld();
@@ -411,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (row_ok) {
+      if (row_ok && half == 0) {
         if (args.row_m) args.row_m[ro] = m_sc;
         if (args.row_s) args.row_s[ro] = rowsum;
         if (args.row_arg) args.row_arg[ro] = a;
