@@ -70,7 +70,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         return self
@@ -403,8 +403,8 @@ def run_ours(args):
         "roofline": rl,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": hp.h2d_bytes(),
                 "d2h_bytes_per_step": hp.d2h_bytes(), "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": 5 * args.steps,
-        "gpu_launches_per_step": {"ra_softmax_fwd_vec_kernel": 1, "attn_fwd_tc_kernel": 1, "bf16_to_f16_kernel": 1,
+        "gpu_launches": 6 * args.steps,
+        "gpu_launches_per_step": {"ra_softmax_fwd_vec_kernel": 1, "attn_fwd_tc_kernel": 1, "bf16_to_f16_kernel": 2,
                                   "attn_bwd_dq_tc_kernel": 1, "attn_bwd_dkdv_tc_kernel": 1},
         "clocks": clocks.summary(),
     }
@@ -453,7 +453,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host")

@@ -194,6 +194,14 @@ ra_status_t ra_device_status(void* stream);
  */
 void ra_set_wait_limit_ns(uint64_t limit_ns);
 
+/*
+ * ra_debug_force_timeout -- test knob for the failure path (0 = off, the default).
+ * When on, every later tensor-core kernel launch first waits on a barrier that nothing
+ * arrives on, so it gives up after the wait limit, winds down as described above and
+ * reports RA_ERR_TIMEOUT through ra_device_status().  Results of those calls are undefined.
+ */
+void ra_debug_force_timeout(int on);
+
 /* Size of the device array behind ra_attention_bwd_noalloc (32 MiB). */
 #define RA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -54,6 +54,7 @@ _SIGNATURES = {
     "ra_attention_bwd": ([_vp] * 12 + [_i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp], _i32),
     "ra_device_status": ([_vp], _i32),
     "ra_set_wait_limit_ns": ([_u64], None),
+    "ra_debug_force_timeout": ([_i32], None),
 }
 
 
@@ -211,3 +212,8 @@ def device_status(stream=None):
 def set_wait_limit_ns(ns):
     """Limit on every device-side wait of later launches (0 restores the 2 s default)."""
     lib().ra_set_wait_limit_ns(int(ns))
+
+
+def debug_force_timeout(on):
+    """Test knob: make later tensor-core launches take their timeout and wind-down path."""
+    lib().ra_debug_force_timeout(1 if on else 0)

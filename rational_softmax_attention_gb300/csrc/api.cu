@@ -18,6 +18,7 @@ constexpr int kMaxDevices = 64;
 unsigned int* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_force_timeout{0};
 
 ra_status_t status_ptr_for_current_device(unsigned int** out) {
   int dev = 0;
@@ -38,6 +39,7 @@ ra_status_t make_ctx(LaunchCtx* ctx) {
   if (st != RA_OK) return st;
   ctx->status = p;
   ctx->wait_limit_ns = g_wait_limit_ns.load();
+  ctx->force_timeout = g_force_timeout.load();
   return RA_OK;
 }
 
@@ -127,6 +129,8 @@ const char* ra_status_string(ra_status_t status) {
 void ra_set_wait_limit_ns(uint64_t limit_ns) {
   g_wait_limit_ns.store(limit_ns == 0 ? 2000000000ull : static_cast<unsigned long long>(limit_ns));
 }
+
+void ra_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
 
 ra_status_t ra_device_status(void* stream) {
   unsigned int* p = nullptr;

@@ -246,6 +246,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         return true;
       };
       bool ok = mbar_wait(qdo_full, 0, abort_flag, ctx);
+      // test knob: nothing is committed to `drain` yet, so this wait can only time out
+      if (ok && ctx.force_timeout) ok = mbar_wait(drain, 0, abort_flag, ctx);
       for (int j = 0; j < nkt && ok; ++j) {
         // S_j = Q K_j^T
         const int ks = j % C::NKS, sb = j & 1;
@@ -615,6 +617,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
                      aP = smem_u32(sP), aDS = smem_u32(sDS);
       bool ok = mbar_wait(kv_full, 0, abort_flag, ctx);
+      // test knob: nothing is committed to `drain` yet, so this wait can only time out
+      if (ok && ctx.force_timeout) ok = mbar_wait(drain, 0, abort_flag, ctx);
       for (int it = 0; it < nq && ok; ++it) {
         const int qs = it % C::NQS, ds = it % C::NDS;
         const uint32_t par = it & 1u;

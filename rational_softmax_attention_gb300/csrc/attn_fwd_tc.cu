@@ -245,6 +245,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         return true;
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, ctx);
+      // test knob: nothing is committed to `drain` yet, so this wait can only time out
+      if (ok && ctx.force_timeout) ok = mbar_wait(drain, 0, abort_flag, ctx);
       for (int j = 0; j < nkt && ok; ++j) ok = mma_s();   // pass 1
       if (ok) ok = mma_s();                                // pass 2
       for (int j = 1; j < nkt && ok; ++j) {

@@ -24,6 +24,9 @@ constexpr unsigned int kStatusRange = 4u;
 struct LaunchCtx {
   unsigned int* status;   // library-owned device word (one per device)
   unsigned long long wait_limit_ns;
+  // Test knob: the MMA thread of each tensor-core kernel first waits on a barrier that no
+  // one arrives on, so that the timeout and wind-down path runs deterministically.
+  int force_timeout;
 };
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {

@@ -1,10 +1,11 @@
 """Device-side failure handling without a GPU fault.
 
-The wait limit is shrunk to 1 ns, so every wait that is not already satisfied gives
-up at once: the kernel raises its abort flag, drains its in-flight copies and
-tensor-core work, frees its tensor memory and returns.  The status word must then
-read RA_ERR_TIMEOUT, and the context must stay usable: the next normal call is
-checked against the oracle.  One small CTA per kernel keeps the drain bounded.
+With ra_debug_force_timeout on, the MMA thread of each tensor-core kernel first waits on
+a barrier that nothing arrives on ("a flag that nothing sets"); with the wait limit set
+to 2 ms that wait gives up, the kernel raises its abort flag, every role winds down
+(in-flight copies and tensor-core work drained, tensor memory freed) and the kernel
+returns.  The status word must read RA_ERR_TIMEOUT, and the context must stay usable:
+the next normal call is checked against the oracle.  Small problems keep it short.
 """
 import pytest
 import torch
@@ -17,27 +18,29 @@ from rational_softmax_attention_gb300.inputs import attention_inputs
 pytestmark = pytest.mark.gpu
 
 
-def _normal_forward_matches(q, k, v):
-    o, *_ = ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.125, causal=False,
-                                    out_dtype=torch.float32)
+class forced_timeout:
+    def __enter__(self):
+        ra.set_wait_limit_ns(2_000_000)
+        ra.debug_force_timeout(True)
+
+    def __exit__(self, *exc):
+        ra.debug_force_timeout(False)
+        ra.set_wait_limit_ns(0)
+
+
+def test_forward_wait_timeout_is_reported_and_the_context_survives():
+    q, k, v = attention_inputs(1, 2, 256, 384, 64, seed=11, dtype=torch.bfloat16, with_dout=False)
+    assert ra.device_status() == "RA_OK"
+    with forced_timeout():
+        ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.125, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        status = ra.device_status()
+    assert status == "RA_ERR_TIMEOUT"
+    o, *_ = ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.125, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert ra.device_status() == "RA_OK"
     O, *_ = oracle.ra_attention_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), scale=0.125)
     parity.assert_close_bf16(parity.f64(o), O, "O after a timed-out call")
-
-
-def test_forward_wait_timeout_is_reported_and_the_context_survives():
-    q, k, v = attention_inputs(1, 1, 128, 384, 64, seed=11, dtype=torch.bfloat16, with_dout=False)
-    assert ra.device_status() == "RA_OK"
-    ra.set_wait_limit_ns(1)
-    try:
-        ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), scale=0.125, out_dtype=torch.float32)
-        torch.cuda.synchronize()
-        status = ra.device_status()
-    finally:
-        ra.set_wait_limit_ns(0)
-    assert status == "RA_ERR_TIMEOUT"
-    _normal_forward_matches(q, k, v)
 
 
 def test_backward_wait_timeout_is_reported_and_the_context_survives():
@@ -46,13 +49,10 @@ def test_backward_wait_timeout_is_reported_and_the_context_survives():
     o, rm, rs, ra_, _ = ra.ra_attention_forward(qg, kg, vg, scale=0.125, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert ra.device_status() == "RA_OK"
-    ra.set_wait_limit_ns(1)
-    try:
+    with forced_timeout():
         ra.ra_attention_backward(qg, kg, vg, o, dog, rm, rs, ra_, scale=0.125)
         torch.cuda.synchronize()
         status = ra.device_status()
-    finally:
-        ra.set_wait_limit_ns(0)
     assert status == "RA_ERR_TIMEOUT"
     dq, dk, dv = ra.ra_attention_backward(qg, kg, vg, o, dog, rm, rs, ra_, scale=0.125)
     torch.cuda.synchronize()
