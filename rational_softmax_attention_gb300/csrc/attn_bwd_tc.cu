@@ -54,10 +54,11 @@ __device__ __forceinline__ void st_tile16(uint8_t* tile, int r, int chunk, uint4
   *reinterpret_cast<uint4*>(tile + half * BOX_BYTES + r * 128 + ((c ^ (r & 7)) << 4)) = val;
 }
 
-// 1/w0 and 1/w1 (w in [0.5, 1]) from one rcp.approx of w0 w1.
+// 1/w0 and 1/w1 (w in [0.5, 1]) from one rcp.approx of w0 w1 (two scalar products, so
+// the pair is born in adjacent registers for the f32x2 arithmetic that follows).
 __device__ __forceinline__ float2 rcp_pair(float w0, float w1) {
   const float R = rcp_approx(w0 * w1);
-  return __fmul2_rn(make_float2(R, R), make_float2(w1, w0));
+  return make_float2(R * w1, R * w0);
 }
 
 // Row of 8 bf16 from global memory as floats.

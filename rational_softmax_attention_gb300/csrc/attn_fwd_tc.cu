@@ -72,6 +72,48 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = OFF_XCH + 4 * BM * 4 + 1024;   // + slack for 1024-byte alignment
 };
 
+// phi for two scores of a row: w = sat(base - c2 s) = (1+u)/2, one reciprocal for the pair
+// (R = 1/(w0 w1), so 1/w0 = R w1), q = 1/w - 1 as a single FMA, phi = ((q^2)^2)^2 in f32x2.
+__device__ __forceinline__ float2 phi_pair(float s0, float s1, float c2, float base) {
+  const float w0 = fma_sat(s0, -c2, base);
+  const float w1 = fma_sat(s1, -c2, base);
+  const float R = rcp_approx(w0 * w1);
+  const float2 qq = make_float2(fmaf(R, w1, -1.0f), fmaf(R, w0, -1.0f));
+  const float2 q2 = __fmul2_rn(qq, qq);
+  const float2 q4 = __fmul2_rn(q2, q2);
+  return __fmul2_rn(q4, q4);
+}
+
+// Pass-2 work of one 64-column half tile: phi, the fp16 P chunks in the swizzled tile,
+// and the partial row sum.  MASKED: columns past `lim` (causal diagonal, ragged tail) get
+// s = -inf, hence w = 1 and phi = 0.
+template <bool MASKED>
+__device__ __forceinline__ float2 pass2_half_tile(const uint32_t (&sv)[2][32], uint8_t* prow, int row_local,
+                                                  int cbase, int col0, int lim, float c2, float base) {
+  float2 tsum2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    uint32_t packed[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = c8 * 8 + 2 * e;
+      float s0 = __uint_as_float(sv[c >> 5][c & 31]);
+      float s1 = __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]);
+      if (MASKED) {
+        if (col0 + c > lim) s0 = -INFINITY;
+        if (col0 + c + 1 > lim) s1 = -INFINITY;
+      }
+      const float2 ph = phi_pair(s0, s1, c2, base);
+      tsum2 = __fadd2_rn(tsum2, ph);
+      packed[e] = pack_f16x2_sat(ph.x, ph.y);
+    }
+    const int chunk = (cbase >> 3) + c8;   // 16-byte chunk of the 128-key row
+    *reinterpret_cast<uint4*>(prow + (chunk >> 3) * BOX_BYTES + (((chunk & 7) ^ (row_local & 7)) << 4)) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+  return tsum2;
+}
+
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
 
@@ -373,33 +415,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = warp_wait(&p_empty[pb], ((j >> 1) & 1u) ^ 1u);
       if (!ok) break;
       uint8_t* prow = sP + pb * C::P_BYTES + row_local * 128;
-      float2 tsum2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint32_t packed[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = c8 * 8 + 2 * e;
-          float s0 = SV(c), s1 = SV(c + 1);
-          if (need_mask) {
-            if (col0 + c > lim) s0 = -INFINITY;
-            if (col0 + c + 1 > lim) s1 = -INFINITY;
-          }
-          const float w0 = fma_sat(s0, -c2, base);
-          const float w1 = fma_sat(s1, -c2, base);
-          const float R = rcp_approx(w0 * w1);
-          const float2 r = __fmul2_rn(make_float2(R, R), make_float2(w1, w0));
-          const float2 qq = __fadd2_rn(r, make_float2(-1.0f, -1.0f));
-          const float2 q2 = __fmul2_rn(qq, qq);
-          const float2 q4 = __fmul2_rn(q2, q2);
-          const float2 ph = __fmul2_rn(q4, q4);
-          tsum2 = __fadd2_rn(tsum2, ph);
-          packed[e] = pack_f16x2_sat(ph.x, ph.y);
-        }
-        const int chunk = (cbase >> 3) + c8;   // 16-byte chunk of the 128-key row
-        *reinterpret_cast<uint4*>(prow + (chunk >> 3) * BOX_BYTES + (((chunk & 7) ^ (row_local & 7)) << 4)) =
-            make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      }
+      const float2 tsum2 = need_mask ? pass2_half_tile<true>(sv, prow, row_local, cbase, col0, lim, c2, base)
+                                     : pass2_half_tile<false>(sv, prow, row_local, cbase, col0, lim, c2, base);
       fence_proxy_async_smem();
       const float tsum = tsum2.x + tsum2.y;
       const unsigned any_live = __any_sync(0xffffffffu, tsum > 0.0f);
