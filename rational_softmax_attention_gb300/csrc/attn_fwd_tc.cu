@@ -43,12 +43,16 @@ namespace {
 
 constexpr int BM = 128;   // query rows per CTA: the MMA M and the 128 TMEM lanes
 constexpr int BN = 128;   // keys per tile: the N of Q K^T and the K of P V
-// 8 softmax warps: warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the same query
-// rows) and split each tile's 128 key columns 64 / 64, two warps per scheduler.
-constexpr int SOFTMAX_WARPS = 8;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
-constexpr int THREADS = 320;
+// 16 softmax warps, four per scheduler: warps w, w + 4, w + 8, w + 12 share TMEM lanes
+// 32 (w % 4) .. + 31 (the same query rows) and split each tile's 128 key columns into
+// NPART parts of WCOLS.  More warps per scheduler hide the latencies of the per-score
+// chain (TMEM load, FMA, reciprocal, conversion, shared-memory store).
+constexpr int SOFTMAX_WARPS = 16;
+constexpr int NPART = SOFTMAX_WARPS / 4;
+constexpr int WCOLS = 128 / NPART;
+constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
+constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
+constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S0 = 0;
 constexpr uint32_t TMEM_S1 = 128;
@@ -67,9 +71,9 @@ struct FwdCfg {
   // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain
   static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int MISC_BYTES = 96;   // tmem base, abort flag, live votes [2][8]
-  static constexpr int OFF_XCH = OFF_MISC + MISC_BYTES;   // [2][128] floats + [2][128] ints: half partials
-  static constexpr int SMEM_BYTES = OFF_XCH + 4 * BM * 4 + 1024;   // + slack for 1024-byte alignment
+  static constexpr int MISC_BYTES = 16 + 2 * SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes
+  static constexpr int OFF_XCH = OFF_MISC + MISC_BYTES;   // [NPART][128] floats + [NPART][128] ints
+  static constexpr int SMEM_BYTES = OFF_XCH + 2 * NPART * BM * 4 + 1024;   // + slack for 1024-byte alignment
 };
 
 // phi for two scores of a row: w = sat(base - c2 s) = (1+u)/2, one reciprocal for the pair
@@ -84,15 +88,16 @@ __device__ __forceinline__ float2 phi_pair(float s0, float s1, float c2, float b
   return __fmul2_rn(q4, q4);
 }
 
-// Pass-2 work of one 64-column half tile: phi, the fp16 P chunks in the swizzled tile,
-// and the partial row sum.  MASKED: columns past `lim` (causal diagonal, ragged tail) get
-// s = -inf, hence w = 1 and phi = 0.
+// Pass-2 work of one WCOLS-column part of a tile: phi, the fp16 P chunks in the swizzled
+// tile, and the partial row sum.  MASKED: columns past `lim` (causal diagonal, ragged
+// tail) get s = -inf, hence w = 1 and phi = 0.
 template <bool MASKED>
-__device__ __forceinline__ float2 pass2_half_tile(const uint32_t (&sv)[2][32], uint8_t* prow, int row_local,
-                                                  int cbase, int col0, int lim, float c2, float base) {
+__device__ __forceinline__ float2 pass2_part_tile(const uint32_t (&sv)[WCOLS / 32][32], uint8_t* prow,
+                                                  int row_local, int cbase, int col0, int lim, float c2,
+                                                  float base) {
   float2 tsum2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) {
+  for (int c8 = 0; c8 < WCOLS / 8; ++c8) {
     uint32_t packed[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -307,28 +312,28 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------------ softmax warps
     // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key columns
-    // [64 (w / 4), 64 (w / 4) + 64) of every tile; the row maximum, its argmax and the
-    // row sum are combined across the two halves through shared memory.
+    // [WCOLS (w / 4), WCOLS (w / 4) + WCOLS) of every tile; the row maximum, its argmax
+    // and the row sum are combined across the NPART parts through shared memory.
     const int quarter = warp & 3;
-    const int half = warp >> 2;
-    const int cbase = half * 64;
+    const int part = warp >> 2;
+    const int cbase = part * WCOLS;
     const int row_local = quarter * 32 + lane;   // TMEM lane
     const int row = q0 + row_local;
     const int lim = s.causal ? min(row, s.NK - 1) : s.NK - 1;   // last key this row may see
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* xf = reinterpret_cast<float*>(smem + C::OFF_XCH);          // [2][BM]
-    int* xi = reinterpret_cast<int*>(smem + C::OFF_XCH + 2 * BM * 4);  // [2][BM]
-    auto group_sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+    float* xf = reinterpret_cast<float*>(smem + C::OFF_XCH);              // [NPART][BM]
+    int* xi = reinterpret_cast<int*>(smem + C::OFF_XCH + NPART * BM * 4);  // [NPART][BM]
+    auto group_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(32 * SOFTMAX_WARPS) : "memory"); };
     auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
       int r = 1;
       if (lane == 0) r = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
-    uint32_t sv[2][32];
+    uint32_t sv[WCOLS / 32][32];
     auto load_s = [&](int sb) {
       const uint32_t col = lane_addr + (sb ? TMEM_S1 : TMEM_S0) + cbase;
-      tmem_ld32(col + 0, sv[0]);
-      tmem_ld32(col + 32, sv[1]);
+#pragma unroll
+      for (int k = 0; k < WCOLS / 32; ++k) tmem_ld32(col + 32 * k, sv[k]);
       tc_wait_ld();
     };
 #define SV(c) u2f(sv[(c) >> 5][(c) & 31])
@@ -337,7 +342,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t sidx = 0;
     float m = -INFINITY;
     int a = -1;
-    // pass 1: running maximum of the raw scores q.k over this half's columns (scale > 0
+    // pass 1: running maximum of the raw scores q.k over this part's columns (scale > 0
     // keeps the argmax)
     for (int j = 0; j < nkt && ok; ++j) {
       const int sb = sidx & 1;
@@ -351,11 +356,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(&s_empty[sb]);
       ++sidx;
       const int col0 = j * BN + cbase;   // key index of local column 0
-      const bool need_mask = col0 + 63 > lim;
+      const bool need_mask = col0 + WCOLS - 1 > lim;
       float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
       if (!need_mask) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 8) {
+        for (int c = 0; c < WCOLS; c += 8) {
           t0 = max3f(t0, SV(c), SV(c + 1));
           t1 = max3f(t1, SV(c + 2), SV(c + 3));
           t2 = max3f(t2, SV(c + 4), SV(c + 5));
@@ -363,7 +368,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < WCOLS; ++c) {
           const float x = (col0 + c <= lim) ? SV(c) : -INFINITY;
           if ((c & 3) == 0) t0 = fmaxf(t0, x);
           if ((c & 3) == 1) t1 = fmaxf(t1, x);
@@ -373,23 +378,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const float tmax = fmaxf(fmaxf(t0, t1), fmaxf(t2, t3));
       if (tmax > m) {   // strictly greater: an earlier tile keeps ties (lowest index)
-        int idx = 64;
+        int idx = WCOLS;
 #pragma unroll
-        for (int c = 63; c >= 0; --c)
+        for (int c = WCOLS - 1; c >= 0; --c)
           if (SV(c) == tmax && col0 + c <= lim) idx = c;
         m = tmax;
         a = col0 + idx;
       }
     }
-    // combine the two halves (reached by all eight warps, also after a wait gave up)
-    xf[half * BM + row_local] = m;
-    xi[half * BM + row_local] = a;
+    // combine the parts (reached by every softmax warp, also after a wait gave up): the
+    // maximum, and among the parts that attain it the lowest index
+    xf[part * BM + row_local] = m;
+    xi[part * BM + row_local] = a;
     group_sync();
-    {
-      const float m0 = xf[row_local], m1 = xf[BM + row_local];
-      const int a0 = xi[row_local], a1 = xi[BM + row_local];
-      m = fmaxf(m0, m1);
-      a = (m0 > m1) ? a0 : (m1 > m0) ? a1 : ((a0 >= 0 && (a1 < 0 || a0 < a1)) ? a0 : a1);
+    m = xf[row_local];
+#pragma unroll
+    for (int p = 1; p < NPART; ++p) m = fmaxf(m, xf[p * BM + row_local]);
+    a = -1;
+#pragma unroll
+    for (int p = 0; p < NPART; ++p) {
+      const int ap = xi[p * BM + row_local];
+      if (xf[p * BM + row_local] == m && ap >= 0 && (a < 0 || ap < a)) a = ap;
     }
     group_sync();   // xf is reused for the row sum
 
@@ -410,13 +419,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(&s_empty[sb]);
       ++sidx;
       const int col0 = j * BN + cbase;
-      const bool need_mask = col0 + 63 > lim;
+      const bool need_mask = col0 + WCOLS - 1 > lim;
       const int pb = j & 1;
       ok = warp_wait(&p_empty[pb], ((j >> 1) & 1u) ^ 1u);
       if (!ok) break;
       uint8_t* prow = sP + pb * C::P_BYTES + row_local * 128;
-      const float2 tsum2 = need_mask ? pass2_half_tile<true>(sv, prow, row_local, cbase, col0, lim, c2, base)
-                                     : pass2_half_tile<false>(sv, prow, row_local, cbase, col0, lim, c2, base);
+      const float2 tsum2 = need_mask ? pass2_part_tile<true>(sv, prow, row_local, cbase, col0, lim, c2, base)
+                                     : pass2_part_tile<false>(sv, prow, row_local, cbase, col0, lim, c2, base);
       fence_proxy_async_smem();
       const float tsum = tsum2.x + tsum2.y;
       const unsigned any_live = __any_sync(0xffffffffu, tsum > 0.0f);
@@ -426,18 +435,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       rowsum += tsum;
     }
 #undef SV
-    xf[half * BM + row_local] = rowsum;
+    xf[part * BM + row_local] = rowsum;
     group_sync();
-    rowsum = xf[row_local] + xf[BM + row_local];
+    rowsum = xf[row_local];
+#pragma unroll
+    for (int p = 1; p < NPART; ++p) rowsum += xf[p * BM + row_local];
     if (ok) ok = warp_wait(o_full, 0);
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < s.NQ;
       const float inv = 1.0f / rowsum;
       const size_t ro = static_cast<size_t>(bh) * s.NQ + (row_ok ? row : 0);
-      // each half of the warps stores half of the D columns of its rows
+      // the parts store 32-column slices of the D output columns of their rows
 #pragma unroll
-      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+      for (int c0 = part * 32; c0 < D; c0 += NPART * 32) {
         uint32_t ov[32];
         tmem_ld32(lane_addr + TMEM_O + c0, ov);
         tc_wait_ld();
@@ -462,7 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (row_ok && half == 0) {
+      if (row_ok && part == 0) {
         if (args.row_m) args.row_m[ro] = m_sc;
         if (args.row_s) args.row_s[ro] = rowsum;
         if (args.row_arg) args.row_arg[ro] = a;
