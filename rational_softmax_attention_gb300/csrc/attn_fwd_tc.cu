@@ -47,7 +47,7 @@ constexpr int BN = 128;   // keys per tile: the N of Q K^T and the K of P V
 // 32 (w % 4) .. + 31 (the same query rows) and split each tile's 128 key columns into
 // NPART parts of WCOLS.  More warps per scheduler hide the latencies of the per-score
 // chain (TMEM load, FMA, reciprocal, conversion, shared-memory store).
-constexpr int SOFTMAX_WARPS = 16;
+constexpr int SOFTMAX_WARPS = 8;
 constexpr int NPART = SOFTMAX_WARPS / 4;
 constexpr int WCOLS = 128 / NPART;
 constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
@@ -62,7 +62,9 @@ constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16 (12
 template <int D>
 struct FwdCfg {
   static constexpr int TILE_BYTES = BN * D * 2;   // a Q, K or V tile: D/64 boxes
-  static constexpr int NSTAGE = (D == 128) ? 3 : 4;
+  // Ring depth: enough K/V tiles in flight to cover the L2 -> shared-memory TMA latency
+  // at one tile consumed per ~512 tensor cycles.
+  static constexpr int NSTAGE = (D == 128) ? 4 : 8;
   static constexpr int P_BYTES = BM * BN * 2;     // P tile: two 64-key halves of 16 KB
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = OFF_Q + TILE_BYTES;
@@ -73,7 +75,12 @@ struct FwdCfg {
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int MISC_BYTES = 16 + 2 * SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes
   static constexpr int OFF_XCH = OFF_MISC + MISC_BYTES;   // [NPART][128] floats + [NPART][128] ints
-  static constexpr int SMEM_BYTES = OFF_XCH + 2 * NPART * BM * 4 + 1024;   // + slack for 1024-byte alignment
+  static constexpr int USED = OFF_XCH + 2 * NPART * BM * 4;
+  // alignment slack only where it fits; otherwise the kernel requires (and checks) a
+  // 1024-byte aligned dynamic shared-memory base
+  static constexpr int SLACK = (USED + 1024 <= 232448) ? 1024 : 0;
+  static constexpr int SMEM_BYTES = USED + SLACK;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 // phi for two scores of a row: w = sat(base - c2 s) = (1+u)/2, one reciprocal for the pair
@@ -128,7 +135,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   using C = FwdCfg<D>;
   constexpr int NST = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t mis = smem_u32(smem_raw) & 1023u;
+  if (C::SLACK == 0 && mis != 0) {   // uniform across the CTA: nothing launched yet
+    if (threadIdx.x == 0) atomicOr(ctx.status, kStatusBadSmem);
+    return;
+  }
+  uint8_t* smem = smem_raw + ((1024u - mis) & 1023u);
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sRing = smem + C::OFF_RING;
   uint8_t* sP = smem + C::OFF_P;
