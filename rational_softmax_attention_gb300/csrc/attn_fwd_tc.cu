@@ -10,22 +10,28 @@
 // running-max rescaling of standard flash attention does not exist here; the
 // row maximum must be final before any phi is formed.
 //
-// One CTA owns one 128-row query tile of one (batch, head) and runs both passes
-// over the key tiles that the tile can see (all of them, or up to the diagonal
-// when causal), so Q stays in shared memory and m_i stays in a register:
-//   warp 4      TMA producer: Q once, then K tiles (pass 1), then K and V tiles
-//               interleaved in the order the MMA warp consumes them (pass 2),
+// One CTA owns TWO 128-row query tiles (A: rows q0 .. q0+127, B: q0+128 .. q0+255) of
+// one (batch, head) and runs both passes over the key tiles they can see.  Every K and
+// V tile brought into shared memory serves both query tiles: the tile loads into one
+// SM top out near 40-46 bytes per clock, and one query tile per CTA would need about
+// 62 bytes per clock to keep the tensor core busy (K twice and V once per 1536
+// tensor cycles at D = 128); two query tiles halve that.
+//   warp 8      TMA producer: Q_A and Q_B once, then K tiles (pass 1), then K and V
+//               tiles interleaved in the order the MMA thread consumes them (pass 2),
 //               through a ring of NSTAGE shared-memory stages.
-//   warp 5      MMA issuer (one thread): S = Q K^T into one of two TMEM score
-//               buffers (128 x 128 fp32), and in pass 2 O += P V into a TMEM
-//               accumulator (128 x D fp32), one K step behind the scores so the
-//               tensor core computes S_{j+1} while the softmax warps work on S_j.
-//   warps 0-3   softmax warpgroup, thread t owns query row t (TMEM lane t):
-//               pass 1 reads S and keeps the running max and lowest argmax;
-//               pass 2 reads S, forms phi on the FMA pipe (no exp), writes
-//               P = fp16(phi) into a 128-byte-swizzled shared-memory tile for the
-//               P V product, sums phi in fp32, and votes whether the tile is live.
-//               Epilogue: O = acc / sum(phi), row statistics for the backward.
+//   warp 9      MMA issuer (one thread): S_A = Q_A K^T and S_B = Q_B K^T into two
+//               TMEM score buffers (128 x 128 fp32 each); in pass 2 also
+//               O_A += P_A V and O_B += P_B V into two TMEM accumulators (128 x D fp32),
+//               issued as S_A(j+1), O_A(j), S_B(j+1), O_B(j) so that each softmax
+//               warpgroup has three products' time to turn S(j+1) into P(j+1).
+//   warps 0-3   softmax warpgroup of query tile A, warps 4-7 that of tile B; thread t of
+//               a warpgroup owns query row t (TMEM lane t) and all 128 key columns:
+//               pass 1 keeps the running max of the raw scores and the tile of its first
+//               occurrence, pass 2 the lowest column holding it in that tile;
+//               pass 2 forms phi on the FMA pipe (no exp), writes P = fp16(phi) into
+//               its 128-byte-swizzled shared-memory tile, sums phi in fp32, and votes
+//               whether the tile is live.  Epilogue: O = acc / sum(phi) and the row
+//               statistics for the backward.
 //   V arrives as the fp16 copy the C-ABI layer made once per call (exact for bf16
 //   values up to 65504), so the P V product runs in fp16 and P is rounded to 2^-11
 //   rather than 2^-8.  Q K^T stays in bf16.
@@ -41,41 +47,35 @@
 namespace raattn {
 namespace {
 
-constexpr int BM = 128;   // query rows per CTA: the MMA M and the 128 TMEM lanes
+constexpr int BM = 128;   // query rows per tile: the MMA M and the 128 TMEM lanes
 constexpr int BN = 128;   // keys per tile: the N of Q K^T and the K of P V
-// 16 softmax warps, four per scheduler: warps w, w + 4, w + 8, w + 12 share TMEM lanes
-// 32 (w % 4) .. + 31 (the same query rows) and split each tile's 128 key columns into
-// NPART parts of WCOLS.  More warps per scheduler hide the latencies of the per-score
-// chain (TMEM load, FMA, reciprocal, conversion, shared-memory store).
-constexpr int SOFTMAX_WARPS = 8;
-constexpr int NPART = SOFTMAX_WARPS / 4;
-constexpr int WCOLS = 128 / NPART;
+constexpr int NGROUP = 2;                            // query tiles per CTA
+constexpr int GROUP_WARPS = 4;                       // one warpgroup per query tile
+constexpr int SOFTMAX_WARPS = NGROUP * GROUP_WARPS;  // 8
 constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
 constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
 constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_S0 = 0;
-constexpr uint32_t TMEM_S1 = 128;
-constexpr uint32_t TMEM_O = 256;
-constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16 (128 B per row)
+constexpr uint32_t TMEM_S = 0;     // S of query tile g at column 128 g
+constexpr uint32_t TMEM_O = 256;   // O of query tile g at column 256 + 128 g
+constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 16-bit values (128 B per row)
 
 template <int D>
 struct FwdCfg {
   static constexpr int TILE_BYTES = BN * D * 2;   // a Q, K or V tile: D/64 boxes
-  // Ring depth: enough K/V tiles in flight to cover the L2 -> shared-memory TMA latency
-  // at one tile consumed per ~512 tensor cycles.
-  static constexpr int NSTAGE = (D == 128) ? 4 : 8;
+  // Ring depth: K/V tiles in flight; each stage serves two products (S_A and S_B, or
+  // O_A and O_B).
+  static constexpr int NSTAGE = (D == 128) ? 3 : 6;
   static constexpr int P_BYTES = BM * BN * 2;     // P tile: two 64-key halves of 16 KB
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_RING = OFF_Q + TILE_BYTES;
-  static constexpr int OFF_P = OFF_RING + NSTAGE * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_Q = 0;                 // Q_A, Q_B
+  static constexpr int OFF_RING = OFF_Q + NGROUP * TILE_BYTES;
+  static constexpr int OFF_P = OFF_RING + NSTAGE * TILE_BYTES;   // P_A, P_B
+  static constexpr int OFF_BAR = OFF_P + NGROUP * P_BYTES;
   // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain
-  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 + 2;
+  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 4 * NGROUP + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int MISC_BYTES = 16 + 2 * SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes
-  static constexpr int OFF_XCH = OFF_MISC + MISC_BYTES;   // [NPART][128] floats + [NPART][128] ints
-  static constexpr int USED = OFF_XCH + 2 * NPART * BM * 4;
+  static constexpr int MISC_BYTES = 16 + SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes
+  static constexpr int USED = OFF_MISC + MISC_BYTES;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
   // 1024-byte aligned dynamic shared-memory base
   static constexpr int SLACK = (USED + 1024 <= 232448) ? 1024 : 0;
@@ -83,51 +83,83 @@ struct FwdCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
-// phi for two scores of a row: w = sat(base - c2 s) = (1+u)/2, one reciprocal for the pair
-// (R = 1/(w0 w1), so 1/w0 = R w1), q = 1/w - 1 as a single FMA, phi = ((q^2)^2)^2 in f32x2.
-__device__ __forceinline__ float2 phi_pair(float s0, float s1, float c2, float base) {
-  const float w0 = fma_sat(s0, -c2, base);
-  const float w1 = fma_sat(s1, -c2, base);
-  const float R = rcp_approx(w0 * w1);
-  const float2 qq = make_float2(fmaf(R, w1, -1.0f), fmaf(R, w0, -1.0f));
-  const float2 q2 = __fmul2_rn(qq, qq);
-  const float2 q4 = __fmul2_rn(q2, q2);
-  return __fmul2_rn(q4, q4);
-}
-
-// Pass-2 work of one WCOLS-column part of a tile: phi, the fp16 P chunks in the swizzled
-// tile, and the partial row sum.  MASKED: columns past `lim` (causal diagonal, ragged
-// tail) get s = -inf, hence w = 1 and phi = 0.
-template <bool MASKED>
-__device__ __forceinline__ float2 pass2_part_tile(const uint32_t (&sv)[WCOLS / 32][32], uint8_t* prow,
-                                                  int row_local, int cbase, int col0, int lim, float c2,
-                                                  float base) {
-  float2 tsum2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-  for (int c8 = 0; c8 < WCOLS / 8; ++c8) {
-    uint32_t packed[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int c = c8 * 8 + 2 * e;
-      float s0 = __uint_as_float(sv[c >> 5][c & 31]);
-      float s1 = __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]);
-      if (MASKED) {
-        if (col0 + c > lim) s0 = -INFINITY;
-        if (col0 + c + 1 > lim) s1 = -INFINITY;
-      }
-      const float2 ph = phi_pair(s0, s1, c2, base);
-      tsum2 = __fadd2_rn(tsum2, ph);
-      packed[e] = pack_f16x2_sat(ph.x, ph.y);
-    }
-    const int chunk = (cbase >> 3) + c8;   // 16-byte chunk of the 128-key row
-    *reinterpret_cast<uint4*>(prow + (chunk >> 3) * BOX_BYTES + (((chunk & 7) ^ (row_local & 7)) << 4)) =
-        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  }
-  return tsum2;
+// phi for four scores of a row (columns c .. c+3): w = sat(base - c2 s) = (1+u)/2.  The
+// reciprocals come from one packed product of the pairs A = (w0, w1), B = (w2, w3):
+// R = 1/(A B) = (1/(w0 w2), 1/(w1 w3)), so R B = (1/w0, 1/w1) and R A = (1/w2, 1/w3);
+// q = 1/w - 1 is one packed FMA per pair and phi = ((q^2)^2)^2 three packed products.
+__device__ __forceinline__ void phi_quad(float s0, float s1, float s2, float s3, float c2, float base,
+                                         float2& pa, float2& pb) {
+  const float2 A = make_float2(fma_sat(s0, -c2, base), fma_sat(s1, -c2, base));
+  const float2 B = make_float2(fma_sat(s2, -c2, base), fma_sat(s3, -c2, base));
+  const float2 P = __fmul2_rn(A, B);
+  const float2 R = make_float2(rcp_approx(P.x), rcp_approx(P.y));
+  const float2 minus1 = make_float2(-1.0f, -1.0f);
+  float2 qa = __ffma2_rn(R, B, minus1);
+  float2 qb = __ffma2_rn(R, A, minus1);
+  qa = __fmul2_rn(qa, qa);
+  qb = __fmul2_rn(qb, qb);
+  qa = __fmul2_rn(qa, qa);
+  qb = __fmul2_rn(qb, qb);
+  pa = __fmul2_rn(qa, qa);
+  pb = __fmul2_rn(qb, qb);
 }
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
+// Pass-2 arithmetic of one 64-key half of a row, held in h (two 32-column chunks): phi
+// as packed fp16 pairs in pk (four per 16-byte chunk of P) and the partial row sum.
+// MASKED: columns past `lim` (causal diagonal, ragged tail) get s = -inf, hence w = 1
+// and phi = 0.
+template <bool MASKED>
+__device__ __forceinline__ float2 phi_half(const uint32_t (&h)[2][32], uint32_t (&pk)[32], int col0, int lim,
+                                           float c2, float base) {
+  float2 tsum2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int c = c8 * 8 + e;
+      x[e] = u2f(h[c >> 5][c & 31]);
+      if (MASKED && col0 + c > lim) x[e] = -INFINITY;
+    }
+    float2 p0, p1, p2, p3;
+    phi_quad(x[0], x[1], x[2], x[3], c2, base, p0, p1);
+    phi_quad(x[4], x[5], x[6], x[7], c2, base, p2, p3);
+    tsum2 = __fadd2_rn(tsum2, __fadd2_rn(__fadd2_rn(p0, p1), __fadd2_rn(p2, p3)));
+    pk[4 * c8 + 0] = pack_f16x2_sat(p0.x, p0.y);
+    pk[4 * c8 + 1] = pack_f16x2_sat(p1.x, p1.y);
+    pk[4 * c8 + 2] = pack_f16x2_sat(p2.x, p2.y);
+    pk[4 * c8 + 3] = pack_f16x2_sat(p3.x, p3.y);
+  }
+  return tsum2;
+}
+
+// One 64-key half of a P row (128 bytes) into its half of the 128-byte-swizzled tile:
+// 16-byte chunk c lands at position c xor (row mod 8).
+__device__ __forceinline__ void store_p_half(const uint32_t (&pk)[32], uint8_t* phalf_row, int row_local) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(phalf_row + ((c ^ (row_local & 7)) << 4)) =
+        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+}
+
+template <bool MASKED>
+__device__ __forceinline__ float2 phi_store_half(const uint32_t (&h)[2][32], uint8_t* phalf_row, int row_local,
+                                                 int col0, int lim, float c2, float base) {
+  uint32_t pk[32];
+  const float2 t = phi_half<MASKED>(h, pk, col0, lim, c2, base);
+  store_p_half(pk, phalf_row, row_local);
+  return t;
+}
+
+// Lowest column of a 32-column chunk whose score equals m (visible columns only), or 32.
+__device__ __forceinline__ int find_in_chunk(const uint32_t (&v)[32], float m, int col0, int lim) {
+  int idx = 32;
+#pragma unroll
+  for (int c = 31; c >= 0; --c) idx = (u2f(v[c]) == m && col0 + c <= lim) ? c : idx;
+  return idx;
+}
 
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -148,29 +180,31 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* q_full = bars;
   uint64_t* ring_full = bars + 1;
   uint64_t* ring_empty = ring_full + NST;
-  uint64_t* s_full = ring_empty + NST;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* p_empty = p_full + 2;
-  uint64_t* o_full = p_empty + 2;
+  uint64_t* s_full = ring_empty + NST;   // [NGROUP]
+  uint64_t* s_empty = s_full + NGROUP;
+  uint64_t* p_full = s_empty + NGROUP;
+  uint64_t* p_empty = p_full + NGROUP;
+  uint64_t* o_full = p_empty + NGROUP;
   uint64_t* drain = o_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);   // [2][8]
+  volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);   // [NGROUP][GROUP_WARPS]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int BH = s.B * s.H;
   const int nqt = (s.NQ + BM - 1) / BM;
+  const int nct = (nqt + NGROUP - 1) / NGROUP;   // CTAs per (batch, head)
   const int item = blockIdx.x;
   // Head-major order: the ~150 resident CTAs share a few heads, so each head's K and V
-  // (4 MB at N = 8192, D = 128) stay in L2 across its query tiles.  Causal: within a
-  // head the longest query tiles (largest index) go first.
-  const int bh = item / nqt;
-  const int qt = s.causal ? (nqt - 1 - item % nqt) : (item % nqt);
-  const int q0 = qt * BM;
-  const int last_key = s.causal ? min(s.NK - 1, min(s.NQ - 1, q0 + BM - 1)) : s.NK - 1;
-  const int nkt = last_key / BN + 1;
+  // stay in L2 across its query tiles.  Causal: within a head the longest CTAs go first.
+  const int bh = item / nct;
+  const int ct = s.causal ? (nct - 1 - item % nct) : (item % nct);
+  const int q0 = ct * (NGROUP * BM);
+  // last key any row of the CTA may see, and per query tile
+  auto last_key_of = [&](int rows_end) {   // rows_end: one past the last row of the range
+    return s.causal ? min(s.NK - 1, min(s.NQ - 1, rows_end - 1)) : s.NK - 1;
+  };
+  const int nkt = last_key_of(q0 + NGROUP * BM) / BN + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -178,11 +212,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&ring_full[i], 1);
       mbar_init(&ring_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], SOFTMAX_WARPS);   // one arrival per softmax warp
-      mbar_init(&p_full[i], SOFTMAX_WARPS);
-      mbar_init(&p_empty[i], 1);
+    for (int g = 0; g < NGROUP; ++g) {
+      mbar_init(&s_full[g], 1);
+      mbar_init(&s_empty[g], GROUP_WARPS);   // one arrival per warp of the group
+      mbar_init(&p_full[g], GROUP_WARPS);
+      mbar_init(&p_empty[g], 1);
     }
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
@@ -204,9 +238,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&args.tm_q);
       tma_prefetch_desc(&args.tm_k);
       tma_prefetch_desc(&args.tm_v);
-      mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
+      mbar_arrive_expect_tx(q_full, NGROUP * C::TILE_BYTES);
+      for (int g = 0; g < NGROUP; ++g)
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * BOX_BYTES, &args.tm_q, q_full, c * 64, q0, bh);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sQ + g * C::TILE_BYTES + c * BOX_BYTES, &args.tm_q, q_full, c * 64, q0 + g * BM, bh);
       uint32_t it = 0;
       uint32_t last_par[NST];
       bool issued[NST];
@@ -228,8 +264,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++it;
         return true;
       };
+      // All CTAs of a head walk its key tiles in step, so the first touch of each K and
+      // V tile would expose a full DRAM miss to every one of them: pass 1 prefetches K
+      // KPF tiles ahead of its loads into L2, and every V tile for pass 2.
+      constexpr int KPF = 4;
+      auto prefetch = [&](const CUtensorMap* map, int j) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_3d(map, c * 64, j * BN, bh);
+      };
+      for (int j = 0; j < KPF && j < nkt; ++j) prefetch(&args.tm_k, j);
       bool ok = true;
-      for (int j = 0; j < nkt && ok; ++j) ok = issue(&args.tm_k, j);         // pass 1: K_0 .. K_{n-1}
+      for (int j = 0; j < nkt && ok; ++j) {                                  // pass 1: K_0 .. K_{n-1}
+        if (j + KPF < nkt) prefetch(&args.tm_k, j + KPF);
+        prefetch(&args.tm_v, j);
+        ok = issue(&args.tm_k, j);
+      }
       if (ok) ok = issue(&args.tm_k, 0);                                     // pass 2: K_0, then
       for (int j = 1; j < nkt && ok; ++j) {                                  //   K_j, V_{j-1}
         ok = issue(&args.tm_k, j);
@@ -246,73 +295,100 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_fp16_f32(BM, D, 0, 1);   // P and V in fp16
       const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sRing), sPa = smem_u32(sP);
-      uint32_t it = 0, sidx = 0;
+      // key tiles each query tile can see (0 for a tile wholly past N_Q): only those
+      // count as visited (query tile, key tile) pairs
+      int nkt_g[NGROUP];
+      for (int g = 0; g < NGROUP; ++g)
+        nkt_g[g] = (q0 + g * BM < s.NQ) ? last_key_of(q0 + (g + 1) * BM) / BN + 1 : 0;
+      uint32_t pos = 0;               // ring position (K and V tiles in producer order)
+      uint32_t sc[NGROUP] = {0, 0};   // S products issued per query tile
       unsigned long long visited = 0, skipped = 0;
-      bool o_started = false;
-      auto mma_s = [&]() -> bool {   // S[sidx & 1] = Q K^T, K from ring slot `it`
-        const int st = it % NST;
-        const uint32_t par = (it / NST) & 1u;
-        const int sb = sidx & 1;
-        const uint32_t spar = (sidx >> 1) & 1u;
-        if (!mbar_wait(&ring_full[st], par, abort_flag, ctx)) return false;
-        if (!mbar_wait(&s_empty[sb], spar ^ 1u, abort_flag, ctx)) return false;
+      bool o_started[NGROUP] = {false, false};
+      auto ring_wait = [&](uint32_t p, uint32_t& addr) -> bool {
+        const int st = p % NST;
+        if (!mbar_wait(&ring_full[st], (p / NST) & 1u, abort_flag, ctx)) return false;
         tc_fence_after();
-        const uint32_t kaddr = sRa + st * C::TILE_BYTES;
-        const uint32_t dcol = tmem + (sb ? TMEM_S1 : TMEM_S0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          tc_mma_f16(dcol, smem_desc_sw128(sQa + off, 16, 1024), smem_desc_sw128(kaddr + off, 16, 1024),
-                     idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&ring_empty[st]);
-        tc_commit(&s_full[sb]);
-        ++it;
-        ++sidx;
+        addr = sRa + st * C::TILE_BYTES;
         return true;
       };
-      auto mma_pv = [&](int t) -> bool {   // O += P_t V_t, V from ring slot `it`
-        const int pb = t & 1;
-        const uint32_t ppar = (t >> 1) & 1u;
-        const int st = it % NST;
-        if (!mbar_wait(&p_full[pb], ppar, abort_flag, ctx)) return false;
-        if (!mbar_wait(&ring_full[st], (it / NST) & 1u, abort_flag, ctx)) return false;
+      // descriptors as (low word + offset / 16, constant high word): one add per operand
+      constexpr uint32_t HI = sdesc_hi_sw128(1024);
+      const uint32_t q_lo = sdesc_lo(sQa, 16), p_lo = sdesc_lo(sPa, 16);
+      auto mma_s = [&](int g, uint32_t kaddr) -> bool {   // S_g = Q_g K^T
+        if (!mbar_wait(&s_empty[g], (sc[g] & 1u) ^ 1u, abort_flag, ctx)) return false;
+        tc_fence_after();
+        const uint32_t qlo = q_lo + g * (C::TILE_BYTES >> 4);
+        const uint32_t klo = sdesc_lo(kaddr, 16);
+        const uint32_t dcol = tmem + TMEM_S + g * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+          tc_mma_f16(dcol, sdesc(qlo + off, HI), sdesc(klo + off, HI), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[g]);
+        ++sc[g];
+        return true;
+      };
+      auto mma_pv = [&](int g, int j, uint32_t vaddr) -> bool {   // O_g += P_g V_j
+        if (!mbar_wait(&p_full[g], j & 1u, abort_flag, ctx)) return false;
         tc_fence_after();
         int any = 0;
 #pragma unroll
-        for (int w = 0; w < SOFTMAX_WARPS; ++w) any |= live[pb * SOFTMAX_WARPS + w];
-        const bool is_live = any != 0;
-        ++visited;
-        if (is_live) {
-          const uint32_t vaddr = sRa + st * C::TILE_BYTES;
-          const uint32_t paddr = sPa + pb * C::P_BYTES;
+        for (int w = 0; w < GROUP_WARPS; ++w) any |= live[g * GROUP_WARPS + w];
+        if (j < nkt_g[g]) {
+          ++visited;
+          if (any == 0) ++skipped;
+        }
+        if (any != 0) {
+          const uint32_t plo = p_lo + g * (C::P_BYTES >> 4);
+          const uint32_t vlo = sdesc_lo(vaddr, BOX_BYTES);
+          const uint32_t dcol = tmem + TMEM_O + g * 128;
+          const uint32_t acc0 = o_started[g] ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;   // P: K-major, 16 keys = 32 B
-            const uint32_t boff = kk * 16 * 128;                            // V: MN-major, 16 key rows
-            tc_mma_f16(tmem + TMEM_O, smem_desc_sw128(paddr + aoff, 16, 1024),
-                       smem_desc_sw128(vaddr + boff, BOX_BYTES, 1024), idesc_pv,
-                       (o_started || kk > 0) ? 1u : 0u);
+            const uint32_t aoff = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;   // P: K-major, 16 keys = 32 B
+            const uint32_t boff = (kk * 16 * 128) >> 4;                            // V: MN-major, 16 key rows
+            tc_mma_f16(dcol, sdesc(plo + aoff, HI), sdesc(vlo + boff, HI), idesc_pv, kk > 0 ? 1u : acc0);
           }
-          o_started = true;
-        } else {
-          ++skipped;
+          o_started[g] = true;
         }
-        tc_commit(&ring_empty[st]);
-        tc_commit(&p_empty[pb]);
-        ++it;
+        tc_commit(&p_empty[g]);
         return true;
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, ctx);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
       if (ok && ctx.force_timeout) ok = mbar_wait(drain, 0, abort_flag, ctx);
-      for (int j = 0; j < nkt && ok; ++j) ok = mma_s();   // pass 1
-      if (ok) ok = mma_s();                                // pass 2
-      for (int j = 1; j < nkt && ok; ++j) {
-        ok = mma_s();
-        if (ok) ok = mma_pv(j - 1);
+      uint32_t ka = 0, va = 0;
+      // pass 1: S_A(j), S_B(j) from one K tile
+      for (int j = 0; j < nkt && ok; ++j) {
+        ok = ring_wait(pos, ka);
+        for (int g = 0; g < NGROUP && ok; ++g) ok = mma_s(g, ka);
+        if (ok) tc_commit(&ring_empty[pos % NST]);
+        ++pos;
       }
-      if (ok) ok = mma_pv(nkt - 1);
+      // pass 2: S_A(0), S_B(0); then per j: S_A(j+1), O_A(j), S_B(j+1), O_B(j)
+      if (ok) ok = ring_wait(pos, ka);
+      for (int g = 0; g < NGROUP && ok; ++g) ok = mma_s(g, ka);
+      if (ok) tc_commit(&ring_empty[pos % NST]);
+      ++pos;
+      for (int j = 0; j < nkt && ok; ++j) {
+        const bool more = j + 1 < nkt;
+        uint32_t kpos = 0;
+        if (more) {
+          kpos = pos++;
+          ok = ring_wait(kpos, ka);
+          if (ok) ok = mma_s(0, ka);
+        }
+        const uint32_t vpos = pos++;
+        if (ok) ok = ring_wait(vpos, va);
+        if (ok) ok = mma_pv(0, j, va);
+        if (more && ok) {
+          for (int g = 1; g < NGROUP && ok; ++g) ok = mma_s(g, ka);
+          if (ok) tc_commit(&ring_empty[kpos % NST]);
+        }
+        for (int g = 1; g < NGROUP && ok; ++g) ok = mma_pv(g, j, va);
+        if (ok) tc_commit(&ring_empty[vpos % NST]);
+      }
       if (ok) tc_commit(o_full);
       tc_commit(drain);
       drain_wait(drain, 0, ctx);
@@ -322,31 +398,32 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------------ softmax warps
-    // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key columns
-    // [WCOLS (w / 4), WCOLS (w / 4) + WCOLS) of every tile; the row maximum, its argmax
-    // and the row sum are combined across the NPART parts through shared memory.
-    const int quarter = warp & 3;
-    const int part = warp >> 2;
-    const int cbase = part * WCOLS;
+    // ------------------------------------------------------------------ softmax warpgroups
+    // Warp w serves query tile g = w / 4 and TMEM lanes 32 (w % 4) .. + 31 (its rows).
+    const int g = warp / GROUP_WARPS;
+    const int quarter = warp % GROUP_WARPS;
     const int row_local = quarter * 32 + lane;   // TMEM lane
-    const int row = q0 + row_local;
+    const int row = q0 + g * BM + row_local;
     const int lim = s.causal ? min(row, s.NK - 1) : s.NK - 1;   // last key this row may see
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* xf = reinterpret_cast<float*>(smem + C::OFF_XCH);              // [NPART][BM]
-    int* xi = reinterpret_cast<int*>(smem + C::OFF_XCH + NPART * BM * 4);  // [NPART][BM]
-    auto group_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(32 * SOFTMAX_WARPS) : "memory"); };
+    const uint32_t scol = lane_addr + TMEM_S + g * 128;
     auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
       int r = 1;
       if (lane == 0) r = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
-    uint32_t sv[WCOLS / 32][32];
-    auto load_s = [&](int sb) {
-      const uint32_t col = lane_addr + (sb ? TMEM_S1 : TMEM_S0) + cbase;
+    uint32_t sv[BN / 32][32];
+    // S_g into registers, then hand the buffer back to the MMA thread
+    auto take_s = [&](uint32_t idx) -> bool {
+      if (!warp_wait(&s_full[g], idx & 1u)) return false;
+      tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < WCOLS / 32; ++k) tmem_ld32(col + 32 * k, sv[k]);
+      for (int k = 0; k < BN / 32; ++k) tmem_ld32(scol + 32 * k, sv[k]);
       tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[g]);
+      return true;
     };
 #define SV(c) u2f(sv[(c) >> 5][(c) & 31])
 
@@ -354,115 +431,105 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t sidx = 0;
     float m = -INFINITY;
     int a = -1;
-    // pass 1: running maximum of the raw scores q.k over this part's columns (scale > 0
-    // keeps the argmax)
+    int jm = 0;   // 32-column chunk (tile * 4 + chunk) holding the first occurrence of the maximum
+    // pass 1: running maximum of the raw scores q.k (scale > 0 keeps the argmax)
     for (int j = 0; j < nkt && ok; ++j) {
-      const int sb = sidx & 1;
-      const uint32_t spar = (sidx >> 1) & 1u;
-      ok = warp_wait(&s_full[sb], spar);
+      ok = take_s(sidx++);
       if (!ok) break;
-      tc_fence_after();
-      load_s(sb);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[sb]);
-      ++sidx;
-      const int col0 = j * BN + cbase;   // key index of local column 0
-      const bool need_mask = col0 + WCOLS - 1 > lim;
-      float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
-      if (!need_mask) {
+      const int col0 = j * BN;   // key index of column 0
+      // maximum of each 32-column chunk; the first chunk (in key order) that raises the
+      // running maximum strictly is remembered, so ties keep the lowest index
+      float cm[BN / 32];
+      if (col0 + BN - 1 <= lim) {
 #pragma unroll
-        for (int c = 0; c < WCOLS; c += 8) {
-          t0 = max3f(t0, SV(c), SV(c + 1));
-          t1 = max3f(t1, SV(c + 2), SV(c + 3));
-          t2 = max3f(t2, SV(c + 4), SV(c + 5));
-          t3 = max3f(t3, SV(c + 6), SV(c + 7));
+        for (int k = 0; k < BN / 32; ++k) {
+          float u0 = -INFINITY, u1 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            u0 = max3f(u0, u2f(sv[k][c]), u2f(sv[k][c + 1]));
+            u1 = max3f(u1, u2f(sv[k][c + 2]), u2f(sv[k][c + 3]));
+          }
+          cm[k] = fmaxf(u0, u1);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < WCOLS; ++c) {
-          const float x = (col0 + c <= lim) ? SV(c) : -INFINITY;
-          if ((c & 3) == 0) t0 = fmaxf(t0, x);
-          if ((c & 3) == 1) t1 = fmaxf(t1, x);
-          if ((c & 3) == 2) t2 = fmaxf(t2, x);
-          if ((c & 3) == 3) t3 = fmaxf(t3, x);
+        for (int k = 0; k < BN / 32; ++k) {
+          float u0 = -INFINITY, u1 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            u0 = fmaxf(u0, (col0 + 32 * k + c <= lim) ? u2f(sv[k][c]) : -INFINITY);
+            u1 = fmaxf(u1, (col0 + 32 * k + c + 1 <= lim) ? u2f(sv[k][c + 1]) : -INFINITY);
+          }
+          cm[k] = fmaxf(u0, u1);
         }
       }
-      const float tmax = fmaxf(fmaxf(t0, t1), fmaxf(t2, t3));
-      if (tmax > m) {   // strictly greater: an earlier tile keeps ties (lowest index)
-        int idx = WCOLS;
 #pragma unroll
-        for (int c = WCOLS - 1; c >= 0; --c)
-          if (SV(c) == tmax && col0 + c <= lim) idx = c;
-        m = tmax;
-        a = col0 + idx;
+      for (int k = 0; k < BN / 32; ++k) {
+        jm = (cm[k] > m) ? (j * (BN / 32) + k) : jm;
+        m = fmaxf(m, cm[k]);
       }
     }
-    // combine the parts (reached by every softmax warp, also after a wait gave up): the
-    // maximum, and among the parts that attain it the lowest index
-    xf[part * BM + row_local] = m;
-    xi[part * BM + row_local] = a;
-    group_sync();
-    m = xf[row_local];
-#pragma unroll
-    for (int p = 1; p < NPART; ++p) m = fmaxf(m, xf[p * BM + row_local]);
-    a = -1;
-#pragma unroll
-    for (int p = 0; p < NPART; ++p) {
-      const int ap = xi[p * BM + row_local];
-      if (xf[p * BM + row_local] == m && ap >= 0 && (a < 0 || ap < a)) a = ap;
-    }
-    group_sync();   // xf is reused for the row sum
 
-    // pass 2: phi, sum(phi), P tiles
+    // pass 2: phi, sum(phi), P tiles.  Per tile: the first 64 columns are loaded and their
+    // phi formed in registers; the second 64 columns are loaded and the score buffer handed
+    // back; then, once the previous product has released the P tile, both halves are stored.
     const float m_sc = m * s.scale;
     const float c2 = s.scale * (1.0f / 32.0f);
     const float base = fmaf(m_sc, 1.0f / 32.0f, 0.5f);
+    uint8_t* prow = sP + g * C::P_BYTES + row_local * 128;
     float rowsum = 0.0f;
     for (int j = 0; j < nkt && ok; ++j) {
-      const int sb = sidx & 1;
-      const uint32_t spar = (sidx >> 1) & 1u;
-      ok = warp_wait(&s_full[sb], spar);
+      ok = warp_wait(&s_full[g], sidx & 1u);
       if (!ok) break;
+      ++sidx;
       tc_fence_after();
-      load_s(sb);
+      const int col0 = j * BN;
+      const bool masked = col0 + BN - 1 > lim;
+      const bool arg_tile = j == (jm >> 2);
+      uint32_t h[2][32];
+      tmem_ld32(scol, h[0]);
+      tmem_ld32(scol + 32, h[1]);
+      tc_wait_ld();
+      if (arg_tile && (jm & 3) < 2)   // lowest visible column holding the maximum
+        a = col0 + ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 32, lim) : find_in_chunk(h[0], m, col0, lim));
+      uint32_t pk[32];
+      float2 tsum2 = masked ? phi_half<true>(h, pk, col0, lim, c2, base)
+                            : phi_half<false>(h, pk, col0, lim, c2, base);
+      tmem_ld32(scol + 64, h[0]);
+      tmem_ld32(scol + 96, h[1]);
+      tc_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[sb]);
-      ++sidx;
-      const int col0 = j * BN + cbase;
-      const bool need_mask = col0 + WCOLS - 1 > lim;
-      const int pb = j & 1;
-      ok = warp_wait(&p_empty[pb], ((j >> 1) & 1u) ^ 1u);
+      if (lane == 0) mbar_arrive(&s_empty[g]);
+      if (arg_tile && (jm & 3) >= 2)
+        a = col0 + 64 +
+            ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 96, lim) : find_in_chunk(h[0], m, col0 + 64, lim));
+      // the P tile is free once the previous O_g += P_g V product has completed
+      ok = warp_wait(&p_empty[g], (j & 1u) ^ 1u);
       if (!ok) break;
-      uint8_t* prow = sP + pb * C::P_BYTES + row_local * 128;
-      const float2 tsum2 = need_mask ? pass2_part_tile<true>(sv, prow, row_local, cbase, col0, lim, c2, base)
-                                     : pass2_part_tile<false>(sv, prow, row_local, cbase, col0, lim, c2, base);
+      store_p_half(pk, prow, row_local);
+      const float2 t2 = masked ? phi_store_half<true>(h, prow + BOX_BYTES, row_local, col0 + 64, lim, c2, base)
+                               : phi_store_half<false>(h, prow + BOX_BYTES, row_local, col0 + 64, lim, c2, base);
+      tsum2 = __fadd2_rn(tsum2, t2);
       fence_proxy_async_smem();
       const float tsum = tsum2.x + tsum2.y;
       const unsigned any_live = __any_sync(0xffffffffu, tsum > 0.0f);
-      if (lane == 0) live[pb * SOFTMAX_WARPS + warp] = any_live ? 1 : 0;
+      if (lane == 0) live[g * GROUP_WARPS + quarter] = any_live ? 1 : 0;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[pb]);
+      if (lane == 0) mbar_arrive(&p_full[g]);
       rowsum += tsum;
     }
 #undef SV
-    xf[part * BM + row_local] = rowsum;
-    group_sync();
-    rowsum = xf[row_local];
-#pragma unroll
-    for (int p = 1; p < NPART; ++p) rowsum += xf[p * BM + row_local];
     if (ok) ok = warp_wait(o_full, 0);
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < s.NQ;
       const float inv = 1.0f / rowsum;
       const size_t ro = static_cast<size_t>(bh) * s.NQ + (row_ok ? row : 0);
-      // the parts store 32-column slices of the D output columns of their rows
 #pragma unroll
-      for (int c0 = part * 32; c0 < D; c0 += NPART * 32) {
+      for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ov[32];
-        tmem_ld32(lane_addr + TMEM_O + c0, ov);
+        tmem_ld32(lane_addr + TMEM_O + g * 128 + c0, ov);
         tc_wait_ld();
         if (row_ok) {
           if (args.out_bf16) {
@@ -485,7 +552,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (row_ok && part == 0) {
+      if (row_ok) {
         if (args.row_m) args.row_m[ro] = m_sc;
         if (args.row_s) args.row_s[ro] = rowsum;
         if (args.row_arg) args.row_arg[ro] = a;
@@ -509,7 +576,8 @@ cudaError_t launch_fwd_d(const AttnShape& s, const FwdTcArgs& a, const LaunchCtx
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int nqt = (s.NQ + BM - 1) / BM;
-  const unsigned grid = static_cast<unsigned>(nqt) * static_cast<unsigned>(s.B * s.H);
+  const int nct = (nqt + NGROUP - 1) / NGROUP;
+  const unsigned grid = static_cast<unsigned>(nct) * static_cast<unsigned>(s.B * s.H);
   attn_fwd_tc_kernel<D><<<grid, THREADS, C::SMEM_BYTES, st>>>(s, a, ctx);
   return cudaGetLastError();
 }
@@ -521,5 +589,6 @@ cudaError_t launch_attn_fwd_tc(const AttnShape& s, const FwdTcArgs& a, const Lau
   if (s.D == 64) return launch_fwd_d<64>(s, a, ctx, st);
   return cudaErrorInvalidValue;
 }
+
 
 }  // namespace raattn

@@ -128,6 +128,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// Bring one box of a tensor map into L2 ahead of its load (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0), "r"(c1),
+               "r"(c2)
+               : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (tensor core reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -201,6 +208,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= 1ull << 46;            // descriptor version for tcgen05
   d |= 2ull << 61;            // swizzle mode: 128-byte
   return d;
+}
+
+// The same descriptor as two 32-bit words.  The start address sits in bits [0, 14) of
+// the low word, so adding (offset >> 4) to the low word moves the start by `offset` bytes
+// (no carry into the leading-offset field while the address stays below 256 KB, which
+// holds for every shared-memory address): one integer add per MMA operand.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);   // SBO, version 1, 128-byte swizzle
+}
+__device__ __forceinline__ uint64_t sdesc(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Instruction descriptor for kind::f16 with fp32 accumulator; A and B share one
