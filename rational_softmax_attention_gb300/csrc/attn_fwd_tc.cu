@@ -19,15 +19,17 @@
 //   warp 8      TMA producer: Q_A and Q_B once, then K tiles (pass 1), then K and V
 //               tiles interleaved in the order the MMA thread consumes them (pass 2),
 //               through a ring of NSTAGE shared-memory stages.
-//   warp 9      MMA issuer (one thread): S_A = Q_A K^T and S_B = Q_B K^T into two
-//               TMEM score buffers (128 x 128 fp32 each); in pass 2 also
-//               O_A += P_A V and O_B += P_B V into two TMEM accumulators (128 x D fp32),
-//               issued as S_A(j+1), O_A(j), S_B(j+1), O_B(j) so that each softmax
-//               warpgroup has three products' time to turn S(j+1) into P(j+1).
+//   warps 9, 10 MMA issuers, one thread per query tile g: S_g = Q_g K^T into its TMEM
+//               score buffer (128 x 128 fp32); in pass 2 also O_g += P_g V into its TMEM
+//               accumulator (128 x D fp32), issued as S_g(j+1) then O_g(j) so the softmax
+//               warpgroup works on S_g(j+1) while O_g(j) runs.  Each issuer waits on its
+//               own barriers; a wait stalls the issuing thread for a few hundred cycles,
+//               longer than the two 64-cycle products the tensor queue holds, and with two
+//               issuers the other tile's products keep the tensor core busy meanwhile.
 //   warps 0-3   softmax warpgroup of query tile A, warps 4-7 that of tile B; thread t of
 //               a warpgroup owns query row t (TMEM lane t) and all 128 key columns:
-//               pass 1 keeps the running max of the raw scores and the tile of its first
-//               occurrence, pass 2 the lowest column holding it in that tile;
+//               pass 1 keeps the running max of the raw scores and the 32-column chunk
+//               of its first occurrence, pass 2 the lowest column holding it there;
 //               pass 2 forms phi on the FMA pipe (no exp), writes P = fp16(phi) into
 //               its 128-byte-swizzled shared-memory tile, sums phi in fp32, and votes
 //               whether the tile is live.  Epilogue: O = acc / sum(phi) and the row
@@ -38,10 +40,11 @@
 //
 // phi on the FMA pipe: w = (1+u)/2 = 0.5 + (m - s)/32 (scaled units) computed with
 // one saturating FMA, so every u >= 1 (and every masked entry, fed as -inf) gives
-// w = 1; q = 1/w - 1; phi = ((q^2)^2)^2.  The reciprocals are taken two at a
-// time from one rcp.approx of w0*w1 (then 1/w0 = R w1, 1/w1 = R w0), halving the
-// special-function-unit work, and the rest runs as packed f32x2 operations.
-// At w = 1 the computed q is below 3e-7, so phi rounds to exactly 0.0.
+// w = 1; q = 1/w - 1; phi = ((q^2)^2)^2.  Four scores share two reciprocals: with the
+// pairs A = (w0, w1), B = (w2, w3), R = 1/(A B) elementwise gives R B = (1/w0, 1/w1)
+// and R A = (1/w2, 1/w3), halving the special-function-unit work, and the rest runs
+// as packed f32x2 operations.  At w = 1 the computed q is below 3e-7, so phi rounds to
+// exactly 0.0.
 #include "kernels.cuh"
 
 namespace raattn {
@@ -53,8 +56,8 @@ constexpr int NGROUP = 2;                            // query tiles per CTA
 constexpr int GROUP_WARPS = 4;                       // one warpgroup per query tile
 constexpr int SOFTMAX_WARPS = NGROUP * GROUP_WARPS;  // 8
 constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
-constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
-constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+constexpr int MMA_WARP = SOFTMAX_WARPS + 1;          // MMA_WARP + g issues the products of query tile g
+constexpr int THREADS = 32 * (SOFTMAX_WARPS + 1 + NGROUP);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S = 0;     // S of query tile g at column 128 g
 constexpr uint32_t TMEM_O = 256;   // O of query tile g at column 256 + 128 g
@@ -71,8 +74,9 @@ struct FwdCfg {
   static constexpr int OFF_RING = OFF_Q + NGROUP * TILE_BYTES;
   static constexpr int OFF_P = OFF_RING + NSTAGE * TILE_BYTES;   // P_A, P_B
   static constexpr int OFF_BAR = OFF_P + NGROUP * P_BYTES;
-  // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain
-  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 4 * NGROUP + 2;
+  // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2],
+  // drain[2]
+  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 6 * NGROUP;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int MISC_BYTES = 16 + SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes
   static constexpr int USED = OFF_MISC + MISC_BYTES;
@@ -184,8 +188,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* s_empty = s_full + NGROUP;
   uint64_t* p_full = s_empty + NGROUP;
   uint64_t* p_empty = p_full + NGROUP;
-  uint64_t* o_full = p_empty + NGROUP;
-  uint64_t* drain = o_full + 1;
+  uint64_t* o_full = p_empty + NGROUP;   // [NGROUP]
+  uint64_t* drain = o_full + NGROUP;     // [NGROUP]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);   // [NGROUP][GROUP_WARPS]
@@ -210,16 +214,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < NST; ++i) {
       mbar_init(&ring_full[i], 1);
-      mbar_init(&ring_empty[i], 1);
+      mbar_init(&ring_empty[i], NGROUP);   // one commit per issuer
     }
     for (int g = 0; g < NGROUP; ++g) {
       mbar_init(&s_full[g], 1);
       mbar_init(&s_empty[g], GROUP_WARPS);   // one arrival per warp of the group
       mbar_init(&p_full[g], GROUP_WARPS);
       mbar_init(&p_empty[g], 1);
+      mbar_init(&o_full[g], 1);
+      mbar_init(&drain[g], 1);
     }
-    mbar_init(o_full, 1);
-    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -264,21 +268,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++it;
         return true;
       };
-      // All CTAs of a head walk its key tiles in step, so the first touch of each K and
-      // V tile would expose a full DRAM miss to every one of them: pass 1 prefetches K
-      // KPF tiles ahead of its loads into L2, and every V tile for pass 2.
-      constexpr int KPF = 4;
-      auto prefetch = [&](const CUtensorMap* map, int j) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_3d(map, c * 64, j * BN, bh);
-      };
-      for (int j = 0; j < KPF && j < nkt; ++j) prefetch(&args.tm_k, j);
       bool ok = true;
-      for (int j = 0; j < nkt && ok; ++j) {                                  // pass 1: K_0 .. K_{n-1}
-        if (j + KPF < nkt) prefetch(&args.tm_k, j + KPF);
-        prefetch(&args.tm_v, j);
-        ok = issue(&args.tm_k, j);
-      }
+      for (int j = 0; j < nkt && ok; ++j) ok = issue(&args.tm_k, j);         // pass 1: K_0 .. K_{n-1}
       if (ok) ok = issue(&args.tm_k, 0);                                     // pass 2: K_0, then
       for (int j = 1; j < nkt && ok; ++j) {                                  //   K_j, V_{j-1}
         ok = issue(&args.tm_k, j);
@@ -289,21 +280,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int i = 0; i < NST; ++i)
         if (issued[i]) drain_wait(&ring_full[i], last_par[i], ctx);
     }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp >= MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuers
+    // One thread per query tile g issues S_g and O_g products and does its own waits:
+    // a wait costs the issuing thread a few hundred cycles, and with two issuers the
+    // tensor core runs the other tile's queued products meanwhile.
+    const int g = warp - MMA_WARP;
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_fp16_f32(BM, D, 0, 1);   // P and V in fp16
-      const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sRing), sPa = smem_u32(sP);
-      // key tiles each query tile can see (0 for a tile wholly past N_Q): only those
+      const uint32_t sRa = smem_u32(sRing);
+      // descriptors as (low word + offset / 16, constant high word): one add per operand
+      constexpr uint32_t HI = sdesc_hi_sw128(1024);
+      const uint32_t qlo = sdesc_lo(smem_u32(sQ) + g * C::TILE_BYTES, 16);
+      const uint32_t plo = sdesc_lo(smem_u32(sP) + g * C::P_BYTES, 16);
+      const uint32_t scol = tmem + TMEM_S + g * 128;
+      const uint32_t ocol = tmem + TMEM_O + g * 128;
+      // key tiles this query tile can see (0 for a tile wholly past N_Q): only those
       // count as visited (query tile, key tile) pairs
-      int nkt_g[NGROUP];
-      for (int g = 0; g < NGROUP; ++g)
-        nkt_g[g] = (q0 + g * BM < s.NQ) ? last_key_of(q0 + (g + 1) * BM) / BN + 1 : 0;
-      uint32_t pos = 0;               // ring position (K and V tiles in producer order)
-      uint32_t sc[NGROUP] = {0, 0};   // S products issued per query tile
+      const int nkt_g = (q0 + g * BM < s.NQ) ? last_key_of(q0 + (g + 1) * BM) / BN + 1 : 0;
+      uint32_t pos = 0;   // ring position (K and V tiles in producer order)
+      uint32_t sc = 0;    // S products issued
       unsigned long long visited = 0, skipped = 0;
-      bool o_started[NGROUP] = {false, false};
+      bool o_started = false;
       auto ring_wait = [&](uint32_t p, uint32_t& addr) -> bool {
         const int st = p % NST;
         if (!mbar_wait(&ring_full[st], (p / NST) & 1u, abort_flag, ctx)) return false;
@@ -311,64 +310,57 @@ __global__ void __launch_bounds__(THREADS, 1)
         addr = sRa + st * C::TILE_BYTES;
         return true;
       };
-      // descriptors as (low word + offset / 16, constant high word): one add per operand
-      constexpr uint32_t HI = sdesc_hi_sw128(1024);
-      const uint32_t q_lo = sdesc_lo(sQa, 16), p_lo = sdesc_lo(sPa, 16);
-      auto mma_s = [&](int g, uint32_t kaddr) -> bool {   // S_g = Q_g K^T
-        if (!mbar_wait(&s_empty[g], (sc[g] & 1u) ^ 1u, abort_flag, ctx)) return false;
+      auto mma_s = [&](uint32_t kaddr) -> bool {   // S_g = Q_g K^T
+        if (!mbar_wait(&s_empty[g], (sc & 1u) ^ 1u, abort_flag, ctx)) return false;
         tc_fence_after();
-        const uint32_t qlo = q_lo + g * (C::TILE_BYTES >> 4);
         const uint32_t klo = sdesc_lo(kaddr, 16);
-        const uint32_t dcol = tmem + TMEM_S + g * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
-          tc_mma_f16(dcol, sdesc(qlo + off, HI), sdesc(klo + off, HI), idesc_qk, kk > 0 ? 1u : 0u);
+          tc_mma_f16(scol, sdesc(qlo + off, HI), sdesc(klo + off, HI), idesc_qk, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[g]);
-        ++sc[g];
+        ++sc;
         return true;
       };
-      auto mma_pv = [&](int g, int j, uint32_t vaddr) -> bool {   // O_g += P_g V_j
+      auto mma_pv = [&](int j, uint32_t vaddr) -> bool {   // O_g += P_g V_j
         if (!mbar_wait(&p_full[g], j & 1u, abort_flag, ctx)) return false;
         tc_fence_after();
         int any = 0;
 #pragma unroll
-        for (int w = 0; w < GROUP_WARPS; ++w) any |= live[g * GROUP_WARPS + w];
-        if (j < nkt_g[g]) {
+        for (int w = 0; w < GROUP_WARPS; ++w) any |= live[g * GROUP_WARPS + w];   // warps of tile g
+        if (j < nkt_g) {
           ++visited;
           if (any == 0) ++skipped;
         }
         if (any != 0) {
-          const uint32_t plo = p_lo + g * (C::P_BYTES >> 4);
           const uint32_t vlo = sdesc_lo(vaddr, BOX_BYTES);
-          const uint32_t dcol = tmem + TMEM_O + g * 128;
-          const uint32_t acc0 = o_started[g] ? 1u : 0u;
+          const uint32_t acc0 = o_started ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint32_t aoff = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;   // P: K-major, 16 keys = 32 B
             const uint32_t boff = (kk * 16 * 128) >> 4;                            // V: MN-major, 16 key rows
-            tc_mma_f16(dcol, sdesc(plo + aoff, HI), sdesc(vlo + boff, HI), idesc_pv, kk > 0 ? 1u : acc0);
+            tc_mma_f16(ocol, sdesc(plo + aoff, HI), sdesc(vlo + boff, HI), idesc_pv, kk > 0 ? 1u : acc0);
           }
-          o_started[g] = true;
+          o_started = true;
         }
         tc_commit(&p_empty[g]);
         return true;
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, ctx);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
-      if (ok && ctx.force_timeout) ok = mbar_wait(drain, 0, abort_flag, ctx);
+      if (ok && ctx.force_timeout) ok = mbar_wait(&drain[g], 0, abort_flag, ctx);
       uint32_t ka = 0, va = 0;
-      // pass 1: S_A(j), S_B(j) from one K tile
+      // pass 1: S_g(j) for every key tile; a ring stage is free once both issuers commit
       for (int j = 0; j < nkt && ok; ++j) {
         ok = ring_wait(pos, ka);
-        for (int g = 0; g < NGROUP && ok; ++g) ok = mma_s(g, ka);
+        if (ok) ok = mma_s(ka);
         if (ok) tc_commit(&ring_empty[pos % NST]);
         ++pos;
       }
-      // pass 2: S_A(0), S_B(0); then per j: S_A(j+1), O_A(j), S_B(j+1), O_B(j)
+      // pass 2: S_g(0); then per j: S_g(j+1), O_g(j)
       if (ok) ok = ring_wait(pos, ka);
-      for (int g = 0; g < NGROUP && ok; ++g) ok = mma_s(g, ka);
+      if (ok) ok = mma_s(ka);
       if (ok) tc_commit(&ring_empty[pos % NST]);
       ++pos;
       for (int j = 0; j < nkt && ok; ++j) {
@@ -377,21 +369,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (more) {
           kpos = pos++;
           ok = ring_wait(kpos, ka);
-          if (ok) ok = mma_s(0, ka);
+          if (ok) ok = mma_s(ka);
+          if (ok) tc_commit(&ring_empty[kpos % NST]);
         }
         const uint32_t vpos = pos++;
         if (ok) ok = ring_wait(vpos, va);
-        if (ok) ok = mma_pv(0, j, va);
-        if (more && ok) {
-          for (int g = 1; g < NGROUP && ok; ++g) ok = mma_s(g, ka);
-          if (ok) tc_commit(&ring_empty[kpos % NST]);
-        }
-        for (int g = 1; g < NGROUP && ok; ++g) ok = mma_pv(g, j, va);
+        if (ok) ok = mma_pv(j, va);
         if (ok) tc_commit(&ring_empty[vpos % NST]);
       }
-      if (ok) tc_commit(o_full);
-      tc_commit(drain);
-      drain_wait(drain, 0, ctx);
+      if (ok) tc_commit(&o_full[g]);
+      tc_commit(&drain[g]);
+      drain_wait(&drain[g], 0, ctx);
       if (ok && args.tile_counts) {
         atomicAdd(&args.tile_counts[0], visited);
         atomicAdd(&args.tile_counts[1], skipped);
@@ -520,7 +508,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       rowsum += tsum;
     }
 #undef SV
-    if (ok) ok = warp_wait(o_full, 0);
+    if (ok) ok = warp_wait(&o_full[g], 0);
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < s.NQ;

@@ -128,13 +128,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
-// Bring one box of a tensor map into L2 ahead of its load (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0), "r"(c1),
-               "r"(c2)
-               : "memory");
-}
-
 // Make generic-proxy writes to shared memory visible to the async proxy (tensor core reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
