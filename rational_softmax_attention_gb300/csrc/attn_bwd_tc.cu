@@ -101,8 +101,8 @@ struct DqCfg {
   static constexpr int OFF_E = OFF_V + NVS * TILE;
   static constexpr int OFF_BAR = OFF_E + E_BYTES;
   // qdo_full, k_full[NKS], k_empty[NKS], v_full[NVS], v_empty[NVS], s_full[2], s_free[2],
-  // dp_full, dp_free, e_full, e_free, dq_full, drain
-  static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 4 + 6;
+  // dp_full, dp_free, e_full, e_free, dq_full, drain[2]
+  static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 4 + 7;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_XCH = OFF_MISC + 16;   // [2][128] floats: per-half partials of D_i, then R_i
   static constexpr int SMEM_BYTES = OFF_XCH + 2 * BM * 4 + 1024;
@@ -112,8 +112,11 @@ constexpr uint32_t DQ_TM_S0 = 0, DQ_TM_S1 = 128, DQ_TM_DP = 256, DQ_TM_DQ = 384;
 // rows) and split each key tile's 128 columns 64 / 64, two warps per scheduler.
 constexpr int DQ_SOFTMAX_WARPS = 8;
 constexpr int DQ_PRODUCER_WARP = 8;
+// two MMA-issuing threads: warp 9 issues S and dP, warp 10 issues dQ.  A barrier wait
+// stalls its issuing thread for a few hundred cycles, longer than the two 64-cycle
+// products the tensor queue holds; the other issuer's products fill that time.
 constexpr int DQ_MMA_WARP = 9;
-constexpr int DQ_THREADS = 320;
+constexpr int DQ_THREADS = 352;
 
 __device__ __forceinline__ void softmax8_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -141,7 +144,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint64_t* e_full = dp_free + 1;
   uint64_t* e_free = e_full + 1;
   uint64_t* dq_full = e_free + 1;
-  uint64_t* drain = dq_full + 1;
+  uint64_t* drain = dq_full + 1;   // [2], one per issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     mbar_init(qdo_full, 1);
     for (int i = 0; i < C::NKS; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
+      mbar_init(&k_empty[i], 2);   // S_j (issuer 0) and dQ_j (issuer 1) both read K_j
     }
     for (int i = 0; i < C::NVS; ++i) {
       mbar_init(&v_full[i], 1);
@@ -176,7 +179,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     mbar_init(e_full, DQ_SOFTMAX_WARPS);
     mbar_init(e_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -228,61 +232,69 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       for (int j = max(0, v_issued - C::NVS); j < v_issued; ++j)
         drain_wait(&v_full[j % C::NVS], (j / C::NVS) & 1u, ctx);
     }
-  } else if (warp == DQ_MMA_WARP) {
+  } else if (warp >= DQ_MMA_WARP) {
+    const int who = warp - DQ_MMA_WARP;   // 0: S and dP products; 1: dQ products
     if (lane == 0) {
       constexpr uint32_t idesc_ss = idesc_fp16_f32(BM, BN, 0, 0);
       constexpr uint32_t idesc_kmn = idesc_fp16_f32(BM, D, 0, 1);
-      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aK = smem_u32(sK), aV = smem_u32(sV),
-                     aE = smem_u32(sE);
-      auto do_dq = [&](int t) -> bool {   // dQ += E_t K_t
-        if (!mbar_wait(e_full, t & 1u, abort_flag, ctx)) return false;
-        tc_fence_after();
-        const uint32_t kaddr = aK + (t % C::NKS) * C::TILE;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          tc_mma_f16(tmem + DQ_TM_DQ, smem_desc_sw128(aE + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024),
-                     smem_desc_sw128(kaddr + kk * 2048, BOX_BYTES, 1024), idesc_kmn, (t > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&k_empty[t % C::NKS]);
-        tc_commit(e_free);
-        return true;
-      };
+      constexpr uint32_t HI = sdesc_hi_sw128(1024);
+      const uint32_t qlo = sdesc_lo(smem_u32(sQ), 16), dolo = sdesc_lo(smem_u32(sDO), 16),
+                     elo = sdesc_lo(smem_u32(sE), 16);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       bool ok = mbar_wait(qdo_full, 0, abort_flag, ctx);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
-      if (ok && ctx.force_timeout) ok = mbar_wait(drain, 0, abort_flag, ctx);
-      for (int j = 0; j < nkt && ok; ++j) {
-        // S_j = Q K_j^T
-        const int ks = j % C::NKS, sb = j & 1;
-        ok = mbar_wait(&k_full[ks], (j / C::NKS) & 1u, abort_flag, ctx) &&
-             mbar_wait(&s_free[sb], ((j >> 1) & 1u) ^ 1u, abort_flag, ctx);
-        if (!ok) break;
-        tc_fence_after();
+      if (ok && ctx.force_timeout) ok = mbar_wait(&drain[who], 0, abort_flag, ctx);
+      if (who == 0) {
+        for (int j = 0; j < nkt && ok; ++j) {
+          // S_j = Q K_j^T
+          const int ks = j % C::NKS, sb = j & 1;
+          ok = mbar_wait(&k_full[ks], (j / C::NKS) & 1u, abort_flag, ctx) &&
+               mbar_wait(&s_free[sb], ((j >> 1) & 1u) ^ 1u, abort_flag, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t klo = sdesc_lo(aK + ks * C::TILE, 16);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          tc_mma_f16(tmem + (sb ? DQ_TM_S1 : DQ_TM_S0), smem_desc_sw128(aQ + off, 16, 1024),
-                     smem_desc_sw128(aK + ks * C::TILE + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&s_full[sb]);
-        // dP_j = dO V_j^T
-        const int vs = j % C::NVS;
-        ok = mbar_wait(&v_full[vs], (j / C::NVS) & 1u, abort_flag, ctx) &&
-             mbar_wait(dp_free, (j & 1u) ^ 1u, abort_flag, ctx);
-        if (!ok) break;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+            tc_mma_f16(tmem + (sb ? DQ_TM_S1 : DQ_TM_S0), sdesc(qlo + off, HI), sdesc(klo + off, HI), idesc_ss,
+                       kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[sb]);
+          tc_commit(&k_empty[ks]);
+          // dP_j = dO V_j^T
+          const int vs = j % C::NVS;
+          ok = mbar_wait(&v_full[vs], (j / C::NVS) & 1u, abort_flag, ctx) &&
+               mbar_wait(dp_free, (j & 1u) ^ 1u, abort_flag, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vlo = sdesc_lo(aV + vs * C::TILE, 16);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          tc_mma_f16(tmem + DQ_TM_DP, smem_desc_sw128(aDO + off, 16, 1024),
-                     smem_desc_sw128(aV + vs * C::TILE + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+            tc_mma_f16(tmem + DQ_TM_DP, sdesc(dolo + off, HI), sdesc(vlo + off, HI), idesc_ss, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&v_empty[vs]);
+          tc_commit(dp_full);
         }
-        tc_commit(&v_empty[vs]);
-        tc_commit(dp_full);
-        if (j >= 1) ok = do_dq(j - 1);
+      } else {
+        for (int t = 0; t < nkt && ok; ++t) {   // dQ += E_t K_t
+          const int ks = t % C::NKS;
+          ok = mbar_wait(e_full, t & 1u, abort_flag, ctx) &&
+               mbar_wait(&k_full[ks], (t / C::NKS) & 1u, abort_flag, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t klo = sdesc_lo(aK + ks * C::TILE, BOX_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            tc_mma_f16(tmem + DQ_TM_DQ, sdesc(elo + (((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4), HI),
+                       sdesc(klo + ((kk * 2048) >> 4), HI), idesc_kmn, (t > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&k_empty[ks]);
+          tc_commit(e_free);
+        }
+        if (ok) tc_commit(dq_full);
       }
-      if (ok) ok = do_dq(nkt - 1);
-      if (ok) tc_commit(dq_full);
-      tc_commit(drain);
-      drain_wait(drain, 0, ctx);
+      tc_commit(&drain[who]);
+      drain_wait(&drain[who], 0, ctx);
     }
   } else {
     // ------------------------------------------------------------------ softmax warps (row = query)
@@ -470,8 +482,8 @@ struct DkvCfg {
   static constexpr int ST_BYTES = 5 * BM * 4;
   static constexpr int OFF_BAR = OFF_ST + ST_BYTES;
   // kv_full, q_full[NQS], q_empty[NQS], do_full[NDS], do_empty[NDS],
-  // st_full, st_free, dpt_full, dpt_free, p_full, p_free, acc_full, drain
-  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 8;
+  // st_full, st_free, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2]
+  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 9;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int USED = OFF_MISC + 16;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
@@ -484,8 +496,9 @@ constexpr uint32_t KV_TM_ST = 0, KV_TM_DPT = 128, KV_TM_DV = 256, KV_TM_DK = 384
 // and split each tile's 128 query columns 64 / 64, two warps per scheduler.
 constexpr int KV_SOFTMAX_WARPS = 8;
 constexpr int KV_PRODUCER_WARP = 8;
+// two MMA-issuing threads: warp 9 issues S^T and dP^T, warp 10 issues dV and dK
 constexpr int KV_MMA_WARP = 9;
-constexpr int KV_THREADS = 320;
+constexpr int KV_THREADS = 352;
 
 __device__ __forceinline__ void softmax_group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -524,7 +537,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* p_full = dpt_free + 1;
   uint64_t* p_free = p_full + 1;
   uint64_t* acc_full = p_free + 1;
-  uint64_t* drain = acc_full + 1;
+  uint64_t* drain = acc_full + 1;   // [2], one per issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -546,11 +559,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     mbar_init(kv_full, 1);
     for (int i = 0; i < C::NQS; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
+      mbar_init(&q_empty[i], 2);   // S^T (issuer 0) and dK (issuer 1) read Q_i
     }
     for (int i = 0; i < C::NDS; ++i) {
       mbar_init(&do_full[i], 1);
-      mbar_init(&do_empty[i], 1);
+      mbar_init(&do_empty[i], 2);   // dP^T (issuer 0) and dV (issuer 1) read dO_i
     }
     mbar_init(st_full, 1);
     mbar_init(st_free, KV_SOFTMAX_WARPS);
@@ -559,7 +572,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     mbar_init(p_full, KV_SOFTMAX_WARPS);
     mbar_init(p_free, 1);
     mbar_init(acc_full, 1);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -611,62 +625,72 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       for (int it = max(0, d_issued - C::NDS); it < d_issued; ++it)
         drain_wait(&do_full[it % C::NDS], (it / C::NDS) & 1u, ctx);
     }
-  } else if (warp == KV_MMA_WARP) {
+  } else if (warp >= KV_MMA_WARP) {
+    const int who = warp - KV_MMA_WARP;   // 0: S^T and dP^T products; 1: dV and dK products
     if (lane == 0) {
       constexpr uint32_t idesc_ss = idesc_fp16_f32(BN, BM, 0, 0);
       constexpr uint32_t idesc_kmn = idesc_fp16_f32(BN, D, 0, 1);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
-                     aP = smem_u32(sP), aDS = smem_u32(sDS);
+      constexpr uint32_t HI = sdesc_hi_sw128(1024);
+      const uint32_t klo = sdesc_lo(smem_u32(sK), 16), vlo = sdesc_lo(smem_u32(sV), 16),
+                     plo = sdesc_lo(smem_u32(sP), 16), dslo = sdesc_lo(smem_u32(sDS), 16);
+      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
       bool ok = mbar_wait(kv_full, 0, abort_flag, ctx);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
-      if (ok && ctx.force_timeout) ok = mbar_wait(drain, 0, abort_flag, ctx);
+      if (ok && ctx.force_timeout) ok = mbar_wait(&drain[who], 0, abort_flag, ctx);
       for (int it = 0; it < nq && ok; ++it) {
         const int qs = it % C::NQS, ds = it % C::NDS;
         const uint32_t par = it & 1u;
-        // S^T = K Q_i^T
-        ok = mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
-             mbar_wait(st_free, par ^ 1u, abort_flag, ctx);
-        if (!ok) break;
-        tc_fence_after();
+        if (who == 0) {
+          // S^T = K Q_i^T
+          ok = mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
+               mbar_wait(st_free, par ^ 1u, abort_flag, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qlo = sdesc_lo(aQ + qs * C::TILE, 16);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          tc_mma_f16(tmem + KV_TM_ST, smem_desc_sw128(aK + off, 16, 1024),
-                     smem_desc_sw128(aQ + qs * C::TILE + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(st_full);
-        // dP^T = V dO_i^T
-        ok = mbar_wait(&do_full[ds], (it / C::NDS) & 1u, abort_flag, ctx) &&
-             mbar_wait(dpt_free, par ^ 1u, abort_flag, ctx);
-        if (!ok) break;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+            tc_mma_f16(tmem + KV_TM_ST, sdesc(klo + off, HI), sdesc(qlo + off, HI), idesc_ss, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(st_full);
+          tc_commit(&q_empty[qs]);
+          // dP^T = V dO_i^T
+          ok = mbar_wait(&do_full[ds], (it / C::NDS) & 1u, abort_flag, ctx) &&
+               mbar_wait(dpt_free, par ^ 1u, abort_flag, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dolo = sdesc_lo(aDO + ds * C::TILE, 16);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          tc_mma_f16(tmem + KV_TM_DPT, smem_desc_sw128(aV + off, 16, 1024),
-                     smem_desc_sw128(aDO + ds * C::TILE + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(dpt_full);
-        // dV += P^T dO_i, dK += dS^T Q_i
-        ok = mbar_wait(p_full, par, abort_flag, ctx);
-        if (!ok) break;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+            tc_mma_f16(tmem + KV_TM_DPT, sdesc(vlo + off, HI), sdesc(dolo + off, HI), idesc_ss, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(dpt_full);
+          tc_commit(&do_empty[ds]);
+        } else {
+          // dV += P^T dO_i, dK += dS^T Q_i
+          ok = mbar_wait(p_full, par, abort_flag, ctx) &&
+               mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
+               mbar_wait(&do_full[ds], (it / C::NDS) & 1u, abort_flag, ctx);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qmn = sdesc_lo(aQ + qs * C::TILE, BOX_BYTES), domn = sdesc_lo(aDO + ds * C::TILE, BOX_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_f16(tmem + KV_TM_DV, smem_desc_sw128(aP + aoff, 16, 1024),
-                     smem_desc_sw128(aDO + ds * C::TILE + kk * 2048, BOX_BYTES, 1024), idesc_kmn, acc);
-          tc_mma_f16(tmem + KV_TM_DK, smem_desc_sw128(aDS + aoff, 16, 1024),
-                     smem_desc_sw128(aQ + qs * C::TILE + kk * 2048, BOX_BYTES, 1024), idesc_kmn, acc);
+          for (int kk = 0; kk < BM / 16; ++kk) {
+            const uint32_t aoff = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+            const uint32_t boff = (kk * 2048) >> 4;
+            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+            tc_mma_f16(tmem + KV_TM_DV, sdesc(plo + aoff, HI), sdesc(domn + boff, HI), idesc_kmn, acc);
+            tc_mma_f16(tmem + KV_TM_DK, sdesc(dslo + aoff, HI), sdesc(qmn + boff, HI), idesc_kmn, acc);
+          }
+          tc_commit(&do_empty[ds]);
+          tc_commit(&q_empty[qs]);
+          tc_commit(p_free);
         }
-        tc_commit(&do_empty[ds]);
-        tc_commit(&q_empty[qs]);
-        tc_commit(p_free);
       }
-      if (ok) tc_commit(acc_full);
-      tc_commit(drain);
-      drain_wait(drain, 0, ctx);
+      if (ok && who == 1) tc_commit(acc_full);
+      tc_commit(&drain[who]);
+      drain_wait(&drain[who], 0, ctx);
     }
   } else {
     // ------------------------------------------------------------------ softmax warps (row = key)
