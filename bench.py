@@ -450,6 +450,27 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case():
+    """A small fixed case for ncu captures: ra_softmax on fp32 [8192, 8192] and attention
+    forward + backward at B2 H16 N8192 D128 bf16 (inputs ~0.3 GB, larger than L2), twice."""
+    import torch
+
+    import rational_softmax_attention_gb300 as ra
+    from rational_softmax_attention_gb300.inputs import attention_inputs, softmax_inputs
+
+    q, k, v, do = (t.cuda() for t in attention_inputs(2, 16, 8192, 8192, 128, seed=0, sigma_qk=3.0))
+    x = softmax_inputs(8192, 8192, seed=1, sigma=4.0).cuda()
+    for _ in range(2):
+        ra.ra_softmax(x)
+        o, rm, rs, rarg, _ = ra.ra_attention_forward(q, k, v, scale=128 ** -0.5, out_dtype=torch.float32)
+        ra.ra_attention_backward(q, k, v, o, do, rm, rs, rarg, scale=128 ** -0.5)
+    torch.cuda.synchronize()
+    status = ra.device_status()
+    print("profile case status", status)
+    if status != "RA_OK":
+        raise SystemExit(1)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,7 +478,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run only the small fixed case used for ncu captures, then exit")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        run_profile_case()
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
