@@ -74,9 +74,9 @@ struct FwdCfg {
   static constexpr int OFF_RING = OFF_Q + NGROUP * TILE_BYTES;
   static constexpr int OFF_P = OFF_RING + NSTAGE * TILE_BYTES;   // P_A, P_B
   static constexpr int OFF_BAR = OFF_P + NGROUP * P_BYTES;
-  // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2],
-  // drain[2]
-  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 6 * NGROUP;
+  // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2][2], s_empty[2][2], p_full[2], p_empty[2],
+  // o_full[2], drain[2]
+  static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 * NGROUP;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int MISC_BYTES = 16 + SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes
   static constexpr int USED = OFF_MISC + MISC_BYTES;
@@ -184,9 +184,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* q_full = bars;
   uint64_t* ring_full = bars + 1;
   uint64_t* ring_empty = ring_full + NST;
-  uint64_t* s_full = ring_empty + NST;   // [NGROUP]
-  uint64_t* s_empty = s_full + NGROUP;
-  uint64_t* p_full = s_empty + NGROUP;
+  uint64_t* s_full = ring_empty + NST;     // [NGROUP][2]: score buffer b of query tile g at 2 g + b
+  uint64_t* s_empty = s_full + 2 * NGROUP;
+  uint64_t* p_full = s_empty + 2 * NGROUP;
   uint64_t* p_empty = p_full + NGROUP;
   uint64_t* o_full = p_empty + NGROUP;   // [NGROUP]
   uint64_t* drain = o_full + NGROUP;     // [NGROUP]
@@ -217,8 +217,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&ring_empty[i], NGROUP);   // one commit per issuer
     }
     for (int g = 0; g < NGROUP; ++g) {
-      mbar_init(&s_full[g], 1);
-      mbar_init(&s_empty[g], GROUP_WARPS);   // one arrival per warp of the group
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&s_full[2 * g + b], 1);
+        mbar_init(&s_empty[2 * g + b], GROUP_WARPS);   // one arrival per warp of the group
+      }
       mbar_init(&p_full[g], GROUP_WARPS);
       mbar_init(&p_empty[g], 1);
       mbar_init(&o_full[g], 1);
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // count as visited (query tile, key tile) pairs
       const int nkt_g = (q0 + g * BM < s.NQ) ? last_key_of(q0 + (g + 1) * BM) / BN + 1 : 0;
       uint32_t pos = 0;   // ring position (K and V tiles in producer order)
-      uint32_t sc = 0;    // S products issued
+      uint32_t uc0 = 0, uc1 = 0;   // S products issued into score buffer 0 and 1
       unsigned long long visited = 0, skipped = 0;
       bool o_started = false;
       auto ring_wait = [&](uint32_t p, uint32_t& addr) -> bool {
@@ -310,17 +312,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         addr = sRa + st * C::TILE_BYTES;
         return true;
       };
-      auto mma_s = [&](uint32_t kaddr) -> bool {   // S_g = Q_g K^T
-        if (!mbar_wait(&s_empty[g], (sc & 1u) ^ 1u, abort_flag, ctx)) return false;
+      // S_g = Q_g K^T into score buffer b (buffer 1 exists in pass 1 only: it is the O_g
+      // region, free until the first O_g product of pass 2)
+      auto mma_s = [&](uint32_t kaddr, int b) -> bool {
+        const uint32_t use = b ? uc1 : uc0;
+        if (!mbar_wait(&s_empty[2 * g + b], (use & 1u) ^ 1u, abort_flag, ctx)) return false;
         tc_fence_after();
         const uint32_t klo = sdesc_lo(kaddr, 16);
+        const uint32_t dcol = scol + 256u * b;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
-          tc_mma_f16(scol, sdesc(qlo + off, HI), sdesc(klo + off, HI), idesc_qk, kk > 0 ? 1u : 0u);
+          tc_mma_f16(dcol, sdesc(qlo + off, HI), sdesc(klo + off, HI), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[g]);
-        ++sc;
+        tc_commit(&s_full[2 * g + b]);
+        if (b) ++uc1; else ++uc0;
         return true;
       };
       auto mma_pv = [&](int j, uint32_t vaddr) -> bool {   // O_g += P_g V_j
@@ -354,13 +360,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       // pass 1: S_g(j) for every key tile; a ring stage is free once both issuers commit
       for (int j = 0; j < nkt && ok; ++j) {
         ok = ring_wait(pos, ka);
-        if (ok) ok = mma_s(ka);
+        if (ok) ok = mma_s(ka, j & 1);
         if (ok) tc_commit(&ring_empty[pos % NST]);
         ++pos;
       }
       // pass 2: S_g(0); then per j: S_g(j+1), O_g(j)
       if (ok) ok = ring_wait(pos, ka);
-      if (ok) ok = mma_s(ka);
+      if (ok) ok = mma_s(ka, 0);
       if (ok) tc_commit(&ring_empty[pos % NST]);
       ++pos;
       for (int j = 0; j < nkt && ok; ++j) {
@@ -369,7 +375,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (more) {
           kpos = pos++;
           ok = ring_wait(kpos, ka);
-          if (ok) ok = mma_s(ka);
+          if (ok) ok = mma_s(ka, 0);
           if (ok) tc_commit(&ring_empty[kpos % NST]);
         }
         const uint32_t vpos = pos++;
@@ -402,15 +408,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     uint32_t sv[BN / 32][32];
     // S_g into registers, then hand the buffer back to the MMA thread
-    auto take_s = [&](uint32_t idx) -> bool {
-      if (!warp_wait(&s_full[g], idx & 1u)) return false;
+    // pass-1 tile j sits in score buffer j & 1, as that buffer's use j >> 1
+    auto take_s = [&](int b, uint32_t use) -> bool {
+      if (!warp_wait(&s_full[2 * g + b], use & 1u)) return false;
       tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < BN / 32; ++k) tmem_ld32(scol + 32 * k, sv[k]);
+      for (int k = 0; k < BN / 32; ++k) tmem_ld32(scol + 256u * b + 32 * k, sv[k]);
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[g]);
+      if (lane == 0) mbar_arrive(&s_empty[2 * g + b]);
       return true;
     };
 #define SV(c) u2f(sv[(c) >> 5][(c) & 31])
@@ -422,7 +429,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int jm = 0;   // 32-column chunk (tile * 4 + chunk) holding the first occurrence of the maximum
     // pass 1: running maximum of the raw scores q.k (scale > 0 keeps the argmax)
     for (int j = 0; j < nkt && ok; ++j) {
-      ok = take_s(sidx++);
+      ok = take_s(j & 1, static_cast<uint32_t>(j) >> 1);
       if (!ok) break;
       const int col0 = j * BN;   // key index of column 0
       // maximum of each 32-column chunk; the first chunk (in key order) that raises the
@@ -466,8 +473,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float base = fmaf(m_sc, 1.0f / 32.0f, 0.5f);
     uint8_t* prow = sP + g * C::P_BYTES + row_local * 128;
     float rowsum = 0.0f;
+    sidx = static_cast<uint32_t>(nkt + 1) >> 1;   // pass 1 used buffer 0 for tiles 0, 2, 4, ...
     for (int j = 0; j < nkt && ok; ++j) {
-      ok = warp_wait(&s_full[g], sidx & 1u);
+      ok = warp_wait(&s_full[2 * g], sidx & 1u);   // buffer 0
       if (!ok) break;
       ++sidx;
       tc_fence_after();
@@ -488,7 +496,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[g]);
+      if (lane == 0) mbar_arrive(&s_empty[2 * g]);
       if (arg_tile && (jm & 3) >= 2)
         a = col0 + 64 +
             ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 96, lim) : find_in_chunk(h[0], m, col0 + 64, lim));
