@@ -61,6 +61,25 @@ __device__ __forceinline__ float2 rcp_pair(float w0, float w1) {
   return make_float2(R * w1, R * w0);
 }
 
+// The backward coefficient q^7 (1/w)^2 for four scores x of a row, w = sat(base - c2 x) =
+// (1+u)/2, q = 1/w - 1.  Four entries share two reciprocals: with the pairs A = (w0, w1),
+// B = (w2, w3), R = 1/(A B) elementwise gives R B = (1/w0, 1/w1) and R A = (1/w2, 1/w3).
+__device__ __forceinline__ float2 coef_pair(float2 rw) {   // rw = 1/w for two entries
+  const float2 q = __fadd2_rn(rw, make_float2(-1.0f, -1.0f));
+  const float2 q2 = __fmul2_rn(q, q);
+  const float2 q4 = __fmul2_rn(q2, q2);
+  const float2 q7 = __fmul2_rn(__fmul2_rn(q4, q2), q);
+  return __fmul2_rn(q7, __fmul2_rn(rw, rw));
+}
+__device__ __forceinline__ void coef_quad(const float (&x)[4], float c2, float base, float2& ca, float2& cb) {
+  const float2 A = make_float2(fma_sat(x[0], -c2, base), fma_sat(x[1], -c2, base));
+  const float2 B = make_float2(fma_sat(x[2], -c2, base), fma_sat(x[3], -c2, base));
+  const float2 P = __fmul2_rn(A, B);
+  const float2 R = make_float2(rcp_approx(P.x), rcp_approx(P.y));
+  ca = coef_pair(__fmul2_rn(R, B));
+  cb = coef_pair(__fmul2_rn(R, A));
+}
+
 // Row of 8 bf16 from global memory as floats.
 __device__ __forceinline__ void load8_bf16(const void* p, float* out) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -347,7 +366,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const float c2 = s.scale * (1.0f / 32.0f);
     const float cE = 0.25f * inv_s;
     const int lim = s.causal ? min(i, s.NK - 1) : s.NK - 1;
-    float R = 0.0f;
+    const float2 cE2 = make_float2(cE, cE), mcED2 = make_float2(-cE * Di, -cE * Di);
+    float2 R2 = make_float2(0.0f, 0.0f);
     bool ok = true;
     uint32_t sv[2][32];
 #define SV(c) sv[(c) >> 5][(c) & 31]
@@ -367,22 +387,22 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (lane == 0) mbar_arrive(&s_free[sb]);
       const int col0 = j * BN + cbase;   // key index of local column 0
       const bool need_mask = col0 + 63 > lim;
-      // coefficient q^7 (1/w)^2 / (4 s_i) per entry, in place
+      // coefficient q^7 (1/w)^2 per entry, in place; the factor 1/(4 s_i) is applied with
+      // dP - D_i below.  Four entries share two reciprocals (coef_quad).
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float s0 = u2f(SV(c)), s1 = u2f(SV(c + 1));
+      for (int c = 0; c < 64; c += 4) {
+        float x[4] = {u2f(SV(c)), u2f(SV(c + 1)), u2f(SV(c + 2)), u2f(SV(c + 3))};
         if (need_mask) {
-          if (col0 + c > lim) s0 = -INFINITY;
-          if (col0 + c + 1 > lim) s1 = -INFINITY;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (col0 + c + t > lim) x[t] = -INFINITY;
         }
-        const float2 rr = rcp_pair(fma_sat(s0, -c2, base), fma_sat(s1, -c2, base));
-        const float2 qq = __fadd2_rn(rr, make_float2(-1.0f, -1.0f));
-        const float2 q2 = __fmul2_rn(qq, qq);
-        const float2 q4 = __fmul2_rn(q2, q2);
-        const float2 q7 = __fmul2_rn(__fmul2_rn(q4, q2), qq);
-        const float2 coef = __fmul2_rn(__fmul2_rn(q7, __fmul2_rn(rr, rr)), make_float2(cE, cE));
-        SV(c) = __float_as_uint(coef.x);
-        SV(c + 1) = __float_as_uint(coef.y);
+        float2 ca, cb;
+        coef_quad(x, c2, base, ca, cb);
+        SV(c) = __float_as_uint(ca.x);
+        SV(c + 1) = __float_as_uint(ca.y);
+        SV(c + 2) = __float_as_uint(cb.x);
+        SV(c + 3) = __float_as_uint(cb.y);
       }
       if (a >= col0 && a < col0 + 64) {   // the argmax entry takes -R_i, not E
 #pragma unroll
@@ -408,10 +428,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const int c = cc * 32 + e * 8 + 2 * t;
-            const float e0 = u2f(SV(c)) * (u2f(dv[e * 8 + 2 * t]) - Di);
-            const float e1 = u2f(SV(c + 1)) * (u2f(dv[e * 8 + 2 * t + 1]) - Di);
-            R += e0 + e1;
-            pk[t] = pack_f16x2_sat(e0, e1);
+            // E = coef (dP - D_i) / (4 s_i) = coef (cE dP - cE D_i)
+            const float2 dpp = make_float2(u2f(dv[e * 8 + 2 * t]), u2f(dv[e * 8 + 2 * t + 1]));
+            const float2 ee = __fmul2_rn(make_float2(u2f(SV(c)), u2f(SV(c + 1))), __ffma2_rn(dpp, cE2, mcED2));
+            R2 = __fadd2_rn(R2, ee);
+            pk[t] = pack_f16x2_sat(ee.x, ee.y);
           }
           st_tile16(sE, r, (cbase + cc * 32 + e * 8) >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
@@ -422,6 +443,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
 #undef SV
     // R_i over both halves (reached by all eight warps, also after a wait gave up)
+    float R = R2.x + R2.y;
     xch[half * BM + r] = R;
     softmax8_sync();
     R = xch[r] + xch[BM + r];
@@ -729,7 +751,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         const size_t qo = so + (q_ok ? ii : 0);
         st_base[threadIdx.x] = q_ok ? args.ws_base[qo] : 2.0f;
         st_invs[threadIdx.x] = q_ok ? args.ws_invs[qo] : 0.0f;
-        st_d[threadIdx.x] = q_ok ? args.ws_d[qo] : 0.0f;
+        st_d[threadIdx.x] = q_ok ? 0.25f * args.ws_d[qo] : 0.0f;   // D_i / 4
         st_r[threadIdx.x] = q_ok ? args.ws_r[qo] : 0.0f;
         st_a[threadIdx.x] = q_ok ? args.row_arg[qo] : -1;
       }
@@ -746,7 +768,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       const bool need_mask = !j_ok || (s.causal && i0 + cbase < j);
       const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
       warp_wait(p_free, par ^ 1u);
-      // P^T and the dS coefficient q^7 (1/w)^2 / (4 s_i), in place
+      // P^T and the dS coefficient q^7 (1/w)^2 / s_i (in place); the factor 1/4 comes with
+      // dP^T - D_i below.  Four entries share two reciprocals (as in coef_quad).
 #pragma unroll
       for (int c = 0; c < 64; c += 8) {
         uint32_t pk[4];
@@ -762,19 +785,20 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             for (int t = 0; t < 4; ++t)
               if (cg + t < first_vis) x[t] = -INFINITY;
           }
-          const float2 ra = rcp_pair(fma_sat(x[0], -c2, b4.x), fma_sat(x[1], -c2, b4.y));
-          const float2 rb = rcp_pair(fma_sat(x[2], -c2, b4.z), fma_sat(x[3], -c2, b4.w));
+          const float2 A = make_float2(fma_sat(x[0], -c2, b4.x), fma_sat(x[1], -c2, b4.y));
+          const float2 B = make_float2(fma_sat(x[2], -c2, b4.z), fma_sat(x[3], -c2, b4.w));
+          const float2 PR = __fmul2_rn(A, B);
+          const float2 R = make_float2(rcp_approx(PR.x), rcp_approx(PR.y));
+          const float2 ra = __fmul2_rn(R, B), rb = __fmul2_rn(R, A);   // 1/w
           const float2 iva = make_float2(i4.x, i4.y), ivb = make_float2(i4.z, i4.w);
-          const float2 qa = __fadd2_rn(ra, make_float2(-1.0f, -1.0f));
-          const float2 qb = __fadd2_rn(rb, make_float2(-1.0f, -1.0f));
+          const float2 m1 = make_float2(-1.0f, -1.0f);
+          const float2 qa = __fadd2_rn(ra, m1), qb = __fadd2_rn(rb, m1);
           const float2 qa2 = __fmul2_rn(qa, qa), qb2 = __fmul2_rn(qb, qb);
           const float2 qa4 = __fmul2_rn(qa2, qa2), qb4 = __fmul2_rn(qb2, qb2);
           const float2 pa = __fmul2_rn(__fmul2_rn(qa4, qa4), iva);
           const float2 pb = __fmul2_rn(__fmul2_rn(qb4, qb4), ivb);
-          const float2 ca = __fmul2_rn(__fmul2_rn(__fmul2_rn(qa4, qa2), qa),
-                                       __fmul2_rn(__fmul2_rn(ra, ra), __fmul2_rn(iva, make_float2(0.25f, 0.25f))));
-          const float2 cbv = __fmul2_rn(__fmul2_rn(__fmul2_rn(qb4, qb2), qb),
-                                        __fmul2_rn(__fmul2_rn(rb, rb), __fmul2_rn(ivb, make_float2(0.25f, 0.25f))));
+          const float2 ca = __fmul2_rn(__fmul2_rn(__fmul2_rn(qa4, qa2), qa), __fmul2_rn(__fmul2_rn(ra, ra), iva));
+          const float2 cbv = __fmul2_rn(__fmul2_rn(__fmul2_rn(qb4, qb2), qb), __fmul2_rn(__fmul2_rn(rb, rb), ivb));
           SV(cb) = __float_as_uint(ca.x);
           SV(cb + 1) = __float_as_uint(ca.y);
           SV(cb + 2) = __float_as_uint(cbv.x);
@@ -804,18 +828,23 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           float dsv[8];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const float4 d4 = *reinterpret_cast<const float4*>(st_d + cg + 4 * h);
+            const float4 d4 = *reinterpret_cast<const float4*>(st_d + cg + 4 * h);   // D_i / 4
             const float4 r4 = *reinterpret_cast<const float4*>(st_r + cg + 4 * h);
             const int4 a4 = *reinterpret_cast<const int4*>(st_a + cg + 4 * h);
-            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
             const float rr4[4] = {r4.x, r4.y, r4.z, r4.w};
             const int aa[4] = {a4.x, a4.y, a4.z, a4.w};
+            const int c = cb + 4 * h;
+            const float2 q4 = make_float2(0.25f, 0.25f);
+            // coef (dP - D_i) / 4 = coef (dP / 4 - D_i / 4)
+            const float2 v0 = __fmul2_rn(make_float2(u2f(SV(c)), u2f(SV(c + 1))),
+                                         __ffma2_rn(make_float2(u2f(dv[e * 8 + 4 * h]), u2f(dv[e * 8 + 4 * h + 1])), q4,
+                                                    make_float2(-d4.x, -d4.y)));
+            const float2 v1 = __fmul2_rn(make_float2(u2f(SV(c + 2)), u2f(SV(c + 3))),
+                                         __ffma2_rn(make_float2(u2f(dv[e * 8 + 4 * h + 2]), u2f(dv[e * 8 + 4 * h + 3])), q4,
+                                                    make_float2(-d4.z, -d4.w)));
+            const float v[4] = {v0.x, v0.y, v1.x, v1.y};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int c = cb + 4 * h + t;
-              const float v = u2f(SV(c)) * (u2f(dv[e * 8 + 4 * h + t]) - dd[t]);
-              dsv[4 * h + t] = (aa[t] == j) ? -rr4[t] : v;
-            }
+            for (int t = 0; t < 4; ++t) dsv[4 * h + t] = (aa[t] == j) ? -rr4[t] : v[t];
           }
           st_tile16(sDS, r, cg >> 3,
                     make_uint4(pack_f16x2_sat(dsv[0], dsv[1]), pack_f16x2_sat(dsv[2], dsv[3]),
