@@ -58,6 +58,7 @@ constexpr int SOFTMAX_WARPS = NGROUP * GROUP_WARPS;  // 8
 constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
 constexpr int MMA_WARP = SOFTMAX_WARPS + 1;          // MMA_WARP + g issues the products of query tile g
 constexpr int THREADS = 32 * (SOFTMAX_WARPS + 1 + NGROUP);
+constexpr int CAUSAL_HEADS = 8;   // causal CTA order: heads per longest-first group
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S = 0;     // S of query tile g at column 128 g
 constexpr uint32_t TMEM_O = 256;   // O of query tile g at column 256 + 128 g
@@ -200,9 +201,21 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nct = (nqt + NGROUP - 1) / NGROUP;   // CTAs per (batch, head)
   const int item = blockIdx.x;
   // Head-major order: the ~150 resident CTAs share a few heads, so each head's K and V
-  // stay in L2 across its query tiles.  Causal: within a head the longest CTAs go first.
-  const int bh = item / nct;
-  const int ct = s.causal ? (nct - 1 - item % nct) : (item % nct);
+  // stay in L2 across its query tiles.  Causal: CTA lengths differ, so heads are taken in
+  // groups of CAUSAL_HEADS (their K and V, a few tens of MB, still fit in L2) and within a
+  // group the longest CTAs of all its heads go first; only the last group's short CTAs are
+  // left for the tail.
+  int bh, ct;
+  if (s.causal) {
+    const int grp = item / (CAUSAL_HEADS * nct);
+    const int gsize = min(CAUSAL_HEADS, s.B * s.H - grp * CAUSAL_HEADS);
+    const int i = item - grp * CAUSAL_HEADS * nct;
+    ct = nct - 1 - i / gsize;
+    bh = grp * CAUSAL_HEADS + i % gsize;
+  } else {
+    bh = item / nct;
+    ct = item % nct;
+  }
   const int q0 = ct * (NGROUP * BM);
   // last key any row of the CTA may see, and per query tile
   auto last_key_of = [&](int rows_end) {   // rows_end: one past the last row of the range
