@@ -112,7 +112,12 @@ def _ptr(t):
 
 
 class HotPath:
-    """Preallocated device buffers and the C-ABI calls of one step."""
+    """Preallocated device buffers and the C-ABI calls of one step.
+
+    Inputs and outputs come in two device sets, so that the end-to-end loop can copy the
+    next step's inputs in (and the last step's results out) while a step computes.  The
+    row statistics and workspaces are used only inside a step, on the compute stream, and
+    exist once."""
 
     def __init__(self, dev, host_inputs, w, sw):
         import ctypes
@@ -122,23 +127,24 @@ class HotPath:
         import rational_softmax_attention_gb300 as ra
         self.torch, self.ra, self.ctypes = torch, ra, ctypes
         self.L = ra.lib()
+        self.dev = dev
         self.w, self.sw = w, sw
         self.host_in = host_inputs
-        self.dev_in = [t.to(dev) for t in host_inputs]
-        q, k, v, do, x = self.dev_in
-        B, H, N, D = q.shape
+        B, H, N, D = host_inputs[0].shape
         f32 = torch.float32
-        self.o = torch.empty((B, H, N, D), dtype=f32, device=dev)
+        self.sets = []
+        for _ in range(2):
+            dev_in = [t.to(dev) for t in host_inputs]
+            o = torch.empty((B, H, N, D), dtype=f32, device=dev)
+            dq = torch.empty((B, H, N, D), dtype=f32, device=dev)
+            outs = [o, dq, torch.empty_like(dq), torch.empty_like(dq), torch.empty_like(dev_in[4])]
+            self.sets.append((dev_in, outs))
+        self.dev_in, self.outs = self.sets[0]
         self.rm = torch.empty((B, H, N), dtype=f32, device=dev)
         self.rs = torch.empty((B, H, N), dtype=f32, device=dev)
         self.ra_ = torch.empty((B, H, N), dtype=torch.int32, device=dev)
-        self.dq = torch.empty((B, H, N, D), dtype=f32, device=dev)
-        self.dk = torch.empty_like(self.dq)
-        self.dv = torch.empty_like(self.dq)
-        self.y = torch.empty_like(x)
         self.ws = torch.empty(self.L.ra_attention_bwd_workspace_size(B, H, N, N, D), dtype=torch.uint8, device=dev)
         self.fws = torch.empty(self.L.ra_attention_fwd_workspace_size(B, H, N, N, D), dtype=torch.uint8, device=dev)
-        self.outs = [self.o, self.dq, self.dk, self.dv, self.y]
         self.host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in self.outs]
         self.shape = (B, H, N, D)
 
@@ -146,44 +152,85 @@ class HotPath:
         if code != 0:
             raise RuntimeError(f"{name}: {self.L.ra_status_string(code).decode()}")
 
-    def softmax(self, st):
-        x = self.dev_in[4]
-        self._check("ra_softmax_fwd", self.L.ra_softmax_fwd(_ptr(x), _ptr(self.y), x.shape[0], x.shape[1], 0, st))
+    def softmax(self, st, b=0):
+        x = self.sets[b][0][4]
+        y = self.sets[b][1][4]
+        self._check("ra_softmax_fwd", self.L.ra_softmax_fwd(_ptr(x), _ptr(y), x.shape[0], x.shape[1], 0, st))
 
-    def fwd(self, st, counts=None):
-        q, k, v, _, _ = self.dev_in
+    def fwd(self, st, counts=None, b=0):
+        q, k, v, _, _ = self.sets[b][0]
+        o = self.sets[b][1][0]
         B, H, N, D = self.shape
         self._check("ra_attention_fwd", self.L.ra_attention_fwd(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(self.o), _ptr(self.rm), _ptr(self.rs), _ptr(self.ra_), _ptr(counts),
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(self.rm), _ptr(self.rs), _ptr(self.ra_), _ptr(counts),
             _ptr(self.fws), B, H, N, N, D, float(self.w.scale), int(self.w.causal), 1, 0, st))
 
-    def bwd(self, st):
-        q, k, v, do, _ = self.dev_in
+    def bwd(self, st, b=0):
+        q, k, v, do, _ = self.sets[b][0]
+        o, dq, dk, dv, _ = self.sets[b][1]
         B, H, N, D = self.shape
         self._check("ra_attention_bwd", self.L.ra_attention_bwd(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(self.o), _ptr(do), _ptr(self.rm), _ptr(self.rs), _ptr(self.ra_),
-            _ptr(self.dq), _ptr(self.dk), _ptr(self.dv), _ptr(self.ws), B, H, N, N, D, float(self.w.scale),
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(self.rm), _ptr(self.rs), _ptr(self.ra_),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(self.ws), B, H, N, N, D, float(self.w.scale),
             int(self.w.causal), 1, 0, 0, st))
 
-    def step(self, st, events=None):
+    def step(self, st, events=None, b=0):
         if events:
             events[0].record()
-        self.softmax(st)
+        self.softmax(st, b)
         if events:
             events[1].record()
-        self.fwd(st)
+        self.fwd(st, None, b)
         if events:
             events[2].record()
-        self.bwd(st)
+        self.bwd(st, b)
         if events:
             events[3].record()
 
-    def step_e2e(self, st):
-        for d, h in zip(self.dev_in, self.host_in):
-            d.copy_(h, non_blocking=True)
-        self.step(st)
-        for h, d in zip(self.host_out, self.outs):
-            h.copy_(d, non_blocking=True)
+    def run_e2e(self, stream, steps):
+        """`steps` end-to-end steps, timed with events on `stream`, returned in ms.
+
+        Step i copies its inputs from pinned host memory into device set i % 2 on an H2D
+        stream, computes on `stream`, and copies every output back to pinned host memory
+        on a D2H stream.  Set b is refilled only after the step that last read it has
+        finished, and recomputed only after its previous results have left the device.
+        The closing event waits for the last D2H copy, so every step's copies lie inside
+        the timed region."""
+        torch = self.torch
+        st = self.ctypes.c_void_p(stream.cuda_stream)
+        h2d = torch.cuda.Stream(self.dev)
+        d2h = torch.cuda.Stream(self.dev)
+        done = [torch.cuda.Event() for _ in range(2)]      # step on set b finished
+        drained = [torch.cuda.Event() for _ in range(2)]   # outputs of set b copied out
+        loaded = [torch.cuda.Event() for _ in range(2)]    # inputs of set b copied in
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h2d.wait_event(e0)
+        d2h.wait_event(e0)
+        for i in range(steps):
+            b = i % 2
+            dev_in, outs = self.sets[b]
+            if i >= 2:
+                h2d.wait_event(done[b])
+            with torch.cuda.stream(h2d):
+                for d, h in zip(dev_in, self.host_in):
+                    d.copy_(h, non_blocking=True)
+            loaded[b].record(h2d)
+            stream.wait_event(loaded[b])
+            if i >= 2:
+                stream.wait_event(drained[b])
+            self.step(st, None, b)
+            done[b].record(stream)
+            d2h.wait_event(done[b])
+            with torch.cuda.stream(d2h):
+                for h, d in zip(self.host_out, outs):
+                    h.copy_(d, non_blocking=True)
+            drained[b].record(d2h)
+        for b in range(min(2, steps)):
+            stream.wait_event(drained[b])
+        e1.record(stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1)
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.host_in)
@@ -302,17 +349,11 @@ def run_ours(args):
     bwd_fl = flops_step - fwd_fl
     sm_bytes = 2.0 * x.numel() * 4
 
-    # end to end: pinned host inputs -> device, the step, results -> pinned host buffers
-    for _ in range(max(1, args.warmup)):
-        hp.step_e2e(st)
+    # end to end: pinned host inputs -> device, the step, results -> pinned host buffers,
+    # with the copies of neighbouring steps overlapping the compute (HotPath.run_e2e)
+    hp.run_e2e(stream, max(3, args.warmup))
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        hp.step_e2e(st)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = hp.run_e2e(stream, args.steps)
     if dist is not None:
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)

@@ -58,7 +58,7 @@ constexpr int SOFTMAX_WARPS = NGROUP * GROUP_WARPS;  // 8
 constexpr int PRODUCER_WARP = SOFTMAX_WARPS;
 constexpr int MMA_WARP = SOFTMAX_WARPS + 1;          // MMA_WARP + g issues the products of query tile g
 constexpr int THREADS = 32 * (SOFTMAX_WARPS + 1 + NGROUP);
-constexpr int CAUSAL_HEADS = 8;   // causal CTA order: heads per longest-first group
+constexpr int CAUSAL_HEADS = 64;  // causal CTA order: heads per longest-first group
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S = 0;     // S of query tile g at column 128 g
 constexpr uint32_t TMEM_O = 256;   // O of query tile g at column 256 + 128 g
@@ -202,9 +202,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int item = blockIdx.x;
   // Head-major order: the ~150 resident CTAs share a few heads, so each head's K and V
   // stay in L2 across its query tiles.  Causal: CTA lengths differ, so heads are taken in
-  // groups of CAUSAL_HEADS (their K and V, a few tens of MB, still fit in L2) and within a
-  // group the longest CTAs of all its heads go first; only the last group's short CTAs are
-  // left for the tail.
+  // groups of CAUSAL_HEADS and within a group the longest CTAs of all its heads go first;
+  // only the last group's short CTAs are left for the tail.  With 64 heads per group the
+  // resident CTAs still come two or three to a head, of nearly equal length, so they walk
+  // that head's keys together and L2 serves the repeated reads.
   int bh, ct;
   if (s.causal) {
     const int grp = item / (CAUSAL_HEADS * nct);
