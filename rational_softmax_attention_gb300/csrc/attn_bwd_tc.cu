@@ -501,7 +501,7 @@ struct DkvCfg {
   static constexpr int OFF_P = OFF_DO + NDS * TILE;
   static constexpr int OFF_DS = OFF_P + A_BYTES;
   static constexpr int OFF_ST = OFF_DS + A_BYTES;          // per-query constants of one tile
-  static constexpr int ST_BYTES = 5 * BM * 4;
+  static constexpr int ST_BYTES = 5 * BM * 4 + 16;         // + 128-bit mask: argmax in this key tile
   static constexpr int OFF_BAR = OFF_ST + ST_BYTES;
   // kv_full, q_full[NQS], q_empty[NQS], do_full[NDS], do_empty[NDS],
   // st_full, st_free, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2]
@@ -546,6 +546,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   float* st_d = st_base + 2 * BM;
   float* st_r = st_base + 3 * BM;
   int* st_a = reinterpret_cast<int*>(st_base + 4 * BM);
+  uint32_t* st_amask = reinterpret_cast<uint32_t*>(st_base + 5 * BM);   // bit i: a_i in [k0, k0 + BN)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* q_full = kv_full + 1;
@@ -753,7 +754,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         st_invs[threadIdx.x] = q_ok ? args.ws_invs[qo] : 0.0f;
         st_d[threadIdx.x] = q_ok ? 0.25f * args.ws_d[qo] : 0.0f;   // D_i / 4
         st_r[threadIdx.x] = q_ok ? args.ws_r[qo] : 0.0f;
-        st_a[threadIdx.x] = q_ok ? args.row_arg[qo] : -1;
+        const int ai = q_ok ? args.row_arg[qo] : -1;
+        st_a[threadIdx.x] = ai;
+        // about BM / N_K * BN of a tile's queries have their argmax among this CTA's keys
+        const uint32_t bits = __ballot_sync(0xffffffffu, ai >= k0 && ai < k0 + BN);
+        if (lane == 0) st_amask[warp] = bits;
       }
       softmax_group_sync();
       warp_wait(st_full, par);
@@ -768,8 +773,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       const bool need_mask = !j_ok || (s.causal && i0 + cbase < j);
       const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
       warp_wait(p_free, par ^ 1u);
-      // P^T and the dS coefficient q^7 (1/w)^2 / s_i (in place); the factor 1/4 comes with
-      // dP^T - D_i below.  Four entries share two reciprocals (as in coef_quad).
+      // P^T = q^8 / s_i and the dS coefficient q^7 (1/w)^2 / s_i = q^7 (1 + q)^2 / s_i (in
+      // place): with t = q^7 / s_i, P = t q and the coefficient is t + P (2 + q).  The factor
+      // 1/4 comes with dP^T - D_i below.  Four entries share two reciprocals (as in coef_quad).
 #pragma unroll
       for (int c = 0; c < 64; c += 8) {
         uint32_t pk[4];
@@ -789,16 +795,15 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           const float2 B = make_float2(fma_sat(x[2], -c2, b4.z), fma_sat(x[3], -c2, b4.w));
           const float2 PR = __fmul2_rn(A, B);
           const float2 R = make_float2(rcp_approx(PR.x), rcp_approx(PR.y));
-          const float2 ra = __fmul2_rn(R, B), rb = __fmul2_rn(R, A);   // 1/w
-          const float2 iva = make_float2(i4.x, i4.y), ivb = make_float2(i4.z, i4.w);
-          const float2 m1 = make_float2(-1.0f, -1.0f);
-          const float2 qa = __fadd2_rn(ra, m1), qb = __fadd2_rn(rb, m1);
+          const float2 m1 = make_float2(-1.0f, -1.0f), two = make_float2(2.0f, 2.0f);
+          const float2 qa = __ffma2_rn(R, B, m1), qb = __ffma2_rn(R, A, m1);   // 1/w - 1
           const float2 qa2 = __fmul2_rn(qa, qa), qb2 = __fmul2_rn(qb, qb);
-          const float2 qa4 = __fmul2_rn(qa2, qa2), qb4 = __fmul2_rn(qb2, qb2);
-          const float2 pa = __fmul2_rn(__fmul2_rn(qa4, qa4), iva);
-          const float2 pb = __fmul2_rn(__fmul2_rn(qb4, qb4), ivb);
-          const float2 ca = __fmul2_rn(__fmul2_rn(__fmul2_rn(qa4, qa2), qa), __fmul2_rn(__fmul2_rn(ra, ra), iva));
-          const float2 cbv = __fmul2_rn(__fmul2_rn(__fmul2_rn(qb4, qb2), qb), __fmul2_rn(__fmul2_rn(rb, rb), ivb));
+          const float2 qa7 = __fmul2_rn(__fmul2_rn(qa2, qa2), __fmul2_rn(qa2, qa));
+          const float2 qb7 = __fmul2_rn(__fmul2_rn(qb2, qb2), __fmul2_rn(qb2, qb));
+          const float2 ta = __fmul2_rn(qa7, make_float2(i4.x, i4.y)), tb = __fmul2_rn(qb7, make_float2(i4.z, i4.w));
+          const float2 pa = __fmul2_rn(ta, qa), pb = __fmul2_rn(tb, qb);
+          const float2 ca = __ffma2_rn(pa, __fadd2_rn(qa, two), ta);
+          const float2 cbv = __ffma2_rn(pb, __fadd2_rn(qb, two), tb);
           SV(cb) = __float_as_uint(ca.x);
           SV(cb + 1) = __float_as_uint(ca.y);
           SV(cb + 2) = __float_as_uint(cbv.x);
@@ -808,7 +813,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         }
         st_tile16(sP, r, (cbase + c) >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
       }
-      // dS^T = coef (dP^T - D_i), with -R_i where this key is the query's argmax
+      // dS^T = coef (dP^T - D_i); the entries (a_i, i) where this key is the query's argmax
+      // take -R_i afterwards
       warp_wait(dpt_full, par);
       tc_fence_after();
 #pragma unroll
@@ -825,14 +831,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         for (int e = 0; e < 4; ++e) {
           const int cb = cc * 32 + e * 8;
           const int cg = cbase + cb;
-          float dsv[8];
+          uint32_t pk[4];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const float4 d4 = *reinterpret_cast<const float4*>(st_d + cg + 4 * h);   // D_i / 4
-            const float4 r4 = *reinterpret_cast<const float4*>(st_r + cg + 4 * h);
-            const int4 a4 = *reinterpret_cast<const int4*>(st_a + cg + 4 * h);
-            const float rr4[4] = {r4.x, r4.y, r4.z, r4.w};
-            const int aa[4] = {a4.x, a4.y, a4.z, a4.w};
             const int c = cb + 4 * h;
             const float2 q4 = make_float2(0.25f, 0.25f);
             // coef (dP - D_i) / 4 = coef (dP / 4 - D_i / 4)
@@ -842,13 +844,27 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             const float2 v1 = __fmul2_rn(make_float2(u2f(SV(c + 2)), u2f(SV(c + 3))),
                                          __ffma2_rn(make_float2(u2f(dv[e * 8 + 4 * h + 2]), u2f(dv[e * 8 + 4 * h + 3])), q4,
                                                     make_float2(-d4.z, -d4.w)));
-            const float v[4] = {v0.x, v0.y, v1.x, v1.y};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) dsv[4 * h + t] = (aa[t] == j) ? -rr4[t] : v[t];
+            pk[2 * h] = pack_f16x2_sat(v0.x, v0.y);
+            pk[2 * h + 1] = pack_f16x2_sat(v1.x, v1.y);
           }
-          st_tile16(sDS, r, cg >> 3,
-                    make_uint4(pack_f16x2_sat(dsv[0], dsv[1]), pack_f16x2_sat(dsv[2], dsv[3]),
-                               pack_f16x2_sat(dsv[4], dsv[5]), pack_f16x2_sat(dsv[6], dsv[7])));
+          st_tile16(sDS, r, cg >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        }
+      }
+      // argmax entries of this warp's columns and rows: -R_i replaces the value at
+      // (a_i - k0, i) (the thread owning that key row wrote it above)
+#pragma unroll
+      for (int wd = 0; wd < 2; ++wd) {
+        uint32_t bits = st_amask[(cbase >> 5) + wd];
+        while (bits) {
+          const int col = cbase + 32 * wd + __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (st_a[col] - k0 == r) {
+            const int chunk = col >> 3;
+            const uint32_t h16 = pack_f16x2_sat(-st_r[col], 0.0f) & 0xffffu;
+            *reinterpret_cast<unsigned short*>(sDS + (chunk >> 3) * BOX_BYTES + r * 128 +
+                                               (((chunk & 7) ^ (r & 7)) << 4) + (col & 7) * 2) =
+                static_cast<unsigned short>(h16);
+          }
         }
       }
       fence_proxy_async_smem();
