@@ -135,12 +135,13 @@ size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 
 /*
  * ra_attention_bwd_workspace_size -- bytes of device workspace ra_attention_bwd needs
- * for these sizes (either input dtype): four float arrays of B*H*N_Q entries
- * (D_i = dO_i . O_i, the argmax correction R_i, and two per-row constants of the
- * recomputed weights), then fp16 copies of q, dout, k and v, which the tensor-core
- * path multiplies in fp16 (exact for bf16 values up to 65504; P, E and dS are then
- * rounded to fp16 rather than bf16 before their products).  Each piece is padded to
- * 256 bytes.  Returns 0 for invalid sizes.
+ * for these sizes (either input dtype): per (batch*head, 128-row query tile) a block
+ * of five 128-entry arrays (two constants of the recomputed weights, D_i = dO_i . O_i,
+ * the argmax correction R_i and the argmax index), at least two float arrays of
+ * B*H*N_Q entries, then fp16 copies of q, dout, k and v, which the tensor-core path
+ * multiplies in fp16 (exact for bf16 values up to 65504; P, E and dS are then rounded
+ * to fp16 rather than bf16 before their products).  Each piece is padded to 256
+ * bytes.  Returns 0 for invalid sizes.
  */
 size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 

@@ -1,6 +1,7 @@
 // The C ABI of libraattn (declared in include/raattn.h): argument validation,
 // TMA tensor-map construction, the device status word, and dispatch to the
 // kernels.  Nothing here allocates device memory.
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -83,18 +84,22 @@ bool make_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int D) {
   return make_map_16bit(map, base, BH, N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
-// Backward workspace: four per-row float arrays, then (tensor-core path only) fp16
-// copies of Q, K, V and dO; every piece starts on a 256-byte boundary.
+// Backward workspace.  CUDA-core path: D_i and R_i per row.  Tensor-core path: the
+// per-query-tile constant blocks, then the fp16 copies of Q, dO, K and V.  Every piece
+// starts on a 256-byte boundary.
 struct BwdLayout {
-  size_t per_row, q16, kv16, total_f32, total_tc;
+  size_t per_row, consts, head, q16, kv16, total_f32, total_tc;
   BwdLayout(int B, int H, int NQ, int NK, int D) {
     auto pad = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t bh = static_cast<size_t>(B) * H;
+    const size_t nqt = (static_cast<size_t>(NQ) + 127) / 128;
     per_row = pad(bh * NQ * sizeof(float));
+    consts = pad(bh * nqt * kConstBlockFloats * sizeof(float));
+    total_f32 = 2 * per_row;
+    head = std::max(total_f32, consts);
     q16 = pad(bh * NQ * D * 2);
     kv16 = pad(bh * NK * D * 2);
-    total_f32 = 4 * per_row;
-    total_tc = total_f32 + 2 * q16 + 2 * kv16;
+    total_tc = head + 2 * q16 + 2 * kv16;
   }
 };
 
@@ -262,10 +267,10 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
   if (make_ctx(&ctx) != RA_OK) return RA_ERR_LAUNCH;
   BwdTcArgs a;
   const int BH = B * H;
-  a.q16 = ws + lay.total_f32;
-  a.do16 = ws + lay.total_f32 + lay.q16;
-  a.k16 = ws + lay.total_f32 + 2 * lay.q16;
-  a.v16 = ws + lay.total_f32 + 2 * lay.q16 + lay.kv16;
+  a.q16 = ws + lay.head;
+  a.do16 = ws + lay.head + lay.q16;
+  a.k16 = ws + lay.head + 2 * lay.q16;
+  a.v16 = ws + lay.head + 2 * lay.q16 + lay.kv16;
   const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (!make_map_16bit(&a.tm_q, a.q16, BH, N_Q, D, f16) || !make_map_16bit(&a.tm_k, a.k16, BH, N_K, D, f16) ||
       !make_map_16bit(&a.tm_v, a.v16, BH, N_K, D, f16) || !make_map_16bit(&a.tm_do, a.do16, BH, N_Q, D, f16))
@@ -283,10 +288,7 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
   a.dk = dk;
   a.dv = dv;
   a.grad_bf16 = grad_dtype == RA_BF16 ? 1 : 0;
-  a.ws_d = ws_d;
-  a.ws_r = ws_r;
-  a.ws_base = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * per);
-  a.ws_invs = reinterpret_cast<float*>(static_cast<char*>(workspace) + 3 * per);
+  a.ws_consts = reinterpret_cast<float*>(ws);
   const cudaError_t e = launch_attn_bwd_tc(s, a, ctx, st);
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }

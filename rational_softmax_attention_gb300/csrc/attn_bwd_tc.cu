@@ -450,11 +450,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     if (ok) ok = warp_wait(dq_full, 0);
     if (ok) {
       tc_fence_after();
-      if (i_ok && half == 0) {
-        args.ws_d[ro] = Di;
-        args.ws_r[ro] = R;
-        args.ws_base[ro] = base;
-        args.ws_invs[ro] = inv_s;
+      if (half == 0) {   // this query tile's constant block for the dK/dV kernel
+        float* blk = args.ws_consts + (static_cast<size_t>(bh) * nqt + qt) * kConstBlockFloats;
+        blk[r] = base;   // 2 past N_Q: w = 1, zero weight
+        blk[BM + r] = i_ok ? inv_s : 0.0f;
+        blk[2 * BM + r] = i_ok ? 0.25f * Di : 0.0f;
+        blk[3 * BM + r] = i_ok ? R : 0.0f;
+        reinterpret_cast<int*>(blk)[4 * BM + r] = i_ok ? args.row_arg[ro] : -1;
       }
       const char* krow = reinterpret_cast<const char*>(args.k_raw) + (static_cast<size_t>(bh) * s.NK + a) * D * 2;
       // each half of the warps stores half of the D columns of its rows
@@ -500,18 +502,27 @@ struct DkvCfg {
   static constexpr int OFF_DO = OFF_Q + NQS * TILE;
   static constexpr int OFF_P = OFF_DO + NDS * TILE;
   static constexpr int OFF_DS = OFF_P + A_BYTES;
-  static constexpr int OFF_ST = OFF_DS + A_BYTES;          // per-query constants of one tile
-  static constexpr int ST_BYTES = 5 * BM * 4 + 16;         // + 128-bit mask: argmax in this key tile
-  static constexpr int OFF_BAR = OFF_ST + ST_BYTES;
+  // Per-query constants of one query tile, in two single-buffered parts with their own
+  // lifetimes: X (base_i, 1/s_i) is read in the P^T loop, Y (D_i/4, R_i, a_i) in the dS^T
+  // loop and the argmax fix-up.  X of the next tile arrives while the warps are in the
+  // dS^T loop, Y while they are in the next P^T loop.
+  static constexpr int OFF_CX = OFF_DS + A_BYTES;
+  static constexpr int CX_BYTES = 2 * BM * 4;
+  static constexpr int OFF_CY = OFF_CX + CX_BYTES;
+  static constexpr int CY_BYTES = 3 * BM * 4;
+  static constexpr int OFF_BAR = OFF_CY + CY_BYTES;
   // kv_full, q_full[NQS], q_empty[NQS], do_full[NDS], do_empty[NDS],
-  // st_full, st_free, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2]
-  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 9;
+  // st_full, st_free, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2],
+  // cx_full, cx_empty, cy_full, cy_empty
+  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 13;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int USED = OFF_MISC + 16;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
   // 1024-byte aligned dynamic shared-memory base
   static constexpr int SLACK = (USED + 1024 <= 232448) ? 1024 : 0;
   static constexpr int SMEM_BYTES = USED + SLACK;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(CX_BYTES + CY_BYTES == kConstBlockFloats * 4, "constant block layout");
 };
 constexpr uint32_t KV_TM_ST = 0, KV_TM_DPT = 128, KV_TM_DV = 256, KV_TM_DK = 384;
 // 8 softmax warps: warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the same key rows)
@@ -521,8 +532,6 @@ constexpr int KV_PRODUCER_WARP = 8;
 // two MMA-issuing threads: warp 9 issues S^T and dP^T, warp 10 issues dV and dK
 constexpr int KV_MMA_WARP = 9;
 constexpr int KV_THREADS = 352;
-
-__device__ __forceinline__ void softmax_group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(KV_THREADS, 1)
@@ -541,12 +550,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint8_t* sDO = smem + C::OFF_DO;
   uint8_t* sP = smem + C::OFF_P;
   uint8_t* sDS = smem + C::OFF_DS;
-  float* st_base = reinterpret_cast<float*>(smem + C::OFF_ST);
+  float* st_base = reinterpret_cast<float*>(smem + C::OFF_CX);
   float* st_invs = st_base + BM;
-  float* st_d = st_base + 2 * BM;
-  float* st_r = st_base + 3 * BM;
-  int* st_a = reinterpret_cast<int*>(st_base + 4 * BM);
-  uint32_t* st_amask = reinterpret_cast<uint32_t*>(st_base + 5 * BM);   // bit i: a_i in [k0, k0 + BN)
+  float* st_d = reinterpret_cast<float*>(smem + C::OFF_CY);
+  float* st_r = st_d + BM;
+  int* st_a = reinterpret_cast<int*>(st_d + 2 * BM);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* q_full = kv_full + 1;
@@ -561,6 +569,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* p_free = p_full + 1;
   uint64_t* acc_full = p_free + 1;
   uint64_t* drain = acc_full + 1;   // [2], one per issuer
+  uint64_t* cx_full = drain + 2;
+  uint64_t* cx_empty = cx_full + 1;
+  uint64_t* cy_full = cx_empty + 1;
+  uint64_t* cy_empty = cy_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -597,6 +609,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     mbar_init(acc_full, 1);
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
+    mbar_init(cx_full, 1);
+    mbar_init(cx_empty, KV_SOFTMAX_WARPS);
+    mbar_init(cy_full, 1);
+    mbar_init(cy_empty, KV_SOFTMAX_WARPS);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -622,10 +638,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         tma_load_3d(sV + c * BOX_BYTES, &args.tm_v, kv_full, c * 64, k0, bh);
       }
       bool ok = true;
-      int q_issued = 0, d_issued = 0;
+      int q_issued = 0, d_issued = 0, cx_issued = 0, cy_issued = 0;
       for (int it = 0; it < nq && ok; ++it) {
         const int i0 = (qt0 + it) * BM;
         const int qs = it % C::NQS;
+        const uint32_t cpar = (it & 1u) ^ 1u;
+        const float* blk = args.ws_consts + (static_cast<size_t>(bh) * nqt + qt0 + it) * kConstBlockFloats;
         ok = mbar_wait(&q_empty[qs], ((it / C::NQS) & 1u) ^ 1u, abort_flag, ctx);
         if (!ok) break;
         mbar_arrive_expect_tx(&q_full[qs], C::TILE);
@@ -633,6 +651,16 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sQ + qs * C::TILE + c * BOX_BYTES, &args.tm_q, &q_full[qs], c * 64, i0, bh);
         q_issued = it + 1;
+        ok = mbar_wait(cx_empty, cpar, abort_flag, ctx);
+        if (!ok) break;
+        mbar_arrive_expect_tx(cx_full, C::CX_BYTES);
+        bulk_load_1d(st_base, blk, C::CX_BYTES, cx_full);
+        cx_issued = it + 1;
+        ok = mbar_wait(cy_empty, cpar, abort_flag, ctx);
+        if (!ok) break;
+        mbar_arrive_expect_tx(cy_full, C::CY_BYTES);
+        bulk_load_1d(st_d, blk + 2 * BM, C::CY_BYTES, cy_full);
+        cy_issued = it + 1;
         const int ds = it % C::NDS;
         ok = mbar_wait(&do_empty[ds], ((it / C::NDS) & 1u) ^ 1u, abort_flag, ctx);
         if (!ok) break;
@@ -647,6 +675,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         drain_wait(&q_full[it % C::NQS], (it / C::NQS) & 1u, ctx);
       for (int it = max(0, d_issued - C::NDS); it < d_issued; ++it)
         drain_wait(&do_full[it % C::NDS], (it / C::NDS) & 1u, ctx);
+      if (cx_issued > 0) drain_wait(cx_full, (cx_issued - 1) & 1u, ctx);
+      if (cy_issued > 0) drain_wait(cy_full, (cy_issued - 1) & 1u, ctx);
     }
   } else if (warp >= KV_MMA_WARP) {
     const int who = warp - KV_MMA_WARP;   // 0: S^T and dP^T products; 1: dV and dK products
@@ -726,7 +756,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     const int j = k0 + r;
     const bool j_ok = j < s.NK;
     const size_t ko = static_cast<size_t>(bh) * s.NK + (j_ok ? j : s.NK - 1);
-    const size_t so = static_cast<size_t>(bh) * s.NQ;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = s.scale * (1.0f / 32.0f);
     bool ok = true;
@@ -744,23 +773,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     for (int it = 0; it < nq; ++it) {
       const int i0 = (qt0 + it) * BM;
       const uint32_t par = it & 1u;
-      // per-query constants of this tile (queries past N_Q get base 2: zero weight)
-      softmax_group_sync();
-      if (threadIdx.x < BM) {
-        const int ii = i0 + threadIdx.x;
-        const bool q_ok = ii < s.NQ;
-        const size_t qo = so + (q_ok ? ii : 0);
-        st_base[threadIdx.x] = q_ok ? args.ws_base[qo] : 2.0f;
-        st_invs[threadIdx.x] = q_ok ? args.ws_invs[qo] : 0.0f;
-        st_d[threadIdx.x] = q_ok ? 0.25f * args.ws_d[qo] : 0.0f;   // D_i / 4
-        st_r[threadIdx.x] = q_ok ? args.ws_r[qo] : 0.0f;
-        const int ai = q_ok ? args.row_arg[qo] : -1;
-        st_a[threadIdx.x] = ai;
-        // about BM / N_K * BN of a tile's queries have their argmax among this CTA's keys
-        const uint32_t bits = __ballot_sync(0xffffffffu, ai >= k0 && ai < k0 + BN);
-        if (lane == 0) st_amask[warp] = bits;
-      }
-      softmax_group_sync();
+      // this tile's per-query constants X (queries past N_Q carry base 2: zero weight)
+      warp_wait(cx_full, par);
       warp_wait(st_full, par);
       tc_fence_after();
       tmem_ld32(lane_addr + KV_TM_ST + cbase, sv[0]);
@@ -813,8 +827,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         }
         st_tile16(sP, r, (cbase + c) >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx_empty);   // this warp's reads of X are done
       // dS^T = coef (dP^T - D_i); the entries (a_i, i) where this key is the query's argmax
       // take -R_i afterwards
+      warp_wait(cy_full, par);
       warp_wait(dpt_full, par);
       tc_fence_after();
 #pragma unroll
@@ -850,26 +867,28 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           st_tile16(sDS, r, cg >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
       }
-      // argmax entries of this warp's columns and rows: -R_i replaces the value at
-      // (a_i - k0, i) (the thread owning that key row wrote it above)
+      // Argmax entries in this warp's rows and columns: -R_i replaces the value at
+      // (a_i - k0, i).  Lane l looks at columns cbase + l and cbase + 32 + l; about
+      // BN / N_K of a tile's queries have their argmax among this CTA's keys.
+      __syncwarp();   // the row owners' stores above come first
 #pragma unroll
       for (int wd = 0; wd < 2; ++wd) {
-        uint32_t bits = st_amask[(cbase >> 5) + wd];
-        while (bits) {
-          const int col = cbase + 32 * wd + __ffs(bits) - 1;
-          bits &= bits - 1;
-          if (st_a[col] - k0 == r) {
-            const int chunk = col >> 3;
-            const uint32_t h16 = pack_f16x2_sat(-st_r[col], 0.0f) & 0xffffu;
-            *reinterpret_cast<unsigned short*>(sDS + (chunk >> 3) * BOX_BYTES + r * 128 +
-                                               (((chunk & 7) ^ (r & 7)) << 4) + (col & 7) * 2) =
-                static_cast<unsigned short>(h16);
-          }
+        const int col = cbase + 32 * wd + lane;
+        const int rr = st_a[col] - k0;
+        if (rr >= quarter * 32 && rr < quarter * 32 + 32) {
+          const int chunk = col >> 3;
+          const uint32_t h16 = pack_f16x2_sat(-st_r[col], 0.0f) & 0xffffu;
+          *reinterpret_cast<unsigned short*>(sDS + (chunk >> 3) * BOX_BYTES + rr * 128 +
+                                             (((chunk & 7) ^ (rr & 7)) << 4) + (col & 7) * 2) =
+              static_cast<unsigned short>(h16);
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) {
+        mbar_arrive(cy_empty);   // this warp's reads of Y are done
+        mbar_arrive(p_full);
+      }
     }
 #undef SV
     if (nq > 0) warp_wait(acc_full, 0);

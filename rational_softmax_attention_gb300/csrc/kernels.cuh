@@ -68,11 +68,14 @@ struct BwdTcArgs {
   void* dk;
   void* dv;
   int grad_bf16;
-  float* ws_d;      // [B*H*NQ]  D_i = dO_i . O_i
-  float* ws_r;      // [B*H*NQ]  R_i = sum_j E_ij (argmax excluded)
-  float* ws_base;   // [B*H*NQ]  0.5 + row_m_i / 32 (so w = (1+u)/2 = base - scale*s/32)
-  float* ws_invs;   // [B*H*NQ]  1 / row_s_i
+  // Per-query constants, one 2560-byte block per (batch*head, 128-row query tile), written
+  // by the dQ kernel and bulk-copied by the dK/dV kernel: [5][128] of
+  //   base_i = 0.5 + scale * row_m_i / 32 (so w = (1+u)/2 = base_i - scale * s / 32),
+  //   1 / row_s_i, D_i / 4 (D_i = dO_i . O_i), R_i = sum_j E_ij (argmax excluded), and
+  //   the argmax index a_i (int32 bits); rows past N_Q hold 2, 0, 0, 0, -1.
+  float* ws_consts;
 };
+constexpr int kConstBlockFloats = 5 * 128;
 cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st);
 
 }  // namespace raattn
