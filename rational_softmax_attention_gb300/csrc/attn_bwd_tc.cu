@@ -513,8 +513,8 @@ struct DkvCfg {
   static constexpr int OFF_BAR = OFF_CY + CY_BYTES;
   // kv_full, q_full[NQS], q_empty[NQS], do_full[NDS], do_empty[NDS],
   // st_full, st_free, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2],
-  // cx_full, cx_empty, cy_full, cy_empty
-  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 13;
+  // cx_full, cx_empty, cy_full, cy_empty, ds_full, ds_free
+  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 15;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int USED = OFF_MISC + 16;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
@@ -573,6 +573,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* cx_empty = cx_full + 1;
   uint64_t* cy_full = cx_empty + 1;
   uint64_t* cy_empty = cy_full + 1;
+  uint64_t* ds_full = cy_empty + 1;   // dS^T tile written (P^T has p_full / p_free)
+  uint64_t* ds_free = ds_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -613,6 +615,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     mbar_init(cx_empty, KV_SOFTMAX_WARPS);
     mbar_init(cy_full, 1);
     mbar_init(cy_empty, KV_SOFTMAX_WARPS);
+    mbar_init(ds_full, KV_SOFTMAX_WARPS);
+    mbar_init(ds_free, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -656,11 +660,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         mbar_arrive_expect_tx(cx_full, C::CX_BYTES);
         bulk_load_1d(st_base, blk, C::CX_BYTES, cx_full);
         cx_issued = it + 1;
-        ok = mbar_wait(cy_empty, cpar, abort_flag, ctx);
-        if (!ok) break;
-        mbar_arrive_expect_tx(cy_full, C::CY_BYTES);
-        bulk_load_1d(st_d, blk + 2 * BM, C::CY_BYTES, cy_full);
-        cy_issued = it + 1;
         const int ds = it % C::NDS;
         ok = mbar_wait(&do_empty[ds], ((it / C::NDS) & 1u) ^ 1u, abort_flag, ctx);
         if (!ok) break;
@@ -669,6 +668,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sDO + ds * C::TILE + c * BOX_BYTES, &args.tm_do, &do_full[ds], c * 64, i0, bh);
         d_issued = it + 1;
+        ok = mbar_wait(cy_empty, cpar, abort_flag, ctx);
+        if (!ok) break;
+        mbar_arrive_expect_tx(cy_full, C::CY_BYTES);
+        bulk_load_1d(st_d, blk + 2 * BM, C::CY_BYTES, cy_full);
+        cy_issued = it + 1;
       }
       drain_wait(kv_full, 0, ctx);
       for (int it = max(0, q_issued - C::NQS); it < q_issued; ++it)
@@ -721,24 +725,35 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           tc_commit(dpt_full);
           tc_commit(&do_empty[ds]);
         } else {
-          // dV += P^T dO_i, dK += dS^T Q_i
-          ok = mbar_wait(p_full, par, abort_flag, ctx) &&
-               mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
-               mbar_wait(&do_full[ds], (it / C::NDS) & 1u, abort_flag, ctx);
+          // dV += P^T dO_i as soon as P^T is written (its release lets the softmax warps
+          // write the next P^T and the producer load the next dO), then dK += dS^T Q_i.
+          // Q_i and dO_i arrived long before: waiting on them first leaves a single wait
+          // between the softmax warps' arrival and the first product.
+          ok = mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
+               mbar_wait(&do_full[ds], (it / C::NDS) & 1u, abort_flag, ctx) &&
+               mbar_wait(p_full, par, abort_flag, ctx);
           if (!ok) break;
           tc_fence_after();
           const uint32_t qmn = sdesc_lo(aQ + qs * C::TILE, BOX_BYTES), domn = sdesc_lo(aDO + ds * C::TILE, BOX_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk) {
             const uint32_t aoff = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
-            const uint32_t boff = (kk * 2048) >> 4;
-            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-            tc_mma_f16(tmem + KV_TM_DV, sdesc(plo + aoff, HI), sdesc(domn + boff, HI), idesc_kmn, acc);
-            tc_mma_f16(tmem + KV_TM_DK, sdesc(dslo + aoff, HI), sdesc(qmn + boff, HI), idesc_kmn, acc);
+            tc_mma_f16(tmem + KV_TM_DV, sdesc(plo + aoff, HI), sdesc(domn + ((kk * 2048) >> 4), HI), idesc_kmn,
+                       (it > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&do_empty[ds]);
-          tc_commit(&q_empty[qs]);
           tc_commit(p_free);
+          ok = mbar_wait(ds_full, par, abort_flag, ctx);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk) {
+            const uint32_t aoff = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+            tc_mma_f16(tmem + KV_TM_DK, sdesc(dslo + aoff, HI), sdesc(qmn + ((kk * 2048) >> 4), HI), idesc_kmn,
+                       (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&q_empty[qs]);
+          tc_commit(ds_free);
         }
       }
       if (ok && who == 1) tc_commit(acc_full);
@@ -827,11 +842,16 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         }
         st_tile16(sP, r, (cbase + c) >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
       }
+      fence_proxy_async_smem();   // P^T stores -> the tensor core
       __syncwarp();
-      if (lane == 0) mbar_arrive(cx_empty);   // this warp's reads of X are done
+      if (lane == 0) {
+        mbar_arrive(cx_empty);   // this warp's reads of X are done
+        mbar_arrive(p_full);
+      }
       // dS^T = coef (dP^T - D_i); the entries (a_i, i) where this key is the query's argmax
       // take -R_i afterwards
       warp_wait(cy_full, par);
+      warp_wait(ds_free, par ^ 1u);   // dK of the previous tile has read dS^T
       warp_wait(dpt_full, par);
       tc_fence_after();
 #pragma unroll
@@ -887,7 +907,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(cy_empty);   // this warp's reads of Y are done
-        mbar_arrive(p_full);
+        mbar_arrive(ds_full);
       }
     }
 #undef SV
