@@ -494,14 +494,13 @@ template <int D>
 struct DkvCfg {
   static constexpr int TILE = BN * D * 2;
   static constexpr int NQS = 2;                    // Q stages
-  static constexpr int NDS = (D == 128) ? 1 : 2;   // dO stages
-  static constexpr int A_BYTES = BN * BM * 2;      // P^T or dS^T tile (keys x queries, bf16)
+  static constexpr int NDS = 2;                    // dO stages
+  static constexpr int A_BYTES = BN * BM * 2;      // dS^T tile (keys x queries, fp16)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + NQS * TILE;
-  static constexpr int OFF_P = OFF_DO + NDS * TILE;
-  static constexpr int OFF_DS = OFF_P + A_BYTES;
+  static constexpr int OFF_DS = OFF_DO + NDS * TILE;
   // Per-query constants of one query tile, in two single-buffered parts with their own
   // lifetimes: X (base_i, 1/s_i) is read in the P^T loop, Y (D_i/4, R_i, a_i) in the dS^T
   // loop and the argmax fix-up.  X of the next tile arrives while the warps are in the
@@ -512,9 +511,9 @@ struct DkvCfg {
   static constexpr int CY_BYTES = 3 * BM * 4;
   static constexpr int OFF_BAR = OFF_CY + CY_BYTES;
   // kv_full, q_full[NQS], q_empty[NQS], do_full[NDS], do_empty[NDS],
-  // st_full, st_free, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2],
+  // st_full, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2],
   // cx_full, cx_empty, cy_full, cy_empty, ds_full, ds_free
-  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 15;
+  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 14;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int USED = OFF_MISC + 16;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
@@ -548,7 +547,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sDO = smem + C::OFF_DO;
-  uint8_t* sP = smem + C::OFF_P;
   uint8_t* sDS = smem + C::OFF_DS;
   float* st_base = reinterpret_cast<float*>(smem + C::OFF_CX);
   float* st_invs = st_base + BM;
@@ -562,8 +560,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* do_full = q_empty + C::NQS;
   uint64_t* do_empty = do_full + C::NDS;
   uint64_t* st_full = do_empty + C::NDS;
-  uint64_t* st_free = st_full + 1;
-  uint64_t* dpt_full = st_free + 1;
+  uint64_t* dpt_full = st_full + 1;
   uint64_t* dpt_free = dpt_full + 1;
   uint64_t* p_full = dpt_free + 1;
   uint64_t* p_free = p_full + 1;
@@ -603,7 +600,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       mbar_init(&do_empty[i], 2);   // dP^T (issuer 0) and dV (issuer 1) read dO_i
     }
     mbar_init(st_full, 1);
-    mbar_init(st_free, KV_SOFTMAX_WARPS);
     mbar_init(dpt_full, 1);
     mbar_init(dpt_free, KV_SOFTMAX_WARPS);
     mbar_init(p_full, KV_SOFTMAX_WARPS);
@@ -689,7 +685,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       constexpr uint32_t idesc_kmn = idesc_fp16_f32(BN, D, 0, 1);
       constexpr uint32_t HI = sdesc_hi_sw128(1024);
       const uint32_t klo = sdesc_lo(smem_u32(sK), 16), vlo = sdesc_lo(smem_u32(sV), 16),
-                     plo = sdesc_lo(smem_u32(sP), 16), dslo = sdesc_lo(smem_u32(sDS), 16);
+                     dslo = sdesc_lo(smem_u32(sDS), 16);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
       bool ok = mbar_wait(kv_full, 0, abort_flag, ctx);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
@@ -700,7 +696,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         if (who == 0) {
           // S^T = K Q_i^T
           ok = mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
-               mbar_wait(st_free, par ^ 1u, abort_flag, ctx);
+               mbar_wait(p_free, par ^ 1u, abort_flag, ctx);
           if (!ok) break;
           tc_fence_after();
           const uint32_t qlo = sdesc_lo(aQ + qs * C::TILE, 16);
@@ -725,8 +721,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           tc_commit(dpt_full);
           tc_commit(&do_empty[ds]);
         } else {
-          // dV += P^T dO_i as soon as P^T is written (its release lets the softmax warps
-          // write the next P^T and the producer load the next dO), then dK += dS^T Q_i.
+          // dV += P^T dO_i as soon as P^T is written (its release lets S^T of the next
+          // tile be issued and the producer load the next dO), then dK += dS^T Q_i.
           // Q_i and dO_i arrived long before: waiting on them first leaves a single wait
           // between the softmax warps' arrival and the first product.
           ok = mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
@@ -737,9 +733,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           const uint32_t qmn = sdesc_lo(aQ + qs * C::TILE, BOX_BYTES), domn = sdesc_lo(aDO + ds * C::TILE, BOX_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk) {
-            const uint32_t aoff = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
-            tc_mma_f16(tmem + KV_TM_DV, sdesc(plo + aoff, HI), sdesc(domn + ((kk * 2048) >> 4), HI), idesc_kmn,
-                       (it > 0 || kk > 0) ? 1u : 0u);
+            // P^T from tensor memory: the softmax warps of query half kk / 4 wrote it, 8
+            // columns per 16 queries, over the first 32 of their 64 S^T columns
+            tc_mma_f16_ts(tmem + KV_TM_DV, tmem + KV_TM_ST + 64 * (kk >> 2) + 8 * (kk & 3),
+                          sdesc(domn + ((kk * 2048) >> 4), HI), idesc_kmn, (it > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&do_empty[ds]);
           tc_commit(p_free);
@@ -795,19 +792,18 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       tmem_ld32(lane_addr + KV_TM_ST + cbase, sv[0]);
       tmem_ld32(lane_addr + KV_TM_ST + cbase + 32, sv[1]);
       tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(st_free);
       // masked: key past N_K, or (causal) query i0 + c < j
       const bool need_mask = !j_ok || (s.causal && i0 + cbase < j);
       const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
-      warp_wait(p_free, par ^ 1u);
       // P^T = q^8 / s_i and the dS coefficient q^7 (1/w)^2 / s_i = q^7 (1 + q)^2 / s_i (in
       // place): with t = q^7 / s_i, P = t q and the coefficient is t + P (2 + q).  The factor
       // 1/4 comes with dP^T - D_i below.  Four entries share two reciprocals (as in coef_quad).
+      // P^T goes to tensor memory as fp16 pairs over the first 32 of this warp's 64 S^T
+      // columns (already read; S^T of the next tile is issued only after dV has read P^T).
+      uint32_t pt[16];
 #pragma unroll
       for (int c = 0; c < 64; c += 8) {
-        uint32_t pk[4];
+        uint32_t* pk = pt + ((c & 31) >> 1);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int cb = c + 4 * h;        // local column
@@ -840,9 +836,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           pk[2 * h] = pack_f16x2_sat(pa.x, pa.y);
           pk[2 * h + 1] = pack_f16x2_sat(pb.x, pb.y);
         }
-        st_tile16(sP, r, (cbase + c) >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        if ((c & 31) == 24) tmem_st16(lane_addr + KV_TM_ST + cbase + ((c & 32) >> 1), pt);
       }
-      fence_proxy_async_smem();   // P^T stores -> the tensor core
+      tc_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(cx_empty);   // this warp's reads of X are done
