@@ -524,13 +524,15 @@ struct DkvCfg {
   static_assert(CX_BYTES + CY_BYTES == kConstBlockFloats * 4, "constant block layout");
 };
 constexpr uint32_t KV_TM_ST = 0, KV_TM_DPT = 128, KV_TM_DV = 256, KV_TM_DK = 384;
-// 8 softmax warps: warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the same key rows)
-// and split each tile's 128 query columns 64 / 64, two warps per scheduler.
-constexpr int KV_SOFTMAX_WARPS = 8;
-constexpr int KV_PRODUCER_WARP = 8;
-// two MMA-issuing threads: warp 9 issues S^T and dP^T, warp 10 issues dV and dK
-constexpr int KV_MMA_WARP = 9;
-constexpr int KV_THREADS = 352;
+// 16 softmax warps, four per scheduler: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its key
+// rows) and query columns [KV_COLS (w / 4), KV_COLS (w / 4) + KV_COLS) of every tile.
+constexpr int KV_SOFTMAX_WARPS = 16;
+constexpr int KV_COLS = BM * 4 / KV_SOFTMAX_WARPS;   // 32
+constexpr int KV_PRODUCER_WARP = KV_SOFTMAX_WARPS;
+// two MMA-issuing threads: the first issues S^T and dP^T, the second dV and dK
+constexpr int KV_MMA_WARP = KV_SOFTMAX_WARPS + 1;
+constexpr int KV_THREADS = 32 * (KV_SOFTMAX_WARPS + 3);
+static_assert(KV_COLS % 32 == 0, "whole 32-column TMEM loads per softmax warp");
 
 template <int D>
 __global__ void __launch_bounds__(KV_THREADS, 1)
@@ -733,9 +735,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           const uint32_t qmn = sdesc_lo(aQ + qs * C::TILE, BOX_BYTES), domn = sdesc_lo(aDO + ds * C::TILE, BOX_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk) {
-            // P^T from tensor memory: the softmax warps of query half kk / 4 wrote it, 8
-            // columns per 16 queries, over the first 32 of their 64 S^T columns
-            tc_mma_f16_ts(tmem + KV_TM_DV, tmem + KV_TM_ST + 64 * (kk >> 2) + 8 * (kk & 3),
+            // P^T from tensor memory: the softmax warps of queries 16 kk .. 16 kk + 15 wrote
+            // it over the first half of their S^T columns, 8 columns per 16 queries
+            tc_mma_f16_ts(tmem + KV_TM_DV,
+                          tmem + KV_TM_ST + (16 * kk / KV_COLS) * KV_COLS + (16 * kk % KV_COLS) / 2,
                           sdesc(domn + ((kk * 2048) >> 4), HI), idesc_kmn, (it > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&do_empty[ds]);
@@ -762,8 +765,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (key rows) and query columns
     // [64 (w / 4), 64 (w / 4) + 64) of every tile.
     const int quarter = warp & 3;
-    const int half = warp >> 2;
-    const int cbase = half * 64;
+    const int part = warp >> 2;
+    const int cbase = part * KV_COLS;
     const int r = quarter * 32 + lane;
     const int j = k0 + r;
     const bool j_ok = j < s.NK;
@@ -780,7 +783,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       if (lane == 0) okv = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, okv, 0) != 0;
     };
-    uint32_t sv[2][32];
+    uint32_t sv[KV_COLS / 32][32];
 #define SV(c) sv[(c) >> 5][(c) & 31]
     for (int it = 0; it < nq; ++it) {
       const int i0 = (qt0 + it) * BM;
@@ -789,8 +792,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       warp_wait(cx_full, par);
       warp_wait(st_full, par);
       tc_fence_after();
-      tmem_ld32(lane_addr + KV_TM_ST + cbase, sv[0]);
-      tmem_ld32(lane_addr + KV_TM_ST + cbase + 32, sv[1]);
+#pragma unroll
+      for (int h = 0; h < KV_COLS / 32; ++h) tmem_ld32(lane_addr + KV_TM_ST + cbase + 32 * h, sv[h]);
       tc_wait_ld();
       // masked: key past N_K, or (causal) query i0 + c < j
       const bool need_mask = !j_ok || (s.causal && i0 + cbase < j);
@@ -798,11 +801,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       // P^T = q^8 / s_i and the dS coefficient q^7 (1/w)^2 / s_i = q^7 (1 + q)^2 / s_i (in
       // place): with t = q^7 / s_i, P = t q and the coefficient is t + P (2 + q).  The factor
       // 1/4 comes with dP^T - D_i below.  Four entries share two reciprocals (as in coef_quad).
-      // P^T goes to tensor memory as fp16 pairs over the first 32 of this warp's 64 S^T
+      // P^T goes to tensor memory as fp16 pairs over the first half of this warp's S^T
       // columns (already read; S^T of the next tile is issued only after dV has read P^T).
       uint32_t pt[16];
 #pragma unroll
-      for (int c = 0; c < 64; c += 8) {
+      for (int c = 0; c < KV_COLS; c += 8) {
         uint32_t* pk = pt + ((c & 31) >> 1);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -852,11 +855,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       warp_wait(dpt_full, par);
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < KV_COLS / 32; ++cc) {
         uint32_t dv[32];
         tmem_ld32(lane_addr + KV_TM_DPT + cbase + cc * 32, dv);
         tc_wait_ld();
-        if (cc == 1) {
+        if (cc == KV_COLS / 32 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(dpt_free);
@@ -885,11 +888,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         }
       }
       // Argmax entries in this warp's rows and columns: -R_i replaces the value at
-      // (a_i - k0, i).  Lane l looks at columns cbase + l and cbase + 32 + l; about
+      // (a_i - k0, i).  Lane l looks at columns cbase + l (+ 32 ...); about
       // BN / N_K of a tile's queries have their argmax among this CTA's keys.
       __syncwarp();   // the row owners' stores above come first
 #pragma unroll
-      for (int wd = 0; wd < 2; ++wd) {
+      for (int wd = 0; wd < KV_COLS / 32; ++wd) {
         const int col = cbase + 32 * wd + lane;
         const int rr = st_a[col] - k0;
         if (rr >= quarter * 32 && rr < quarter * 32 + 32) {
@@ -911,9 +914,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     if (nq > 0) warp_wait(acc_full, 0);
     if (ok) {
       tc_fence_after();
-      // each half of the warps stores half of the D columns of its key rows
+      // the warps of a row quarter store 32-column chunks of its key rows in turn
 #pragma unroll
-      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+      for (int c0 = part * 32; c0 < D; c0 += 32 * (KV_SOFTMAX_WARPS / 4)) {
         uint32_t av[32], kv[32];
         tmem_ld32(lane_addr + KV_TM_DV + c0, av);
         tmem_ld32(lane_addr + KV_TM_DK + c0, kv);
