@@ -123,28 +123,43 @@ struct DqCfg {
   // dp_full, dp_free, e_full, e_free, dq_full, drain[2]
   static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 4 + 7;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int OFF_XCH = OFF_MISC + 16;   // [2][128] floats: per-half partials of D_i, then R_i
-  static constexpr int SMEM_BYTES = OFF_XCH + 2 * BM * 4 + 1024;
+  static constexpr int OFF_XCH = OFF_MISC + 16;   // [4][128] floats: per-part partials of D_i, then R_i
+  static constexpr int USED = OFF_XCH + 4 * BM * 4;
+  // alignment slack only where it fits; otherwise the kernel requires (and checks) a
+  // 1024-byte aligned dynamic shared-memory base
+  static constexpr int SLACK = (USED + 1024 <= 232448) ? 1024 : 0;
+  static constexpr int SMEM_BYTES = USED + SLACK;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 constexpr uint32_t DQ_TM_S0 = 0, DQ_TM_S1 = 128, DQ_TM_DP = 256, DQ_TM_DQ = 384;
-// 8 softmax warps: warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the same query
-// rows) and split each key tile's 128 columns 64 / 64, two warps per scheduler.
-constexpr int DQ_SOFTMAX_WARPS = 8;
-constexpr int DQ_PRODUCER_WARP = 8;
-// two MMA-issuing threads: warp 9 issues S and dP, warp 10 issues dQ.  A barrier wait
+// 16 softmax warps, four per scheduler: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its query
+// rows) and key columns [32 (w / 4), 32 (w / 4) + 32) of every tile.
+constexpr int DQ_SOFTMAX_WARPS = 16;
+constexpr int DQ_COLS = BN * 4 / DQ_SOFTMAX_WARPS;   // 32
+constexpr int DQ_PARTS = DQ_SOFTMAX_WARPS / 4;       // warps sharing a row quarter
+constexpr int DQ_PRODUCER_WARP = DQ_SOFTMAX_WARPS;
+// two MMA-issuing threads: the first issues S and dP, the second dQ.  A barrier wait
 // stalls its issuing thread for a few hundred cycles, longer than the two 64-cycle
 // products the tensor queue holds; the other issuer's products fill that time.
-constexpr int DQ_MMA_WARP = 9;
-constexpr int DQ_THREADS = 352;
+constexpr int DQ_MMA_WARP = DQ_SOFTMAX_WARPS + 1;
+constexpr int DQ_THREADS = 32 * (DQ_SOFTMAX_WARPS + 3);
+static_assert(DQ_COLS == 32, "one 32-column TMEM load per softmax warp and tile");
 
-__device__ __forceinline__ void softmax8_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void softmax_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(DQ_SOFTMAX_WARPS * 32) : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t mis = smem_u32(smem_raw) & 1023u;
+  if (C::SLACK == 0 && mis != 0) {   // uniform across the CTA: nothing launched yet
+    if (threadIdx.x == 0) atomicOr(ctx.status, kStatusBadSmem);
+    return;
+  }
+  uint8_t* smem = smem_raw + ((1024u - mis) & 1023u);
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sDO = smem + C::OFF_DO;
   uint8_t* sK = smem + C::OFF_K;
@@ -318,17 +333,17 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   } else {
     // ------------------------------------------------------------------ softmax warps (row = query)
     // Warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key columns
-    // [64 (w / 4), 64 (w / 4) + 64) of every tile; D_i and R_i are combined across
-    // the two halves through shared memory.
+    // [32 (w / 4), 32 (w / 4) + 32) of every tile; D_i and R_i are combined across the
+    // four parts of a row through shared memory.
     const int quarter = warp & 3;
-    const int half = warp >> 2;
-    const int cbase = half * 64;
+    const int part = warp >> 2;
+    const int cbase = part * DQ_COLS;
     const int r = quarter * 32 + lane;
     const int i = q0 + r;
     const bool i_ok = i < s.NQ;
     const size_t ro = static_cast<size_t>(bh) * s.NQ + (i_ok ? i : s.NQ - 1);
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);   // [2][BM]
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);   // [DQ_PARTS][BM]
     auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
       int okv = 1;
       if (lane == 0) okv = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
@@ -337,12 +352,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const float m_sc = args.row_m[ro];
     const float inv_s = 1.0f / args.row_s[ro];
     const int a = min(max(args.row_arg[ro], 0), s.NK - 1);
-    // D_i = dO_i . O_i: each half of the warps sums half of the D dimensions
+    // D_i = dO_i . O_i: each part of the warps sums D / DQ_PARTS of the dimensions
     {
-      float part = 0.0f;
+      float acc = 0.0f;
       const char* dorow = reinterpret_cast<const char*>(args.dout) + ro * D * 2;
 #pragma unroll 4
-      for (int d = half * (D / 2); d < (half + 1) * (D / 2); d += 8) {
+      for (int d = part * (D / DQ_PARTS); d < (part + 1) * (D / DQ_PARTS); d += 8) {
         float g[8], o[8];
         load8_bf16(dorow + d * 2, g);
         if (args.o_bf16) {
@@ -354,13 +369,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           o[4] = x1.x; o[5] = x1.y; o[6] = x1.z; o[7] = x1.w;
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) part = fmaf(g[e], o[e], part);
+        for (int e = 0; e < 8; ++e) acc = fmaf(g[e], o[e], acc);
       }
-      xch[half * BM + r] = part;
+      xch[part * BM + r] = acc;
     }
-    softmax8_sync();
-    const float Di = xch[r] + xch[BM + r];
-    softmax8_sync();   // xch is reused for R_i after the loop
+    softmax_sync();
+    float Di = 0.0f;
+#pragma unroll
+    for (int pp = 0; pp < DQ_PARTS; ++pp) Di += xch[pp * BM + r];
+    softmax_sync();   // xch is reused for R_i after the loop
     // rows past N_Q read zero-filled Q rows (s = 0): base 2 saturates every w to 1, weight 0
     const float base = i_ok ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
     const float c2 = s.scale * (1.0f / 32.0f);
@@ -369,8 +386,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const float2 cE2 = make_float2(cE, cE), mcED2 = make_float2(-cE * Di, -cE * Di);
     float2 R2 = make_float2(0.0f, 0.0f);
     bool ok = true;
-    uint32_t sv[2][32];
-#define SV(c) sv[(c) >> 5][(c) & 31]
+    uint32_t sv[32];
+#define SV(c) sv[c]
     for (int j = 0; j < nkt && ok; ++j) {
       const int sb = j & 1;
       ok = warp_wait(&s_full[sb], (j >> 1) & 1u);
@@ -378,19 +395,18 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       tc_fence_after();
       {
         const uint32_t col = lane_addr + (sb ? DQ_TM_S1 : DQ_TM_S0) + cbase;
-        tmem_ld32(col, sv[0]);
-        tmem_ld32(col + 32, sv[1]);
+        tmem_ld32(col, sv);
         tc_wait_ld();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
       const int col0 = j * BN + cbase;   // key index of local column 0
-      const bool need_mask = col0 + 63 > lim;
+      const bool need_mask = col0 + DQ_COLS - 1 > lim;
       // coefficient q^7 (1/w)^2 per entry, in place; the factor 1/(4 s_i) is applied with
       // dP - D_i below.  Four entries share two reciprocals (coef_quad).
 #pragma unroll
-      for (int c = 0; c < 64; c += 4) {
+      for (int c = 0; c < DQ_COLS; c += 4) {
         float x[4] = {u2f(SV(c)), u2f(SV(c + 1)), u2f(SV(c + 2)), u2f(SV(c + 3))};
         if (need_mask) {
 #pragma unroll
@@ -404,20 +420,20 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         SV(c + 2) = __float_as_uint(cb.x);
         SV(c + 3) = __float_as_uint(cb.y);
       }
-      if (a >= col0 && a < col0 + 64) {   // the argmax entry takes -R_i, not E
+      if (a >= col0 && a < col0 + DQ_COLS) {   // the argmax entry takes -R_i, not E
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < DQ_COLS; ++c)
           if (col0 + c == a) SV(c) = 0u;
       }
       ok = warp_wait(e_free, (j & 1u) ^ 1u) && warp_wait(dp_full, j & 1u);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < DQ_COLS / 32; ++cc) {
         uint32_t dv[32];
         tmem_ld32(lane_addr + DQ_TM_DP + cbase + cc * 32, dv);
         tc_wait_ld();
-        if (cc == 1) {
+        if (cc == DQ_COLS / 32 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(dp_free);
@@ -442,15 +458,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (lane == 0) mbar_arrive(e_full);
     }
 #undef SV
-    // R_i over both halves (reached by all eight warps, also after a wait gave up)
-    float R = R2.x + R2.y;
-    xch[half * BM + r] = R;
-    softmax8_sync();
-    R = xch[r] + xch[BM + r];
+    // R_i over the parts (reached by every softmax warp, also after a wait gave up)
+    xch[part * BM + r] = R2.x + R2.y;
+    softmax_sync();
+    float R = 0.0f;
+#pragma unroll
+    for (int pp = 0; pp < DQ_PARTS; ++pp) R += xch[pp * BM + r];
     if (ok) ok = warp_wait(dq_full, 0);
     if (ok) {
       tc_fence_after();
-      if (half == 0) {   // this query tile's constant block for the dK/dV kernel
+      if (part == 0) {   // this query tile's constant block for the dK/dV kernel
         float* blk = args.ws_consts + (static_cast<size_t>(bh) * nqt + qt) * kConstBlockFloats;
         blk[r] = base;   // 2 past N_Q: w = 1, zero weight
         blk[BM + r] = i_ok ? inv_s : 0.0f;
@@ -459,9 +476,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         reinterpret_cast<int*>(blk)[4 * BM + r] = i_ok ? args.row_arg[ro] : -1;
       }
       const char* krow = reinterpret_cast<const char*>(args.k_raw) + (static_cast<size_t>(bh) * s.NK + a) * D * 2;
-      // each half of the warps stores half of the D columns of its rows
+      // the warps of a row quarter store 32-column chunks of its rows in turn
 #pragma unroll
-      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+      for (int c0 = part * 32; c0 < D; c0 += 32 * DQ_PARTS) {
         uint32_t acc[32];
         tmem_ld32(lane_addr + DQ_TM_DQ + c0, acc);
         tc_wait_ld();
