@@ -111,17 +111,15 @@ template <int D>
 struct DqCfg {
   static constexpr int TILE = BN * D * 2;
   static constexpr int NKS = 3;                    // K stages: K_j lives from S_j to dQ_j
-  static constexpr int NVS = (D == 128) ? 1 : 2;   // V stages
-  static constexpr int E_BYTES = BM * BN * 2;
+  static constexpr int NVS = 2;                    // V stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = TILE;
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NKS * TILE;
-  static constexpr int OFF_E = OFF_V + NVS * TILE;
-  static constexpr int OFF_BAR = OFF_E + E_BYTES;
-  // qdo_full, k_full[NKS], k_empty[NKS], v_full[NVS], v_empty[NVS], s_full[2], s_free[2],
-  // dp_full, dp_free, e_full, e_free, dq_full, drain[2]
-  static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 4 + 7;
+  static constexpr int OFF_BAR = OFF_V + NVS * TILE;
+  // qdo_full, k_full[NKS], k_empty[NKS], v_full[NVS], v_empty[NVS], s_full[2], e_free[2],
+  // dp_full, dp_free, e_full, dq_full, drain[2]
+  static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 10;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_XCH = OFF_MISC + 16;   // [4][128] floats: per-part partials of D_i, then R_i
   static constexpr int USED = OFF_XCH + 4 * BM * 4;
@@ -164,7 +162,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint8_t* sDO = smem + C::OFF_DO;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sE = smem + C::OFF_E;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* qdo_full = bars;
   uint64_t* k_full = qdo_full + 1;
@@ -172,12 +169,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint64_t* v_full = k_empty + C::NKS;
   uint64_t* v_empty = v_full + C::NVS;
   uint64_t* s_full = v_empty + C::NVS;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* dp_full = s_free + 2;
+  // e_free[b]: the dQ product has read E from score buffer b (E_j is written over S_j)
+  uint64_t* e_free = s_full + 2;
+  uint64_t* dp_full = e_free + 2;
   uint64_t* dp_free = dp_full + 1;
   uint64_t* e_full = dp_free + 1;
-  uint64_t* e_free = e_full + 1;
-  uint64_t* dq_full = e_free + 1;
+  uint64_t* dq_full = e_full + 1;
   uint64_t* drain = dq_full + 1;   // [2], one per issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -206,12 +203,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], DQ_SOFTMAX_WARPS);
+      mbar_init(&e_free[i], 1);
     }
     mbar_init(dp_full, 1);
     mbar_init(dp_free, DQ_SOFTMAX_WARPS);
     mbar_init(e_full, DQ_SOFTMAX_WARPS);
-    mbar_init(e_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
@@ -272,8 +268,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       constexpr uint32_t idesc_ss = idesc_fp16_f32(BM, BN, 0, 0);
       constexpr uint32_t idesc_kmn = idesc_fp16_f32(BM, D, 0, 1);
       constexpr uint32_t HI = sdesc_hi_sw128(1024);
-      const uint32_t qlo = sdesc_lo(smem_u32(sQ), 16), dolo = sdesc_lo(smem_u32(sDO), 16),
-                     elo = sdesc_lo(smem_u32(sE), 16);
+      const uint32_t qlo = sdesc_lo(smem_u32(sQ), 16), dolo = sdesc_lo(smem_u32(sDO), 16);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       bool ok = mbar_wait(qdo_full, 0, abort_flag, ctx);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
@@ -282,8 +277,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         for (int j = 0; j < nkt && ok; ++j) {
           // S_j = Q K_j^T
           const int ks = j % C::NKS, sb = j & 1;
+          // buffer sb is free once the dQ product of tile j - 2 has read E_{j-2} from it
+          // (the softmax warps loaded S_{j-2} before writing E_{j-2})
           ok = mbar_wait(&k_full[ks], (j / C::NKS) & 1u, abort_flag, ctx) &&
-               mbar_wait(&s_free[sb], ((j >> 1) & 1u) ^ 1u, abort_flag, ctx);
+               mbar_wait(&e_free[sb], ((j >> 1) & 1u) ^ 1u, abort_flag, ctx);
           if (!ok) break;
           tc_fence_after();
           const uint32_t klo = sdesc_lo(aK + ks * C::TILE, 16);
@@ -318,12 +315,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t klo = sdesc_lo(aK + ks * C::TILE, BOX_BYTES);
+          // E_t from tensor memory: fp16 pairs over the first half of each softmax warp's
+          // columns of score buffer t & 1, 8 columns per 16 keys
+          const uint32_t ecol = tmem + ((t & 1) ? DQ_TM_S1 : DQ_TM_S0);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            tc_mma_f16(tmem + DQ_TM_DQ, sdesc(elo + (((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4), HI),
-                       sdesc(klo + ((kk * 2048) >> 4), HI), idesc_kmn, (t > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_f16_ts(tmem + DQ_TM_DQ, ecol + (16 * kk / DQ_COLS) * DQ_COLS + (16 * kk % DQ_COLS) / 2,
+                          sdesc(klo + ((kk * 2048) >> 4), HI), idesc_kmn, (t > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&k_empty[ks]);
-          tc_commit(e_free);
+          tc_commit(&e_free[t & 1]);
         }
         if (ok) tc_commit(dq_full);
       }
@@ -398,9 +398,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         tmem_ld32(col, sv);
         tc_wait_ld();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
       const int col0 = j * BN + cbase;   // key index of local column 0
       const bool need_mask = col0 + DQ_COLS - 1 > lim;
       // coefficient q^7 (1/w)^2 per entry, in place; the factor 1/(4 s_i) is applied with
@@ -425,7 +422,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         for (int c = 0; c < DQ_COLS; ++c)
           if (col0 + c == a) SV(c) = 0u;
       }
-      ok = warp_wait(e_free, (j & 1u) ^ 1u) && warp_wait(dp_full, j & 1u);
+      ok = warp_wait(dp_full, j & 1u);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -438,22 +435,21 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(dp_free);
         }
+        // E = coef (dP - D_i) / (4 s_i) = coef (cE dP - cE D_i), as fp16 pairs over the first
+        // half of this warp's (already read) columns of score buffer sb
+        uint32_t e16[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int c = cc * 32 + e * 8 + 2 * t;
-            // E = coef (dP - D_i) / (4 s_i) = coef (cE dP - cE D_i)
-            const float2 dpp = make_float2(u2f(dv[e * 8 + 2 * t]), u2f(dv[e * 8 + 2 * t + 1]));
-            const float2 ee = __fmul2_rn(make_float2(u2f(SV(c)), u2f(SV(c + 1))), __ffma2_rn(dpp, cE2, mcED2));
-            R2 = __fadd2_rn(R2, ee);
-            pk[t] = pack_f16x2_sat(ee.x, ee.y);
-          }
-          st_tile16(sE, r, (cbase + cc * 32 + e * 8) >> 3, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        for (int t = 0; t < 16; ++t) {
+          const int c = cc * 32 + 2 * t;
+          const float2 dpp = make_float2(u2f(dv[2 * t]), u2f(dv[2 * t + 1]));
+          const float2 ee = __fmul2_rn(make_float2(u2f(SV(c)), u2f(SV(c + 1))), __ffma2_rn(dpp, cE2, mcED2));
+          R2 = __fadd2_rn(R2, ee);
+          e16[t] = pack_f16x2_sat(ee.x, ee.y);
         }
+        tmem_st16(lane_addr + (sb ? DQ_TM_S1 : DQ_TM_S0) + cbase + 16 * cc, e16);
       }
-      fence_proxy_async_smem();
+      tc_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(e_full);
     }
