@@ -517,7 +517,9 @@ struct DkvCfg {
   // Per-query constants of one query tile, in two single-buffered parts with their own
   // lifetimes: X (base_i, 1/s_i) is read in the P^T loop, Y (D_i/4, R_i, a_i) in the dS^T
   // loop and the argmax fix-up.  X of the next tile arrives while the warps are in the
-  // dS^T loop, Y while they are in the next P^T loop.
+  // dS^T loop, Y while they are in the next P^T loop.  Each copy completes on the barrier
+  // the softmax warps wait on anyway (X with S^T on st_full, Y with dP^T on dpt_full), so
+  // a tile costs them two waits.
   static constexpr int OFF_CX = OFF_DS + A_BYTES;
   static constexpr int CX_BYTES = 2 * BM * 4;
   static constexpr int OFF_CY = OFF_CX + CX_BYTES;
@@ -525,8 +527,8 @@ struct DkvCfg {
   static constexpr int OFF_BAR = OFF_CY + CY_BYTES;
   // kv_full, q_full[NQS], q_empty[NQS], do_full[NDS], do_empty[NDS],
   // st_full, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2],
-  // cx_full, cx_empty, cy_full, cy_empty, ds_full, ds_free
-  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 14;
+  // cx_empty, cy_empty, ds_full, ds_free
+  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 12;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int USED = OFF_MISC + 16;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
@@ -574,17 +576,15 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* q_empty = q_full + C::NQS;
   uint64_t* do_full = q_empty + C::NQS;
   uint64_t* do_empty = do_full + C::NDS;
-  uint64_t* st_full = do_empty + C::NDS;
-  uint64_t* dpt_full = st_full + 1;
+  uint64_t* st_full = do_empty + C::NDS;   // S^T committed and constants X landed
+  uint64_t* dpt_full = st_full + 1;   // dP^T committed and constants Y landed (after dK read dS^T)
   uint64_t* dpt_free = dpt_full + 1;
   uint64_t* p_full = dpt_free + 1;
   uint64_t* p_free = p_full + 1;
   uint64_t* acc_full = p_free + 1;
   uint64_t* drain = acc_full + 1;   // [2], one per issuer
-  uint64_t* cx_full = drain + 2;
-  uint64_t* cx_empty = cx_full + 1;
-  uint64_t* cy_full = cx_empty + 1;
-  uint64_t* cy_empty = cy_full + 1;
+  uint64_t* cx_empty = drain + 2;
+  uint64_t* cy_empty = cx_empty + 1;
   uint64_t* ds_full = cy_empty + 1;   // dS^T tile written (P^T has p_full / p_free)
   uint64_t* ds_free = ds_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -614,17 +614,15 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 2);   // dP^T (issuer 0) and dV (issuer 1) read dO_i
     }
-    mbar_init(st_full, 1);
-    mbar_init(dpt_full, 1);
+    mbar_init(st_full, 2);   // issuer 0's commit + the producer's arrival for X
+    mbar_init(dpt_full, 2);   // issuer 0's commit + the producer's arrival for Y
     mbar_init(dpt_free, KV_SOFTMAX_WARPS);
     mbar_init(p_full, KV_SOFTMAX_WARPS);
     mbar_init(p_free, 1);
     mbar_init(acc_full, 1);
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
-    mbar_init(cx_full, 1);
     mbar_init(cx_empty, KV_SOFTMAX_WARPS);
-    mbar_init(cy_full, 1);
     mbar_init(cy_empty, KV_SOFTMAX_WARPS);
     mbar_init(ds_full, KV_SOFTMAX_WARPS);
     mbar_init(ds_free, 1);
@@ -666,10 +664,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sQ + qs * C::TILE + c * BOX_BYTES, &args.tm_q, &q_full[qs], c * 64, i0, bh);
         q_issued = it + 1;
+        // X(it) completes on st_full phase it: the warps' arrivals on cx_empty for tile it - 1
+        // come after their wait on phase it - 1
         ok = mbar_wait(cx_empty, cpar, abort_flag, ctx);
         if (!ok) break;
-        mbar_arrive_expect_tx(cx_full, C::CX_BYTES);
-        bulk_load_1d(st_base, blk, C::CX_BYTES, cx_full);
+        mbar_arrive_expect_tx(st_full, C::CX_BYTES);
+        bulk_load_1d(st_base, blk, C::CX_BYTES, st_full);
         cx_issued = it + 1;
         const int ds = it % C::NDS;
         ok = mbar_wait(&do_empty[ds], ((it / C::NDS) & 1u) ^ 1u, abort_flag, ctx);
@@ -679,10 +679,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sDO + ds * C::TILE + c * BOX_BYTES, &args.tm_do, &do_full[ds], c * 64, i0, bh);
         d_issued = it + 1;
-        ok = mbar_wait(cy_empty, cpar, abort_flag, ctx);
+        // Y(it) completes on dpt_full phase it.  It is issued once dK of tile it - 1 has read
+        // the dS^T tile, so a warp that sees dpt_full phase it may overwrite that tile.
+        ok = mbar_wait(cy_empty, cpar, abort_flag, ctx) && mbar_wait(ds_free, cpar, abort_flag, ctx);
         if (!ok) break;
-        mbar_arrive_expect_tx(cy_full, C::CY_BYTES);
-        bulk_load_1d(st_d, blk + 2 * BM, C::CY_BYTES, cy_full);
+        mbar_arrive_expect_tx(dpt_full, C::CY_BYTES);
+        bulk_load_1d(st_d, blk + 2 * BM, C::CY_BYTES, dpt_full);
         cy_issued = it + 1;
       }
       drain_wait(kv_full, 0, ctx);
@@ -690,8 +692,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         drain_wait(&q_full[it % C::NQS], (it / C::NQS) & 1u, ctx);
       for (int it = max(0, d_issued - C::NDS); it < d_issued; ++it)
         drain_wait(&do_full[it % C::NDS], (it / C::NDS) & 1u, ctx);
-      if (cx_issued > 0) drain_wait(cx_full, (cx_issued - 1) & 1u, ctx);
-      if (cy_issued > 0) drain_wait(cy_full, (cy_issued - 1) & 1u, ctx);
+      // the last X and Y copies (their phases also need the issuer's commit, which a CTA
+      // winding down after a timeout may never make: the drain bound ends the wait then)
+      if (cx_issued > 0) drain_wait(st_full, (cx_issued - 1) & 1u, ctx);
+      if (cy_issued > 0) drain_wait(dpt_full, (cy_issued - 1) & 1u, ctx);
     }
   } else if (warp >= KV_MMA_WARP) {
     const int who = warp - KV_MMA_WARP;   // 0: S^T and dP^T products; 1: dV and dK products
@@ -801,8 +805,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     for (int it = 0; it < nq; ++it) {
       const int i0 = (qt0 + it) * BM;
       const uint32_t par = it & 1u;
-      // this tile's per-query constants X (queries past N_Q carry base 2: zero weight)
-      warp_wait(cx_full, par);
+      // S^T and this tile's per-query constants X (queries past N_Q carry base 2: zero weight)
       warp_wait(st_full, par);
       tc_fence_after();
 #pragma unroll
@@ -863,8 +866,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       }
       // dS^T = coef (dP^T - D_i); the entries (a_i, i) where this key is the query's argmax
       // take -R_i afterwards
-      warp_wait(cy_full, par);
-      warp_wait(ds_free, par ^ 1u);   // dK of the previous tile has read dS^T
+      // dP^T, the constants Y, and (through the producer) dK of the previous tile done
       warp_wait(dpt_full, par);
       tc_fence_after();
 #pragma unroll
