@@ -39,9 +39,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int PRODUCER_WARP = 4;
-constexpr int MMA_WARP = 5;
-constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BOX_BYTES = 128 * 64 * 2;
 
@@ -52,13 +49,6 @@ __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ void st_tile16(uint8_t* tile, int r, int chunk, uint4 val) {
   const int half = chunk >> 3, c = chunk & 7;
   *reinterpret_cast<uint4*>(tile + half * BOX_BYTES + r * 128 + ((c ^ (r & 7)) << 4)) = val;
-}
-
-// 1/w0 and 1/w1 (w in [0.5, 1]) from one rcp.approx of w0 w1 (two scalar products, so
-// the pair is born in adjacent registers for the f32x2 arithmetic that follows).
-__device__ __forceinline__ float2 rcp_pair(float w0, float w1) {
-  const float R = rcp_approx(w0 * w1);
-  return make_float2(R * w1, R * w0);
 }
 
 // The backward coefficient q^7 (1/w)^2 for four scores x of a row, w = sat(base - c2 x) =
@@ -92,20 +82,6 @@ __device__ __forceinline__ void load8_bf16(const void* p, float* out) {
   }
 }
 
-__device__ __forceinline__ void store_row32(void* base, size_t idx, const float* v, int bf16) {
-  if (bf16) {
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + idx);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      dst[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-  } else {
-    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-  }
-}
-
 // ============================================================================ dQ kernel
 template <int D>
 struct DqCfg {
@@ -128,6 +104,7 @@ struct DqCfg {
   static constexpr int SLACK = (USED + 1024 <= 232448) ? 1024 : 0;
   static constexpr int SMEM_BYTES = USED + SLACK;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(OFF_BAR - OFF_K >= 16 * 4096, "epilogue staging: 4 KB per softmax warp in the K/V stages");
 };
 constexpr uint32_t DQ_TM_S0 = 0, DQ_TM_S1 = 128, DQ_TM_DP = 256, DQ_TM_DQ = 384;
 // 16 softmax warps, four per scheduler: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its query
@@ -181,7 +158,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int BH = s.B * s.H;
   const int nqt = (s.NQ + BM - 1) / BM;
   const int item = blockIdx.x;
   // head-major order (K/V of a head shared in L2), longest causal query tiles first
@@ -472,23 +448,29 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         reinterpret_cast<int*>(blk)[4 * BM + r] = i_ok ? args.row_arg[ro] : -1;
       }
       const char* krow = reinterpret_cast<const char*>(args.k_raw) + (static_cast<size_t>(bh) * s.NK + a) * D * 2;
-      // the warps of a row quarter store 32-column chunks of its rows in turn
+      // the warps of a row quarter store 32-column chunks of its rows in turn, through
+      // 4 KB per warp of the K/V stages (free: dq_full means every product has completed)
+      uint8_t* stage = sK + warp * 4096;
+      const int wrow0 = q0 + quarter * 32;   // first row of this warp
+      const size_t row0 = static_cast<size_t>(bh) * s.NQ + wrow0;
+      const int n_ok = max(0, min(32, s.NQ - wrow0));
 #pragma unroll
       for (int c0 = part * 32; c0 < D; c0 += 32 * DQ_PARTS) {
         uint32_t acc[32];
         tmem_ld32(lane_addr + DQ_TM_DQ + c0, acc);
         tc_wait_ld();
-        if (i_ok) {
-          float out[32];
+        float out[32];
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            float kv[8];
-            load8_bf16(krow + (c0 + e) * 2, kv);
+        for (int e = 0; e < 32; e += 8) {
+          float kv[8];
+          load8_bf16(krow + (c0 + e) * 2, kv);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) out[e + t] = s.scale * fmaf(-R, kv[t], u2f(acc[e + t]));
-          }
-          store_row32(args.dq, ro * D + c0, out, args.grad_bf16);
+          for (int t = 0; t < 8; ++t) out[e + t] = s.scale * fmaf(-R, kv[t], u2f(acc[e + t]));
         }
+        if (args.grad_bf16)
+          warp_store_block32<true>(stage, out, args.dq, row0, D, c0, n_ok, lane);
+        else
+          warp_store_block32<false>(stage, out, args.dq, row0, D, c0, n_ok, lane);
       }
     }
     tc_fence_before();
@@ -537,6 +519,7 @@ struct DkvCfg {
   static constexpr int SMEM_BYTES = USED + SLACK;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(CX_BYTES + CY_BYTES == kConstBlockFloats * 4, "constant block layout");
+  static_assert(OFF_CX - OFF_Q >= 16 * 4096, "epilogue staging: 4 KB per softmax warp in the Q/dO stages");
 };
 constexpr uint32_t KV_TM_ST = 0, KV_TM_DPT = 128, KV_TM_DV = 256, KV_TM_DK = 384;
 // 16 softmax warps, four per scheduler: warp w owns TMEM lanes 32 (w % 4) .. + 31 (its key
@@ -592,7 +575,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int BH = s.B * s.H;
   const int nqt = (s.NQ + BM - 1) / BM;
   const int item = blockIdx.x;
   // head-major order (Q/dO of a head shared in L2); within a head ascending key tiles,
@@ -787,7 +769,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     const int r = quarter * 32 + lane;
     const int j = k0 + r;
     const bool j_ok = j < s.NK;
-    const size_t ko = static_cast<size_t>(bh) * s.NK + (j_ok ? j : s.NK - 1);
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = s.scale * (1.0f / 32.0f);
     bool ok = true;
@@ -929,22 +910,30 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     if (nq > 0) warp_wait(acc_full, 0);
     if (ok) {
       tc_fence_after();
-      // the warps of a row quarter store 32-column chunks of its key rows in turn
+      // the warps of a row quarter store 32-column chunks of its key rows in turn, through
+      // 4 KB per warp of the Q/dO stages (free: acc_full means every product has completed)
+      uint8_t* stage = sQ + warp * 4096;
+      const int wrow0 = k0 + quarter * 32;   // first key row of this warp
+      const size_t row0 = static_cast<size_t>(bh) * s.NK + wrow0;
+      const int n_ok = max(0, min(32, s.NK - wrow0));
 #pragma unroll
       for (int c0 = part * 32; c0 < D; c0 += 32 * (KV_SOFTMAX_WARPS / 4)) {
         uint32_t av[32], kv[32];
         tmem_ld32(lane_addr + KV_TM_DV + c0, av);
         tmem_ld32(lane_addr + KV_TM_DK + c0, kv);
         tc_wait_ld();
-        if (j_ok) {
-          float ov[32], okv[32];
+        float ov[32], okv[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            ov[e] = nq > 0 ? u2f(av[e]) : 0.0f;
-            okv[e] = nq > 0 ? s.scale * u2f(kv[e]) : 0.0f;
-          }
-          store_row32(args.dv, ko * D + c0, ov, args.grad_bf16);
-          store_row32(args.dk, ko * D + c0, okv, args.grad_bf16);
+        for (int e = 0; e < 32; ++e) {
+          ov[e] = nq > 0 ? u2f(av[e]) : 0.0f;
+          okv[e] = nq > 0 ? s.scale * u2f(kv[e]) : 0.0f;
+        }
+        if (args.grad_bf16) {
+          warp_store_block32<true>(stage, ov, args.dv, row0, D, c0, n_ok, lane);
+          warp_store_block32<true>(stage, okv, args.dk, row0, D, c0, n_ok, lane);
+        } else {
+          warp_store_block32<false>(stage, ov, args.dv, row0, D, c0, n_ok, lane);
+          warp_store_block32<false>(stage, okv, args.dk, row0, D, c0, n_ok, lane);
         }
       }
     }

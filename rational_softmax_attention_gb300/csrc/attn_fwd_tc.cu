@@ -536,31 +536,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool row_ok = row < s.NQ;
       const float inv = 1.0f / rowsum;
       const size_t ro = static_cast<size_t>(bh) * s.NQ + (row_ok ? row : 0);
+      // O rows leave through this query tile's P tile (free: o_full means the last P V
+      // product has read it), 4 KB per warp, in whole row segments
+      uint8_t* stage = sP + g * C::P_BYTES + quarter * 4096;
+      const int wrow0 = q0 + g * BM + quarter * 32;   // first row of this warp
+      const size_t row0 = static_cast<size_t>(bh) * s.NQ + wrow0;
+      const int n_ok = max(0, min(32, s.NQ - wrow0));
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ov[32];
         tmem_ld32(lane_addr + TMEM_O + g * 128 + c0, ov);
         tc_wait_ld();
-        if (row_ok) {
-          if (args.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.o) + ro * D + c0);
+        float o[32];
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 pk;
-              pk.x = pack_bf16x2(u2f(ov[v4 * 8 + 0]) * inv, u2f(ov[v4 * 8 + 1]) * inv);
-              pk.y = pack_bf16x2(u2f(ov[v4 * 8 + 2]) * inv, u2f(ov[v4 * 8 + 3]) * inv);
-              pk.z = pack_bf16x2(u2f(ov[v4 * 8 + 4]) * inv, u2f(ov[v4 * 8 + 5]) * inv);
-              pk.w = pack_bf16x2(u2f(ov[v4 * 8 + 6]) * inv, u2f(ov[v4 * 8 + 7]) * inv);
-              dst[v4] = pk;
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.o) + ro * D + c0);
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              dst[v4] = make_float4(u2f(ov[v4 * 4 + 0]) * inv, u2f(ov[v4 * 4 + 1]) * inv,
-                                    u2f(ov[v4 * 4 + 2]) * inv, u2f(ov[v4 * 4 + 3]) * inv);
-          }
-        }
+        for (int e = 0; e < 32; ++e) o[e] = u2f(ov[e]) * inv;
+        if (args.out_bf16)
+          warp_store_block32<true>(stage, o, args.o, row0, D, c0, n_ok, lane);
+        else
+          warp_store_block32<false>(stage, o, args.o, row0, D, c0, n_ok, lane);
       }
       if (row_ok) {
         if (args.row_m) args.row_m[ro] = m_sc;

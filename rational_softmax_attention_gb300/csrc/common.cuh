@@ -305,4 +305,40 @@ __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
   return r;
 }
 
+// One warp stores a block of 32 rows x 32 values, row t held by lane t in v[], to rows
+// row0 .. row0 + 31 (only the first n_ok of them) of a row-major fp32 or bf16 matrix with
+// `ld` elements per row, columns c0 .. c0 + 31.  The block passes through 4 KB of shared
+// memory (16-byte chunks of a row at position chunk ^ (row % 8), so neither side conflicts)
+// and leaves in whole 64- or 128-byte row segments instead of one 16-byte piece per row.
+template <bool BF16>
+__device__ __forceinline__ void warp_store_block32(uint8_t* stage, const float (&v)[32], void* out, size_t row0,
+                                                   int ld, int c0, int n_ok, int lane) {
+  constexpr int CH = BF16 ? 4 : 8;   // 16-byte chunks per row segment
+  __syncwarp();                      // the previous block has left the stage
+#pragma unroll
+  for (int k = 0; k < CH; ++k) {
+    uint4 u;
+    if (BF16) {
+      u = make_uint4(pack_bf16x2(v[8 * k + 0], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                     pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+    } else {
+      u = make_uint4(__float_as_uint(v[4 * k + 0]), __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                     __float_as_uint(v[4 * k + 3]));
+    }
+    *reinterpret_cast<uint4*>(stage + lane * 128 + ((k ^ (lane & 7)) << 4)) = u;
+  }
+  __syncwarp();
+  constexpr int RPI = 32 / CH;   // rows per store instruction
+  const int k = lane % CH;
+#pragma unroll
+  for (int it = 0; it < CH; ++it) {
+    const int rr = it * RPI + lane / CH;
+    const uint4 u = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((k ^ (rr & 7)) << 4));
+    if (rr < n_ok) {
+      char* dst = reinterpret_cast<char*>(out) + ((row0 + rr) * static_cast<size_t>(ld) + c0) * (BF16 ? 2 : 4);
+      *reinterpret_cast<uint4*>(dst + k * 16) = u;
+    }
+  }
+}
+
 }  // namespace raattn
