@@ -390,6 +390,31 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     causal_ms = c0.elapsed_time(c1) / args.steps
     causal_fl = attn_flops(wc.B, wc.H, wc.N, wc.N, wc.D, True, False)
+    del qc, kc, vc, oc, rmc, rsc, rac
+
+    # ra_softmax backward on the step's softmax workload (reported beside the step): x, the
+    # forward's p, and a seeded dy; 16 B per element (x, p, dy read, dx written)
+    xs, ps = hp.dev_in[4], hp.outs[4]
+    dys = softmax_inputs(sw.rows, sw.cols, seed=sw.seed + 1, sigma=1.0).to(dev)
+    dxs = torch.empty_like(dys)
+
+    def softmax_bwd():
+        code = hp.L.ra_softmax_bwd(_ptr(xs), _ptr(ps), _ptr(dys), _ptr(dxs), sw.rows, sw.cols, 0, st)
+        if code != 0:
+            raise RuntimeError("ra_softmax_bwd failed")
+    hp.softmax(st)   # p for the timed x
+    for _ in range(3):
+        softmax_bwd()
+    torch.cuda.synchronize(dev)
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(args.steps):
+        softmax_bwd()
+    b1.record(stream)
+    torch.cuda.synchronize(dev)
+    smb_ms = b0.elapsed_time(b1) / args.steps
+    smb_bytes = 4.0 * x.numel() * 4
+    del dys, dxs
 
     peaks, peak_src = load_peaks()
     tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -440,6 +465,9 @@ def run_ours(args):
             "ra_attention_fwd_causal_b4h16n8192d128": {"ms": causal_ms,
                                                        "TFLOP_per_s": causal_fl / (causal_ms * 1e-3) / 1e12,
                                                        "frac_bf16_burst": causal_fl / (causal_ms * 1e-3) / 1e12 / tc_burst},
+            "ra_softmax_bwd": {"ms": smb_ms, "GB_per_s": smb_bytes / (smb_ms * 1e-3) / 1e9,
+                               "frac_hbm": smb_bytes / (smb_ms * 1e-3) / 1e9 / hbm_peak,
+                               "algorithmic": "16 B per element (x, p, dy read; dx written)"},
         },
         "roofline": rl,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": hp.h2d_bytes(),

@@ -119,10 +119,16 @@ def ra_softmax(x):
     return y
 
 
-def ra_softmax_backward(x, p, dy):
-    """Closed-form gradient of sum(dy * ra_softmax(x)) with respect to x (last dimension)."""
+def ra_softmax_backward(x, p, dy, out=None):
+    """Closed-form gradient of sum(dy * ra_softmax(x)) with respect to x (last dimension).
+
+    out: optional tensor for dx, shaped like x; it may be dy itself (gradient in place)."""
     _require_cuda(x, p, dy)
-    dx = torch.empty_like(x)
+    if out is not None:
+        _require_cuda(out)
+        if out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+            raise ValueError("out must be a contiguous tensor shaped like x")
+    dx = torch.empty_like(x) if out is None else out
     cols = x.shape[-1]
     rows = x.numel() // cols
     _check("ra_softmax_bwd", lib().ra_softmax_bwd(_ptr(x), _ptr(p), _ptr(dy), _ptr(dx), rows, cols,

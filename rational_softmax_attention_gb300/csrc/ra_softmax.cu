@@ -170,6 +170,81 @@ __global__ void __launch_bounds__(THREADS) ra_softmax_bwd_kernel(const float* x,
   if (threadIdx.x == 0 && amin >= 0 && amin < cols) dr[amin] = -rsum;
 }
 
+// The same backward with the row held in registers (cols % 4 == 0, cols <= THREADS*4*VPT,
+// 16-byte aligned rows): x, p and dy are read once with 128-bit loads and dx written once,
+// 16 bytes per element in all.  dx may equal dy (the row is read before any write).
+template <int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) ra_softmax_bwd_vec_kernel(const float* x, const float* p,
+                                                                     const float* dy, float* dx, int cols) {
+  __shared__ float red[THREADS / 32];
+  __shared__ int red_idx[THREADS / 32];
+  const size_t off = blockIdx.x * static_cast<size_t>(cols);
+  const float4* xr = reinterpret_cast<const float4*>(x + off);
+  const float4* pr = reinterpret_cast<const float4*>(p + off);
+  const float4* gr = reinterpret_cast<const float4*>(dy + off);
+  float4* dr = reinterpret_cast<float4*>(dx + off);
+  const int n4 = cols >> 2;
+  float4 xv[VPT], pv[VPT], gv[VPT];
+  float m = -INFINITY, d = 0.0f;
+  int a = cols;   // lowest column of this thread's maximum (columns are visited in increasing order)
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < n4) {
+      xv[i] = __ldcs(xr + idx);
+      pv[i] = __ldcs(pr + idx);
+      gv[i] = __ldcs(gr + idx);
+      const float e4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (e4[k] > m) {
+          m = e4[k];
+          a = 4 * idx + k;
+        }
+      d = fmaf(pv[i].x, gv[i].x, d);
+      d = fmaf(pv[i].y, gv[i].y, d);
+      d = fmaf(pv[i].z, gv[i].z, d);
+      d = fmaf(pv[i].w, gv[i].w, d);
+    }
+  }
+  // row maximum, then the lowest column holding it
+  const float mall = block_max<THREADS>(m, red);
+  int cand = (m == mall) ? a : cols;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red_idx[warp] = cand;
+  __syncthreads();
+  int amin = red_idx[0];
+#pragma unroll
+  for (int w = 1; w < THREADS / 32; ++w) amin = min(amin, red_idx[w]);
+  // (red_idx is not written again; block_sum below synchronises before red is reused)
+  d = block_sum<THREADS>(d, red);   // D = sum_k p_k dy_k
+  float rsum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < n4) {
+      const float xs[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+      const float ps[4] = {pv[i].x, pv[i].y, pv[i].z, pv[i].w};
+      const float gs[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+      float es[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float delta = mall - xs[k];
+        es[k] = (4 * idx + k != amin && delta < 16.0f)
+                    ? __fdividef(256.0f * ps[k] * (gs[k] - d), (16.0f - delta) * (16.0f + delta))
+                    : 0.0f;
+        rsum += es[k];
+      }
+      __stcs(dr + idx, make_float4(es[0], es[1], es[2], es[3]));
+    }
+  }
+  rsum = block_sum<THREADS>(rsum, red);
+  // the thread that stored the argmax's four columns overwrites that column
+  if (amin < cols && threadIdx.x == (amin >> 2) % THREADS) dx[off + amin] = -rsum;
+}
+
 // ----------------------------------------------------------------------------
 // launchers
 // ----------------------------------------------------------------------------
@@ -194,6 +269,24 @@ cudaError_t launch_ra_softmax_fwd_f32(const float* x, float* y, int64_t rows, in
 
 cudaError_t launch_ra_softmax_bwd_f32(const float* x, const float* p, const float* dy, float* dx, int64_t rows,
                                       int64_t cols, cudaStream_t st) {
+  const bool vec_ok = (cols % 4 == 0) && cols <= 8192 && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
+                      ((reinterpret_cast<uintptr_t>(p) & 15u) == 0) && ((reinterpret_cast<uintptr_t>(dy) & 15u) == 0) &&
+                      ((reinterpret_cast<uintptr_t>(dx) & 15u) == 0);
+  if (vec_ok) {
+    const unsigned grid = static_cast<unsigned>(rows);
+    const int c = static_cast<int>(cols);
+    // at most four 16-byte vectors per array and thread: three arrays held in registers
+    // leave room for several rows in flight per SM
+    if (cols <= 1024)
+      ra_softmax_bwd_vec_kernel<256, 1><<<grid, 256, 0, st>>>(x, p, dy, dx, c);
+    else if (cols <= 2048)
+      ra_softmax_bwd_vec_kernel<256, 2><<<grid, 256, 0, st>>>(x, p, dy, dx, c);
+    else if (cols <= 4096)
+      ra_softmax_bwd_vec_kernel<256, 4><<<grid, 256, 0, st>>>(x, p, dy, dx, c);
+    else
+      ra_softmax_bwd_vec_kernel<512, 4><<<grid, 512, 0, st>>>(x, p, dy, dx, c);
+    return cudaGetLastError();
+  }
   ra_softmax_bwd_kernel<256><<<static_cast<unsigned>(rows), 256, 0, st>>>(x, p, dy, dx, cols);
   return cudaGetLastError();
 }

@@ -71,7 +71,8 @@ def test_ra_softmax_in_place_and_misaligned_rows():
     parity.assert_close_fp32(got, want2, "offset rows")
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 5), (4, 64), (2, 1000), (2, 8192)])
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 5), (4, 64), (2, 1000), (5, 2052), (3, 4096), (2, 8192),
+                                       (2, 8196)])
 def test_ra_softmax_backward_matches_oracle(rows, cols):
     g = torch.Generator().manual_seed(cols)
     x = torch.randn(rows, cols, generator=g) * 4.0
@@ -82,3 +83,24 @@ def test_ra_softmax_backward_matches_oracle(rows, cols):
     torch.cuda.synchronize()
     want = oracle.ra_softmax_bwd(x.double().numpy(), dy.double().numpy())
     parity.assert_close_fp32(parity.f64(dx), want, f"ra_softmax_bwd[{rows}x{cols}]")
+
+
+def test_ra_softmax_backward_ties_and_in_place():
+    """Rows whose maximum occurs twice, in columns held by different threads: the gradient of
+    the maximum goes to the lowest of them (as in the oracle).  dx written over dy."""
+    g = torch.Generator().manual_seed(11)
+    rows, cols = 6, 8192
+    x = torch.randn(rows, cols, generator=g) * 4.0
+    for r, (c1, c2) in enumerate([(5, 4000), (4000, 5), (1023, 1024), (0, 8191), (8190, 8191), (17, 17 + 4 * 256)]):
+        top = float(x[r].max()) + 1.0
+        x[r, c1] = top
+        x[r, c2] = top
+    dy = torch.randn(rows, cols, generator=g)
+    xg = x.cuda()
+    p = ra.ra_softmax(xg)
+    dyg = dy.cuda()
+    dx = ra.ra_softmax_backward(xg, p, dyg, out=dyg)
+    torch.cuda.synchronize()
+    assert dx.data_ptr() == dyg.data_ptr()
+    want = oracle.ra_softmax_bwd(x.double().numpy(), dy.double().numpy())
+    parity.assert_close_fp32(parity.f64(dx), want, "ra_softmax_bwd ties, in place")
