@@ -416,6 +416,28 @@ def run_ours(args):
     smb_bytes = 4.0 * x.numel() * 4
     del dys, dxs
 
+    # the RaAttention module at the page's example shape (dim 768, 12 heads, causal,
+    # x [2, 128, 768], bf16): forward + backward through the module, seeded weights
+    torch.manual_seed(0)
+    mod = hp.ra.RaAttention(768, num_heads=12, causal=True).to(device=dev, dtype=torch.bfloat16)
+    gx = torch.Generator().manual_seed(1)
+    xm = torch.randn(2, 128, 768, generator=gx).to(dev, torch.bfloat16).requires_grad_(True)
+    dym = torch.randn(2, 128, 768, generator=gx).to(dev, torch.bfloat16)
+
+    def module_step():
+        mod(xm).backward(dym)
+    for _ in range(3):
+        module_step()
+    torch.cuda.synchronize(dev)
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m0.record(torch.cuda.current_stream(dev))
+    for _ in range(args.steps):
+        module_step()
+    m1.record(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize(dev)
+    mod_ms = m0.elapsed_time(m1) / args.steps
+    del mod, xm, dym
+
     peaks, peak_src = load_peaks()
     tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     tc_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -468,6 +490,9 @@ def run_ours(args):
             "ra_softmax_bwd": {"ms": smb_ms, "GB_per_s": smb_bytes / (smb_ms * 1e-3) / 1e9,
                                "frac_hbm": smb_bytes / (smb_ms * 1e-3) / 1e9 / hbm_peak,
                                "algorithmic": "16 B per element (x, p, dy read; dx written)"},
+            "ra_attention_module_b2n128d768h12_causal": {
+                "ms_fwd_bwd": mod_ms, "tokens_per_s": 2 * 128 / (mod_ms * 1e-3),
+                "note": "latency-bound (24 heads of one 128-row tile); no roofline claim"},
         },
         "roofline": rl,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": hp.h2d_bytes(),

@@ -16,4 +16,5 @@ from .ra_oracle import (  # noqa: F401
     ra_softmax,
     ra_softmax_bwd,
 )
+from .ra_module import layer_norm, ra_attention_module_bwd, ra_attention_module_fwd  # noqa: F401
 from .ra_tiled import ra_attention_tiled_head  # noqa: F401

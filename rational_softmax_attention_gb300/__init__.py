@@ -20,7 +20,7 @@ import re
 import torch
 
 __all__ = [
-    "RaError", "lib", "ra_softmax", "ra_softmax_backward", "ra_attention", "ra_attention_forward",
+    "RaError", "lib", "ra_softmax", "ra_softmax_backward", "ra_attention", "ra_attention_forward", "RaAttention",
     "ra_attention_backward", "device_status", "set_wait_limit_ns", "exported_symbols", "LIB_PATH",
 ]
 
@@ -207,6 +207,42 @@ class _RaAttentionFn(torch.autograd.Function):
 def ra_attention(q, k, v, is_causal=False, scale=None):
     """Rational-softmax attention, a drop-in for scaled_dot_product_attention (no mask/dropout)."""
     return _RaAttentionFn.apply(q.contiguous(), k.contiguous(), v.contiguous(), bool(is_causal), scale)
+
+
+class RaAttention(torch.nn.Module):
+    """Multi-head attention with ra_softmax (page "Ra-Family: Rational Neural Architecture",
+    section 3, "ra_attention & RaAttention").
+
+    x [B, N, dim] -> one projection to q, k, v of every head ([B, heads, N, dim/heads])
+    -> optional layer normalisation of q and k over the head dimension (qk_norm)
+    -> ra_attention (this library's kernels, with autograd) -> heads merged -> output
+    projection.  The two projections are plain library GEMMs (torch Linear, cuBLAS).
+    Dropout is not part of this path: attn_drop and proj_drop must be 0.
+    """
+
+    def __init__(self, dim, num_heads=8, qkv_bias=False, qk_norm=False, attn_drop=0.0, proj_drop=0.0,
+                 causal=False, device=None, dtype=None):
+        super().__init__()
+        if dim % num_heads != 0:
+            raise ValueError("dim must be a multiple of num_heads")
+        if attn_drop != 0.0 or proj_drop != 0.0:
+            raise NotImplementedError("dropout is not supported (attn_drop and proj_drop must be 0)")
+        self.num_heads = num_heads
+        self.head_dim = dim // num_heads
+        self.causal = bool(causal)
+        kw = {"device": device, "dtype": dtype}
+        self.qkv = torch.nn.Linear(dim, 3 * dim, bias=qkv_bias, **kw)
+        self.q_norm = torch.nn.LayerNorm(self.head_dim, eps=1e-5, **kw) if qk_norm else None
+        self.k_norm = torch.nn.LayerNorm(self.head_dim, eps=1e-5, **kw) if qk_norm else None
+        self.proj = torch.nn.Linear(dim, dim, **kw)
+
+    def forward(self, x):
+        B, N, C = x.shape
+        q, k, v = self.qkv(x).reshape(B, N, 3, self.num_heads, self.head_dim).permute(2, 0, 3, 1, 4).unbind(0)
+        if self.q_norm is not None:
+            q, k = self.q_norm(q), self.k_norm(k)
+        o = ra_attention(q, k, v, is_causal=self.causal)
+        return self.proj(o.transpose(1, 2).reshape(B, N, C))
 
 
 def device_status(stream=None):
