@@ -62,9 +62,10 @@ const char* ra_status_string(ra_status_t status);
  *   x, y     device pointers to rows*cols elements of `dtype`, row-major.  y may
  *            equal x (in place); partial overlap is an error the call cannot see.
  *   rows     >= 1; cols >= 1 (cols == 1 gives p = 1).
- *   dtype    RA_F32 (RA_BF16 returns RA_ERR_UNSUPPORTED in this build).
+ *   dtype    RA_F32, or RA_BF16 (bf16 in and out, fp32 arithmetic, each probability
+ *            rounded once to bf16).
  * Errors: RA_ERR_ARG for null pointers, rows/cols < 1, rows*cols overflowing
- * int64; RA_ERR_UNSUPPORTED for dtype != RA_F32; RA_ERR_LAUNCH on launch failure.
+ * int64, an unknown dtype; RA_ERR_LAUNCH on launch failure.
  */
 ra_status_t ra_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols,
                            ra_dtype_t dtype, void* stream);

@@ -109,7 +109,7 @@ def _require_cuda(*ts):
 
 
 def ra_softmax(x):
-    """ra_softmax along the last dimension of a float32 CUDA tensor."""
+    """ra_softmax along the last dimension of a float32 or bfloat16 CUDA tensor (same dtype out)."""
     _require_cuda(x)
     y = torch.empty_like(x)
     cols = x.shape[-1]

@@ -154,9 +154,11 @@ ra_status_t ra_device_status(void* stream) {
 ra_status_t ra_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, ra_dtype_t dtype, void* stream) {
   if (!x || !y || rows < 1 || cols < 1 || !dtype_ok(dtype)) return RA_ERR_ARG;
   if (rows > INT_MAX || cols > (INT64_MAX / rows)) return RA_ERR_ARG;
-  if (dtype != RA_F32) return RA_ERR_UNSUPPORTED;
-  const cudaError_t e = launch_ra_softmax_fwd_f32(static_cast<const float*>(x), static_cast<float*>(y), rows, cols,
-                                                  static_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      dtype == RA_BF16
+          ? launch_ra_softmax_fwd_bf16(x, y, rows, cols, static_cast<cudaStream_t>(stream))
+          : launch_ra_softmax_fwd_f32(static_cast<const float*>(x), static_cast<float*>(y), rows, cols,
+                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
 

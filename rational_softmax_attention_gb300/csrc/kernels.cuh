@@ -8,6 +8,7 @@ namespace raattn {
 
 // ra_softmax (ra_softmax.cu)
 cudaError_t launch_ra_softmax_fwd_f32(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t st);
+cudaError_t launch_ra_softmax_fwd_bf16(const void* x, void* y, int64_t rows, int64_t cols, cudaStream_t st);
 cudaError_t launch_ra_softmax_bwd_f32(const float* x, const float* p, const float* dy, float* dx, int64_t rows,
                                       int64_t cols, cudaStream_t st);
 

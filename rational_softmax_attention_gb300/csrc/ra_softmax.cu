@@ -119,6 +119,82 @@ __global__ void __launch_bounds__(THREADS) ra_softmax_fwd_generic_kernel(const f
   for (int64_t c = threadIdx.x; c < cols; c += THREADS) yr[c] = ra_phi_fast(m - xr[c]) * inv;
 }
 
+// bf16 in and out, fp32 arithmetic: eight values per 16-byte access (cols % 8 == 0,
+// cols <= THREADS*8*VPT, 16-byte aligned rows), each probability rounded once to bf16.
+// x may equal y.
+__device__ __forceinline__ void unpack_bf16x8(const uint4 u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+template <int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS) ra_softmax_fwd_bf16_vec_kernel(const uint16_t* x, uint16_t* y,
+                                                                          int cols) {
+  __shared__ float red[THREADS / 32];
+  const size_t row = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * static_cast<size_t>(cols));
+  uint4* yr = reinterpret_cast<uint4*>(y + row * static_cast<size_t>(cols));
+  const int n8 = cols >> 3;
+  float v[VPT][8];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < n8) {
+      unpack_bf16x8(__ldcs(xr + idx), v[i]);
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) m = max3f(m, v[i][e], v[i][e + 1]);
+    }
+  }
+  m = block_max<THREADS>(m, red);
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < n8) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[i][e] = ra_phi_fast(m - v[i][e]);
+        s += v[i][e];
+      }
+    }
+  }
+  s = block_sum<THREADS>(s, red);
+  const float inv = 1.0f / s;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < n8)
+      __stcs(yr + idx, make_uint4(pack_bf16x2(v[i][0] * inv, v[i][1] * inv), pack_bf16x2(v[i][2] * inv, v[i][3] * inv),
+                                  pack_bf16x2(v[i][4] * inv, v[i][5] * inv), pack_bf16x2(v[i][6] * inv, v[i][7] * inv)));
+  }
+}
+
+// bf16, any cols and alignment: three sweeps over the row in global memory.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) ra_softmax_fwd_bf16_generic_kernel(const uint16_t* x, uint16_t* y,
+                                                                              int64_t cols) {
+  __shared__ float red[THREADS / 32];
+  const size_t row = blockIdx.x;
+  const uint16_t* xr = x + row * static_cast<size_t>(cols);
+  uint16_t* yr = y + row * static_cast<size_t>(cols);
+  auto ld = [&](int64_t c) { return __uint_as_float(static_cast<uint32_t>(xr[c]) << 16); };
+  float m = -INFINITY;
+  for (int64_t c = threadIdx.x; c < cols; c += THREADS) m = fmaxf(m, ld(c));
+  m = block_max<THREADS>(m, red);
+  float s = 0.0f;
+  for (int64_t c = threadIdx.x; c < cols; c += THREADS) s += ra_phi_fast(m - ld(c));
+  s = block_sum<THREADS>(s, red);
+  const float inv = 1.0f / s;
+  // every thread reads its columns of x before writing the same columns of y (x may equal y)
+  for (int64_t c = threadIdx.x; c < cols; c += THREADS)
+    yr[c] = static_cast<uint16_t>(pack_bf16x2(ra_phi_fast(m - ld(c)) * inv, 0.0f) & 0xffffu);
+}
+
 // Backward: dx_j = p_j (dy_j - D) / (1 - u_j^2) for j != a with u_j < 1, 0 for u_j >= 1,
 // dx_a = -(sum of the others); D = sum_k p_k dy_k, a = lowest index of the row max of x.
 // 1/(1-u^2) is written as 256 / ((16 - Delta)(16 + Delta)).
@@ -264,6 +340,26 @@ cudaError_t launch_ra_softmax_fwd_f32(const float* x, float* y, int64_t rows, in
   if (vec_ok && cols <= 8192) return launch_vec<256, 8>(x, y, rows, static_cast<int>(cols), st);
   if (vec_ok && cols <= 16384) return launch_vec<512, 8>(x, y, rows, static_cast<int>(cols), st);
   ra_softmax_fwd_generic_kernel<256><<<static_cast<unsigned>(rows), 256, 0, st>>>(x, y, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ra_softmax_fwd_bf16(const void* x, void* y, int64_t rows, int64_t cols, cudaStream_t st) {
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  uint16_t* ys = static_cast<uint16_t*>(y);
+  const bool vec_ok = (cols % 8 == 0) && cols <= 8192 && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
+                      ((reinterpret_cast<uintptr_t>(y) & 15u) == 0);
+  const unsigned grid = static_cast<unsigned>(rows);
+  const int c = static_cast<int>(vec_ok ? cols : 0);
+  if (vec_ok && cols <= 1024)
+    ra_softmax_fwd_bf16_vec_kernel<128, 1><<<grid, 128, 0, st>>>(xs, ys, c);
+  else if (vec_ok && cols <= 2048)
+    ra_softmax_fwd_bf16_vec_kernel<256, 1><<<grid, 256, 0, st>>>(xs, ys, c);
+  else if (vec_ok && cols <= 4096)
+    ra_softmax_fwd_bf16_vec_kernel<256, 2><<<grid, 256, 0, st>>>(xs, ys, c);
+  else if (vec_ok)
+    ra_softmax_fwd_bf16_vec_kernel<128, 8><<<grid, 128, 0, st>>>(xs, ys, c);
+  else
+    ra_softmax_fwd_bf16_generic_kernel<256><<<grid, 256, 0, st>>>(xs, ys, cols);
   return cudaGetLastError();
 }
 

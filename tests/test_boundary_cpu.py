@@ -61,7 +61,7 @@ def test_softmax_validation(lib):
     assert lib.ra_softmax_fwd(FAKE, FAKE, 4, -1, 0, S) == 1
     assert lib.ra_softmax_fwd(FAKE, FAKE, 4, 4, 7, S) == 1
     assert lib.ra_softmax_fwd(FAKE, FAKE, 1 << 40, 1 << 30, 0, S) == 1    # overflow
-    assert lib.ra_softmax_fwd(FAKE, FAKE, 4, 4, 1, S) == 2                # bf16 not in this build
+    assert lib.ra_softmax_fwd(NULL, FAKE, 4, 4, 1, S) == 1                # bf16: validated like fp32
     assert lib.ra_softmax_bwd(FAKE, NULL, FAKE, FAKE, 4, 4, 0, S) == 1
 
 

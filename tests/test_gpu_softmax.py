@@ -1,4 +1,6 @@
 """GPU parity of the ra_softmax row kernels against the float64 oracle (fp32: max-abs 2e-5)."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -104,3 +106,59 @@ def test_ra_softmax_backward_ties_and_in_place():
     assert dx.data_ptr() == dyg.data_ptr()
     want = oracle.ra_softmax_bwd(x.double().numpy(), dy.double().numpy())
     parity.assert_close_fp32(parity.f64(dx), want, "ra_softmax_bwd ties, in place")
+
+
+def _assert_bf16_rounding_of(got, want, what):
+    """got is want (float64) computed in fp32 and rounded once to bf16: within half a bf16 ulp
+    of want (2^(floor(log2 |want|) - 8), bf16 keeping 8 significant bits) plus the fp32
+    arithmetic (1e-6 absolute) of every element."""
+    got = np.asarray(got, dtype=np.float64)
+    aw = np.abs(want)
+    half_ulp = np.where(aw > 0, 2.0 ** (np.floor(np.log2(np.where(aw > 0, aw, 1.0))) - 8), 0.0)
+    bound = half_ulp + 1e-6
+    bad = np.abs(got - want) > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond half a bf16 ulp, worst {np.abs(got - want).max():.3e}"
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (4, 512), (5, 1000), (3, 4096), (3, 8192), (2, 8200), (3, 7)])
+def test_ra_softmax_bf16_matches_oracle(rows, cols):
+    x = softmax_inputs(rows, cols, seed=rows * 11 + cols, sigma=4.0).to(torch.bfloat16)
+    got = ra.ra_softmax(x.cuda())
+    torch.cuda.synchronize()
+    assert got.dtype == torch.bfloat16
+    want, *_ = oracle.ra_softmax(x.double().numpy())
+    _assert_bf16_rounding_of(parity.f64(got), want, f"ra_softmax bf16 [{rows}x{cols}]")
+
+
+def test_ra_softmax_bf16_in_place_and_misaligned():
+    x = softmax_inputs(3, 4096, seed=21, sigma=4.0).to(torch.bfloat16)
+    want, *_ = oracle.ra_softmax(x.double().numpy())
+    xg = x.cuda()
+    lib = ra.lib()
+    code = lib.ra_softmax_fwd(ctypes.c_void_p(xg.data_ptr()), ctypes.c_void_p(xg.data_ptr()), 3, 4096, 1,
+                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    torch.cuda.synchronize()
+    _assert_bf16_rounding_of(parity.f64(xg), want, "ra_softmax bf16 in place")
+    # rows 2 bytes off a 16-byte boundary take the generic kernel
+    buf = softmax_inputs(1, 4 * 64 + 1, seed=22, sigma=3.0).to(torch.bfloat16).cuda()
+    view = buf[0, 1:].reshape(4, 64)
+    out = torch.empty((4, 64), dtype=torch.bfloat16, device="cuda")
+    code = lib.ra_softmax_fwd(ctypes.c_void_p(view.data_ptr()), ctypes.c_void_p(out.data_ptr()), 4, 64, 1,
+                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    torch.cuda.synchronize()
+    want2, *_ = oracle.ra_softmax(view.double().cpu().numpy())
+    _assert_bf16_rounding_of(parity.f64(out), want2, "ra_softmax bf16 offset rows")
+
+
+def test_ra_softmax_bf16_full_workload_sampled_rows():
+    """The bench's [16384, 8192] workload in bf16: every row through the kernel, 64 sampled
+    rows against the oracle."""
+    w = RA_SOFTMAX_LONG_ROWS
+    x = softmax_inputs(w.rows, w.cols, seed=w.seed, sigma=w.sigma).to(torch.bfloat16)
+    got = ra.ra_softmax(x.cuda())
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(0).choice(w.rows, size=64, replace=False)
+    want, *_ = oracle.ra_softmax(x[rows].double().numpy())
+    _assert_bf16_rounding_of(parity.f64(got[rows]), want, "ra_softmax bf16 full workload")
