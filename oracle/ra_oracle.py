@@ -114,9 +114,11 @@ def ra_softmax_bwd(x, dy, allowed=None, argmax=None):
         p, m, s, a = ra_softmax(x, allowed)
     else:
         a = np.asarray(argmax, dtype=np.int64)
-        m = np.take_along_axis(x, a[..., None], axis=-1)[..., 0]
+        # a row with no allowed entry carries argmax -1: its phi, p and gradient are 0
+        m = np.take_along_axis(x, np.maximum(a, 0)[..., None], axis=-1)[..., 0]
         phi = np.where(allowed, ra_phi(np.where(allowed, m[..., None] - x, SUPPORT)), 0.0)
-        p = phi / phi.sum(axis=-1, keepdims=True)
+        tot = phi.sum(axis=-1, keepdims=True)
+        p = phi / np.where(tot > 0, tot, 1.0)
     D = (p * dy).sum(axis=-1, keepdims=True)
     u = (m[..., None] - x) / SUPPORT
     live = allowed & (u < 1.0)
@@ -140,22 +142,32 @@ def default_scale(D, scale):
     return 1.0 / np.sqrt(D) if (scale is None or scale <= 0) else float(scale)
 
 
-def ra_attention_head_fwd(q, k, v, scale, causal):
-    """One (batch, head): O = ra_softmax(scale * q k^T [+ causal mask]) v.
+def _allowed(n_q, n_k, causal, mask):
+    """Entries that take part: the causal mask (if any) and a boolean attn_mask [N_Q, N_K]
+    (True = the query may attend to the key), as scaled_dot_product_attention reads them."""
+    allowed = _causal_allowed(n_q, n_k) if causal else np.ones((n_q, n_k), dtype=bool)
+    if mask is not None:
+        allowed = allowed & np.asarray(mask, dtype=bool)
+    return allowed
+
+
+def ra_attention_head_fwd(q, k, v, scale, causal, mask=None):
+    """One (batch, head): O = ra_softmax(scale * q k^T [+ causal mask] [+ attn_mask]) v.
 
     Page "Ra-Family: Rational Neural Architecture", section 3, ra_attention
     bullets (functional form, drop-in for scaled_dot_product_attention).
-    q: [N_Q, D], k, v: [N_K, D] float64.  Returns O [N_Q, D] and the per-row
-    statistics (m = max scaled score, s = sum phi, a = argmax key index).
+    q: [N_Q, D], k, v: [N_K, D] float64; mask: optional boolean [N_Q, N_K].
+    Returns O [N_Q, D] and the per-row statistics (m = max scaled score,
+    s = sum phi, a = argmax key index); a row with no allowed key gives O = 0.
     """
     S = scale * (q @ k.T)
-    allowed = _causal_allowed(q.shape[0], k.shape[0]) if causal else np.ones(S.shape, dtype=bool)
+    allowed = _allowed(q.shape[0], k.shape[0], causal, mask)
     P, m, s, a = ra_softmax(S, allowed)
     O = P @ v
     return O, m, s, a
 
 
-def ra_attention_head_bwd(q, k, v, do, scale, causal, argmax=None):
+def ra_attention_head_bwd(q, k, v, do, scale, causal, argmax=None, mask=None):
     """One (batch, head): gradients of sum(do * O) with respect to q, k, v.
 
     The score gradient dS is ra_softmax_bwd applied to the materialised scores
@@ -165,13 +177,15 @@ def ra_attention_head_bwd(q, k, v, do, scale, causal, argmax=None):
     then formed with x_max = S[i, argmax_i] as well.
     """
     S = scale * (q @ k.T)
-    allowed = _causal_allowed(q.shape[0], k.shape[0]) if causal else np.ones(S.shape, dtype=bool)
+    allowed = _allowed(q.shape[0], k.shape[0], causal, mask)
     if argmax is None:
         P, _, _, _ = ra_softmax(S, allowed)
     else:
-        m = np.take_along_axis(S, np.asarray(argmax, dtype=np.int64)[:, None], axis=-1)
+        am = np.asarray(argmax, dtype=np.int64)
+        m = np.take_along_axis(S, np.maximum(am, 0)[:, None], axis=-1)   # rows with argmax -1 have no allowed key
         phi = np.where(allowed, ra_phi(np.where(allowed, m - S, SUPPORT)), 0.0)
-        P = phi / phi.sum(axis=-1, keepdims=True)
+        tot = phi.sum(axis=-1, keepdims=True)
+        P = phi / np.where(tot > 0, tot, 1.0)
     dP = do @ v.T
     dS = ra_softmax_bwd(S, dP, allowed, argmax=argmax)
     dq = scale * (dS @ k)
@@ -180,9 +194,20 @@ def ra_attention_head_bwd(q, k, v, do, scale, causal, argmax=None):
     return dq, dk, dv
 
 
-def ra_attention_fwd(q, k, v, scale=None, causal=False):
+def _head_mask(mask, b, h):
+    """The [N_Q, N_K] slice of a mask broadcastable to [B, H, N_Q, N_K] (or None)."""
+    if mask is None:
+        return None
+    m = np.asarray(mask, dtype=bool)
+    while m.ndim < 4:
+        m = m[None]
+    return m[b if m.shape[0] > 1 else 0, h if m.shape[1] > 1 else 0]
+
+
+def ra_attention_fwd(q, k, v, scale=None, causal=False, mask=None):
     """Batched [B, H, N, D] forward, one head at a time (float64).
 
+    mask: optional boolean attn_mask broadcastable to [B, H, N_Q, N_K].
     Returns O [B,H,N_Q,D], m [B,H,N_Q], s [B,H,N_Q], a [B,H,N_Q].
     """
     q = np.asarray(q, dtype=np.float64)
@@ -196,12 +221,13 @@ def ra_attention_fwd(q, k, v, scale=None, causal=False):
     a = np.zeros((B, H, n_q), dtype=np.int64)
     for b in range(B):
         for h in range(H):
-            O[b, h], m[b, h], s[b, h], a[b, h] = ra_attention_head_fwd(q[b, h], k[b, h], v[b, h], scale, causal)
+            O[b, h], m[b, h], s[b, h], a[b, h] = ra_attention_head_fwd(q[b, h], k[b, h], v[b, h], scale, causal,
+                                                                       _head_mask(mask, b, h))
     return O, m, s, a
 
 
-def ra_attention_bwd(q, k, v, do, scale=None, causal=False):
-    """Batched [B, H, N, D] backward, one head at a time (float64)."""
+def ra_attention_bwd(q, k, v, do, scale=None, causal=False, mask=None):
+    """Batched [B, H, N, D] backward, one head at a time (float64); mask as in ra_attention_fwd."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -213,7 +239,8 @@ def ra_attention_bwd(q, k, v, do, scale=None, causal=False):
     dv = np.zeros(v.shape)
     for b in range(B):
         for h in range(H):
-            dq[b, h], dk[b, h], dv[b, h] = ra_attention_head_bwd(q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+            dq[b, h], dk[b, h], dv[b, h] = ra_attention_head_bwd(q[b, h], k[b, h], v[b, h], do[b, h], scale, causal,
+                                                                 mask=_head_mask(mask, b, h))
     return dq, dk, dv
 
 
