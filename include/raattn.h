@@ -208,6 +208,58 @@ void ra_debug_force_timeout(int on);
 #define RA_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /*
+ * Boolean attention masks (scaled_dot_product_attention's attn_mask: nonzero / true = the
+ * query may attend to the key), applied together with `causal`.  Page "Ra-Family: Rational
+ * Neural Architecture", section 3, ra_attention (a drop-in for scaled_dot_product_attention).
+ * The masked calls take the mask bit-packed: bit (c % 32) of word c / 32 of a row is set when
+ * column c may be attended; rows of ra_attention_mask_words(columns) uint32 words.  A mask has
+ * MB x MH heads (MB = 1 or B, MH = 1 or H: shared across the batch and/or the heads); head
+ * (b, h) uses mask head (MB > 1 ? b : 0) * MH + (MH > 1 ? h : 0).  A query row with no
+ * attendable key gives O = 0, row_s = 0, row_arg = -1 and zero gradients.
+ * Masks apply to RA_BF16 inputs (the tensor-core path); with RA_F32 inputs the masked calls
+ * return RA_ERR_UNSUPPORTED.
+ */
+
+/* ra_attention_mask_words -- uint32 words per packed row of `n` columns (whole 128-column
+ * tiles: a multiple of 4); 0 for n < 1. */
+int ra_attention_mask_words(int n);
+
+/*
+ * ra_attention_mask_pack -- bit-packs a mask of G heads, [G, N_Q, N_K] bytes (row-major,
+ * nonzero = may attend), into
+ *   mask_q   [G, N_Q, ra_attention_mask_words(N_K)] uint32 (rows = queries), and/or
+ *   mask_k   [G, N_K, ra_attention_mask_words(N_Q)] uint32 (the transpose: rows = keys).
+ * Either output may be NULL (not both); outputs are 16-byte aligned device memory owned by
+ * the caller.  The forward needs mask_q, the backward both.  Errors: RA_ERR_ARG for null
+ * pointers, sizes < 1 or misaligned outputs; RA_ERR_LAUNCH on launch failure.
+ */
+ra_status_t ra_attention_mask_pack(const void* mask, int G, int N_Q, int N_K, uint32_t* mask_q, uint32_t* mask_k,
+                                   void* stream);
+
+/*
+ * ra_attention_fwd_masked -- ra_attention_fwd with a packed mask (mask_q from
+ * ra_attention_mask_pack, MB x MH heads).  Arguments, results and errors otherwise as
+ * ra_attention_fwd; RA_ERR_ARG also for a null or misaligned mask_q or MB, MH not in
+ * {1, B} x {1, H}.
+ */
+ra_status_t ra_attention_fwd_masked(const void* q, const void* k, const void* v, void* o, float* row_m,
+                                    float* row_s, int32_t* row_arg, int64_t* tile_counts, void* workspace, int B,
+                                    int H, int N_Q, int N_K, int D, float scale, int causal, ra_dtype_t in_dtype,
+                                    ra_dtype_t out_dtype, const uint32_t* mask_q, int MB, int MH, void* stream);
+
+/*
+ * ra_attention_bwd_masked -- ra_attention_bwd for a masked forward: the same packed mask in
+ * both layouts (mask_q, mask_k from one ra_attention_mask_pack call), MB x MH heads.
+ * Arguments, results and errors otherwise as ra_attention_bwd.
+ */
+ra_status_t ra_attention_bwd_masked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                    const float* row_m, const float* row_s, const int32_t* row_arg, void* dq,
+                                    void* dk, void* dv, void* workspace, int B, int H, int N_Q, int N_K, int D,
+                                    float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t o_dtype,
+                                    ra_dtype_t grad_dtype, const uint32_t* mask_q, const uint32_t* mask_k, int MB,
+                                    int MH, void* stream);
+
+/*
  * ra_attention_bwd_noalloc -- ra_attention_bwd without a caller-supplied workspace.
  * The pages have no counterpart: this entry point exists for callers that cannot
  * allocate device memory, such as code inside a framework that owns the allocator and

@@ -8,7 +8,7 @@ library is not built, or the tensors are not on a CUDA device, the calls raise.
 Functional API, after the page "Ra-Family: Rational Neural Architecture",
 section 3 "Rational Attention & Softmax":
     ra_softmax(x)                                   last-dim rational soft-argmax
-    ra_attention(q, k, v, is_causal=False, scale=None)   drop-in for SDPA, autograd-aware
+    ra_attention(q, k, v, attn_mask=None, is_causal=False, scale=None)   drop-in for SDPA, autograd-aware
 plus the explicit forward/backward entry points used by tests and benchmarks.
 """
 from __future__ import annotations
@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "RaError", "lib", "ra_softmax", "ra_softmax_backward", "ra_attention", "ra_attention_forward", "RaAttention",
-    "ra_attention_backward", "device_status", "set_wait_limit_ns", "exported_symbols", "LIB_PATH",
+    "ra_attention_backward", "pack_attn_mask", "device_status", "set_wait_limit_ns", "exported_symbols", "LIB_PATH",
 ]
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
@@ -52,6 +52,12 @@ _SIGNATURES = {
     "ra_attention_fwd_workspace_size": ([_i32, _i32, _i32, _i32, _i32], ctypes.c_size_t),
     "ra_attention_bwd_workspace_size": ([_i32, _i32, _i32, _i32, _i32], ctypes.c_size_t),
     "ra_attention_bwd": ([_vp] * 12 + [_i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp], _i32),
+    "ra_attention_mask_words": ([_i32], _i32),
+    "ra_attention_mask_pack": ([_vp, _i32, _i32, _i32, _vp, _vp, _vp], _i32),
+    "ra_attention_fwd_masked": ([_vp] * 9 + [_i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _i32, _i32,
+                                               _vp], _i32),
+    "ra_attention_bwd_masked": ([_vp] * 12 + [_i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp, _vp,
+                                                _i32, _i32, _vp], _i32),
     "ra_device_status": ([_vp], _i32),
     "ra_set_wait_limit_ns": ([_u64], None),
     "ra_debug_force_timeout": ([_i32], None),
@@ -136,10 +142,37 @@ def ra_softmax_backward(x, p, dy, out=None):
     return dx
 
 
-def ra_attention_forward(q, k, v, *, scale=None, causal=False, out_dtype=None, with_stats=True,
-                         tile_counts=False):
-    """O = ra_softmax(scale q k^T [causal]) v for [B, H, N, D] tensors.
+def pack_attn_mask(attn_mask, B, H, n_q, n_k):
+    """Bit-packs a boolean attn_mask broadcastable to [B, H, N_Q, N_K] (True = the query may
+    attend to the key, as in scaled_dot_product_attention) for the masked attention calls.
 
+    Returns (mask_q, mask_k, MB, MH): the packed mask with a row per query and with a row
+    per key, and how many batch and head entries it has (1 = shared)."""
+    if attn_mask.dtype != torch.bool:
+        raise NotImplementedError("only boolean attention masks are supported")
+    _require_cuda(attn_mask.contiguous())
+    m = attn_mask
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    if m.dim() != 4:
+        raise ValueError("attn_mask must broadcast to [B, H, N_Q, N_K]")
+    MB, MH = m.shape[0], m.shape[1]
+    if MB not in (1, B) or MH not in (1, H):
+        raise ValueError("attn_mask must broadcast to [B, H, N_Q, N_K]")
+    m8 = m.expand(MB, MH, n_q, n_k).contiguous().view(torch.uint8)
+    L = lib()
+    mask_q = torch.empty((MB * MH, n_q, L.ra_attention_mask_words(n_k)), dtype=torch.int32, device=m.device)
+    mask_k = torch.empty((MB * MH, n_k, L.ra_attention_mask_words(n_q)), dtype=torch.int32, device=m.device)
+    _check("ra_attention_mask_pack", L.ra_attention_mask_pack(_ptr(m8), MB * MH, n_q, n_k, _ptr(mask_q),
+                                                                _ptr(mask_k), _stream(m.device)))
+    return mask_q, mask_k, MB, MH
+
+
+def ra_attention_forward(q, k, v, *, scale=None, causal=False, out_dtype=None, with_stats=True,
+                         tile_counts=False, mask=None):
+    """O = ra_softmax(scale q k^T [causal] [mask]) v for [B, H, N, D] tensors.
+
+    mask: None, or the tuple pack_attn_mask returns (bf16 inputs only).
     Returns (o, row_m, row_s, row_arg, counts): the statistics are None unless
     with_stats; counts is an int64 CUDA tensor [pairs visited, pairs skipped]
     when tile_counts, else None.
@@ -160,16 +193,24 @@ def ra_attention_forward(q, k, v, *, scale=None, causal=False, out_dtype=None, w
     ws = None
     if q.dtype == torch.bfloat16:
         ws = torch.empty(L.ra_attention_fwd_workspace_size(B, H, NQ, NK, D), dtype=torch.uint8, device=q.device)
-    _check("ra_attention_fwd", L.ra_attention_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(rm), _ptr(rs), _ptr(ra), _ptr(counts), _ptr(ws),
-        B, H, NQ, NK, D, float(scale or 0.0), 1 if causal else 0, _dtype_code(q.dtype), _dtype_code(out_dtype),
-        _stream(q.device)))
+    if mask is None:
+        _check("ra_attention_fwd", L.ra_attention_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(rm), _ptr(rs), _ptr(ra), _ptr(counts), _ptr(ws),
+            B, H, NQ, NK, D, float(scale or 0.0), 1 if causal else 0, _dtype_code(q.dtype), _dtype_code(out_dtype),
+            _stream(q.device)))
+    else:
+        mask_q, _, MB, MH = mask
+        _check("ra_attention_fwd_masked", L.ra_attention_fwd_masked(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(rm), _ptr(rs), _ptr(ra), _ptr(counts), _ptr(ws),
+            B, H, NQ, NK, D, float(scale or 0.0), 1 if causal else 0, _dtype_code(q.dtype), _dtype_code(out_dtype),
+            _ptr(mask_q), MB, MH, _stream(q.device)))
     return o, rm, rs, ra, counts
 
 
 def ra_attention_backward(q, k, v, o, dout, row_m, row_s, row_arg, *, scale=None, causal=False,
-                          grad_dtype=torch.float32, workspace=None):
-    """Gradients (dq, dk, dv) of sum(dout * O) for the forward that produced o and the row statistics."""
+                          grad_dtype=torch.float32, workspace=None, mask=None):
+    """Gradients (dq, dk, dv) of sum(dout * O) for the forward that produced o and the row
+    statistics; mask as given to that forward."""
     _require_cuda(q, k, v, o, dout, row_m, row_s, row_arg)
     B, H, NQ, D = q.shape
     NK = k.shape[2]
@@ -180,33 +221,47 @@ def ra_attention_backward(q, k, v, o, dout, row_m, row_s, row_arg, *, scale=None
     dq = torch.empty((B, H, NQ, D), dtype=grad_dtype, device=q.device)
     dk = torch.empty((B, H, NK, D), dtype=grad_dtype, device=q.device)
     dv = torch.empty((B, H, NK, D), dtype=grad_dtype, device=q.device)
-    _check("ra_attention_bwd", L.ra_attention_bwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(row_m), _ptr(row_s), _ptr(row_arg),
-        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), B, H, NQ, NK, D, float(scale or 0.0),
-        1 if causal else 0, _dtype_code(q.dtype), _dtype_code(o.dtype), _dtype_code(grad_dtype),
-        _stream(q.device)))
+    if mask is None:
+        _check("ra_attention_bwd", L.ra_attention_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(row_m), _ptr(row_s), _ptr(row_arg),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), B, H, NQ, NK, D, float(scale or 0.0),
+            1 if causal else 0, _dtype_code(q.dtype), _dtype_code(o.dtype), _dtype_code(grad_dtype),
+            _stream(q.device)))
+    else:
+        mask_q, mask_k, MB, MH = mask
+        _check("ra_attention_bwd_masked", L.ra_attention_bwd_masked(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(row_m), _ptr(row_s), _ptr(row_arg),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), B, H, NQ, NK, D, float(scale or 0.0),
+            1 if causal else 0, _dtype_code(q.dtype), _dtype_code(o.dtype), _dtype_code(grad_dtype),
+            _ptr(mask_q), _ptr(mask_k), MB, MH, _stream(q.device)))
     return dq, dk, dv
 
 
 class _RaAttentionFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal, scale):
-        o, rm, rs, ra, _ = ra_attention_forward(q, k, v, scale=scale, causal=causal, out_dtype=q.dtype)
+    def forward(ctx, q, k, v, causal, scale, attn_mask):
+        mask = None
+        if attn_mask is not None:
+            mask = pack_attn_mask(attn_mask, q.shape[0], q.shape[1], q.shape[2], k.shape[2])
+        o, rm, rs, ra, _ = ra_attention_forward(q, k, v, scale=scale, causal=causal, out_dtype=q.dtype, mask=mask)
         ctx.save_for_backward(q, k, v, o, rm, rs, ra)
-        ctx.causal, ctx.scale = causal, scale
+        ctx.causal, ctx.scale, ctx.mask = causal, scale, mask
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, rm, rs, ra = ctx.saved_tensors
         dq, dk, dv = ra_attention_backward(q, k, v, o, do.contiguous().to(q.dtype), rm, rs, ra,
-                                           scale=ctx.scale, causal=ctx.causal, grad_dtype=q.dtype)
-        return dq, dk, dv, None, None
+                                           scale=ctx.scale, causal=ctx.causal, grad_dtype=q.dtype, mask=ctx.mask)
+        return dq, dk, dv, None, None, None
 
 
-def ra_attention(q, k, v, is_causal=False, scale=None):
-    """Rational-softmax attention, a drop-in for scaled_dot_product_attention (no mask/dropout)."""
-    return _RaAttentionFn.apply(q.contiguous(), k.contiguous(), v.contiguous(), bool(is_causal), scale)
+def ra_attention(q, k, v, attn_mask=None, is_causal=False, scale=None):
+    """Rational-softmax attention, a drop-in for scaled_dot_product_attention (no dropout).
+
+    attn_mask: optional boolean mask broadcastable to [B, H, N_Q, N_K], True where the query
+    may attend to the key (bf16 inputs only); combined with is_causal."""
+    return _RaAttentionFn.apply(q.contiguous(), k.contiguous(), v.contiguous(), bool(is_causal), scale, attn_mask)
 
 
 class RaAttention(torch.nn.Module):

@@ -179,10 +179,26 @@ size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D) {
   return (static_cast<size_t>(B) * H * N_K * D * 2 + 255) & ~static_cast<size_t>(255);   // fp16 copy of V
 }
 
-ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* o, float* row_m, float* row_s,
-                             int32_t* row_arg, int64_t* tile_counts, void* workspace, int B, int H, int N_Q,
-                             int N_K, int D, float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t out_dtype,
-                             void* stream) {
+}  // extern "C"
+
+namespace raattn {
+namespace {
+
+// Validates a packed mask for (B, H, N_Q, N_K); fills `m` (bits null when there is no mask).
+ra_status_t mask_args(const uint32_t* bits, int MB, int MH, int B, int H, int cols, MaskBits* m) {
+  m->bits = bits;
+  m->words = ra_attention_mask_words(cols);
+  m->mb = MB;
+  m->mh = MH;
+  if (!bits) return RA_OK;
+  if (!aligned16(bits) || !(MB == 1 || MB == B) || !(MH == 1 || MH == H)) return RA_ERR_ARG;
+  return RA_OK;
+}
+
+ra_status_t attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* row_m, float* row_s,
+                          int32_t* row_arg, int64_t* tile_counts, void* workspace, int B, int H, int N_Q, int N_K,
+                          int D, float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t out_dtype, void* stream,
+                          const MaskBits& mask) {
   if (!q || !k || !v || !o || !dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return RA_ERR_ARG;
   if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return RA_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return RA_ERR_ARG;
@@ -197,6 +213,7 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
 
   if (in_dtype == RA_F32) {
     if (!(D == 16 || D == 32 || D == 64 || D == 128)) return RA_ERR_UNSUPPORTED;
+    if (mask.bits) return RA_ERR_UNSUPPORTED;   // masks on the tensor-core (bf16) path only
     if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
     const cudaError_t e = launch_attn_fwd_simt(s, static_cast<const float*>(q), static_cast<const float*>(k),
                                                static_cast<const float*>(v), o, out_dtype == RA_BF16, row_m, row_s,
@@ -223,9 +240,49 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
   a.row_arg = row_arg;
   a.tile_counts = reinterpret_cast<unsigned long long*>(tile_counts);
   a.out_bf16 = out_dtype == RA_BF16 ? 1 : 0;
+  a.mask = mask;
   if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
   if (launch_bf16_to_f16(job, ctx.status, st) != cudaSuccess) return RA_ERR_LAUNCH;
   const cudaError_t e = launch_attn_fwd_tc(s, a, ctx, st);
+  return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace raattn
+
+extern "C" {
+
+ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* o, float* row_m, float* row_s,
+                             int32_t* row_arg, int64_t* tile_counts, void* workspace, int B, int H, int N_Q,
+                             int N_K, int D, float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t out_dtype,
+                             void* stream) {
+  const MaskBits none{nullptr, 0, 1, 1};
+  return attn_fwd_impl(q, k, v, o, row_m, row_s, row_arg, tile_counts, workspace, B, H, N_Q, N_K, D, scale, causal,
+                       in_dtype, out_dtype, stream, none);
+}
+
+ra_status_t ra_attention_fwd_masked(const void* q, const void* k, const void* v, void* o, float* row_m,
+                                    float* row_s, int32_t* row_arg, int64_t* tile_counts, void* workspace, int B,
+                                    int H, int N_Q, int N_K, int D, float scale, int causal, ra_dtype_t in_dtype,
+                                    ra_dtype_t out_dtype, const uint32_t* mask_q, int MB, int MH, void* stream) {
+  if (!mask_q) return RA_ERR_ARG;
+  MaskBits m;
+  const ra_status_t r = mask_args(mask_q, MB, MH, B, H, N_K, &m);
+  if (r != RA_OK) return r;
+  return attn_fwd_impl(q, k, v, o, row_m, row_s, row_arg, tile_counts, workspace, B, H, N_Q, N_K, D, scale, causal,
+                       in_dtype, out_dtype, stream, m);
+}
+
+int ra_attention_mask_words(int n) { return n < 1 ? 0 : ((n + 127) / 128) * 4; }
+
+ra_status_t ra_attention_mask_pack(const void* mask, int G, int N_Q, int N_K, uint32_t* bits_q, uint32_t* bits_k,
+                                   void* stream) {
+  if (!mask || (!bits_q && !bits_k) || G < 1 || N_Q < 1 || N_K < 1) return RA_ERR_ARG;
+  if (static_cast<long long>(G) * N_Q * N_K > (1ll << 40)) return RA_ERR_ARG;
+  if ((bits_q && !aligned16(bits_q)) || (bits_k && !aligned16(bits_k))) return RA_ERR_ARG;
+  const cudaError_t e = launch_mask_pack(static_cast<const uint8_t*>(mask), G, N_Q, N_K, bits_q,
+                                         ra_attention_mask_words(N_K), bits_k, ra_attention_mask_words(N_Q),
+                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
 
@@ -234,11 +291,16 @@ size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D) {
   return BwdLayout(B, H, N_Q, N_K, D).total_tc;   // enough for either path
 }
 
-ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                             const float* row_m, const float* row_s, const int32_t* row_arg, void* dq, void* dk,
-                             void* dv, void* workspace, int B, int H, int N_Q, int N_K, int D, float scale,
-                             int causal, ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype,
-                             void* stream) {
+}  // extern "C"
+
+namespace raattn {
+namespace {
+
+ra_status_t attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* row_m, const float* row_s, const int32_t* row_arg, void* dq, void* dk,
+                          void* dv, void* workspace, int B, int H, int N_Q, int N_K, int D, float scale, int causal,
+                          ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype, void* stream,
+                          const MaskBits& mask_q, const MaskBits& mask_k) {
   if (!q || !k || !v || !o || !dout || !row_m || !row_s || !row_arg || !dq || !dk || !dv || !workspace)
     return RA_ERR_ARG;
   if (!dtype_ok(in_dtype) || !dtype_ok(o_dtype) || !dtype_ok(grad_dtype)) return RA_ERR_ARG;
@@ -258,6 +320,7 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
 
   if (in_dtype == RA_F32) {
     if (!(D == 16 || D == 32 || D == 64 || D == 128)) return RA_ERR_UNSUPPORTED;
+    if (mask_q.bits) return RA_ERR_UNSUPPORTED;   // masks on the tensor-core (bf16) path only
     const cudaError_t e = launch_attn_bwd_simt(
         s, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), o,
         o_dtype == RA_BF16, static_cast<const float*>(dout), row_m, row_s, row_arg, dq, dk, dv,
@@ -291,8 +354,40 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
   a.dv = dv;
   a.grad_bf16 = grad_dtype == RA_BF16 ? 1 : 0;
   a.ws_consts = reinterpret_cast<float*>(ws);
+  a.mask_q = mask_q;
+  a.mask_k = mask_k;
   const cudaError_t e = launch_attn_bwd_tc(s, a, ctx, st);
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace raattn
+
+extern "C" {
+
+ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                             const float* row_m, const float* row_s, const int32_t* row_arg, void* dq, void* dk,
+                             void* dv, void* workspace, int B, int H, int N_Q, int N_K, int D, float scale,
+                             int causal, ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype,
+                             void* stream) {
+  const MaskBits none{nullptr, 0, 1, 1};
+  return attn_bwd_impl(q, k, v, o, dout, row_m, row_s, row_arg, dq, dk, dv, workspace, B, H, N_Q, N_K, D, scale,
+                       causal, in_dtype, o_dtype, grad_dtype, stream, none, none);
+}
+
+ra_status_t ra_attention_bwd_masked(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                    const float* row_m, const float* row_s, const int32_t* row_arg, void* dq,
+                                    void* dk, void* dv, void* workspace, int B, int H, int N_Q, int N_K, int D,
+                                    float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t o_dtype,
+                                    ra_dtype_t grad_dtype, const uint32_t* mask_q, const uint32_t* mask_k, int MB,
+                                    int MH, void* stream) {
+  if (!mask_q || !mask_k) return RA_ERR_ARG;
+  MaskBits mq, mk;
+  ra_status_t r = mask_args(mask_q, MB, MH, B, H, N_K, &mq);
+  if (r == RA_OK) r = mask_args(mask_k, MB, MH, B, H, N_Q, &mk);
+  if (r != RA_OK) return r;
+  return attn_bwd_impl(q, k, v, o, dout, row_m, row_s, row_arg, dq, dk, dv, workspace, B, H, N_Q, N_K, D, scale,
+                       causal, in_dtype, o_dtype, grad_dtype, stream, mq, mk);
 }
 
 }  // extern "C"

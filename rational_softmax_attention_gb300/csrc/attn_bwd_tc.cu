@@ -124,7 +124,8 @@ __device__ __forceinline__ void softmax_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(DQ_SOFTMAX_WARPS * 32) : "memory");
 }
 
-template <int D>
+// MASK: a boolean attention mask (args.mask_q, rows = queries) applies on top of `causal`.
+template <int D, bool MASK>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
   using C = DqCfg<D>;
@@ -326,8 +327,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       return __shfl_sync(0xffffffffu, okv, 0) != 0;
     };
     const float m_sc = args.row_m[ro];
-    const float inv_s = 1.0f / args.row_s[ro];
+    const float row_s = args.row_s[ro];
+    const float inv_s = row_s > 0.0f ? 1.0f / row_s : 0.0f;   // 0: a row with no visible key
     const int a = min(max(args.row_arg[ro], 0), s.NK - 1);
+    // this row's attention-mask words: four per key tile, one per warp part
+    const uint32_t* mrow = nullptr;
+    if (MASK) {
+      const int gm = (args.mask_q.mb > 1 ? bh / s.H : 0) * args.mask_q.mh + (args.mask_q.mh > 1 ? bh % s.H : 0);
+      mrow = args.mask_q.bits + (static_cast<size_t>(gm) * s.NQ + (i_ok ? i : s.NQ - 1)) * args.mask_q.words;
+    }
     // D_i = dO_i . O_i: each part of the warps sums D / DQ_PARTS of the dimensions
     {
       float acc = 0.0f;
@@ -355,7 +363,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     for (int pp = 0; pp < DQ_PARTS; ++pp) Di += xch[pp * BM + r];
     softmax_sync();   // xch is reused for R_i after the loop
     // rows past N_Q read zero-filled Q rows (s = 0): base 2 saturates every w to 1, weight 0
-    const float base = i_ok ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
+    const float base = (i_ok && m_sc > -INFINITY) ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
     const float c2 = s.scale * (1.0f / 32.0f);
     const float cE = 0.25f * inv_s;
     const int lim = s.causal ? min(i, s.NK - 1) : s.NK - 1;
@@ -375,7 +383,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         tc_wait_ld();
       }
       const int col0 = j * BN + cbase;   // key index of local column 0
-      const bool need_mask = col0 + DQ_COLS - 1 > lim;
+      const bool need_mask = MASK || col0 + DQ_COLS - 1 > lim;
+      const uint32_t mw = MASK ? mrow[4 * j + part] : ~0u;
       // coefficient q^7 (1/w)^2 per entry, in place; the factor 1/(4 s_i) is applied with
       // dP - D_i below.  Four entries share two reciprocals (coef_quad).
 #pragma unroll
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         if (need_mask) {
 #pragma unroll
           for (int t = 0; t < 4; ++t)
-            if (col0 + c + t > lim) x[t] = -INFINITY;
+            if (col0 + c + t > lim || (MASK && !((mw >> (c + t)) & 1u))) x[t] = -INFINITY;
         }
         float2 ca, cb;
         coef_quad(x, c2, base, ca, cb);
@@ -532,7 +541,8 @@ constexpr int KV_MMA_WARP = KV_SOFTMAX_WARPS + 1;
 constexpr int KV_THREADS = 32 * (KV_SOFTMAX_WARPS + 3);
 static_assert(KV_COLS % 32 == 0, "whole 32-column TMEM loads per softmax warp");
 
-template <int D>
+// MASK: a boolean attention mask (args.mask_k, rows = keys) applies on top of `causal`.
+template <int D, bool MASK>
 __global__ void __launch_bounds__(KV_THREADS, 1)
     attn_bwd_dkdv_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
   using C = DkvCfg<D>;
@@ -781,6 +791,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       if (lane == 0) okv = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, okv, 0) != 0;
     };
+    // this key row's attention-mask words (the transposed mask): four per query tile
+    const uint32_t* mkey = nullptr;
+    if (MASK) {
+      const int gm = (args.mask_k.mb > 1 ? bh / s.H : 0) * args.mask_k.mh + (args.mask_k.mh > 1 ? bh % s.H : 0);
+      mkey = args.mask_k.bits + (static_cast<size_t>(gm) * s.NK + (j_ok ? j : s.NK - 1)) * args.mask_k.words;
+    }
     uint32_t sv[KV_COLS / 32][32];
 #define SV(c) sv[(c) >> 5][(c) & 31]
     for (int it = 0; it < nq; ++it) {
@@ -793,7 +809,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       for (int h = 0; h < KV_COLS / 32; ++h) tmem_ld32(lane_addr + KV_TM_ST + cbase + 32 * h, sv[h]);
       tc_wait_ld();
       // masked: key past N_K, or (causal) query i0 + c < j
-      const bool need_mask = !j_ok || (s.causal && i0 + cbase < j);
+      const bool need_mask = MASK || !j_ok || (s.causal && i0 + cbase < j);
+      const uint32_t mw = MASK ? mkey[4 * (qt0 + it) + part] : ~0u;
       const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
       // P^T = q^8 / s_i and the dS coefficient q^7 (1/w)^2 / s_i = q^7 (1 + q)^2 / s_i (in
       // place): with t = q^7 / s_i, P = t q and the coefficient is t + P (2 + q).  The factor
@@ -814,7 +831,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           if (need_mask) {
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-              if (cg + t < first_vis) x[t] = -INFINITY;
+              if (cg + t < first_vis || (MASK && !((mw >> (cb + t)) & 1u))) x[t] = -INFINITY;
           }
           const float2 A = make_float2(fma_sat(x[0], -c2, b4.x), fma_sat(x[1], -c2, b4.y));
           const float2 B = make_float2(fma_sat(x[2], -c2, b4.z), fma_sat(x[3], -c2, b4.w));
@@ -953,11 +970,11 @@ cudaError_t set_smem(KernelFn fn, int bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int D>
+template <int D, bool MASK>
 cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
-  cudaError_t e = set_smem(attn_bwd_dq_tc_kernel<D>, DqCfg<D>::SMEM_BYTES);
+  cudaError_t e = set_smem(attn_bwd_dq_tc_kernel<D, MASK>, DqCfg<D>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  e = set_smem(attn_bwd_dkdv_tc_kernel<D>, DkvCfg<D>::SMEM_BYTES);
+  e = set_smem(attn_bwd_dkdv_tc_kernel<D, MASK>, DkvCfg<D>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned BH = static_cast<unsigned>(s.B * s.H);
   const unsigned nqt = static_cast<unsigned>((s.NQ + BM - 1) / BM);
@@ -975,18 +992,19 @@ cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx
   job.count = 4;
   e = launch_bf16_to_f16(job, ctx.status, st);
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_tc_kernel<D><<<nqt * BH, DQ_THREADS, DqCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
+  attn_bwd_dq_tc_kernel<D, MASK><<<nqt * BH, DQ_THREADS, DqCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_tc_kernel<D><<<nkt * BH, KV_THREADS, DkvCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
+  attn_bwd_dkdv_tc_kernel<D, MASK><<<nkt * BH, KV_THREADS, DkvCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
-  if (s.D == 128) return launch_bwd_d<128>(s, a, ctx, st);
-  if (s.D == 64) return launch_bwd_d<64>(s, a, ctx, st);
+  const bool mask = a.mask_q.bits != nullptr;
+  if (s.D == 128) return mask ? launch_bwd_d<128, true>(s, a, ctx, st) : launch_bwd_d<128, false>(s, a, ctx, st);
+  if (s.D == 64) return mask ? launch_bwd_d<64, true>(s, a, ctx, st) : launch_bwd_d<64, false>(s, a, ctx, st);
   return cudaErrorInvalidValue;
 }
 

@@ -114,10 +114,11 @@ __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 // Pass-2 arithmetic of one 64-key half of a row, held in h (two 32-column chunks): phi
 // as packed fp16 pairs in pk (four per 16-byte chunk of P) and the partial row sum.
 // MASKED: columns past `lim` (causal diagonal, ragged tail) get s = -inf, hence w = 1
-// and phi = 0.
-template <bool MASKED>
+// and phi = 0.  BITS: so do columns whose attention-mask bit (mw0 for the first 32
+// columns, mw1 for the second) is clear.
+template <bool MASKED, bool BITS>
 __device__ __forceinline__ float2 phi_half(const uint32_t (&h)[2][32], uint32_t (&pk)[32], int col0, int lim,
-                                           float c2, float base) {
+                                           float c2, float base, uint32_t mw0, uint32_t mw1) {
   float2 tsum2 = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int c8 = 0; c8 < 8; ++c8) {
@@ -127,6 +128,7 @@ __device__ __forceinline__ float2 phi_half(const uint32_t (&h)[2][32], uint32_t 
       const int c = c8 * 8 + e;
       x[e] = u2f(h[c >> 5][c & 31]);
       if (MASKED && col0 + c > lim) x[e] = -INFINITY;
+      if (BITS && !((((c >> 5) ? mw1 : mw0) >> (c & 31)) & 1u)) x[e] = -INFINITY;
     }
     float2 p0, p1, p2, p3;
     phi_quad(x[0], x[1], x[2], x[3], c2, base, p0, p1);
@@ -149,24 +151,26 @@ __device__ __forceinline__ void store_p_half(const uint32_t (&pk)[32], uint8_t* 
         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
-template <bool MASKED>
+template <bool MASKED, bool BITS>
 __device__ __forceinline__ float2 phi_store_half(const uint32_t (&h)[2][32], uint8_t* phalf_row, int row_local,
-                                                 int col0, int lim, float c2, float base) {
+                                                 int col0, int lim, float c2, float base, uint32_t mw0, uint32_t mw1) {
   uint32_t pk[32];
-  const float2 t = phi_half<MASKED>(h, pk, col0, lim, c2, base);
+  const float2 t = phi_half<MASKED, BITS>(h, pk, col0, lim, c2, base, mw0, mw1);
   store_p_half(pk, phalf_row, row_local);
   return t;
 }
 
-// Lowest column of a 32-column chunk whose score equals m (visible columns only), or 32.
-__device__ __forceinline__ int find_in_chunk(const uint32_t (&v)[32], float m, int col0, int lim) {
+// Lowest column of a 32-column chunk whose score equals m (visible columns only: at most
+// `lim`, attention-mask bit set in mword), or 32.
+__device__ __forceinline__ int find_in_chunk(const uint32_t (&v)[32], float m, int col0, int lim, uint32_t mword) {
   int idx = 32;
 #pragma unroll
-  for (int c = 31; c >= 0; --c) idx = (u2f(v[c]) == m && col0 + c <= lim) ? c : idx;
+  for (int c = 31; c >= 0; --c) idx = (u2f(v[c]) == m && col0 + c <= lim && ((mword >> c) & 1u)) ? c : idx;
   return idx;
 }
 
-template <int D>
+// MASK: a boolean attention mask (args.mask) applies on top of `causal`.
+template <int D, bool MASK>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_tc_kernel(const AttnShape s, const __grid_constant__ FwdTcArgs args, const LaunchCtx ctx) {
   using C = FwdCfg<D>;
@@ -420,6 +424,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) r = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
+    // this row's attention-mask words: four per key tile (rows past N_Q read the last row)
+    const uint32_t* mrow = nullptr;
+    if (MASK) {
+      const int gm = (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0);
+      mrow = args.mask.bits + (static_cast<size_t>(gm) * s.NQ + min(row, s.NQ - 1)) * args.mask.words;
+    }
+    auto mask_words = [&](int j, uint32_t (&mw)[4]) {
+      if (MASK) {
+        const uint4 u = *reinterpret_cast<const uint4*>(mrow + 4 * j);
+        mw[0] = u.x;
+        mw[1] = u.y;
+        mw[2] = u.z;
+        mw[3] = u.w;
+      } else {
+        mw[0] = mw[1] = mw[2] = mw[3] = ~0u;
+      }
+    };
     uint32_t sv[BN / 32][32];
     // S_g into registers, then hand the buffer back to the MMA thread
     // pass-1 tile j sits in score buffer j & 1, as that buffer's use j >> 1
@@ -446,10 +467,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = take_s(j & 1, static_cast<uint32_t>(j) >> 1);
       if (!ok) break;
       const int col0 = j * BN;   // key index of column 0
+      uint32_t mw[4];
+      mask_words(j, mw);
       // maximum of each 32-column chunk; the first chunk (in key order) that raises the
       // running maximum strictly is remembered, so ties keep the lowest index
       float cm[BN / 32];
-      if (col0 + BN - 1 <= lim) {
+      if (!MASK && col0 + BN - 1 <= lim) {
 #pragma unroll
         for (int k = 0; k < BN / 32; ++k) {
           float u0 = -INFINITY, u1 = -INFINITY;
@@ -466,8 +489,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           float u0 = -INFINITY, u1 = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            u0 = fmaxf(u0, (col0 + 32 * k + c <= lim) ? u2f(sv[k][c]) : -INFINITY);
-            u1 = fmaxf(u1, (col0 + 32 * k + c + 1 <= lim) ? u2f(sv[k][c + 1]) : -INFINITY);
+            u0 = fmaxf(u0, (col0 + 32 * k + c <= lim && ((mw[k] >> c) & 1u)) ? u2f(sv[k][c]) : -INFINITY);
+            u1 = fmaxf(u1, (col0 + 32 * k + c + 1 <= lim && ((mw[k] >> (c + 1)) & 1u)) ? u2f(sv[k][c + 1])
+                                                                                       : -INFINITY);
           }
           cm[k] = fmaxf(u0, u1);
         }
@@ -484,7 +508,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // back; then, once the previous product has released the P tile, both halves are stored.
     const float m_sc = m * s.scale;
     const float c2 = s.scale * (1.0f / 32.0f);
-    const float base = fmaf(m_sc, 1.0f / 32.0f, 0.5f);
+    // a row with no visible key (possible under an attention mask) keeps m = -inf: base 2
+    // then saturates every w to 1 (phi = 0), and the row's output is 0
+    const float base = (m > -INFINITY) ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
     uint8_t* prow = sP + g * C::P_BYTES + row_local * 128;
     float rowsum = 0.0f;
     sidx = static_cast<uint32_t>(nkt + 1) >> 1;   // pass 1 used buffer 0 for tiles 0, 2, 4, ...
@@ -494,17 +520,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       ++sidx;
       tc_fence_after();
       const int col0 = j * BN;
-      const bool masked = col0 + BN - 1 > lim;
-      const bool arg_tile = j == (jm >> 2);
+      const bool masked = MASK || col0 + BN - 1 > lim;
+      const bool arg_tile = j == (jm >> 2) && m > -INFINITY;
+      uint32_t mw[4];
+      mask_words(j, mw);
       uint32_t h[2][32];
       tmem_ld32(scol, h[0]);
       tmem_ld32(scol + 32, h[1]);
       tc_wait_ld();
       if (arg_tile && (jm & 3) < 2)   // lowest visible column holding the maximum
-        a = col0 + ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 32, lim) : find_in_chunk(h[0], m, col0, lim));
+        a = col0 + ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 32, lim, mw[1])
+                             : find_in_chunk(h[0], m, col0, lim, mw[0]));
       uint32_t pk[32];
-      float2 tsum2 = masked ? phi_half<true>(h, pk, col0, lim, c2, base)
-                            : phi_half<false>(h, pk, col0, lim, c2, base);
+      float2 tsum2 = masked ? phi_half<true, MASK>(h, pk, col0, lim, c2, base, mw[0], mw[1])
+                            : phi_half<false, false>(h, pk, col0, lim, c2, base, ~0u, ~0u);
       tmem_ld32(scol + 64, h[0]);
       tmem_ld32(scol + 96, h[1]);
       tc_wait_ld();
@@ -513,13 +542,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(&s_empty[2 * g]);
       if (arg_tile && (jm & 3) >= 2)
         a = col0 + 64 +
-            ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 96, lim) : find_in_chunk(h[0], m, col0 + 64, lim));
+            ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 96, lim, mw[3])
+                      : find_in_chunk(h[0], m, col0 + 64, lim, mw[2]));
       // the P tile is free once the previous O_g += P_g V product has completed
       ok = warp_wait(&p_empty[g], (j & 1u) ^ 1u);
       if (!ok) break;
       store_p_half(pk, prow, row_local);
-      const float2 t2 = masked ? phi_store_half<true>(h, prow + BOX_BYTES, row_local, col0 + 64, lim, c2, base)
-                               : phi_store_half<false>(h, prow + BOX_BYTES, row_local, col0 + 64, lim, c2, base);
+      const float2 t2 =
+          masked ? phi_store_half<true, MASK>(h, prow + BOX_BYTES, row_local, col0 + 64, lim, c2, base, mw[2], mw[3])
+                 : phi_store_half<false, false>(h, prow + BOX_BYTES, row_local, col0 + 64, lim, c2, base, ~0u, ~0u);
       tsum2 = __fadd2_rn(tsum2, t2);
       fence_proxy_async_smem();
       const float tsum = tsum2.x + tsum2.y;
@@ -534,7 +565,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < s.NQ;
-      const float inv = 1.0f / rowsum;
+      const float inv = rowsum > 0.0f ? 1.0f / rowsum : 0.0f;   // 0: a row with no visible key
       const size_t ro = static_cast<size_t>(bh) * s.NQ + (row_ok ? row : 0);
       // O rows leave through this query tile's P tile (free: o_full means the last P V
       // product has read it), 4 KB per warp, in whole row segments
@@ -572,24 +603,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool MASK>
 cudaError_t launch_fwd_d(const AttnShape& s, const FwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
   using C = FwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int nqt = (s.NQ + BM - 1) / BM;
   const int nct = (nqt + NGROUP - 1) / NGROUP;
   const unsigned grid = static_cast<unsigned>(nct) * static_cast<unsigned>(s.B * s.H);
-  attn_fwd_tc_kernel<D><<<grid, THREADS, C::SMEM_BYTES, st>>>(s, a, ctx);
+  attn_fwd_tc_kernel<D, MASK><<<grid, THREADS, C::SMEM_BYTES, st>>>(s, a, ctx);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd_tc(const AttnShape& s, const FwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
-  if (s.D == 128) return launch_fwd_d<128>(s, a, ctx, st);
-  if (s.D == 64) return launch_fwd_d<64>(s, a, ctx, st);
+  const bool mask = a.mask.bits != nullptr;
+  if (s.D == 128) return mask ? launch_fwd_d<128, true>(s, a, ctx, st) : launch_fwd_d<128, false>(s, a, ctx, st);
+  if (s.D == 64) return mask ? launch_fwd_d<64, true>(s, a, ctx, st) : launch_fwd_d<64, false>(s, a, ctx, st);
   return cudaErrorInvalidValue;
 }
 

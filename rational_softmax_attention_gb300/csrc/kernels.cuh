@@ -12,6 +12,20 @@ cudaError_t launch_ra_softmax_fwd_bf16(const void* x, void* y, int64_t rows, int
 cudaError_t launch_ra_softmax_bwd_f32(const float* x, const float* p, const float* dy, float* dx, int64_t rows,
                                       int64_t cols, cudaStream_t st);
 
+// Boolean attention mask, bit-packed: bit (c % 32) of word c / 32 of a row is set when that
+// column may be attended.  Rows of `words` uint32 (a multiple of 4: whole 128-column tiles,
+// 16-byte aligned), one [rows x words] matrix per mask head g = (mb > 1 ? b : 0) * mh +
+// (mh > 1 ? h : 0), so a mask can be shared across the batch and/or the heads.
+struct MaskBits {
+  const uint32_t* bits;   // null: no mask
+  int words;
+  int mb, mh;
+};
+// Packs a [G, NQ, NK] byte mask (nonzero = may attend) into bits_q [G, NQ, wq] (rows = queries)
+// and bits_k [G, NK, wk] (rows = keys); either may be null (mask.cu).
+cudaError_t launch_mask_pack(const uint8_t* mask, int G, int NQ, int NK, uint32_t* bits_q, int wq, uint32_t* bits_k,
+                             int wk, cudaStream_t st);
+
 // Problem description shared by the attention launchers.
 struct AttnShape {
   int B, H, NQ, NK, D;
@@ -46,6 +60,7 @@ struct FwdTcArgs {
   int32_t* row_arg;
   unsigned long long* tile_counts;   // may be null
   int out_bf16;
+  MaskBits mask;   // rows = queries
 };
 cudaError_t launch_attn_fwd_tc(const AttnShape& s, const FwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st);
 
@@ -75,6 +90,8 @@ struct BwdTcArgs {
   //   1 / row_s_i, D_i / 4 (D_i = dO_i . O_i), R_i = sum_j E_ij (argmax excluded), and
   //   the argmax index a_i (int32 bits); rows past N_Q hold 2, 0, 0, 0, -1.
   float* ws_consts;
+  MaskBits mask_q;   // rows = queries (dQ kernel)
+  MaskBits mask_k;   // the same mask transposed, rows = keys (dK/dV kernel)
 };
 constexpr int kConstBlockFloats = 5 * 128;
 cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st);

@@ -1,0 +1,72 @@
+// Bit-packing of a boolean attention mask for the tensor-core attention kernels.
+//
+// Page "Ra-Family: Rational Neural Architecture", section 3, ra_attention: a drop-in for
+// scaled_dot_product_attention, whose boolean attn_mask marks with True the (query, key)
+// pairs that take part.  The kernels read the mask one 32-column word per row and tile
+// chunk: bits_q with a row per query (forward, dQ kernel) and bits_k with a row per key
+// (dK/dV kernel, whose threads own key rows).
+#include "kernels.cuh"
+
+namespace raattn {
+namespace {
+
+constexpr int WARPS = 8;
+
+// One warp per (mask head, query row, word): lane l reads column 32 w + l, the ballot is the word.
+__global__ void __launch_bounds__(32 * WARPS) mask_pack_rows_kernel(const uint8_t* mask, int NQ, int NK,
+                                                                    uint32_t* bits, int words, long long total) {
+  const long long wid = static_cast<long long>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= total) return;   // uniform across the warp
+  const int w = static_cast<int>(wid % words);
+  const long long row = wid / words;   // g * NQ + i
+  const int c = 32 * w + lane;
+  const bool on = c < NK && mask[row * NK + c] != 0;
+  const uint32_t word = __ballot_sync(0xffffffffu, on);
+  if (lane == 0) bits[row * words + w] = word;
+}
+
+// One warp per (mask head, query word w, block of 32 keys): lane l builds the word of key
+// j0 + l from rows 32 w .. 32 w + 31, reading 32 consecutive bytes of each row.
+__global__ void __launch_bounds__(32 * WARPS) mask_pack_cols_kernel(const uint8_t* mask, int NQ, int NK,
+                                                                    uint32_t* bits, int words, int kblocks,
+                                                                    long long total) {
+  const long long wid = static_cast<long long>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= total) return;
+  const int kb = static_cast<int>(wid % kblocks);
+  const long long rest = wid / kblocks;
+  const int w = static_cast<int>(rest % words);
+  const long long g = rest / words;
+  const int j = 32 * kb + lane;
+  uint32_t word = 0;
+  for (int r = 0; r < 32; ++r) {
+    const int i = 32 * w + r;
+    if (i < NQ && j < NK && mask[(g * NQ + i) * NK + j] != 0) word |= 1u << r;
+  }
+  if (j < NK) bits[(g * NK + j) * words + w] = word;
+}
+
+}  // namespace
+
+cudaError_t launch_mask_pack(const uint8_t* mask, int G, int NQ, int NK, uint32_t* bits_q, int wq, uint32_t* bits_k,
+                             int wk, cudaStream_t st) {
+  if (bits_q) {
+    const long long total = static_cast<long long>(G) * NQ * wq;
+    const unsigned grid = static_cast<unsigned>((total + WARPS - 1) / WARPS);
+    mask_pack_rows_kernel<<<grid, 32 * WARPS, 0, st>>>(mask, NQ, NK, bits_q, wq, total);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (bits_k) {
+    const int kblocks = (NK + 31) / 32;
+    const long long total = static_cast<long long>(G) * wk * kblocks;
+    const unsigned grid = static_cast<unsigned>((total + WARPS - 1) / WARPS);
+    mask_pack_cols_kernel<<<grid, 32 * WARPS, 0, st>>>(mask, NQ, NK, bits_k, wk, kblocks, total);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace raattn

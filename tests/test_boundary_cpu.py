@@ -118,3 +118,31 @@ def test_product_package_never_imports_the_oracle():
                 with open(os.path.join(root, f)) as fh:
                     text = fh.read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def _fwd_masked(lib, mask=FAKE, MB=1, MH=1, B=2, H=2, in_dt=1):
+    return lib.ra_attention_fwd_masked(FAKE, FAKE, FAKE, FAKE, NULL, NULL, NULL, NULL, FAKE, B, H, 8, 8, 64, 0.0, 0,
+                                       in_dt, 0, mask, MB, MH, S)
+
+
+def test_attention_mask_validation(lib):
+    # one 32-bit word per 32 columns, rounded up to whole 128-column tiles
+    assert [lib.ra_attention_mask_words(n) for n in (0, 1, 128, 129, 8192)] == [0, 4, 4, 8, 256]
+    assert _fwd_masked(lib, mask=NULL) == 1
+    assert _fwd_masked(lib, mask=MISALIGNED) == 1
+    assert _fwd_masked(lib, MB=3) == 1                                # MB must be 1 or B
+    assert _fwd_masked(lib, MH=0) == 1
+    assert _fwd_masked(lib, in_dt=0) == 2                             # masks on the bf16 path only
+    bwd = [FAKE] * 12 + [2, 2, 8, 8, 64, 0.0, 0, 1, 0, 0]
+    assert lib.ra_attention_bwd_masked(*bwd, FAKE, NULL, 1, 1, S) == 1  # the key-major copy is required
+    assert lib.ra_attention_bwd_masked(*bwd, FAKE, FAKE, 1, 3, S) == 1
+    assert lib.ra_attention_mask_pack(NULL, 1, 8, 8, FAKE, FAKE, S) == 1
+    assert lib.ra_attention_mask_pack(FAKE, 1, 8, 8, NULL, NULL, S) == 1
+    assert lib.ra_attention_mask_pack(FAKE, 0, 8, 8, FAKE, FAKE, S) == 1
+    assert lib.ra_attention_mask_pack(FAKE, 1, 8, 8, MISALIGNED, NULL, S) == 1
+
+
+def test_pack_attn_mask_rejects_bad_masks():
+    import torch
+    with pytest.raises(NotImplementedError):
+        ra.pack_attn_mask(torch.zeros(4, 4), 1, 1, 4, 4)              # additive float masks are not supported

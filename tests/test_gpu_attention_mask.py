@@ -1,0 +1,151 @@
+"""GPU parity of the masked attention (boolean attn_mask, bf16 tensor-core path) against the
+float64 oracle: packing bit-exact; forward and backward within the bf16 bounds of the other
+attention tests (max-abs 1e-2, mean-abs 1e-3, fp32 outputs and gradients), with the same
+near-tie rule for the argmax."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+import rational_softmax_attention_gb300 as ra
+from rational_softmax_attention_gb300.inputs import attention_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _np_pack(mask, words):
+    """[G, R, C] bool -> [G, R, words] uint32, bit c % 32 of word c // 32."""
+    G, R, C = mask.shape
+    out = np.zeros((G, R, words), dtype=np.uint32)
+    for c in range(C):
+        out[:, :, c // 32] |= mask[:, :, c].astype(np.uint32) << np.uint32(c % 32)
+    return out
+
+
+@pytest.mark.parametrize("G,nq,nk", [(1, 5, 7), (2, 130, 300), (3, 256, 128)])
+def test_mask_packing_is_bit_exact(G, nq, nk):
+    rng = np.random.default_rng(G * 1000 + nq + nk)
+    mask = rng.random((G, nq, nk)) < 0.4
+    # a [G, N_Q, N_K] mask broadcasts as one mask per head of a single batch
+    mq, mk, MB, MH = ra.pack_attn_mask(torch.from_numpy(mask).cuda(), 1, G, nq, nk)
+    torch.cuda.synchronize()
+    wq, wk = ra.lib().ra_attention_mask_words(nk), ra.lib().ra_attention_mask_words(nq)
+    np.testing.assert_array_equal(mq.cpu().numpy().view(np.uint32), _np_pack(mask, wq))
+    np.testing.assert_array_equal(mk.cpu().numpy().view(np.uint32), _np_pack(mask.transpose(0, 2, 1), wk))
+    assert (MB, MH) == (1, G)
+
+
+def _full_mask(mask, B, H):
+    m = np.asarray(mask, dtype=bool)
+    while m.ndim < 4:
+        m = m[None]
+    return np.broadcast_to(m, (B, H) + m.shape[2:])
+
+
+def _check(q, k, v, do, scale, causal, mask, heads=None):
+    """Masked GPU forward + backward against the oracle on the given heads."""
+    qg, kg, vg, dog = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    B, H, nq, _ = q.shape
+    nk = k.shape[2]
+    pm = ra.pack_attn_mask(torch.from_numpy(np.ascontiguousarray(mask)).cuda(), B, H, nq, nk)
+    o, rm, rs, ra_, _ = ra.ra_attention_forward(qg, kg, vg, scale=scale, causal=causal, out_dtype=torch.float32,
+                                                mask=pm)
+    dq, dk, dv = ra.ra_attention_backward(qg, kg, vg, o, dog, rm, rs, ra_, scale=scale, causal=causal,
+                                          grad_dtype=torch.float32, mask=pm)
+    torch.cuda.synchronize()
+    assert ra.device_status() == "RA_OK"
+    full = _full_mask(mask, B, H)
+    for b, h in heads or [(b, h) for b in range(B) for h in range(H)]:
+        qd, kd, vd, dod = (t[b, h].double().numpy() for t in (q, k, v, do))
+        allowed = full[b, h] & (np.tril(np.ones((nq, nk), dtype=bool)) if causal else True)
+        S = np.where(allowed, scale * (qd @ kd.T), -np.inf)
+        a_or = np.where(allowed.any(axis=1), np.argmax(S, axis=1), -1)
+        a_gpu = ra_[b, h].cpu().numpy().astype(np.int64)
+        for i in np.nonzero(a_gpu != a_or)[0]:
+            assert a_or[i] >= 0 and a_gpu[i] >= 0, f"row {i}: argmax {a_gpu[i]} vs {a_or[i]}"
+            m = S[i, a_or[i]]
+            assert S[i, a_gpu[i]] >= m - 1e-3 * max(1.0, abs(m)), f"row {i}: argmax differs beyond a near-tie"
+        wo, wm, ws, wa = oracle.ra_attention_head_fwd(qd, kd, vd, scale, causal, mask=full[b, h])
+        parity.assert_close_bf16(parity.f64(o[b, h]), wo, f"O[{b},{h}]")
+        np.testing.assert_array_equal(rs[b, h].cpu().numpy() == 0, ws == 0)   # empty rows agree
+        gq, gk, gv = oracle.ra_attention_head_bwd(qd, kd, vd, dod, scale, causal, argmax=a_gpu, mask=full[b, h])
+        parity.assert_close_bf16(parity.f64(dq[b, h]), gq, f"dq[{b},{h}]")
+        parity.assert_close_bf16(parity.f64(dk[b, h]), gk, f"dk[{b},{h}]")
+        parity.assert_close_bf16(parity.f64(dv[b, h]), gv, f"dv[{b},{h}]")
+    return o, rs, ra_, dq, dk, dv
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("nq,nk", [(128, 128), (200, 300), (300, 129)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("layout", ["shared", "per_batch", "per_head", "full"])
+def test_masked_attention_matches_oracle(D, nq, nk, causal, layout):
+    B, H = 2, 2
+    q, k, v, do = attention_inputs(B, H, nq, nk, D, seed=nq + 3 * nk + D, sigma_qk=1.0, dtype=torch.bfloat16)
+    rng = np.random.default_rng(nq * nk + D + int(causal))
+    shape = {"shared": (nq, nk), "per_batch": (B, 1, nq, nk), "per_head": (1, H, nq, nk), "full": (B, H, nq, nk)}
+    mask = rng.random(shape[layout]) < 0.5
+    mask[..., 0] = True   # keep one key per row except where a test removes all
+    _check(q, k, v, do, D ** -0.5, causal, mask)
+
+
+def test_all_true_mask_equals_unmasked():
+    q, k, v, _ = attention_inputs(1, 2, 257, 300, 128, seed=5, dtype=torch.bfloat16)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    pm = ra.pack_attn_mask(torch.ones(257, 300, dtype=torch.bool, device="cuda"), 1, 2, 257, 300)
+    a = ra.ra_attention_forward(qg, kg, vg, causal=True, out_dtype=torch.float32, mask=pm)
+    b = ra.ra_attention_forward(qg, kg, vg, causal=True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for x, y in zip(a[:4], b[:4]):
+        assert torch.equal(x, y)
+
+
+def test_fully_masked_rows_give_zeros():
+    B, H, nq, nk = 1, 2, 160, 200
+    q, k, v, do = attention_inputs(B, H, nq, nk, 64, seed=6, dtype=torch.bfloat16)
+    rng = np.random.default_rng(6)
+    mask = rng.random((nq, nk)) < 0.5
+    mask[:, 0] = True
+    empty = [0, 37, 128, 159]
+    mask[empty] = False
+    o, rs, ra_, dq, dk, dv = _check(q, k, v, do, 0.125, False, mask)
+    assert torch.all(o[:, :, empty] == 0) and torch.all(rs[:, :, empty] == 0) and torch.all(ra_[:, :, empty] == -1)
+    assert torch.all(dq[:, :, empty] == 0)
+
+
+def test_key_padding_mask_skips_dead_tiles():
+    """Keys past each batch's length are masked out: whole key tiles are dead, so their
+    P V products are skipped and counted."""
+    B, H, n = 2, 2, 640
+    q, k, v, do = attention_inputs(B, H, n, n, 128, seed=7, dtype=torch.bfloat16)
+    lengths = [200, 640]
+    mask = np.zeros((B, 1, n, n), dtype=bool)
+    for b, L in enumerate(lengths):
+        mask[b, 0, :, :L] = True
+    _check(q, k, v, do, 128 ** -0.5, False, mask, heads=[(0, 0), (1, 1)])
+    pm = ra.pack_attn_mask(torch.from_numpy(mask).cuda(), B, H, n, n)
+    _, _, _, _, counts = ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), tile_counts=True, mask=pm)
+    torch.cuda.synchronize()
+    visited, skipped = (int(c) for c in counts.tolist())
+    # batch 0 (both heads): key tiles 2..4 of every query tile lie past length 200
+    assert visited == B * H * 5 * 5 and skipped == H * 5 * 3
+
+
+def test_autograd_with_attn_mask():
+    q, k, v, do = attention_inputs(1, 2, 96, 96, 64, seed=8, dtype=torch.bfloat16)
+    mask = torch.rand(96, 96, generator=torch.Generator().manual_seed(8)) < 0.6
+    mask[:, 0] = True
+    qg, kg, vg = (t.cuda().requires_grad_(True) for t in (q, k, v))
+    out = ra.ra_attention(qg, kg, vg, attn_mask=mask.cuda(), is_causal=True)
+    out.float().backward(do.cuda().float())
+    torch.cuda.synchronize()
+    for b in range(1):
+        for h in range(2):
+            qd, kd, vd, dod = (t[b, h].double().numpy() for t in (q, k, v, do))
+            wo, *_ = oracle.ra_attention_head_fwd(qd, kd, vd, 0.125, True, mask=mask.numpy())
+            gq, gk, gv = oracle.ra_attention_head_bwd(qd, kd, vd, dod, 0.125, True, mask=mask.numpy())
+            # bf16 outputs and gradients: the fp32 bounds plus half a bf16 ulp of each value
+            for name, got, want in (("O", out, wo), ("dq", qg.grad, gq), ("dk", kg.grad, gk), ("dv", vg.grad, gv)):
+                g = parity.f64(got[b, h])
+                assert np.all(np.abs(g - want) <= 1e-2 + 2.0 ** -8 * np.abs(want)), name

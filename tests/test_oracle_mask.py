@@ -88,3 +88,26 @@ def test_masked_backward_matches_finite_differences(causal):
             mnus[i][idx] -= eps
             num[idx] = (f(*p) - f(*mnus)) / (2 * eps)
         np.testing.assert_allclose(g, num, rtol=1e-5, atol=1e-7, err_msg=f"argument {i}")
+
+
+def test_key_padding_mask_equals_deleting_the_keys():
+    """A mask that removes the same keys from every row is the unmasked attention over the
+    remaining keys: same output; zero dk, dv for the removed keys and the unmasked
+    gradients for the others."""
+    rng = np.random.default_rng(6)
+    q, k, v = _qkv(rng, 1, 2, 6, 9, 4)
+    keep = np.array([0, 2, 3, 5, 8])
+    mask = np.zeros((6, 9), dtype=bool)
+    mask[:, keep] = True
+    O, m, s, _ = oracle.ra_attention_fwd(q, k, v, mask=mask)
+    O2, m2, s2, _ = oracle.ra_attention_fwd(q, k[:, :, keep], v[:, :, keep])
+    np.testing.assert_allclose(O, O2, rtol=0, atol=1e-14)
+    np.testing.assert_array_equal(m, m2)
+    do = rng.normal(size=q.shape)
+    dq, dk, dv = oracle.ra_attention_bwd(q, k, v, do, mask=mask)
+    dq2, dk2, dv2 = oracle.ra_attention_bwd(q, k[:, :, keep], v[:, :, keep], do)
+    np.testing.assert_allclose(dq, dq2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk[:, :, keep], dk2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv[:, :, keep], dv2, rtol=0, atol=1e-13)
+    gone = np.setdiff1d(np.arange(9), keep)
+    assert np.all(dk[:, :, gone] == 0) and np.all(dv[:, :, gone] == 0)
