@@ -204,6 +204,15 @@ void ra_set_wait_limit_ns(uint64_t limit_ns);
  */
 void ra_debug_force_timeout(int on);
 
+/*
+ * ra_debug_fwd_pair -- how later bf16 forward calls with D = 128 are laid out:
+ * 0 (default) as CTA pairs (clusters of two CTAs whose tensor-core products span both
+ * SMs) when N_Q > 256, otherwise one CTA per pair of query tiles; 1 always single CTAs;
+ * 2 always pairs.  Results agree to rounding either way; the knob exists to test and
+ * time both layouts.
+ */
+void ra_debug_fwd_pair(int mode);
+
 /* Size of the device array behind ra_attention_bwd_noalloc (32 MiB). */
 #define RA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

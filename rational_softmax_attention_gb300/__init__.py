@@ -61,6 +61,7 @@ _SIGNATURES = {
     "ra_device_status": ([_vp], _i32),
     "ra_set_wait_limit_ns": ([_u64], None),
     "ra_debug_force_timeout": ([_i32], None),
+    "ra_debug_fwd_pair": ([_i32], None),
 }
 
 
@@ -314,3 +315,9 @@ def set_wait_limit_ns(ns):
 def debug_force_timeout(on):
     """Test knob: make later tensor-core launches take their timeout and wind-down path."""
     lib().ra_debug_force_timeout(1 if on else 0)
+
+
+def debug_fwd_pair(mode):
+    """Layout of later bf16 D = 128 forward calls: 0 automatic (CTA pairs when N_Q > 256),
+    1 single CTAs, 2 CTA pairs."""
+    lib().ra_debug_fwd_pair(int(mode))

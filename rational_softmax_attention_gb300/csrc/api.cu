@@ -20,6 +20,7 @@ unsigned int* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_force_timeout{0};
+std::atomic<int> g_fwd_pair{0};
 
 ra_status_t status_ptr_for_current_device(unsigned int** out) {
   int dev = 0;
@@ -68,13 +69,14 @@ EncodeTiledFn get_encode_fn() {
 
 // 3-D map over a [BH, N, D] 16-bit tensor: box {64, 128, 1}, 128-byte swizzle, zero fill
 // out of bounds (rows past N of a head read as zeros, never the next head's rows).
-bool make_map_16bit(CUtensorMap* map, const void* base, int BH, int N, int D, CUtensorMapDataType type) {
+bool make_map_16bit(CUtensorMap* map, const void* base, int BH, int N, int D, CUtensorMapDataType type,
+                    cuuint32_t box_rows = 128) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -136,6 +138,8 @@ void ra_set_wait_limit_ns(uint64_t limit_ns) {
 }
 
 void ra_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
+
+void ra_debug_fwd_pair(int mode) { g_fwd_pair.store(mode == 1 || mode == 2 ? mode : 0); }
 
 ra_status_t ra_device_status(void* stream) {
   unsigned int* p = nullptr;
@@ -227,8 +231,11 @@ ra_status_t attn_fwd_impl(const void* q, const void* k, const void* v, void* o, 
   FwdTcArgs a;
   const int BH = B * H;
   if (!make_map_bf16(&a.tm_q, q, BH, N_Q, D) || !make_map_bf16(&a.tm_k, k, BH, N_K, D) ||
+      !make_map_16bit(&a.tm_k64, k, BH, N_K, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64) ||
       !make_map_16bit(&a.tm_v, workspace, BH, N_K, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return RA_ERR_LAUNCH;
+  const int pair_mode = g_fwd_pair.load();
+  a.pair = D == 128 && (pair_mode == 2 || (pair_mode == 0 && N_Q > 256)) ? 1 : 0;
   ConvertJob job;
   job.src[0] = static_cast<const uint4*>(v);
   job.dst[0] = static_cast<uint4*>(workspace);

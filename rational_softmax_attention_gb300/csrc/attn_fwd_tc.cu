@@ -63,23 +63,32 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S = 0;     // S of query tile g at column 128 g
 constexpr uint32_t TMEM_O = 256;   // O of query tile g at column 256 + 128 g
 constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 16-bit values (128 B per row)
+constexpr int HALF_BOX_BYTES = 64 * 64 * 2;   // 64 rows x 64 values: a pair CTA's share of a K box
 
-template <int D>
+// PAIR: the kernel runs as a cluster of two CTAs on the two SMs of a TPC.  Each product
+// is one M = 256 tcgen05.mma (cta_group::2) issued by the even CTA: query rows 0..127 of
+// it are the even CTA's tile g, rows 128..255 the odd CTA's, and each CTA holds only half
+// of every K tile (64 keys) and of every V tile (64 of the D columns).  Per SM that halves
+// the K/V copies and the shared-memory reads of the B operands, the limit of the
+// single-CTA form.
+template <int D, bool PAIR>
 struct FwdCfg {
+  static constexpr int NCTA = PAIR ? 2 : 1;
   static constexpr int TILE_BYTES = BN * D * 2;   // a Q, K or V tile: D/64 boxes
+  static constexpr int STAGE_BYTES = TILE_BYTES / NCTA;   // this CTA's part of a K or V tile
   // Ring depth: K/V tiles in flight; each stage serves two products (S_A and S_B, or
   // O_A and O_B).
-  static constexpr int NSTAGE = (D == 128) ? 3 : 6;
+  static constexpr int NSTAGE = NCTA * ((D == 128) ? 3 : 6);
   static constexpr int P_BYTES = BM * BN * 2;     // P tile: two 64-key halves of 16 KB
   static constexpr int OFF_Q = 0;                 // Q_A, Q_B
   static constexpr int OFF_RING = OFF_Q + NGROUP * TILE_BYTES;
-  static constexpr int OFF_P = OFF_RING + NSTAGE * TILE_BYTES;   // P_A, P_B
+  static constexpr int OFF_P = OFF_RING + NSTAGE * STAGE_BYTES;   // P_A, P_B
   static constexpr int OFF_BAR = OFF_P + NGROUP * P_BYTES;
   // q_full, ring_full[NSTAGE], ring_empty[NSTAGE], s_full[2][2], s_empty[2][2], p_full[2], p_empty[2],
   // o_full[2], drain[2]
   static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 * NGROUP;
-  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int MISC_BYTES = 16 + SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes
+  static constexpr int OFF_MISC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;
+  static constexpr int MISC_BYTES = 16 + SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes (16-byte aligned)
   static constexpr int USED = OFF_MISC + MISC_BYTES;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
   // 1024-byte aligned dynamic shared-memory base
@@ -169,12 +178,17 @@ __device__ __forceinline__ int find_in_chunk(const uint32_t (&v)[32], float m, i
   return idx;
 }
 
-// MASK: a boolean attention mask (args.mask) applies on top of `causal`.
-template <int D, bool MASK>
+// MASK: a boolean attention mask (args.mask) applies on top of `causal`.  PAIR: the CTA
+// pair form (FwdCfg).
+template <int D, bool MASK, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_tc_kernel(const AttnShape s, const __grid_constant__ FwdTcArgs args, const LaunchCtx ctx) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, PAIR>;
   constexpr int NST = C::NSTAGE;
+  constexpr int NCTA = C::NCTA;
+  // a pair CTA holds V columns rank * 64 .. + 63: one 128-byte swizzle atom; and no early
+  // return may leave the other CTA of the pair waiting
+  static_assert(!PAIR || (D == 128 && C::SLACK != 0), "CTA pair form: D = 128 with alignment slack");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t mis = smem_u32(smem_raw) & 1023u;
   if (C::SLACK == 0 && mis != 0) {   // uniform across the CTA: nothing launched yet
@@ -197,13 +211,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = o_full + NGROUP;     // [NGROUP]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);   // [NGROUP][GROUP_WARPS]
+  // [NGROUP][GROUP_WARPS] votes of this CTA's softmax warps: whether the last P tile has a
+  // nonzero entry, tagged with its key tile (2 j + live)
+  volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // CTA of the pair; 0 issues the products
   const int nqt = (s.NQ + BM - 1) / BM;
-  const int nct = (nqt + NGROUP - 1) / NGROUP;   // CTAs per (batch, head)
-  const int item = blockIdx.x;
+  const int nct = (nqt + NCTA * NGROUP - 1) / (NCTA * NGROUP);   // work items (CTAs or pairs) per (batch, head)
+  const int item = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   // Head-major order: the ~150 resident CTAs share a few heads, so each head's K and V
   // stay in L2 across its query tiles.  Causal: CTA lengths differ, so heads are taken in
   // groups of CAUSAL_HEADS and within a group the longest CTAs of all its heads go first;
@@ -221,12 +238,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     bh = item / nct;
     ct = item % nct;
   }
-  const int q0 = ct * (NGROUP * BM);
-  // last key any row of the CTA may see, and per query tile
+  const int q0 = ct * (NCTA * NGROUP * BM);
+  // first row of query tile g of CTA r: product g spans rows q0 + NCTA BM g .. + NCTA BM - 1,
+  // the even CTA's tile first
+  auto tile_row0 = [&](int g, int r) { return q0 + (g * NCTA + r) * BM; };
+  // last key any row of the CTA (pair) may see, and per query tile
   auto last_key_of = [&](int rows_end) {   // rows_end: one past the last row of the range
     return s.causal ? min(s.NK - 1, min(s.NQ - 1, rows_end - 1)) : s.NK - 1;
   };
-  const int nkt = last_key_of(q0 + NGROUP * BM) / BN + 1;
+  const int nkt = last_key_of(q0 + NCTA * NGROUP * BM) / BN + 1;
+  // Barrier operations of the pair form: arrivals go to the even CTA's barrier, products and
+  // commits span both CTAs.  Arrivals release, and waits acquire, at CTA scope: what they
+  // order is this SM's own shared and tensor memory (a P tile, the scores a warp has read)
+  // against the pair's tensor-core work, not data that the other CTA's threads read.  A
+  // cluster-scope release costs about a thousand cycles per arrival (measured), on the
+  // critical path of every key tile.  The one value read across the pair by threads, the
+  // odd CTA's live votes, is tagged with its key tile and read after the p_full wait, so a
+  // vote that is not yet visible only makes the product run.
+  auto wait_bar = [&](uint64_t* bar, uint32_t par) { return mbar_wait(bar, par, abort_flag, ctx); };
+  auto arrive_even = [&](uint64_t* bar) {
+    if constexpr (PAIR) mbar_arrive_remote(mapa_shared(smem_u32(bar), 0));
+    else mbar_arrive(bar);
+  };
+  auto commit = [&](uint64_t* bar) {
+    if constexpr (PAIR) tc_commit_pair(bar);
+    else tc_commit(bar);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -237,36 +274,51 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int g = 0; g < NGROUP; ++g) {
       for (int b = 0; b < 2; ++b) {
         mbar_init(&s_full[2 * g + b], 1);
-        mbar_init(&s_empty[2 * g + b], GROUP_WARPS);   // one arrival per warp of the group
+        mbar_init(&s_empty[2 * g + b], NCTA * GROUP_WARPS);   // one arrival per warp of the group(s)
       }
-      mbar_init(&p_full[g], GROUP_WARPS);
+      mbar_init(&p_full[g], NCTA * GROUP_WARPS);
       mbar_init(&p_empty[g], 1);
       mbar_init(&o_full[g], 1);
       mbar_init(&drain[g], 1);
     }
     *abort_flag = 0;
+    for (int i = 0; i < SOFTMAX_WARPS; ++i) live[i] = -1;   // no key tile's tag
     fence_mbarrier_init();
   }
   if (warp == MMA_WARP) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {   // one warp in each CTA: the same columns in both
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const CUtensorMap* tm_k = PAIR ? &args.tm_k64 : &args.tm_k;   // a pair CTA loads 64 keys per tile
       tma_prefetch_desc(&args.tm_q);
-      tma_prefetch_desc(&args.tm_k);
+      tma_prefetch_desc(tm_k);
       tma_prefetch_desc(&args.tm_v);
-      mbar_arrive_expect_tx(q_full, NGROUP * C::TILE_BYTES);
+      // copies into this CTA's shared memory complete on the even CTA's barriers, which
+      // count both CTAs' bytes
+      const bool arms = rank == 0;
+      auto load = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+        if constexpr (PAIR) tma_load_3d_pair(dst, map, mapa_shared(smem_u32(bar), 0), c0, c1, bh);
+        else tma_load_3d(dst, map, bar, c0, c1, bh);
+      };
+      if (arms) mbar_arrive_expect_tx(q_full, NCTA * NGROUP * C::TILE_BYTES);
       for (int g = 0; g < NGROUP; ++g)
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sQ + g * C::TILE_BYTES + c * BOX_BYTES, &args.tm_q, q_full, c * 64, q0 + g * BM, bh);
+          load(sQ + g * C::TILE_BYTES + c * BOX_BYTES, &args.tm_q, q_full, c * 64, tile_row0(g, rank));
       uint32_t it = 0;
       uint32_t last_par[NST];
       bool issued[NST];
@@ -275,40 +327,57 @@ __global__ void __launch_bounds__(THREADS, 1)
         issued[i] = false;
         last_par[i] = 0;
       }
-      auto issue = [&](const CUtensorMap* map, int j) -> bool {
+      auto issue = [&](bool is_v, int j) -> bool {
         const int st = it % NST;
         const uint32_t par = (it / NST) & 1u;
-        if (!mbar_wait(&ring_empty[st], par ^ 1u, abort_flag, ctx)) return false;
-        mbar_arrive_expect_tx(&ring_full[st], C::TILE_BYTES);
+        if (!wait_bar(&ring_empty[st], par ^ 1u)) return false;
+        if (arms) mbar_arrive_expect_tx(&ring_full[st], NCTA * C::STAGE_BYTES);
+        uint8_t* dst = sRing + st * C::STAGE_BYTES;
+        if (PAIR && is_v) {
+          load(dst, &args.tm_v, &ring_full[st], static_cast<int>(rank) * 64, j * BN);   // 64 columns, 128 keys
+        } else {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sRing + st * C::TILE_BYTES + c * BOX_BYTES, map, &ring_full[st], c * 64, j * BN, bh);
+          for (int c = 0; c < D / 64; ++c)
+            load(dst + c * (PAIR ? HALF_BOX_BYTES : BOX_BYTES), is_v ? &args.tm_v : tm_k, &ring_full[st], c * 64,
+                 j * BN + static_cast<int>(rank) * (BN / NCTA));
+        }
         issued[st] = true;
         last_par[st] = par;
         ++it;
         return true;
       };
       bool ok = true;
-      for (int j = 0; j < nkt && ok; ++j) ok = issue(&args.tm_k, j);         // pass 1: K_0 .. K_{n-1}
-      if (ok) ok = issue(&args.tm_k, 0);                                     // pass 2: K_0, then
+      for (int j = 0; j < nkt && ok; ++j) ok = issue(false, j);              // pass 1: K_0 .. K_{n-1}
+      if (ok) ok = issue(false, 0);                                          // pass 2: K_0, then
       for (int j = 1; j < nkt && ok; ++j) {                                  //   K_j, V_{j-1}
-        ok = issue(&args.tm_k, j);
-        if (ok) ok = issue(&args.tm_v, j - 1);
+        ok = issue(false, j);
+        if (ok) ok = issue(true, j - 1);
       }
-      if (ok) ok = issue(&args.tm_v, nkt - 1);                               //   V_{n-1}
-      drain_wait(q_full, 0, ctx);
-      for (int i = 0; i < NST; ++i)
-        if (issued[i]) drain_wait(&ring_full[i], last_par[i], ctx);
+      if (ok) ok = issue(true, nkt - 1);                                     //   V_{n-1}
+      // the barriers that count this CTA's copies are the even CTA's: it drains them for
+      // both, and the pair's closing cluster barrier keeps the odd CTA alive until then
+      if (arms) {
+        drain_wait(q_full, 0, ctx);
+        for (int i = 0; i < NST; ++i)
+          if (issued[i]) drain_wait(&ring_full[i], last_par[i], ctx);
+      }
     }
   } else if (warp >= MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuers
     // One thread per query tile g issues S_g and O_g products and does its own waits:
     // a wait costs the issuing thread a few hundred cycles, and with two issuers the
-    // tensor core runs the other tile's queued products meanwhile.
+    // tensor core runs the other tile's queued products meanwhile.  In a pair only the
+    // even CTA issues; the odd CTA's issuer warps only hold its tensor memory.
     const int g = warp - MMA_WARP;
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_fp16_f32(BM, D, 0, 1);   // P and V in fp16
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(NCTA * BM, BN, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_fp16_f32(NCTA * BM, D, 0, 1);   // P and V in fp16
+      // bytes per 64-column atom of this CTA's K rows (128 keys, or 64 in a pair)
+      constexpr int KATOM = PAIR ? HALF_BOX_BYTES : BOX_BYTES;
+      auto mma = [&](uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+        if constexpr (PAIR) tc_mma_f16_pair(d, a_desc, b_desc, idesc, acc);
+        else tc_mma_f16(d, a_desc, b_desc, idesc, acc);
+      };
       const uint32_t sRa = smem_u32(sRing);
       // descriptors as (low word + offset / 16, constant high word): one add per operand
       constexpr uint32_t HI = sdesc_hi_sw128(1024);
@@ -316,47 +385,65 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t plo = sdesc_lo(smem_u32(sP) + g * C::P_BYTES, 16);
       const uint32_t scol = tmem + TMEM_S + g * 128;
       const uint32_t ocol = tmem + TMEM_O + g * 128;
-      // key tiles this query tile can see (0 for a tile wholly past N_Q): only those
-      // count as visited (query tile, key tile) pairs
-      const int nkt_g = (q0 + g * BM < s.NQ) ? last_key_of(q0 + (g + 1) * BM) / BN + 1 : 0;
+      // key tiles each query tile of product g can see (0 for a tile wholly past N_Q):
+      // only those count as visited (query tile, key tile) pairs
+      auto tile_keys = [&](int r) {
+        const int r0 = tile_row0(g, r);
+        return r0 < s.NQ ? last_key_of(r0 + BM) / BN + 1 : 0;
+      };
+      const int nkt_a = tile_keys(0);
+      const int nkt_b = PAIR ? tile_keys(1) : 0;
       uint32_t pos = 0;   // ring position (K and V tiles in producer order)
       uint32_t uc0 = 0, uc1 = 0;   // S products issued into score buffer 0 and 1
       unsigned long long visited = 0, skipped = 0;
       bool o_started = false;
       auto ring_wait = [&](uint32_t p, uint32_t& addr) -> bool {
         const int st = p % NST;
-        if (!mbar_wait(&ring_full[st], (p / NST) & 1u, abort_flag, ctx)) return false;
+        if (!wait_bar(&ring_full[st], (p / NST) & 1u)) return false;
         tc_fence_after();
-        addr = sRa + st * C::TILE_BYTES;
+        addr = sRa + st * C::STAGE_BYTES;
         return true;
       };
       // S_g = Q_g K^T into score buffer b (buffer 1 exists in pass 1 only: it is the O_g
       // region, free until the first O_g product of pass 2)
       auto mma_s = [&](uint32_t kaddr, int b) -> bool {
         const uint32_t use = b ? uc1 : uc0;
-        if (!mbar_wait(&s_empty[2 * g + b], (use & 1u) ^ 1u, abort_flag, ctx)) return false;
+        if (!wait_bar(&s_empty[2 * g + b], (use & 1u) ^ 1u)) return false;
         tc_fence_after();
         const uint32_t klo = sdesc_lo(kaddr, 16);
         const uint32_t dcol = scol + 256u * b;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
-          tc_mma_f16(dcol, sdesc(qlo + off, HI), sdesc(klo + off, HI), idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t qoff = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;
+          const uint32_t koff = ((kk >> 2) * KATOM + (kk & 3) * 32) >> 4;
+          mma(dcol, sdesc(qlo + qoff, HI), sdesc(klo + koff, HI), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[2 * g + b]);
+        commit(&s_full[2 * g + b]);
         if (b) ++uc1; else ++uc0;
         return true;
       };
       auto mma_pv = [&](int j, uint32_t vaddr) -> bool {   // O_g += P_g V_j
-        if (!mbar_wait(&p_full[g], j & 1u, abort_flag, ctx)) return false;
+        if (!wait_bar(&p_full[g], j & 1u)) return false;   // P tiles and votes of both CTAs
         tc_fence_after();
+        // votes of the warps of product g (the odd CTA's read from its shared memory), each
+        // tagged with its key tile: a vote that is not this tile's counts as live, so the
+        // product is skipped only when every vote is current and dead
+        int v[NCTA * GROUP_WARPS];
+#pragma unroll
+        for (int w = 0; w < GROUP_WARPS; ++w) v[w] = live[g * GROUP_WARPS + w];
+        if constexpr (PAIR) {
+          const uint4 o = ld_shared_cluster_v4(mapa_shared(smem_u32(const_cast<int*>(&live[g * GROUP_WARPS])), 1));
+          v[4] = static_cast<int>(o.x);
+          v[5] = static_cast<int>(o.y);
+          v[6] = static_cast<int>(o.z);
+          v[7] = static_cast<int>(o.w);
+        }
         int any = 0;
 #pragma unroll
-        for (int w = 0; w < GROUP_WARPS; ++w) any |= live[g * GROUP_WARPS + w];   // warps of tile g
-        if (j < nkt_g) {
-          ++visited;
-          if (any == 0) ++skipped;
-        }
+        for (int w = 0; w < NCTA * GROUP_WARPS; ++w) any |= (v[w] >> 1) != j || (v[w] & 1);
+        const int vis = (j < nkt_a ? 1 : 0) + (j < nkt_b ? 1 : 0);
+        visited += vis;
+        if (any == 0) skipped += vis;
         if (any != 0) {
           const uint32_t vlo = sdesc_lo(vaddr, BOX_BYTES);
           const uint32_t acc0 = o_started ? 1u : 0u;
@@ -364,28 +451,28 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint32_t aoff = ((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4;   // P: K-major, 16 keys = 32 B
             const uint32_t boff = (kk * 16 * 128) >> 4;                            // V: MN-major, 16 key rows
-            tc_mma_f16(ocol, sdesc(plo + aoff, HI), sdesc(vlo + boff, HI), idesc_pv, kk > 0 ? 1u : acc0);
+            mma(ocol, sdesc(plo + aoff, HI), sdesc(vlo + boff, HI), idesc_pv, kk > 0 ? 1u : acc0);
           }
           o_started = true;
         }
-        tc_commit(&p_empty[g]);
+        commit(&p_empty[g]);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, ctx);
+      bool ok = wait_bar(q_full, 0);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
-      if (ok && ctx.force_timeout) ok = mbar_wait(&drain[g], 0, abort_flag, ctx);
+      if (ok && ctx.force_timeout) ok = wait_bar(&drain[g], 0);
       uint32_t ka = 0, va = 0;
       // pass 1: S_g(j) for every key tile; a ring stage is free once both issuers commit
       for (int j = 0; j < nkt && ok; ++j) {
         ok = ring_wait(pos, ka);
         if (ok) ok = mma_s(ka, j & 1);
-        if (ok) tc_commit(&ring_empty[pos % NST]);
+        if (ok) commit(&ring_empty[pos % NST]);
         ++pos;
       }
       // pass 2: S_g(0); then per j: S_g(j+1), O_g(j)
       if (ok) ok = ring_wait(pos, ka);
       if (ok) ok = mma_s(ka, 0);
-      if (ok) tc_commit(&ring_empty[pos % NST]);
+      if (ok) commit(&ring_empty[pos % NST]);
       ++pos;
       for (int j = 0; j < nkt && ok; ++j) {
         const bool more = j + 1 < nkt;
@@ -394,15 +481,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           kpos = pos++;
           ok = ring_wait(kpos, ka);
           if (ok) ok = mma_s(ka, 0);
-          if (ok) tc_commit(&ring_empty[kpos % NST]);
+          if (ok) commit(&ring_empty[kpos % NST]);
         }
         const uint32_t vpos = pos++;
         if (ok) ok = ring_wait(vpos, va);
         if (ok) ok = mma_pv(j, va);
-        if (ok) tc_commit(&ring_empty[vpos % NST]);
+        if (ok) commit(&ring_empty[vpos % NST]);
       }
-      if (ok) tc_commit(&o_full[g]);
-      tc_commit(&drain[g]);
+      if (ok) commit(&o_full[g]);
+      commit(&drain[g]);
       drain_wait(&drain[g], 0, ctx);
       if (ok && args.tile_counts) {
         atomicAdd(&args.tile_counts[0], visited);
@@ -415,13 +502,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int g = warp / GROUP_WARPS;
     const int quarter = warp % GROUP_WARPS;
     const int row_local = quarter * 32 + lane;   // TMEM lane
-    const int row = q0 + g * BM + row_local;
+    const int row = tile_row0(g, static_cast<int>(rank)) + row_local;
     const int lim = s.causal ? min(row, s.NK - 1) : s.NK - 1;   // last key this row may see
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t scol = lane_addr + TMEM_S + g * 128;
     auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
       int r = 1;
-      if (lane == 0) r = mbar_wait(bar, par, abort_flag, ctx) ? 1 : 0;
+      if (lane == 0) r = wait_bar(bar, par) ? 1 : 0;
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
     // this row's attention-mask words: four per key tile (rows past N_Q read the last row)
@@ -452,7 +539,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[2 * g + b]);
+      if (lane == 0) arrive_even(&s_empty[2 * g + b]);
       return true;
     };
 #define SV(c) u2f(sv[(c) >> 5][(c) & 31])
@@ -539,7 +626,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[2 * g]);
+      if (lane == 0) arrive_even(&s_empty[2 * g]);
       if (arg_tile && (jm & 3) >= 2)
         a = col0 + 64 +
             ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 96, lim, mw[3])
@@ -555,9 +642,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();
       const float tsum = tsum2.x + tsum2.y;
       const unsigned any_live = __any_sync(0xffffffffu, tsum > 0.0f);
-      if (lane == 0) live[g * GROUP_WARPS + quarter] = any_live ? 1 : 0;
+      if (lane == 0) {
+        live[g * GROUP_WARPS + quarter] = 2 * j + (any_live ? 1 : 0);
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[g]);
+      if (lane == 0) arrive_even(&p_full[g]);
       rowsum += tsum;
     }
 #undef SV
@@ -570,7 +659,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // O rows leave through this query tile's P tile (free: o_full means the last P V
       // product has read it), 4 KB per warp, in whole row segments
       uint8_t* stage = sP + g * C::P_BYTES + quarter * 4096;
-      const int wrow0 = q0 + g * BM + quarter * 32;   // first row of this warp
+      const int wrow0 = tile_row0(g, static_cast<int>(rank)) + quarter * 32;   // first row of this warp
       const size_t row0 = static_cast<size_t>(bh) * s.NQ + wrow0;
       const int n_ok = max(0, min(32, s.NQ - wrow0));
 #pragma unroll
@@ -596,32 +685,59 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   __syncthreads();
+  // a pair's products read both CTAs' shared memory and write both tensor memories: neither
+  // CTA frees them before the even CTA has drained its products
+  if constexpr (PAIR) cluster_sync();
   if (warp == MMA_WARP) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, TMEM_COLS);
+    else tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool PAIR>
 cudaError_t launch_fwd_d(const AttnShape& s, const FwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
-  using C = FwdCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  using C = FwdCfg<D, PAIR>;
+  auto kernel = attn_fwd_tc_kernel<D, MASK, PAIR>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int nqt = (s.NQ + BM - 1) / BM;
-  const int nct = (nqt + NGROUP - 1) / NGROUP;
-  const unsigned grid = static_cast<unsigned>(nct) * static_cast<unsigned>(s.B * s.H);
-  attn_fwd_tc_kernel<D, MASK><<<grid, THREADS, C::SMEM_BYTES, st>>>(s, a, ctx);
-  return cudaGetLastError();
+  const int nct = (nqt + C::NCTA * NGROUP - 1) / (C::NCTA * NGROUP);
+  const unsigned grid = static_cast<unsigned>(nct) * static_cast<unsigned>(s.B * s.H) * C::NCTA;
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, s, a, ctx);
+  } else {
+    kernel<<<grid, THREADS, C::SMEM_BYTES, st>>>(s, a, ctx);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd_tc(const AttnShape& s, const FwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
   const bool mask = a.mask.bits != nullptr;
-  if (s.D == 128) return mask ? launch_fwd_d<128, true>(s, a, ctx, st) : launch_fwd_d<128, false>(s, a, ctx, st);
-  if (s.D == 64) return mask ? launch_fwd_d<64, true>(s, a, ctx, st) : launch_fwd_d<64, false>(s, a, ctx, st);
+  if (s.D == 128 && a.pair) {
+    return mask ? launch_fwd_d<128, true, true>(s, a, ctx, st) : launch_fwd_d<128, false, true>(s, a, ctx, st);
+  }
+  if (s.D == 128) {
+    return mask ? launch_fwd_d<128, true, false>(s, a, ctx, st) : launch_fwd_d<128, false, false>(s, a, ctx, st);
+  }
+  if (s.D == 64) {
+    return mask ? launch_fwd_d<64, true, false>(s, a, ctx, st) : launch_fwd_d<64, false, false>(s, a, ctx, st);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -54,6 +54,7 @@ cudaError_t launch_bf16_to_f16(const ConvertJob& job, unsigned int* status, cuda
 struct FwdTcArgs {
   CUtensorMap tm_q, tm_k;   // bf16 Q and K: 3-D maps {D, N, B*H}, box {64, 128, 1}, 128-byte swizzle
   CUtensorMap tm_v;         // fp16 copy of V (same geometry)
+  CUtensorMap tm_k64;       // K with 64-row boxes {64, 64, 1} (CTA pair form)
   void* o;
   float* row_m;
   float* row_s;
@@ -61,6 +62,7 @@ struct FwdTcArgs {
   unsigned long long* tile_counts;   // may be null
   int out_bf16;
   MaskBits mask;   // rows = queries
+  int pair;        // D = 128: run as CTA pairs (cta_group::2 products)
 };
 cudaError_t launch_attn_fwd_tc(const AttnShape& s, const FwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st);
 

@@ -186,3 +186,24 @@ def test_dead_tiles_are_skipped_and_counted():
     v = v.to(torch.bfloat16)
     o, rm, rs, ra_, counts = check_all(q, k, v, 1.0, False)
     assert int(counts[0]) == 4 * 4 and int(counts[1]) == 4 * 3
+
+
+@pytest.mark.parametrize("nq,nk,causal", [(128, 128, False), (300, 300, True), (513, 700, False), (1000, 1000, True),
+                                          (700, 513, True)])
+def test_cta_pair_and_single_cta_layouts_agree(nq, nk, causal):
+    """The D = 128 forward as clusters of two CTAs (products spanning both SMs) and as
+    single CTAs: both against the oracle, and against each other to fp32 rounding."""
+    q, k, v = attention_inputs(2, 2, nq, nk, 128, seed=nq + 7 * nk, sigma_qk=1.0, dtype=torch.bfloat16,
+                               with_dout=False)
+    outs = {}
+    try:
+        for mode in (1, 2):
+            ra.debug_fwd_pair(mode)
+            outs[mode] = check_all(q, k, v, 128 ** -0.5, causal)
+    finally:
+        ra.debug_fwd_pair(0)
+    single, pair = outs[1], outs[2]
+    assert torch.equal(single[3], pair[3])                     # argmax
+    for a, b in zip(single[:3], pair[:3]):                      # O, row max, row sum
+        np.testing.assert_allclose(a.cpu().numpy(), b.cpu().numpy(), rtol=1e-5, atol=1e-6)
+    assert torch.equal(single[4], pair[4])                     # visited / skipped tile pairs
