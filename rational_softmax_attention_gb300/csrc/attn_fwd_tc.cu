@@ -247,6 +247,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     return s.causal ? min(s.NK - 1, min(s.NQ - 1, rows_end - 1)) : s.NK - 1;
   };
   const int nkt = last_key_of(q0 + NCTA * NGROUP * BM) / BN + 1;
+  // key tiles product g needs (causal: fewer for g = 0, whose rows end earlier); the
+  // producer streams all nkt for the last product, and the other issuer releases the
+  // stages it does not use
+  auto group_keys = [&](int g) { return last_key_of(tile_row0(g, NCTA - 1) + BM) / BN + 1; };
   // Barrier operations of the pair form: arrivals go to the even CTA's barrier, products and
   // commits span both CTAs.  Arrivals release, and waits acquire, at CTA scope: what they
   // order is this SM's own shared and tensor memory (a P tile, the scores a warp has read)
@@ -462,10 +466,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
       if (ok && ctx.force_timeout) ok = wait_bar(&drain[g], 0);
       uint32_t ka = 0, va = 0;
-      // pass 1: S_g(j) for every key tile; a ring stage is free once both issuers commit
+      // pass 1: S_g(j) for every key tile; a ring stage is free once both issuers commit.
+      // Tiles from nkt_g on are only waited for and released: waiting for the fill keeps
+      // this issuer from releasing a stage's next use before the other issuer has read it.
+      const int nkt_g = group_keys(g);
       for (int j = 0; j < nkt && ok; ++j) {
         ok = ring_wait(pos, ka);
-        if (ok) ok = mma_s(ka, j & 1);
+        if (ok && j < nkt_g) ok = mma_s(ka, j & 1);
         if (ok) commit(&ring_empty[pos % NST]);
         ++pos;
       }
@@ -480,12 +487,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (more) {
           kpos = pos++;
           ok = ring_wait(kpos, ka);
-          if (ok) ok = mma_s(ka, 0);
+          if (ok && j + 1 < nkt_g) ok = mma_s(ka, 0);
           if (ok) commit(&ring_empty[kpos % NST]);
         }
         const uint32_t vpos = pos++;
         if (ok) ok = ring_wait(vpos, va);
-        if (ok) ok = mma_pv(j, va);
+        if (ok && j < nkt_g) ok = mma_pv(j, va);
         if (ok) commit(&ring_empty[vpos % NST]);
       }
       if (ok) commit(&o_full[g]);
@@ -550,7 +557,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     int a = -1;
     int jm = 0;   // 32-column chunk (tile * 4 + chunk) holding the first occurrence of the maximum
     // pass 1: running maximum of the raw scores q.k (scale > 0 keeps the argmax)
-    for (int j = 0; j < nkt && ok; ++j) {
+    const int nkt_g = group_keys(g);
+    for (int j = 0; j < nkt_g && ok; ++j) {
       ok = take_s(j & 1, static_cast<uint32_t>(j) >> 1);
       if (!ok) break;
       const int col0 = j * BN;   // key index of column 0
@@ -600,8 +608,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float base = (m > -INFINITY) ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
     uint8_t* prow = sP + g * C::P_BYTES + row_local * 128;
     float rowsum = 0.0f;
-    sidx = static_cast<uint32_t>(nkt + 1) >> 1;   // pass 1 used buffer 0 for tiles 0, 2, 4, ...
-    for (int j = 0; j < nkt && ok; ++j) {
+    sidx = static_cast<uint32_t>(nkt_g + 1) >> 1;   // pass 1 used buffer 0 for tiles 0, 2, 4, ...
+    for (int j = 0; j < nkt_g && ok; ++j) {
       ok = warp_wait(&s_full[2 * g], sidx & 1u);   // buffer 0
       if (!ok) break;
       ++sidx;
