@@ -291,7 +291,7 @@ def run_ours(args):
     import torch
 
     from rational_softmax_attention_gb300.inputs import (ATTN_LONG_CAUSAL, ATTN_LONG_WIDE, RA_SOFTMAX_LONG_ROWS,
-                                                         softmax_inputs, workload_inputs)
+                                                         attention_inputs, softmax_inputs, workload_inputs)
     world, rank, local = dist_env()
     dist = None
     if world > 1:
@@ -458,6 +458,40 @@ def run_ours(args):
     mod_ms = m0.elapsed_time(m1) / args.steps
     del mod, xm, dym
 
+    # fp32-input attention at scale (the CUDA-core FFMA path the 2e-5 fp32 tolerance needs):
+    # B1 H16 N4096 D128, non-causal, forward and backward, 3 timed calls each
+    qf, kf, vf, dof = (t.to(dev) for t in attention_inputs(1, 16, 4096, 4096, 128, seed=11, dtype=torch.float32))
+
+    def fp32_fwd():
+        return hp.ra.ra_attention_forward(qf, kf, vf, causal=False, out_dtype=torch.float32)
+    for _ in range(2):
+        of, rmf, rsf, raf, _ = fp32_fwd()
+    torch.cuda.synchronize(dev)
+    m0.record(torch.cuda.current_stream(dev))
+    for _ in range(3):
+        of, rmf, rsf, raf, _ = fp32_fwd()
+    m1.record(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize(dev)
+    f32_fwd_ms = m0.elapsed_time(m1) / 3
+
+    def fp32_bwd():
+        return hp.ra.ra_attention_backward(qf, kf, vf, of, dof, rmf, rsf, raf, causal=False)
+    fp32_bwd()
+    torch.cuda.synchronize(dev)
+    m0.record(torch.cuda.current_stream(dev))
+    for _ in range(3):
+        fp32_bwd()
+    m1.record(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize(dev)
+    f32_bwd_ms = m0.elapsed_time(m1) / 3
+    if hp.ra.device_status() != "RA_OK":
+        raise RuntimeError("fp32 attention component failed")
+    f32_fwd_fl = attn_flops(1, 16, 4096, 4096, 128, False, False)
+    f32_bwd_fl = attn_flops(1, 16, 4096, 4096, 128, False, True) - f32_fwd_fl
+    # FFMA peak from the unit counts: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz
+    ffma_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    del qf, kf, vf, dof, of, rmf, rsf, raf
+
     peaks, peak_src = load_peaks()
     tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     tc_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -516,6 +550,13 @@ def run_ours(args):
             "ra_attention_module_b2n128d768h12_causal": {
                 "ms_fwd_bwd": mod_ms, "tokens_per_s": 2 * 128 / (mod_ms * 1e-3),
                 "note": "latency-bound (24 heads of one 128-row tile); no roofline claim"},
+            "ra_attention_fp32_b1h16n4096d128": {
+                "fwd_ms": f32_fwd_ms, "fwd_TFLOP_per_s": f32_fwd_fl / (f32_fwd_ms * 1e-3) / 1e12,
+                "bwd_ms": f32_bwd_ms, "bwd_TFLOP_per_s": f32_bwd_fl / (f32_bwd_ms * 1e-3) / 1e12,
+                "bound": "alu", "peak_TFLOP_per_s": ffma_peak,
+                "fwd_frac": f32_fwd_fl / (f32_fwd_ms * 1e-3) / 1e12 / ffma_peak,
+                "bwd_frac": f32_bwd_fl / (f32_bwd_ms * 1e-3) / 1e12 / ffma_peak,
+                "note": "fp32 inputs, FFMA only (no TF32); counted FLOPs; peak = 152 SMs x 128 lanes x 2 x 2.07 GHz"},
         },
         "roofline": rl,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": hp.h2d_bytes(),

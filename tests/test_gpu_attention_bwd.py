@@ -141,3 +141,28 @@ def test_bf16_autograd_function_bf16_gradients():
             for got, ref in ((qg.grad, gq), (kg.grad, gk), (vg.grad, gv)):
                 g = parity.f64(got[b, h])
                 assert np.all(np.abs(g - ref) <= 1e-2 + np.abs(ref) * 2.0 ** -8)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_backward_at_scale(causal):
+    """fp32 inputs at N = 2048, D = 128: dq, dk, dv of a whole head against the oracle within
+    2e-5.  The oracle follows the GPU's argmax, which must be a near-maximum where the two
+    differ."""
+    scale = 128 ** -0.5
+    q, k, v, do = attention_inputs(1, 1, 2048, 2048, 128, seed=31 + int(causal), dtype=torch.float32)
+    qg, kg, vg, dog = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, rm, rs, ra_, _ = ra.ra_attention_forward(qg, kg, vg, scale=scale, causal=causal, out_dtype=torch.float32)
+    dq, dk, dv = ra.ra_attention_backward(qg, kg, vg, o, dog, rm, rs, ra_, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert ra.device_status() == "RA_OK"
+    qd, kd, vd, dod = (t[0, 0].double().numpy() for t in (q, k, v, do))
+    a_gpu = ra_[0, 0].cpu().numpy().astype(np.int64)
+    S = scale * (qd @ kd.T)
+    if causal:
+        S = np.where(np.tril(np.ones_like(S, dtype=bool)), S, -np.inf)
+    m = S.max(axis=1)
+    assert np.all(S[np.arange(2048), a_gpu] >= m - 1e-3 * np.maximum(1.0, np.abs(m)))
+    rq, rk, rv = oracle.ra_attention_head_bwd(qd, kd, vd, dod, scale, causal, argmax=a_gpu)
+    parity.assert_close_fp32(parity.f64(dq[0, 0]), rq, "dq")
+    parity.assert_close_fp32(parity.f64(dk[0, 0]), rk, "dk")
+    parity.assert_close_fp32(parity.f64(dv[0, 0]), rv, "dv")
