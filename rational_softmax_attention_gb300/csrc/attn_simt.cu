@@ -9,8 +9,9 @@
 // dQ) or one key row (dK/dV); thread `part` of a group holds the dimensions
 // d*G + part, so the G partial dot products are summed with G-1 xor shuffles.
 // The other operand is staged in shared memory 32 rows at a time.  Scores are
-// recomputed with exactly the same operation order in every kernel, so the
-// argmax entry has Delta = 0 exactly in the second pass and in the backward.
+// recomputed with exactly the same operation order in every kernel (the
+// register-blocked forward for D = 64 and 128 included), so the argmax entry has
+// Delta = 0 exactly in the second pass and in the backward.
 #include "kernels.cuh"
 
 namespace raattn {
@@ -150,6 +151,235 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnShape s, const f
       if (row_m) row_m[ro] = m;
       if (row_s) row_s[ro] = sum;
       if (row_arg) row_arg[ro] = a;
+    }
+  }
+}
+
+// Register-blocked forward for D = 64 and 128: a CTA of 256 threads owns 64 query rows and
+// streams the keys in tiles of 32.  Thread (ty, tx) holds the scores of rows 4 ty .. 4 ty + 3
+// against keys tx and tx + 16 of the tile, and the output block of the same rows and
+// dimensions D/16 tx .. + D/16 - 1; operands come from padded shared-memory rows as 16-byte
+// loads, several FMAs per load.  Every score keeps the operation order of the kernels above
+// (G = D/32 partial sums over the dimensions d = G c + part, in increasing c, combined as a
+// pairwise tree), so the backward's recomputed scores, the row maximum and the argmax are
+// bitwise the ones of the group-per-row kernels.
+template <int D>
+struct TiledGeom {
+  static constexpr int BQ = 64, BK = 32, THREADS = 256;
+  static constexpr int G = D / 32;        // partial sums per score
+  static constexpr int DT = D / 16;       // output dimensions per thread
+  static constexpr int LDQ = D + 4;       // padded pitch (floats) of the Q and K rows
+  static constexpr int LDP = BQ + 4;      // padded pitch of the transposed P tile
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + BQ * LDQ;
+  static constexpr int OFF_V = OFF_K + BK * LDQ;
+  static constexpr int OFF_P = OFF_V + BK * D;
+  static constexpr int OFF_X = OFF_P + BK * LDP;   // [BQ][16] per-thread partials (max, then sums)
+  static constexpr int OFF_XI = OFF_X + BQ * 16;   // [BQ][16] per-thread argmax
+  static constexpr int OFF_M = OFF_XI + BQ * 16;   // [BQ] row max, [BQ] row argmax
+  static constexpr int FLOATS = OFF_M + 2 * BQ;
+  static constexpr int SMEM_BYTES = FLOATS * 4;
+  static_assert(D == 64 || D == 128, "tiled CUDA-core forward: D = 64 or 128");
+  static_assert(OFF_K % 4 == 0 && OFF_V % 4 == 0 && OFF_P % 4 == 0 && LDQ % 4 == 0 && LDP % 4 == 0, "16-byte rows");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) attn_fwd_simt_tiled_kernel(AttnShape s, const float* __restrict__ q,
+                                                                  const float* __restrict__ k,
+                                                                  const float* __restrict__ v, void* o,
+                                                                  int out_bf16, float* row_m, float* row_s,
+                                                                  int32_t* row_arg) {
+  using T = TiledGeom<D>;
+  constexpr int BQ = T::BQ, BK = T::BK, G = T::G, DT = T::DT, LDQ = T::LDQ, LDP = T::LDP;
+  extern __shared__ float4 smem_f4[];
+  float* sm = reinterpret_cast<float*>(smem_f4);
+  float* Qs = sm + T::OFF_Q;
+  float* Ks = sm + T::OFF_K;
+  float* Vs = sm + T::OFF_V;
+  float* Ps = sm + T::OFF_P;
+  float* Xf = sm + T::OFF_X;
+  int* Xi = reinterpret_cast<int*>(sm + T::OFF_XI);
+  float* Mrow = sm + T::OFF_M;
+  int* Arow = reinterpret_cast<int*>(sm + T::OFF_M + BQ);
+  const int bh = blockIdx.y;
+  const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
+  const int i0 = blockIdx.x * BQ;
+  const float* qh = q + static_cast<size_t>(bh) * s.NQ * D;
+  const float* kh = k + static_cast<size_t>(bh) * s.NK * D;
+  const float* vh = v + static_cast<size_t>(bh) * s.NK * D;
+  const float4 zero4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+
+  // rows of [src] from row0 into a padded tile (zeros past nrows)
+  auto stage = [&](float* dst, int pitch, const float* src, int row0, int rows, int nrows) {
+    for (int e = t; e < rows * (D / 4); e += T::THREADS) {
+      const int r = e / (D / 4), c4 = e % (D / 4);
+      const int row = row0 + r;
+      *reinterpret_cast<float4*>(dst + r * pitch + 4 * c4) =
+          row < nrows ? reinterpret_cast<const float4*>(src + static_cast<size_t>(row) * D)[c4] : zero4;
+    }
+  };
+  stage(Qs, LDQ, qh, i0, BQ, s.NQ);
+  const int last_row = min(s.NQ - 1, i0 + BQ - 1);
+  const int kend = s.causal ? min(s.NK, last_row + 1) : s.NK;
+  int lim[4];   // last key each of this thread's rows may see
+#pragma unroll
+  for (int r = 0; r < 4; ++r) lim[r] = s.causal ? min(i0 + 4 * ty + r, s.NK - 1) : s.NK - 1;
+
+  // scores of rows 4 ty + r against keys tx + 16 c of the staged key tile
+  auto scores = [&](float (&sc)[4][2]) {
+    float p[4][2][G];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int g = 0; g < G; ++g) p[r][c][g] = 0.0f;
+#pragma unroll 4
+    for (int d4 = 0; d4 < D / 4; ++d4) {
+      float4 a[4], b[2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(Qs + (4 * ty + r) * LDQ + 4 * d4);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) b[c] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * c) * LDQ + 4 * d4);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          // dimension 4 d4 + e belongs to partial sum (4 d4 + e) mod G
+          p[r][c][0 % G] = fmaf(a[r].x, b[c].x, p[r][c][0 % G]);
+          p[r][c][1 % G] = fmaf(a[r].y, b[c].y, p[r][c][1 % G]);
+          p[r][c][2 % G] = fmaf(a[r].z, b[c].z, p[r][c][2 % G]);
+          p[r][c][3 % G] = fmaf(a[r].w, b[c].w, p[r][c][3 % G]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float dot = (G == 4) ? (p[r][c][0] + p[r][c][1]) + (p[r][c][2 % G] + p[r][c][3 % G])
+                                   : p[r][c][0] + p[r][c][1 % G];
+        sc[r][c] = dot * s.scale;
+      }
+  };
+
+  // pass 1: row maximum of the scaled scores, lowest index on ties
+  float m[4];
+  int a[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    m[r] = -INFINITY;
+    a[r] = -1;
+  }
+  for (int j0 = 0; j0 < kend; j0 += BK) {
+    __syncthreads();
+    stage(Ks, LDQ, kh, j0, BK, s.NK);
+    __syncthreads();
+    float sc[4][2];
+    scores(sc);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {   // keys tx, then tx + 16: increasing order within the thread
+      const int j = j0 + tx + 16 * c;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (j <= lim[r] && sc[r][c] > m[r]) {
+          m[r] = sc[r][c];
+          a[r] = j;
+        }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    Xf[(4 * ty + r) * 16 + tx] = m[r];
+    Xi[(4 * ty + r) * 16 + tx] = a[r];
+  }
+  __syncthreads();
+  if (t < BQ) {   // combine the 16 threads of a row: the maximum, and the lowest index holding it
+    float bm = -INFINITY;
+    int ba = -1;
+    for (int x = 0; x < 16; ++x) {
+      const float vm = Xf[t * 16 + x];
+      const int va = Xi[t * 16 + x];
+      if (vm > bm) {
+        bm = vm;
+        ba = va;
+      } else if (vm == bm && va >= 0 && (ba < 0 || va < ba)) {
+        ba = va;
+      }
+    }
+    Mrow[t] = bm;
+    Arow[t] = ba;
+  }
+  __syncthreads();
+  float mr[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) mr[r] = Mrow[4 * ty + r];
+
+  // pass 2: phi, sum(phi), phi V (keys in increasing order for every output element)
+  float acc[4][DT];
+  float psum[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    psum[r] = 0.0f;
+#pragma unroll
+    for (int d = 0; d < DT; ++d) acc[r][d] = 0.0f;
+  }
+  for (int j0 = 0; j0 < kend; j0 += BK) {
+    __syncthreads();
+    stage(Ks, LDQ, kh, j0, BK, s.NK);
+    stage(Vs, D, vh, j0, BK, s.NK);
+    __syncthreads();
+    float sc[4][2];
+    scores(sc);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int j = j0 + tx + 16 * c;
+      float ph[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float delta = mr[r] - sc[r][c];
+        ph[r] = (j <= lim[r] && delta < 16.0f) ? phi_exact(delta) : 0.0f;
+        psum[r] += ph[r];
+      }
+      *reinterpret_cast<float4*>(Ps + (tx + 16 * c) * LDP + 4 * ty) = make_float4(ph[0], ph[1], ph[2], ph[3]);
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < BK; ++kk) {
+      const float4 pp = *reinterpret_cast<const float4*>(Ps + kk * LDP + 4 * ty);
+      float vv[DT];
+#pragma unroll
+      for (int e = 0; e < DT / 4; ++e) {
+        const float4 w4 = *reinterpret_cast<const float4*>(Vs + kk * D + DT * tx + 4 * e);
+        vv[4 * e] = w4.x;
+        vv[4 * e + 1] = w4.y;
+        vv[4 * e + 2] = w4.z;
+        vv[4 * e + 3] = w4.w;
+      }
+      const float pr[4] = {pp.x, pp.y, pp.z, pp.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int d = 0; d < DT; ++d) acc[r][d] = fmaf(pr[r], vv[d], acc[r][d]);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 4; ++r) Xf[(4 * ty + r) * 16 + tx] = psum[r];
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int row = i0 + 4 * ty + r;
+    float sum = 0.0f;
+    for (int x = 0; x < 16; ++x) sum += Xf[(4 * ty + r) * 16 + x];
+    if (row >= s.NQ) continue;
+    const size_t ro = static_cast<size_t>(bh) * s.NQ + row;
+    const float inv = 1.0f / sum;
+#pragma unroll
+    for (int d = 0; d < DT; ++d) store_val(o, ro * D + DT * tx + d, acc[r][d] * inv, out_bf16);
+    if (tx == 0) {
+      if (row_m) row_m[ro] = mr[r];
+      if (row_s) row_s[ro] = sum;
+      if (row_arg) row_arg[ro] = Arow[4 * ty + r];
     }
   }
 }
@@ -318,8 +548,18 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_simt_kernel(
 template <int D>
 cudaError_t fwd_simt_d(const AttnShape& s, const float* q, const float* k, const float* v, void* o, bool out_bf16,
                        float* row_m, float* row_s, int32_t* row_arg, cudaStream_t st) {
-  dim3 grid((s.NQ + SimtGeom<D>::ROWS - 1) / SimtGeom<D>::ROWS, s.B * s.H);
-  attn_fwd_simt_kernel<D><<<grid, 128, 0, st>>>(s, q, k, v, o, out_bf16 ? 1 : 0, row_m, row_s, row_arg);
+  if constexpr (D == 64 || D == 128) {
+    using T = TiledGeom<D>;
+    const cudaError_t e = cudaFuncSetAttribute(attn_fwd_simt_tiled_kernel<D>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid((s.NQ + T::BQ - 1) / T::BQ, s.B * s.H);
+    attn_fwd_simt_tiled_kernel<D><<<grid, T::THREADS, T::SMEM_BYTES, st>>>(s, q, k, v, o, out_bf16 ? 1 : 0, row_m,
+                                                                           row_s, row_arg);
+  } else {
+    dim3 grid((s.NQ + SimtGeom<D>::ROWS - 1) / SimtGeom<D>::ROWS, s.B * s.H);
+    attn_fwd_simt_kernel<D><<<grid, 128, 0, st>>>(s, q, k, v, o, out_bf16 ? 1 : 0, row_m, row_s, row_arg);
+  }
   return cudaGetLastError();
 }
 
