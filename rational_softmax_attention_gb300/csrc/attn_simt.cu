@@ -6,8 +6,9 @@
 // the required accuracy (2e-5 absolute) rules out reduced-precision tensor cores.
 //
 // Layout of the work: a group of G = D/32 threads owns one query row (forward,
-// dQ) or one key row (dK/dV); thread `part` of a group holds the dimensions
-// d*G + part, so the G partial dot products are summed with G-1 xor shuffles.
+// dQ) or one key row (dK/dV); thread `part` of a group holds the 4-dimension
+// chunks part, part + G, part + 2G, ... (read from shared memory as 16-byte
+// loads), so the G partial dot products are summed with G-1 xor shuffles.
 // The other operand is staged in shared memory 32 rows at a time.  Scores are
 // recomputed with exactly the same operation order in every kernel (the
 // register-blocked forward for D = 64 and 128 included), so the argmax entry has
@@ -26,6 +27,26 @@ struct SimtGeom {
   static constexpr int ROWS = THREADS / G;           // rows per CTA
   static constexpr int KT = 32;                      // rows of the other operand per stage
 };
+
+// Dimension of local index dl (0 .. DPT-1) of thread `part`: chunk part + G (dl / 4), element dl % 4.
+template <int G>
+__device__ __forceinline__ int dim_of(int dl, int part) {
+  return 4 * (part + G * (dl >> 2)) + (dl & 3);
+}
+
+// The DPT values thread `part` holds of a shared-memory row (16-byte aligned), in local order.
+template <int D>
+__device__ __forceinline__ void load_part(const float* row, int part, float (&out)[SimtGeom<D>::DPT]) {
+  constexpr int G = SimtGeom<D>::G;
+#pragma unroll
+  for (int c = 0; c < SimtGeom<D>::DPT / 4; ++c) {
+    const float4 w = *reinterpret_cast<const float4*>(row + 4 * (part + G * c));
+    out[4 * c] = w.x;
+    out[4 * c + 1] = w.y;
+    out[4 * c + 2] = w.z;
+    out[4 * c + 3] = w.w;
+  }
+}
 
 template <int G>
 __device__ __forceinline__ float group_sum(float v) {
@@ -77,8 +98,8 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnShape s, const f
                                                             float* row_m, float* row_s, int32_t* row_arg) {
   using Gm = SimtGeom<D>;
   constexpr int G = Gm::G, DPT = Gm::DPT, ROWS = Gm::ROWS, KT = Gm::KT;
-  __shared__ float ks[KT][D];
-  __shared__ float vs[KT][D];
+  __shared__ __align__(16) float ks[KT][D];
+  __shared__ __align__(16) float vs[KT][D];
   const int bh = blockIdx.y;
   const int r = threadIdx.x / G, part = threadIdx.x % G;
   const int i = blockIdx.x * ROWS + r;
@@ -89,7 +110,7 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnShape s, const f
 
   float qr[DPT];
 #pragma unroll
-  for (int d = 0; d < DPT; ++d) qr[d] = row_ok ? qh[static_cast<size_t>(i) * D + d * G + part] : 0.0f;
+  for (int d = 0; d < DPT; ++d) qr[d] = row_ok ? qh[static_cast<size_t>(i) * D + dim_of<G>(d, part)] : 0.0f;
   const int last_row = min(s.NQ - 1, static_cast<int>(blockIdx.x) * ROWS + ROWS - 1);
   const int kend = s.causal ? min(s.NK, last_row + 1) : s.NK;
   const int lim = s.causal ? min(i, s.NK - 1) : s.NK - 1;   // last key this row may see
@@ -103,9 +124,11 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnShape s, const f
     __syncthreads();
     const int jn = min(KT, kend - j0);
     for (int jj = 0; jj < jn; ++jj) {
+      float kv[DPT];
+      load_part<D>(ks[jj], part, kv);
       float dot = 0.0f;
 #pragma unroll
-      for (int d = 0; d < DPT; ++d) dot = fmaf(qr[d], ks[jj][d * G + part], dot);
+      for (int d = 0; d < DPT; ++d) dot = fmaf(qr[d], kv[d], dot);
       dot = group_sum<G>(dot);
       const float sc = dot * s.scale;
       const int j = j0 + jj;
@@ -128,9 +151,11 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnShape s, const f
     __syncthreads();
     const int jn = min(KT, kend - j0);
     for (int jj = 0; jj < jn; ++jj) {
+      float kv[DPT];
+      load_part<D>(ks[jj], part, kv);
       float dot = 0.0f;
 #pragma unroll
-      for (int d = 0; d < DPT; ++d) dot = fmaf(qr[d], ks[jj][d * G + part], dot);
+      for (int d = 0; d < DPT; ++d) dot = fmaf(qr[d], kv[d], dot);
       dot = group_sum<G>(dot);
       const float sc = dot * s.scale;
       const int j = j0 + jj;
@@ -138,15 +163,17 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnShape s, const f
       if (j <= lim && delta < 16.0f) {
         const float phi = phi_exact(delta);
         sum += phi;
+        float vv[DPT];
+        load_part<D>(vs[jj], part, vv);
 #pragma unroll
-        for (int d = 0; d < DPT; ++d) acc[d] = fmaf(phi, vs[jj][d * G + part], acc[d]);
+        for (int d = 0; d < DPT; ++d) acc[d] = fmaf(phi, vv[d], acc[d]);
       }
     }
   }
   if (row_ok) {
     const size_t ro = static_cast<size_t>(bh) * s.NQ + i;
 #pragma unroll
-    for (int d = 0; d < DPT; ++d) store_val(o, ro * D + d * G + part, acc[d] / sum, out_bf16);
+    for (int d = 0; d < DPT; ++d) store_val(o, ro * D + dim_of<G>(d, part), acc[d] / sum, out_bf16);
     if (part == 0) {
       if (row_m) row_m[ro] = m;
       if (row_s) row_s[ro] = sum;
@@ -159,10 +186,10 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnShape s, const f
 // streams the keys in tiles of 32.  Thread (ty, tx) holds the scores of rows 4 ty .. 4 ty + 3
 // against keys tx and tx + 16 of the tile, and the output block of the same rows and
 // dimensions D/16 tx .. + D/16 - 1; operands come from padded shared-memory rows as 16-byte
-// loads, several FMAs per load.  Every score keeps the operation order of the kernels above
-// (G = D/32 partial sums over the dimensions d = G c + part, in increasing c, combined as a
-// pairwise tree), so the backward's recomputed scores, the row maximum and the argmax are
-// bitwise the ones of the group-per-row kernels.
+// loads, several FMAs per load.  Every score keeps the operation order of the group kernels
+// (G = D/32 partial sums, partial g over the 4-dimension chunks g, g + G, ... in increasing
+// order, combined as a pairwise tree), so the backward's recomputed scores, the row maximum
+// and the argmax are bitwise the ones of the group-per-row kernels.
 template <int D>
 struct TiledGeom {
   static constexpr int BQ = 64, BK = 32, THREADS = 256;
@@ -184,7 +211,7 @@ struct TiledGeom {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) attn_fwd_simt_tiled_kernel(AttnShape s, const float* __restrict__ q,
+__global__ void __launch_bounds__(256, 2) attn_fwd_simt_tiled_kernel(AttnShape s, const float* __restrict__ q,
                                                                   const float* __restrict__ k,
                                                                   const float* __restrict__ v, void* o,
                                                                   int out_bf16, float* row_m, float* row_s,
@@ -234,23 +261,27 @@ __global__ void __launch_bounds__(256) attn_fwd_simt_tiled_kernel(AttnShape s, c
       for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int g = 0; g < G; ++g) p[r][c][g] = 0.0f;
-#pragma unroll 4
-    for (int d4 = 0; d4 < D / 4; ++d4) {
-      float4 a[4], b[2];
+    // 4-dimension chunk d4 belongs to partial sum d4 mod G (the group kernels' thread part)
+#pragma unroll(4 / G)
+    for (int d0 = 0; d0 < D / 4; d0 += G) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(Qs + (4 * ty + r) * LDQ + 4 * d4);
+      for (int g = 0; g < G; ++g) {
+        const int d4 = d0 + g;
+        float4 a[4], b[2];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) b[c] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * c) * LDQ + 4 * d4);
+        for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(Qs + (4 * ty + r) * LDQ + 4 * d4);
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+        for (int c = 0; c < 2; ++c) b[c] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * c) * LDQ + 4 * d4);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          // dimension 4 d4 + e belongs to partial sum (4 d4 + e) mod G
-          p[r][c][0 % G] = fmaf(a[r].x, b[c].x, p[r][c][0 % G]);
-          p[r][c][1 % G] = fmaf(a[r].y, b[c].y, p[r][c][1 % G]);
-          p[r][c][2 % G] = fmaf(a[r].z, b[c].z, p[r][c][2 % G]);
-          p[r][c][3 % G] = fmaf(a[r].w, b[c].w, p[r][c][3 % G]);
-        }
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            p[r][c][g] = fmaf(a[r].x, b[c].x, p[r][c][g]);
+            p[r][c][g] = fmaf(a[r].y, b[c].y, p[r][c][g]);
+            p[r][c][g] = fmaf(a[r].z, b[c].z, p[r][c][g]);
+            p[r][c][g] = fmaf(a[r].w, b[c].w, p[r][c][g]);
+          }
+      }
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r)
@@ -393,8 +424,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_simt_kernel(
     float* ws_d, float* ws_r) {
   using Gm = SimtGeom<D>;
   constexpr int G = Gm::G, DPT = Gm::DPT, ROWS = Gm::ROWS, KT = Gm::KT;
-  __shared__ float ks[KT][D];
-  __shared__ float vs[KT][D];
+  __shared__ __align__(16) float ks[KT][D];
+  __shared__ __align__(16) float vs[KT][D];
   const int bh = blockIdx.y;
   const int r = threadIdx.x / G, part = threadIdx.x % G;
   const int i = blockIdx.x * ROWS + r;
@@ -408,7 +439,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_simt_kernel(
   float dpart = 0.0f;
 #pragma unroll
   for (int d = 0; d < DPT; ++d) {
-    const size_t idx = ro * D + d * G + part;
+    const size_t idx = ro * D + dim_of<G>(d, part);
     qr[d] = q[idx];
     dor[d] = dout[idx];
     dpart = fmaf(dor[d], load_val(o, idx, o_bf16), dpart);
@@ -432,11 +463,14 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_simt_kernel(
     __syncthreads();
     const int jn = min(KT, kend - j0);
     for (int jj = 0; jj < jn; ++jj) {
+      float kv[DPT], vv[DPT];
+      load_part<D>(ks[jj], part, kv);
+      load_part<D>(vs[jj], part, vv);
       float dot = 0.0f, dp = 0.0f;
 #pragma unroll
       for (int d = 0; d < DPT; ++d) {
-        dot = fmaf(qr[d], ks[jj][d * G + part], dot);
-        dp = fmaf(dor[d], vs[jj][d * G + part], dp);
+        dot = fmaf(qr[d], kv[d], dot);
+        dp = fmaf(dor[d], vv[d], dp);
       }
       dot = group_sum<G>(dot);
       dp = group_sum<G>(dp);
@@ -448,15 +482,15 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_simt_kernel(
         const float e = p * (dp - Di) * inv_one_minus_u2(delta);
         R += e;
 #pragma unroll
-        for (int d = 0; d < DPT; ++d) acc[d] = fmaf(e, ks[jj][d * G + part], acc[d]);
+        for (int d = 0; d < DPT; ++d) acc[d] = fmaf(e, kv[d], acc[d]);
       }
     }
   }
   if (row_ok) {
 #pragma unroll
     for (int d = 0; d < DPT; ++d) {
-      const float ka = kh[static_cast<size_t>(a) * D + d * G + part];
-      store_val(dq, ro * D + d * G + part, s.scale * fmaf(-R, ka, acc[d]), grad_bf16);
+      const float ka = kh[static_cast<size_t>(a) * D + dim_of<G>(d, part)];
+      store_val(dq, ro * D + dim_of<G>(d, part), s.scale * fmaf(-R, ka, acc[d]), grad_bf16);
     }
     if (part == 0) {
       ws_d[ro] = Di;
@@ -474,8 +508,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_simt_kernel(
     const float* __restrict__ ws_r) {
   using Gm = SimtGeom<D>;
   constexpr int G = Gm::G, DPT = Gm::DPT, ROWS = Gm::ROWS, KT = Gm::KT;
-  __shared__ float qs[KT][D];
-  __shared__ float dos[KT][D];
+  __shared__ __align__(16) float qs[KT][D];
+  __shared__ __align__(16) float dos[KT][D];
   __shared__ float st_m[KT], st_inv[KT], st_d[KT], st_r[KT];
   __shared__ int st_a[KT];
   const int bh = blockIdx.y;
@@ -491,8 +525,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_simt_kernel(
   float kr[DPT], vr[DPT], adk[DPT], adv[DPT];
 #pragma unroll
   for (int d = 0; d < DPT; ++d) {
-    kr[d] = k[ko * D + d * G + part];
-    vr[d] = v[ko * D + d * G + part];
+    kr[d] = k[ko * D + dim_of<G>(d, part)];
+    vr[d] = v[ko * D + dim_of<G>(d, part)];
     adk[d] = 0.0f;
     adv[d] = 0.0f;
   }
@@ -513,11 +547,14 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_simt_kernel(
     __syncthreads();
     const int in = min(KT, s.NQ - i0);
     for (int ii = 0; ii < in; ++ii) {
+      float qv[DPT], dov[DPT];
+      load_part<D>(qs[ii], part, qv);
+      load_part<D>(dos[ii], part, dov);
       float dot = 0.0f, dp = 0.0f;
 #pragma unroll
       for (int d = 0; d < DPT; ++d) {
-        dot = fmaf(qs[ii][d * G + part], kr[d], dot);
-        dp = fmaf(dos[ii][d * G + part], vr[d], dp);
+        dot = fmaf(qv[d], kr[d], dot);
+        dp = fmaf(dov[d], vr[d], dp);
       }
       dot = group_sum<G>(dot);
       dp = group_sum<G>(dp);
@@ -530,8 +567,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_simt_kernel(
         const float ds = (j == st_a[ii]) ? -st_r[ii] : p * (dp - st_d[ii]) * inv_one_minus_u2(delta);
 #pragma unroll
         for (int d = 0; d < DPT; ++d) {
-          adk[d] = fmaf(ds, qs[ii][d * G + part], adk[d]);
-          adv[d] = fmaf(p, dos[ii][d * G + part], adv[d]);
+          adk[d] = fmaf(ds, qv[d], adk[d]);
+          adv[d] = fmaf(p, dov[d], adv[d]);
         }
       }
     }
@@ -539,8 +576,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_simt_kernel(
   if (key_ok) {
 #pragma unroll
     for (int d = 0; d < DPT; ++d) {
-      store_val(dk, ko * D + d * G + part, s.scale * adk[d], grad_bf16);
-      store_val(dv, ko * D + d * G + part, adv[d], grad_bf16);
+      store_val(dk, ko * D + dim_of<G>(d, part), s.scale * adk[d], grad_bf16);
+      store_val(dv, ko * D + dim_of<G>(d, part), adv[d], grad_bf16);
     }
   }
 }
