@@ -190,10 +190,64 @@ __global__ void __launch_bounds__(128) attn_fwd_simt_kernel(AttnShape s, const f
 // (G = D/32 partial sums, partial g over the 4-dimension chunks g, g + G, ... in increasing
 // order, combined as a pairwise tree), so the backward's recomputed scores, the row maximum
 // and the argmax are bitwise the ones of the group-per-row kernels.
+// Rows row0 .. row0 + rows - 1 of a [nrows, D] fp32 matrix into a shared tile with row pitch
+// `pitch` floats (16-byte aligned), zeros past nrows; all threads of the block take part.
+template <int D>
+__device__ __forceinline__ void stage_tile(float* dst, int pitch, const float* src, int row0, int rows, int nrows) {
+  for (int e = threadIdx.x; e < rows * (D / 4); e += blockDim.x) {
+    const int r = e / (D / 4), c4 = e % (D / 4);
+    const int row = row0 + r;
+    *reinterpret_cast<float4*>(dst + r * pitch + 4 * c4) =
+        row < nrows ? reinterpret_cast<const float4*>(src + static_cast<size_t>(row) * D)[c4]
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+}
+
+// out[r][c] = dot(A row r, B row 16 c) for r < 4, c < 2 (A, B shared tiles with pitches lda,
+// ldb), in the group kernels' operation order: partial g over the 4-dimension chunks g,
+// g + G, ... in increasing order, the G partials summed as a pairwise tree.
+template <int D>
+__device__ __forceinline__ void block_dot(const float* A, int lda, const float* B, int ldb, float (&out)[4][2]) {
+  constexpr int G = D / 32;
+  float p[4][2][G];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int g = 0; g < G; ++g) p[r][c][g] = 0.0f;
+#pragma unroll(4 / G)
+  for (int d0 = 0; d0 < D / 4; d0 += G) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int d4 = d0 + g;
+      float4 a[4], b[2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(A + r * lda + 4 * d4);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) b[c] = *reinterpret_cast<const float4*>(B + 16 * c * ldb + 4 * d4);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          p[r][c][g] = fmaf(a[r].x, b[c].x, p[r][c][g]);
+          p[r][c][g] = fmaf(a[r].y, b[c].y, p[r][c][g]);
+          p[r][c][g] = fmaf(a[r].z, b[c].z, p[r][c][g]);
+          p[r][c][g] = fmaf(a[r].w, b[c].w, p[r][c][g]);
+        }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      out[r][c] = (G == 4) ? (p[r][c][0] + p[r][c][1]) + (p[r][c][2 % G] + p[r][c][3 % G])
+                           : p[r][c][0] + p[r][c][1 % G];
+}
+
 template <int D>
 struct TiledGeom {
   static constexpr int BQ = 64, BK = 32, THREADS = 256;
-  static constexpr int G = D / 32;        // partial sums per score
   static constexpr int DT = D / 16;       // output dimensions per thread
   static constexpr int LDQ = D + 4;       // padded pitch (floats) of the Q and K rows
   static constexpr int LDP = BQ + 4;      // padded pitch of the transposed P tile
@@ -217,7 +271,7 @@ __global__ void __launch_bounds__(256, 2) attn_fwd_simt_tiled_kernel(AttnShape s
                                                                   int out_bf16, float* row_m, float* row_s,
                                                                   int32_t* row_arg) {
   using T = TiledGeom<D>;
-  constexpr int BQ = T::BQ, BK = T::BK, G = T::G, DT = T::DT, LDQ = T::LDQ, LDP = T::LDP;
+  constexpr int BQ = T::BQ, BK = T::BK, DT = T::DT, LDQ = T::LDQ, LDP = T::LDP;
   extern __shared__ float4 smem_f4[];
   float* sm = reinterpret_cast<float*>(smem_f4);
   float* Qs = sm + T::OFF_Q;
@@ -234,18 +288,8 @@ __global__ void __launch_bounds__(256, 2) attn_fwd_simt_tiled_kernel(AttnShape s
   const float* qh = q + static_cast<size_t>(bh) * s.NQ * D;
   const float* kh = k + static_cast<size_t>(bh) * s.NK * D;
   const float* vh = v + static_cast<size_t>(bh) * s.NK * D;
-  const float4 zero4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 
-  // rows of [src] from row0 into a padded tile (zeros past nrows)
-  auto stage = [&](float* dst, int pitch, const float* src, int row0, int rows, int nrows) {
-    for (int e = t; e < rows * (D / 4); e += T::THREADS) {
-      const int r = e / (D / 4), c4 = e % (D / 4);
-      const int row = row0 + r;
-      *reinterpret_cast<float4*>(dst + r * pitch + 4 * c4) =
-          row < nrows ? reinterpret_cast<const float4*>(src + static_cast<size_t>(row) * D)[c4] : zero4;
-    }
-  };
-  stage(Qs, LDQ, qh, i0, BQ, s.NQ);
+  stage_tile<D>(Qs, LDQ, qh, i0, BQ, s.NQ);
   const int last_row = min(s.NQ - 1, i0 + BQ - 1);
   const int kend = s.causal ? min(s.NK, last_row + 1) : s.NK;
   int lim[4];   // last key each of this thread's rows may see
@@ -254,43 +298,11 @@ __global__ void __launch_bounds__(256, 2) attn_fwd_simt_tiled_kernel(AttnShape s
 
   // scores of rows 4 ty + r against keys tx + 16 c of the staged key tile
   auto scores = [&](float (&sc)[4][2]) {
-    float p[4][2][G];
+    block_dot<D>(Qs + 4 * ty * LDQ, LDQ, Ks + tx * LDQ, LDQ, sc);
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int g = 0; g < G; ++g) p[r][c][g] = 0.0f;
-    // 4-dimension chunk d4 belongs to partial sum d4 mod G (the group kernels' thread part)
-#pragma unroll(4 / G)
-    for (int d0 = 0; d0 < D / 4; d0 += G) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const int d4 = d0 + g;
-        float4 a[4], b[2];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(Qs + (4 * ty + r) * LDQ + 4 * d4);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) b[c] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * c) * LDQ + 4 * d4);
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            p[r][c][g] = fmaf(a[r].x, b[c].x, p[r][c][g]);
-            p[r][c][g] = fmaf(a[r].y, b[c].y, p[r][c][g]);
-            p[r][c][g] = fmaf(a[r].z, b[c].z, p[r][c][g]);
-            p[r][c][g] = fmaf(a[r].w, b[c].w, p[r][c][g]);
-          }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float dot = (G == 4) ? (p[r][c][0] + p[r][c][1]) + (p[r][c][2 % G] + p[r][c][3 % G])
-                                   : p[r][c][0] + p[r][c][1 % G];
-        sc[r][c] = dot * s.scale;
-      }
+      for (int c = 0; c < 2; ++c) sc[r][c] *= s.scale;
   };
 
   // pass 1: row maximum of the scaled scores, lowest index on ties
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(256, 2) attn_fwd_simt_tiled_kernel(AttnShape s
   }
   for (int j0 = 0; j0 < kend; j0 += BK) {
     __syncthreads();
-    stage(Ks, LDQ, kh, j0, BK, s.NK);
+    stage_tile<D>(Ks, LDQ, kh, j0, BK, s.NK);
     __syncthreads();
     float sc[4][2];
     scores(sc);
@@ -356,8 +368,8 @@ __global__ void __launch_bounds__(256, 2) attn_fwd_simt_tiled_kernel(AttnShape s
   }
   for (int j0 = 0; j0 < kend; j0 += BK) {
     __syncthreads();
-    stage(Ks, LDQ, kh, j0, BK, s.NK);
-    stage(Vs, D, vh, j0, BK, s.NK);
+    stage_tile<D>(Ks, LDQ, kh, j0, BK, s.NK);
+    stage_tile<D>(Vs, D, vh, j0, BK, s.NK);
     __syncthreads();
     float sc[4][2];
     scores(sc);
@@ -582,6 +594,287 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_simt_kernel(
   }
 }
 
+// Register-blocked backward for D = 64 and 128, the same blocking as the forward.
+//   dQ kernel: 64 query rows per CTA against 32-key tiles; thread (ty, tx) forms the scores
+//   and dP of rows 4 ty .. + 3 against keys tx, tx + 16 (block_dot: the forward's scores
+//   bitwise), E into a shared tile, then its 4 x D/16 block of dQ += E K; D_i and R_i go to
+//   the workspace for the dK/dV kernel.
+//   dK/dV kernel: 64 keys per CTA against 32-query tiles; thread (ty, tx) forms S^T and dP^T
+//   of keys 4 ty .. + 3 against queries tx, tx + 16, P and dS into shared tiles, then its
+//   4 x D/16 blocks of dV += P^T dO and dK += dS^T Q.
+// Every output element accumulates over the other operand's rows in increasing order.
+template <int D>
+struct TiledBwdGeom {
+  static constexpr int BR = 64, BT = 32, THREADS = 256, DT = D / 16;
+  static constexpr int LDT = D + 4;    // padded pitch of the streamed tiles (read by 16 rows per warp)
+  static constexpr int LDE = BR + 4;   // padded pitch of the E / P / dS tiles
+  // dQ kernel: Q, dO [BR][D]; K, V [BT][LDT]; E^T [BT][LDE]; R partials [BR][16]; m, 1/s, D_i, a [4][BR]
+  static constexpr int DQ_Q = 0, DQ_DO = BR * D, DQ_K = 2 * BR * D, DQ_V = DQ_K + BT * LDT;
+  static constexpr int DQ_E = DQ_V + BT * LDT, DQ_X = DQ_E + BT * LDE, DQ_C = DQ_X + BR * 16;
+  static constexpr int DQ_BYTES = (DQ_C + 4 * BR) * 4;
+  // dK/dV kernel: K, V [BR][D]; Q, dO [BT][LDT]; P, dS [BT][LDE]; m, 1/s, D_i, R_i, a [5][BT]
+  static constexpr int KV_K = 0, KV_V = BR * D, KV_Q = 2 * BR * D, KV_DO = KV_Q + BT * LDT;
+  static constexpr int KV_P = KV_DO + BT * LDT, KV_S = KV_P + BT * LDE, KV_C = KV_S + BT * LDE;
+  static constexpr int KV_BYTES = (KV_C + 5 * BT) * 4;
+  static_assert(D == 64 || D == 128, "tiled CUDA-core backward: D = 64 or 128");
+  static_assert(DQ_K % 4 == 0 && DQ_V % 4 == 0 && DQ_E % 4 == 0 && KV_Q % 4 == 0 && KV_DO % 4 == 0 &&
+                    KV_P % 4 == 0 && KV_S % 4 == 0 && LDT % 4 == 0 && LDE % 4 == 0,
+                "16-byte rows");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 2) attn_bwd_dq_simt_tiled_kernel(
+    AttnShape s, const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    const void* o, int o_bf16, const float* __restrict__ dout, const float* __restrict__ row_m,
+    const float* __restrict__ row_s, const int32_t* __restrict__ row_arg, void* dq, int grad_bf16,
+    float* ws_d, float* ws_r) {
+  using T = TiledBwdGeom<D>;
+  constexpr int BR = T::BR, BT = T::BT, DT = T::DT, LDT = T::LDT, LDE = T::LDE;
+  extern __shared__ float4 smem_f4[];
+  float* sm = reinterpret_cast<float*>(smem_f4);
+  float* Qs = sm + T::DQ_Q;
+  float* Ds = sm + T::DQ_DO;
+  float* Ks = sm + T::DQ_K;
+  float* Vs = sm + T::DQ_V;
+  float* Es = sm + T::DQ_E;
+  float* Xf = sm + T::DQ_X;
+  float* Cm = sm + T::DQ_C;
+  float* Cinv = Cm + BR;
+  float* Cd = Cm + 2 * BR;
+  int* Ca = reinterpret_cast<int*>(Cm + 3 * BR);
+  const int bh = blockIdx.y;
+  const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
+  const int i0 = blockIdx.x * BR;
+  const float* kh = k + static_cast<size_t>(bh) * s.NK * D;
+  const float* vh = v + static_cast<size_t>(bh) * s.NK * D;
+  stage_tile<D>(Qs, D, q + static_cast<size_t>(bh) * s.NQ * D, i0, BR, s.NQ);
+  stage_tile<D>(Ds, D, dout + static_cast<size_t>(bh) * s.NQ * D, i0, BR, s.NQ);
+  __syncthreads();
+  if (t < BR) {   // per-row constants; D_i = dO_i . O_i
+    const int i = i0 + t;
+    float m = 0.0f, inv = 0.0f, di = 0.0f;
+    int a = -1;
+    if (i < s.NQ) {
+      const size_t ro = static_cast<size_t>(bh) * s.NQ + i;
+      m = row_m[ro];
+      inv = 1.0f / row_s[ro];
+      a = row_arg[ro];
+      for (int d = 0; d < D; ++d) di = fmaf(Ds[t * D + d], load_val(o, ro * D + d, o_bf16), di);
+    }
+    Cm[t] = m;
+    Cinv[t] = inv;
+    Cd[t] = di;
+    Ca[t] = a;
+  }
+  __syncthreads();
+  float mr[4], invr[4], dr[4];
+  int ar[4], lim[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int row = 4 * ty + r;
+    mr[r] = Cm[row];
+    invr[r] = Cinv[row];
+    dr[r] = Cd[row];
+    ar[r] = Ca[row];
+    lim[r] = s.causal ? min(i0 + row, s.NK - 1) : s.NK - 1;
+  }
+  const int last_row = min(s.NQ - 1, i0 + BR - 1);
+  const int kend = s.causal ? min(s.NK, last_row + 1) : s.NK;
+  float acc[4][DT];
+  float rpart[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    rpart[r] = 0.0f;
+#pragma unroll
+    for (int d = 0; d < DT; ++d) acc[r][d] = 0.0f;
+  }
+  for (int j0 = 0; j0 < kend; j0 += BT) {
+    __syncthreads();
+    stage_tile<D>(Ks, LDT, kh, j0, BT, s.NK);
+    stage_tile<D>(Vs, LDT, vh, j0, BT, s.NK);
+    __syncthreads();
+    float sc[4][2], dp[4][2];
+    block_dot<D>(Qs + 4 * ty * D, D, Ks + tx * LDT, LDT, sc);
+    block_dot<D>(Ds + 4 * ty * D, D, Vs + tx * LDT, LDT, dp);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int j = j0 + tx + 16 * c;
+      float e4[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float delta = mr[r] - sc[r][c] * s.scale;
+        float e = 0.0f;
+        if (j <= lim[r] && j != ar[r] && delta < 16.0f) {
+          const float p = phi_exact(delta) * invr[r];
+          e = p * (dp[r][c] - dr[r]) * inv_one_minus_u2(delta);
+        }
+        rpart[r] += e;
+        e4[r] = e;
+      }
+      *reinterpret_cast<float4*>(Es + (tx + 16 * c) * LDE + 4 * ty) = make_float4(e4[0], e4[1], e4[2], e4[3]);
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < BT; ++kk) {
+      const float4 e4 = *reinterpret_cast<const float4*>(Es + kk * LDE + 4 * ty);
+      float kv[DT];
+#pragma unroll
+      for (int x = 0; x < DT / 4; ++x) {
+        const float4 w = *reinterpret_cast<const float4*>(Ks + kk * LDT + DT * tx + 4 * x);
+        kv[4 * x] = w.x;
+        kv[4 * x + 1] = w.y;
+        kv[4 * x + 2] = w.z;
+        kv[4 * x + 3] = w.w;
+      }
+      const float er[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int d = 0; d < DT; ++d) acc[r][d] = fmaf(er[r], kv[d], acc[r][d]);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 4; ++r) Xf[(4 * ty + r) * 16 + tx] = rpart[r];
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int row = i0 + 4 * ty + r;
+    float R = 0.0f;
+    for (int x = 0; x < 16; ++x) R += Xf[(4 * ty + r) * 16 + x];
+    if (row >= s.NQ) continue;
+    const size_t ro = static_cast<size_t>(bh) * s.NQ + row;
+#pragma unroll
+    for (int d = 0; d < DT; ++d) {
+      const float ka = kh[static_cast<size_t>(ar[r]) * D + DT * tx + d];
+      store_val(dq, ro * D + DT * tx + d, s.scale * fmaf(-R, ka, acc[r][d]), grad_bf16);
+    }
+    if (tx == 0) {
+      ws_d[ro] = dr[r];
+      ws_r[ro] = R;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) attn_bwd_dkdv_simt_tiled_kernel(
+    AttnShape s, const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    const float* __restrict__ dout, const float* __restrict__ row_m, const float* __restrict__ row_s,
+    const int32_t* __restrict__ row_arg, void* dk, void* dv, int grad_bf16, const float* __restrict__ ws_d,
+    const float* __restrict__ ws_r) {
+  using T = TiledBwdGeom<D>;
+  constexpr int BR = T::BR, BT = T::BT, DT = T::DT, LDT = T::LDT, LDE = T::LDE;
+  extern __shared__ float4 smem_f4[];
+  float* sm = reinterpret_cast<float*>(smem_f4);
+  float* Ks = sm + T::KV_K;
+  float* Vs = sm + T::KV_V;
+  float* Qt = sm + T::KV_Q;
+  float* Dt = sm + T::KV_DO;
+  float* Pt = sm + T::KV_P;
+  float* St = sm + T::KV_S;
+  float* Cm = sm + T::KV_C;
+  float* Cinv = Cm + BT;
+  float* Cd = Cm + 2 * BT;
+  float* Cr = Cm + 3 * BT;
+  int* Ca = reinterpret_cast<int*>(Cm + 4 * BT);
+  const int bh = blockIdx.y;
+  const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
+  const int j0 = blockIdx.x * BR;   // first key of the block
+  const float* qh = q + static_cast<size_t>(bh) * s.NQ * D;
+  const float* doh = dout + static_cast<size_t>(bh) * s.NQ * D;
+  const size_t so = static_cast<size_t>(bh) * s.NQ;
+  stage_tile<D>(Ks, D, k + static_cast<size_t>(bh) * s.NK * D, j0, BR, s.NK);
+  stage_tile<D>(Vs, D, v + static_cast<size_t>(bh) * s.NK * D, j0, BR, s.NK);
+  float adk[4][DT], adv[4][DT];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int d = 0; d < DT; ++d) {
+      adk[r][d] = 0.0f;
+      adv[r][d] = 0.0f;
+    }
+  const int istart = s.causal ? j0 : 0;   // first query any key of the block sees (j <= i)
+  for (int i0 = istart; i0 < s.NQ; i0 += BT) {
+    __syncthreads();
+    stage_tile<D>(Qt, LDT, qh, i0, BT, s.NQ);
+    stage_tile<D>(Dt, LDT, doh, i0, BT, s.NQ);
+    if (t < BT) {
+      const int ii = i0 + t;
+      const bool ok = ii < s.NQ;
+      Cm[t] = ok ? row_m[so + ii] : 0.0f;
+      Cinv[t] = ok ? 1.0f / row_s[so + ii] : 0.0f;
+      Cd[t] = ok ? ws_d[so + ii] : 0.0f;
+      Cr[t] = ok ? ws_r[so + ii] : 0.0f;
+      Ca[t] = ok ? row_arg[so + ii] : -1;
+    }
+    __syncthreads();
+    float sc[4][2], dp[4][2];
+    block_dot<D>(Ks + 4 * ty * D, D, Qt + tx * LDT, LDT, sc);   // S^T: keys x queries
+    block_dot<D>(Vs + 4 * ty * D, D, Dt + tx * LDT, LDT, dp);   // dP^T
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int qi = tx + 16 * c;
+      const int i = i0 + qi;
+      float p4[4], s4[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int j = j0 + 4 * ty + r;
+        const float delta = Cm[qi] - sc[r][c] * s.scale;
+        const bool allowed = j < s.NK && i < s.NQ && (!s.causal || j <= i);
+        float p = 0.0f, ds = 0.0f;
+        if (allowed && delta < 16.0f) {
+          p = phi_exact(delta) * Cinv[qi];
+          ds = (j == Ca[qi]) ? -Cr[qi] : p * (dp[r][c] - Cd[qi]) * inv_one_minus_u2(delta);
+        }
+        p4[r] = p;
+        s4[r] = ds;
+      }
+      *reinterpret_cast<float4*>(Pt + qi * LDE + 4 * ty) = make_float4(p4[0], p4[1], p4[2], p4[3]);
+      *reinterpret_cast<float4*>(St + qi * LDE + 4 * ty) = make_float4(s4[0], s4[1], s4[2], s4[3]);
+    }
+    __syncthreads();
+#pragma unroll 2
+    for (int ii = 0; ii < BT; ++ii) {
+      const float4 p4 = *reinterpret_cast<const float4*>(Pt + ii * LDE + 4 * ty);
+      const float4 s4 = *reinterpret_cast<const float4*>(St + ii * LDE + 4 * ty);
+      float dov[DT], qv[DT];
+#pragma unroll
+      for (int x = 0; x < DT / 4; ++x) {
+        const float4 w = *reinterpret_cast<const float4*>(Dt + ii * LDT + DT * tx + 4 * x);
+        const float4 u = *reinterpret_cast<const float4*>(Qt + ii * LDT + DT * tx + 4 * x);
+        dov[4 * x] = w.x;
+        dov[4 * x + 1] = w.y;
+        dov[4 * x + 2] = w.z;
+        dov[4 * x + 3] = w.w;
+        qv[4 * x] = u.x;
+        qv[4 * x + 1] = u.y;
+        qv[4 * x + 2] = u.z;
+        qv[4 * x + 3] = u.w;
+      }
+      const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+      const float sr[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int d = 0; d < DT; ++d) {
+          adv[r][d] = fmaf(pr[r], dov[d], adv[r][d]);
+          adk[r][d] = fmaf(sr[r], qv[d], adk[r][d]);
+        }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int j = j0 + 4 * ty + r;
+    if (j >= s.NK) continue;
+    const size_t ko = static_cast<size_t>(bh) * s.NK + j;
+#pragma unroll
+    for (int d = 0; d < DT; ++d) {
+      store_val(dk, ko * D + DT * tx + d, s.scale * adk[r][d], grad_bf16);
+      store_val(dv, ko * D + DT * tx + d, adv[r][d], grad_bf16);
+    }
+  }
+}
+
 template <int D>
 cudaError_t fwd_simt_d(const AttnShape& s, const float* q, const float* k, const float* v, void* o, bool out_bf16,
                        float* row_m, float* row_s, int32_t* row_arg, cudaStream_t st) {
@@ -605,15 +898,34 @@ cudaError_t bwd_simt_d(const AttnShape& s, const float* q, const float* k, const
                        bool o_bf16, const float* dout, const float* row_m, const float* row_s,
                        const int32_t* row_arg, void* dq, void* dk, void* dv, bool grad_bf16, float* ws_d,
                        float* ws_r, cudaStream_t st) {
-  dim3 gq((s.NQ + SimtGeom<D>::ROWS - 1) / SimtGeom<D>::ROWS, s.B * s.H);
-  attn_bwd_dq_simt_kernel<D><<<gq, 128, 0, st>>>(s, q, k, v, o, o_bf16 ? 1 : 0, dout, row_m, row_s, row_arg,
-                                                 dq, grad_bf16 ? 1 : 0, ws_d, ws_r);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  dim3 gk((s.NK + SimtGeom<D>::ROWS - 1) / SimtGeom<D>::ROWS, s.B * s.H);
-  attn_bwd_dkdv_simt_kernel<D><<<gk, 128, 0, st>>>(s, q, k, v, dout, row_m, row_s, row_arg, dk, dv,
-                                                   grad_bf16 ? 1 : 0, ws_d, ws_r);
-  return cudaGetLastError();
+  if constexpr (D == 64 || D == 128) {
+    using T = TiledBwdGeom<D>;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_simt_tiled_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::DQ_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_bwd_dkdv_simt_tiled_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             T::KV_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 gq((s.NQ + T::BR - 1) / T::BR, s.B * s.H);
+    attn_bwd_dq_simt_tiled_kernel<D><<<gq, T::THREADS, T::DQ_BYTES, st>>>(
+        s, q, k, v, o, o_bf16 ? 1 : 0, dout, row_m, row_s, row_arg, dq, grad_bf16 ? 1 : 0, ws_d, ws_r);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 gk((s.NK + T::BR - 1) / T::BR, s.B * s.H);
+    attn_bwd_dkdv_simt_tiled_kernel<D><<<gk, T::THREADS, T::KV_BYTES, st>>>(
+        s, q, k, v, dout, row_m, row_s, row_arg, dk, dv, grad_bf16 ? 1 : 0, ws_d, ws_r);
+    return cudaGetLastError();
+  } else {
+    dim3 gq((s.NQ + SimtGeom<D>::ROWS - 1) / SimtGeom<D>::ROWS, s.B * s.H);
+    attn_bwd_dq_simt_kernel<D><<<gq, 128, 0, st>>>(s, q, k, v, o, o_bf16 ? 1 : 0, dout, row_m, row_s, row_arg,
+                                                   dq, grad_bf16 ? 1 : 0, ws_d, ws_r);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 gk((s.NK + SimtGeom<D>::ROWS - 1) / SimtGeom<D>::ROWS, s.B * s.H);
+    attn_bwd_dkdv_simt_kernel<D><<<gk, 128, 0, st>>>(s, q, k, v, dout, row_m, row_s, row_arg, dk, dv,
+                                                     grad_bf16 ? 1 : 0, ws_d, ws_r);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
