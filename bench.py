@@ -48,6 +48,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(value, dist, device):
+    """The largest value over all ranks (the slowest rank's time); the value itself on one rank."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_rank_step, steps, elapsed_ms):
+    """TFLOP/s of the whole job: every rank runs the same step (weak scaling), and the
+    elapsed time is the slowest rank's."""
+    return world * flops_per_rank_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -329,11 +345,7 @@ def run_ours(args):
     status = hp.ra.device_status(stream)
     if status != "RA_OK":
         raise RuntimeError(f"device status after the timed region: {status}")
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     per_call = {"ra_softmax_ms": [], "ra_attention_fwd_ms": [], "ra_attention_bwd_ms": []}
     for e in ev:
         per_call["ra_softmax_ms"].append(e[0].elapsed_time(e[1]))
@@ -344,7 +356,7 @@ def run_ours(args):
     B, H, N, D = hp.shape
     flops_step = attn_flops(B, H, N, N, D, w.causal, True)
     ms_per_step = elapsed_ms / args.steps
-    value = world * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, args.steps, elapsed_ms)
     fwd_fl = attn_flops(B, H, N, N, D, w.causal, False)
     bwd_fl = flops_step - fwd_fl
     sm_bytes = 2.0 * x.numel() * 4
@@ -353,12 +365,8 @@ def run_ours(args):
     # with the copies of neighbouring steps overlapping the compute (HotPath.run_e2e)
     hp.run_e2e(stream, max(3, args.warmup))
     barrier()
-    e2e_ms = hp.run_e2e(stream, args.steps)
-    if dist is not None:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * flops_step * args.steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(hp.run_e2e(stream, args.steps), dist, dev)
+    e2e_value = whole_job_tflops(world, flops_step, args.steps, e2e_ms)
 
     # skipped-tile fraction of the forward (one untimed call with the counters)
     counts = torch.zeros(2, dtype=torch.int64, device=dev)

@@ -47,7 +47,7 @@ typedef enum {
 typedef enum {
   RA_OK = 0,
   RA_ERR_ARG = 1,          /* null pointer, size < 1, overflow, misalignment, bad enum */
-  RA_ERR_UNSUPPORTED = 2,  /* valid request outside what this build implements */
+  RA_ERR_UNSUPPORTED = 2,  /* valid request outside what the library implements */
   RA_ERR_LAUNCH = 3,       /* the CUDA runtime refused the launch or the set-up */
   RA_ERR_TIMEOUT = 4       /* a device-side wait exceeded its limit (see ra_device_status) */
 } ra_status_t;
