@@ -101,9 +101,12 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
  *                be NULL when no backward follows.
  *   tile_counts  optional (NULL allowed) int64[2] in device memory, zeroed then written:
  *                [0] = (query tile, key tile) pairs visited by the second pass,
- *                [1] = pairs whose V tile and P*V product were skipped because every
- *                      entry of the pair lies outside the compact support.
- *                Tiles are 128 x 128 on the tensor-core path.
+ *                [1] = pairs whose P*V product was skipped because every entry of
+ *                      the pair lies outside the compact support (the V tile is still
+ *                      loaded: the decision is taken while it is in flight).
+ *                Tiles are 128 x 128 on the tensor-core path; at D = 128 with N_Q > 256
+ *                two query tiles share each product (CTA pairs), which is skipped
+ *                only when both are.
  *   workspace    device memory of ra_attention_fwd_workspace_size() bytes, 16-byte
  *                aligned, contents on entry irrelevant; required for RA_BF16 inputs
  *                (NULL allowed for RA_F32).  The call writes an fp16 copy of v there
