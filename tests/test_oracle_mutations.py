@@ -1,6 +1,7 @@
 """The oracle's pins catch plausible mistakes: plant one in the oracle (on the CPU) and
 check that a pin fails.  Mutations: wrong power, wrong support width, a dropped
-argmax correction in the backward, swapped query/key operands."""
+argmax correction in the backward, swapped query/key operands, and in the attn_mask
+handling an ignored, a transposed, or an OR-ed (instead of AND-ed) mask."""
 import numpy as np
 import pytest
 
@@ -62,3 +63,54 @@ def test_swapped_operands_are_caught():
     assert np.array_equal(O[0], v[0])
     # swapped: row 0 still sees only key 0, but the later rows change
     assert not np.allclose(O[1:], Ob[1:])
+
+
+def _mask_pins_hold():
+    """The attn_mask pins of tests/test_oracle_mask.py in compact form: a key-padding mask
+    equals deleting the keys, a row with no allowed key gives zeros, a lower-triangular mask
+    equals causal, and an all-True mask leaves causal unchanged."""
+    rng = np.random.default_rng(6)
+    q, k, v = (rng.normal(size=(1, 1, 6, 4)) for _ in range(3))
+    keep = np.array([0, 2, 3, 5])
+    mask = np.zeros((6, 6), dtype=bool)
+    mask[:, keep] = True
+    O, *_ = oracle.ra_attention_fwd(q, k, v, mask=mask)
+    O2, *_ = oracle.ra_attention_fwd(q, k[:, :, keep], v[:, :, keep])
+    pad_ok = O.shape == O2.shape and np.allclose(O, O2, rtol=0, atol=1e-14)
+    empty = mask.copy()
+    empty[2] = False
+    Oe, _, se, ae = oracle.ra_attention_fwd(q, k, v, mask=empty)
+    empty_ok = bool(np.all(Oe[0, 0, 2] == 0) and se[0, 0, 2] == 0 and ae[0, 0, 2] == -1)
+    tri = np.tril(np.ones((6, 6), dtype=bool))
+    causal = oracle.ra_attention_fwd(q, k, v, causal=True)
+    tri_ok = all(np.array_equal(a, b) for a, b in zip(oracle.ra_attention_fwd(q, k, v, mask=tri), causal))
+    ones_ok = all(np.array_equal(a, b) for a, b in
+                  zip(oracle.ra_attention_fwd(q, k, v, causal=True, mask=np.ones((6, 6), dtype=bool)), causal))
+    return pad_ok and empty_ok and tri_ok and ones_ok
+
+
+def test_mask_pins_hold_on_the_unmutated_oracle():
+    assert _mask_pins_hold()
+
+
+_REAL_ALLOWED = ra_oracle._allowed
+
+
+def _ignore_mask(n_q, n_k, causal, mask):
+    return _REAL_ALLOWED(n_q, n_k, causal, None)
+
+
+def _transposed_mask(n_q, n_k, causal, mask):
+    return _REAL_ALLOWED(n_q, n_k, causal, None if mask is None else np.asarray(mask).T)
+
+
+def _mask_or_causal(n_q, n_k, causal, mask):
+    if mask is None or not causal:
+        return _REAL_ALLOWED(n_q, n_k, causal, mask)
+    return _REAL_ALLOWED(n_q, n_k, True, None) | np.asarray(mask, dtype=bool)
+
+
+@pytest.mark.parametrize("mutant", [_ignore_mask, _transposed_mask, _mask_or_causal])
+def test_mask_mutations_are_caught(monkeypatch, mutant):
+    monkeypatch.setattr(ra_oracle, "_allowed", mutant)
+    assert not _mask_pins_hold()
