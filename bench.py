@@ -64,6 +64,19 @@ def whole_job_tflops(world, flops_per_rank_step, steps, elapsed_ms):
     return world * flops_per_rank_step * steps / (elapsed_ms * 1e-3) / 1e12
 
 
+def step_config(w, sw):
+    """The workload of one step (both arms report the same)."""
+    return {
+        "workload": "ra_softmax fp32 [16384, 8192] sigma 4 + ra_attention fwd+bwd B4 H16 N8192 D128 bf16 "
+                    "Q,K sigma 3 scale 1/sqrt(128) non-causal (fp32 O and gradients)",
+        "ra_softmax": {"rows": sw.rows, "cols": sw.cols, "sigma": sw.sigma, "dtype": "f32"},
+        "attention": {"B": w.B, "H": w.H, "N": w.N, "D": w.D, "sigma_qk": w.sigma_qk, "causal": w.causal,
+                      "dtype": "bf16 in, fp32 accumulate, fp32 out"},
+        "l2": "no flush: each step reads > 1.5 GiB of inputs, above the 129 MB L2",
+        "per_gpu": "each rank runs the whole step on its own GPU (no exchange on this path)",
+    }
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -528,15 +541,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded torch.randn (CPU generator), no dataset",
-        "config": {
-            "workload": "ra_softmax fp32 [16384, 8192] sigma 4 + ra_attention fwd+bwd B4 H16 N8192 D128 bf16 "
-                        "Q,K sigma 3 scale 1/sqrt(128) non-causal (fp32 O and gradients)",
-            "ra_softmax": {"rows": sw.rows, "cols": sw.cols, "sigma": sw.sigma, "dtype": "f32"},
-            "attention": {"B": B, "H": H, "N": N, "D": D, "sigma_qk": w.sigma_qk, "causal": w.causal,
-                          "dtype": "bf16 in, fp32 accumulate, fp32 out"},
-            "l2": "no flush: each step reads > 1.5 GiB of inputs, above the 129 MB L2",
-            "per_gpu": "each rank runs the whole step on its own GPU (no exchange on this path)",
-        },
+        "config": step_config(w, sw),
         "components": {
             "ra_softmax": {"ms": med["ra_softmax_ms"], "GB_per_s": sm_gbs, "frac_hbm": sm_gbs / hbm_peak,
                            "frac_hbm_8000": sm_gbs / 8000.0},
@@ -607,8 +612,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
         "data": "synthetic: seeded torch.randn (CPU generator), no dataset",
-        "config": {"workload": "ra_softmax fp32 [16384, 8192] sigma 4 + ra_attention fwd+bwd B4 H16 N8192 D128 bf16 "
-                               "Q,K sigma 3 scale 1/sqrt(128) non-causal (fp32 O and gradients)"},
+        "config": step_config(w, sw),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
                          "sample": desc + " per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

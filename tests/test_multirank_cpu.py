@@ -66,3 +66,28 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("LOCAL_RANK", "1")
     bench.run_reference(types.SimpleNamespace(steps=1, warmup=0))
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_one_complete_line():
+    """bench.py --impl reference on the CPU (one step, no warm-up): one JSON line with the
+    contract's keys, the same metric, unit and config as the measured arm."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {kk: vv for kk, vv in os.environ.items() if kk not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "0"], capture_output=True, text=True, timeout=600, env=env, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["higher_is_better"] is True and d["value"] > 0 and d["steps"] == 1
+    from rational_softmax_attention_gb300.inputs import ATTN_LONG_WIDE, RA_SOFTMAX_LONG_ROWS
+    assert d["config"] == json.loads(json.dumps(bench.step_config(ATTN_LONG_WIDE, RA_SOFTMAX_LONG_ROWS)))
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
