@@ -38,6 +38,15 @@
 //   values up to 65504), so the P V product runs in fp16 and P is rounded to 2^-11
 //   rather than 2^-8.  Q K^T stays in bf16.
 //
+// CTA pairs (D = 128, N_Q > 256): a cluster of two CTAs runs the same roles on four query
+// tiles.  Product g is one M = 256 tcgen05.mma (cta_group::2) issued by the even CTA's
+// issuer g: its rows 0..127 are the even CTA's tile g, rows 128..255 the odd CTA's, and
+// each CTA holds only its half of every K tile (64 keys) and V tile (64 columns).  Both
+// CTAs' copies complete on the even CTA's ring and Q barriers (the even producer arms them
+// for both); the issuer's commits land on both CTAs' barriers; the odd CTA's softmax warps
+// arrive on the even CTA's score-free and P-full barriers; the pair meets at a cluster
+// barrier after set-up and before the tensor memory is freed.
+//
 // phi on the FMA pipe: w = (1+u)/2 = 0.5 + (m - s)/32 (scaled units) computed with
 // one saturating FMA, so every u >= 1 (and every masked entry, fed as -inf) gives
 // w = 1; q = 1/w - 1; phi = ((q^2)^2)^2.  Four scores share two reciprocals: with the
