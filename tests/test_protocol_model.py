@@ -1,22 +1,24 @@
-"""A CPU model of the tensor-core forward kernel's barrier protocol, run on random schedules.
+"""CPU models of the tensor-core kernels' barrier protocols, run on random schedules.
 
-The kernel (attn_fwd_tc.cu) hands work between roles only through mbarriers: a TMA producer
-per CTA, one issuing thread per product g (in the even CTA of a CTA pair), and four softmax
-warps per query tile.  The model replays each role's waits, arrivals, copies, products and
-commits in the kernel's order, with the hardware's rules:
+The kernels hand work between roles only through mbarriers: TMA producers, MMA-issuing
+threads and softmax warps.  Each model replays every role's waits, arrivals, copies,
+products and commits in the kernel's order, with the hardware's rules:
   * a wait on phase k tests the parity of the barrier's phase counter, so it would pass
     wrongly if the barrier were one phase behind and block wrongly if it were two ahead;
   * a phase completes when its expected arrivals have come and its transaction bytes are in
     (copy bytes may land before the arming arrival);
   * copies and products complete asynchronously, a commit arrives once every product its
-    thread issued before it has completed, and a commit of a pair lands on both CTAs.
-For every random schedule it checks that all roles finish (no deadlock), that every wait
-sees exactly the phase it means, that every arrival and copy lands in the phase it is meant
-for, and that no buffer is rewritten while a reader still needs it: ring stages (K and V
-tiles), score buffers (including the O accumulator's columns used as the second pass-1
-buffer), P tiles and O accumulators.  Two planted protocol mistakes must be caught.
+    thread issued before it has completed, and a commit of a CTA pair lands on both CTAs.
+For every random schedule the engine checks that all roles finish (no deadlock), that every
+wait sees exactly the phase it means, and that every arrival and copy lands in the phase it
+is meant for; each model adds checks that no buffer is rewritten while a reader still needs
+it.  Planted protocol mistakes must be caught.
+
+Models: the forward (attn_fwd_tc.cu), as one CTA and as a CTA pair, and the dK/dV kernel
+of the backward (attn_bwd_tc.cu).
 """
 import random
+from collections import defaultdict
 
 import pytest
 
@@ -59,17 +61,82 @@ class Bar:
         return done
 
 
-class Model:
-    """One work item: NCTA CTAs (1, or a pair), two products (query tiles, or pairs of them)."""
+def require(cond, msg):
+    if not cond:
+        raise ProtocolError(msg)
+
+
+def run_roles(roles, rng, max_steps=400000):
+    """Run role generators to completion on a random schedule.  Actions:
+      ("wait", bar, k)            block until phase k of bar has completed
+      ("do", fn)                  run fn now (an arrival, a state change, a check)
+      ("copy", bar, k, fn)        start a copy whose bytes complete phase k of bar; fn on landing
+      ("mma", issuer, fn)         issue a product; fn when it completes (in issue order)
+      ("commit", issuer, arrivals) arrive on each (bar, phase) once the issuer's earlier products completed
+    """
+    state = [None] * len(roles)
+    alive = set(range(len(roles)))
+    tc = defaultdict(list)
+    copies = []
+
+    def advance(i):
+        try:
+            state[i] = next(roles[i])
+        except StopIteration:
+            alive.discard(i)
+            state[i] = None
+
+    for i in range(len(roles)):
+        advance(i)
+    for _ in range(max_steps):
+        if not alive and not copies and not any(tc.values()):
+            return
+        choices = [("role", i) for i in alive if state[i][0] != "wait" or state[i][1].test(state[i][2])]
+        if copies:
+            choices.append(("copy", None))
+        choices += [("tc", g) for g, q in tc.items() if q]
+        if not choices:
+            raise ProtocolError("deadlock: " + ", ".join(
+                f"{state[i][1].name} phase {state[i][2]}" for i in alive if state[i][0] == "wait"))
+        kind, i = rng.choice(choices)
+        if kind == "copy":
+            bar, phase, fn = copies.pop(rng.randrange(len(copies)))
+            bar.complete_tx(phase, 1)
+            if fn:
+                fn()
+        elif kind == "tc":
+            op, payload = tc[i].pop(0)
+            if op == "mma":
+                payload()
+            else:
+                for bar, phase in payload:
+                    bar.arrive(phase)
+        else:
+            a = state[i]
+            if a[0] == "copy":
+                copies.append((a[1], a[2], a[3]))
+            elif a[0] == "mma":
+                tc[a[1]].append(("mma", a[2]))
+            elif a[0] == "commit":
+                tc[a[1]].append(("commit", a[2]))
+            elif a[0] == "do":
+                a[1]()
+            advance(i)
+    raise ProtocolError("schedule did not finish")
+
+
+# ---------------------------------------------------------------------------- forward
+
+class ForwardModel:
+    """One work item of the forward: NCTA CTAs (1, or a pair), two products (query tiles, or
+    pairs of them), NST ring stages, nkt key tiles (nkt_g[g] of them needed by product g)."""
 
     NGROUP, WARPS = 2, 4
 
-    def __init__(self, ncta, nst, nkt, nkt_g, dead, rng, mutation=None):
-        self.ncta, self.nst, self.nkt, self.nkt_g, self.dead, self.rng = ncta, nst, nkt, nkt_g, dead, rng
-        self.mutation = mutation
+    def __init__(self, ncta, nst, nkt, nkt_g, dead, mutation=None):
+        self.ncta, self.nst, self.nkt, self.nkt_g, self.dead, self.mutation = ncta, nst, nkt, nkt_g, dead, mutation
         n, G, W = ncta, self.NGROUP, self.WARPS
         sw = W if mutation == "single_cta_counts" else n * W
-        # barriers that only the even CTA's copy is used of, and per-CTA barriers fed by commits
         self.q_full = Bar("q_full", 1)
         self.ring_full = [Bar(f"ring_full[{i}]", 1) for i in range(nst)]
         self.ring_empty = [[Bar(f"ring_empty[{i}]@{r}", G) for i in range(nst)] for r in range(n)]
@@ -78,18 +145,15 @@ class Model:
         self.p_full = [Bar(f"p_full[{g}]", sw) for g in range(G)]
         self.p_empty = [[Bar(f"p_empty[{g}]@{r}", 1) for g in range(G)] for r in range(n)]
         self.o_full = [[Bar(f"o_full[{g}]@{r}", 1) for g in range(G)] for r in range(n)]
-        # buffer state for the hazard checks
-        self.stage_use = [[-1] * nst for _ in range(n)]       # use whose copy has landed, per CTA
-        self.stage_readers = [dict() for _ in range(nst)]      # use -> products not yet complete
-        self.s_written = {}    # (g, b) -> uses whose product completed
-        self.s_readers = {}    # (g, b, use) -> warps still reading
-        self.p_written = {}    # (g, j) -> warps that wrote P
-        self.pv_done = set()   # (g, j) products complete
-        self.pv_issued = {g: 0 for g in range(G)}
-        self.events = []       # pending asynchronous completions: (ready_check, action, issuer)
-        self.issuer_outstanding = {g: 0 for g in range(G)}
+        self.stage_use = [[-1] * nst for _ in range(n)]   # use whose copy has landed, per CTA
+        self.stage_readers = [defaultdict(int) for _ in range(nst)]
+        self.s_written = defaultdict(set)    # (g, b) -> uses whose product completed
+        self.s_readers = defaultdict(int)    # (g, b, use) -> warps reading
+        self.p_written = defaultdict(set)    # (g, j) -> warps that wrote P
+        self.pv_done = set()
+        self.pv_issued = defaultdict(int)
+        self.outstanding = defaultdict(int)
 
-    # ------------------------------------------------------------------ roles
     def producer(self, r):
         n, nst = self.ncta, self.nst
         arms = r == 0
@@ -103,68 +167,70 @@ class Model:
         for it, _ in enumerate(fills):
             st, use = it % nst, it // nst
             yield ("wait", self.ring_empty[r][st], use - 1)
-            # every product that read this stage's previous use has completed
             for u, left in self.stage_readers[st].items():
-                if u < use and left:
-                    raise ProtocolError(f"stage {st} refilled (use {use}) while use {u} still has readers")
+                require(not (u < use and left), f"stage {st} refilled (use {use}) while use {u} still has readers")
             if arms:
                 yield ("do", lambda st=st, use=use: self.ring_full[st].arrive(use, tx=n))
-            yield ("copy", self.ring_full[st], use, (r, st, use))
+
+            def land(r=r, st=st, use=use):
+                self.stage_use[r][st] = use
+            yield ("copy", self.ring_full[st], use, land)
 
     def issuer(self, g):
-        n, nst, G = self.ncta, self.nst, self.NGROUP
+        n, nst = self.ncta, self.nst
         nkt, nkt_g = self.nkt, self.nkt_g[g]
         yield ("wait", self.q_full, 0)
-        pos = 0
         uses = [0, 0]
 
         def ring_wait(p):
             st, use = p % nst, p // nst
             yield ("wait", self.ring_full[st], use)
             for r in range(n):
-                if self.stage_use[r][st] != use:
-                    raise ProtocolError(f"product reads stage {st} use {use} before CTA {r}'s copy landed")
+                require(self.stage_use[r][st] == use, f"product reads stage {st} use {use} before CTA {r}'s copy landed")
 
         def release(p):
-            st, use = p % nst, p // nst
-            yield ("commit", g, [(self.ring_empty[r][st], use) for r in range(n)])
+            yield ("commit", g, [(self.ring_empty[r][p % nst], p // nst) for r in range(n)])
+
+        def product(reads_stage, done):
+            st, suse = reads_stage
+            self.stage_readers[st][suse] += 1
+            self.outstanding[g] += 1
+
+            def complete():
+                self.stage_readers[st][suse] -= 1
+                self.outstanding[g] -= 1
+                done()
+            return ("mma", g, complete)
 
         def mma_s(p, b):
             use = uses[b]
             yield ("wait", self.s_empty[g][b], use - 1)
-            if any(self.s_readers.get((g, b, u), 0) for u in range(use)):
-                raise ProtocolError(f"S[{g}][{b}] use {use} written while an earlier use is being read")
-            if b == 1 and self.pv_issued[g]:
-                raise ProtocolError(f"pass-1 S into O[{g}]'s columns after a P V product")
-            st, suse = p % nst, p // nst
-            self.stage_readers[st][suse] = self.stage_readers[st].get(suse, 0) + 1
-            yield ("mma", g, ("S", b, use, st, suse))
+            require(not any(self.s_readers[(g, b, u)] for u in range(use)),
+                    f"S[{g}][{b}] use {use} written while an earlier use is being read")
+            require(not (b == 1 and self.pv_issued[g]), f"pass-1 S into O[{g}]'s columns after a P V product")
+            yield product((p % nst, p // nst), lambda: self.s_written[(g, b)].add(use))
             yield ("commit", g, [(self.s_full[r][g][b], use) for r in range(n)])
             uses[b] += 1
 
         def mma_pv(j, p):
             yield ("wait", self.p_full[g], j)
-            if len(self.p_written.get((g, j), ())) != n * self.WARPS:
-                raise ProtocolError(f"P V product {j} issued before every warp wrote P[{g}]")
-            if any(self.s_readers.get((g, 1, u), 0) for u in range(uses[1])):
-                raise ProtocolError(f"P V product into O[{g}] while pass-1 scores in its columns are read")
-            if (g, j) not in self.dead:
-                st, suse = p % nst, p // nst
-                self.stage_readers[st][suse] = self.stage_readers[st].get(suse, 0) + 1
-                self.pv_issued[g] += 1
-                yield ("mma", g, ("PV", j, st, suse))
+            require(len(self.p_written[(g, j)]) == n * self.WARPS, f"P V product {j} issued before every warp wrote P[{g}]")
+            require(not any(self.s_readers[(g, 1, u)] for u in range(uses[1])),
+                    f"P V product into O[{g}] while pass-1 scores in its columns are read")
+            if (g, j) in self.dead:
+                self.pv_done.add((g, j))
             else:
-                yield ("mark_pv", g, j)
+                self.pv_issued[g] += 1
+                yield product((p % nst, p // nst), lambda: self.pv_done.add((g, j)))
             yield ("commit", g, [(self.p_empty[r][g], j) for r in range(n)])
 
+        skip_wait = self.mutation == "release_without_fill"
+        pos = 0
         for j in range(nkt):                                   # pass 1
-            if self.mutation == "release_without_fill" and j >= nkt_g:
-                yield from release(pos)
-                pos += 1
-                continue
-            yield from ring_wait(pos)
-            if j < nkt_g:
-                yield from mma_s(pos, j & 1)
+            if not (skip_wait and j >= nkt_g):
+                yield from ring_wait(pos)
+                if j < nkt_g:
+                    yield from mma_s(pos, j & 1)
             yield from release(pos)
             pos += 1
         yield from ring_wait(pos)                              # pass 2: S(0)
@@ -173,24 +239,18 @@ class Model:
         pos += 1
         for j in range(nkt):
             if j + 1 < nkt:
-                kpos = pos
-                pos += 1
-                if self.mutation == "release_without_fill" and j + 1 >= nkt_g:
-                    yield from release(kpos)
-                else:
-                    yield from ring_wait(kpos)
+                if not (skip_wait and j + 1 >= nkt_g):
+                    yield from ring_wait(pos)
                     if j + 1 < nkt_g:
-                        yield from mma_s(kpos, 0)
-                    yield from release(kpos)
-            vpos = pos
+                        yield from mma_s(pos, 0)
+                yield from release(pos)
+                pos += 1
+            if not (skip_wait and j >= nkt_g):
+                yield from ring_wait(pos)
+                if j < nkt_g:
+                    yield from mma_pv(j, pos)
+            yield from release(pos)
             pos += 1
-            if self.mutation == "release_without_fill" and j >= nkt_g:
-                yield from release(vpos)
-                continue
-            yield from ring_wait(vpos)
-            if j < nkt_g:
-                yield from mma_pv(j, vpos)
-            yield from release(vpos)
         yield ("commit", g, [(self.o_full[r][g], 0) for r in range(n)])
 
     def softmax(self, r, g, w):
@@ -198,12 +258,10 @@ class Model:
 
         def take(b, use):
             yield ("wait", self.s_full[r][g][b], use)
-            if use not in self.s_written.get((g, b), ()):
-                raise ProtocolError(f"S[{g}][{b}] use {use} read before its product completed")
-            key = (g, b, use)
-            self.s_readers[key] = self.s_readers.get(key, 0) + 1
-            yield ("yield",)
-            self.s_readers[key] -= 1
+            require(use in self.s_written[(g, b)], f"S[{g}][{b}] use {use} read before its product completed")
+            self.s_readers[(g, b, use)] += 1
+            yield ("do", lambda: None)
+            self.s_readers[(g, b, use)] -= 1
             yield ("do", lambda: self.s_empty[g][b].arrive(use))
 
         for j in range(nkt_g):                                 # pass 1
@@ -212,121 +270,234 @@ class Model:
         for j in range(nkt_g):                                 # pass 2
             yield from take(0, sidx)
             sidx += 1
-            yield ("wait", self.p_empty[r][g], j - 1)
-            if j > 0 and (g, j - 1) not in self.pv_done:
-                raise ProtocolError(f"P[{g}] rewritten (tile {j}) before P V product {j - 1} completed")
-            self.p_written.setdefault((g, j), set()).add((r, w))
+            if self.mutation != "no_p_free_wait":
+                yield ("wait", self.p_empty[r][g], j - 1)
+            require(j == 0 or (g, j - 1) in self.pv_done, f"P[{g}] rewritten (tile {j}) before P V product {j - 1} completed")
+            self.p_written[(g, j)].add((r, w))
             yield ("do", lambda j=j: self.p_full[g].arrive(j))
         yield ("wait", self.o_full[r][g], 0)
-        if self.pv_issued[g] and self.issuer_outstanding[g]:
-            raise ProtocolError(f"O[{g}] read while products are outstanding")
+        require(self.outstanding[g] == 0, f"O[{g}] read while products are outstanding")
 
-    # ------------------------------------------------------------------ scheduler
-    def run(self):
-        roles = [self.producer(r) for r in range(self.ncta)]
-        roles += [self.issuer(g) for g in range(self.NGROUP)]
-        roles += [self.softmax(r, g, w) for r in range(self.ncta) for g in range(self.NGROUP) for w in range(self.WARPS)]
-        state = [None] * len(roles)   # the action a role is blocked on
-        alive = set(range(len(roles)))
-        commits = {g: [] for g in range(self.NGROUP)}   # per issuer, in issue order: ("mma"|"commit", payload)
-        copies = []
-
-        def advance(i):
-            try:
-                state[i] = next(roles[i])
-            except StopIteration:
-                alive.discard(i)
-                state[i] = None
-
-        for i in range(len(roles)):
-            advance(i)
-        for _ in range(200000):
-            if not alive and not copies and not any(commits.values()):
-                return
-            choices = []
-            for i in list(alive):
-                a = state[i]
-                if a[0] == "wait":
-                    if a[1].test(a[2]):
-                        choices.append(("role", i))
-                else:
-                    choices.append(("role", i))
-            if copies:
-                choices.append(("copy", None))
-            for g, q in commits.items():
-                if q:
-                    choices.append(("tc", g))
-            if not choices:
-                raise ProtocolError("deadlock: " + ", ".join(
-                    f"{state[i][1].name} phase {state[i][2]}" for i in alive if state[i][0] == "wait"))
-            kind, i = self.rng.choice(choices)
-            if kind == "copy":
-                bar, phase, tag = copies.pop(self.rng.randrange(len(copies)))
-                bar.complete_tx(phase, 1)
-                if tag is not None:
-                    r, st, use = tag
-                    self.stage_use[r][st] = use
-                continue
-            if kind == "tc":                  # the oldest tensor-core operation of issuer i completes
-                op, payload = commits[i].pop(0)
-                if op == "mma":
-                    self.issuer_outstanding[i] -= 1
-                    if payload[0] == "S":
-                        _, b, use, st, suse = payload
-                        self.s_written.setdefault((i, b), set()).add(use)
-                    else:
-                        _, j, st, suse = payload
-                        self.pv_done.add((i, j))
-                    self.stage_readers[st][suse] -= 1
-                elif op == "mark":
-                    self.pv_done.add((i, payload))
-                else:
-                    for bar, phase in payload:
-                        bar.arrive(phase)
-                continue
-            a = state[i]
-            if a[0] == "copy":
-                copies.append((a[1], a[2], a[3]))
-            elif a[0] == "mma":
-                self.issuer_outstanding[a[1]] += 1
-                commits[a[1]].append(("mma", a[2]))
-            elif a[0] == "mark_pv":
-                commits[a[1]].append(("mark", a[2]))
-            elif a[0] == "commit":
-                commits[a[1]].append(("commit", a[2]))
-            elif a[0] == "do":
-                a[1]()
-            advance(i)
-        raise ProtocolError("schedule did not finish")
+    def roles(self):
+        out = [self.producer(r) for r in range(self.ncta)] + [self.issuer(g) for g in range(self.NGROUP)]
+        return out + [self.softmax(r, g, w) for r in range(self.ncta) for g in range(self.NGROUP)
+                      for w in range(self.WARPS)]
 
 
-CONFIGS = [
+FWD_CONFIGS = [
     # (CTAs, ring stages, key tiles, key tiles of product 0, dead fraction)
     (1, 3, 1, 1, 0.0), (1, 3, 4, 4, 0.0), (1, 3, 5, 4, 0.3), (1, 6, 3, 3, 0.5), (1, 6, 7, 6, 0.0),
     (2, 6, 1, 1, 0.0), (2, 6, 4, 4, 0.0), (2, 6, 5, 3, 0.3), (2, 6, 9, 7, 0.2), (2, 6, 2, 1, 0.0),
 ]
 
 
-@pytest.mark.parametrize("ncta,nst,nkt,nkt0,dead_frac", CONFIGS)
+@pytest.mark.parametrize("ncta,nst,nkt,nkt0,dead_frac", FWD_CONFIGS)
 def test_forward_protocol_holds_on_random_schedules(ncta, nst, nkt, nkt0, dead_frac):
     for seed in range(60):
         rng = random.Random(seed * 1000 + nkt * 10 + ncta)
         dead = {(g, j) for g in range(2) for j in range(nkt) if rng.random() < dead_frac}
-        Model(ncta, nst, nkt, (nkt0, nkt), dead, rng).run()
+        run_roles(ForwardModel(ncta, nst, nkt, (nkt0, nkt), dead).roles(), rng)
+
+
+def _caught(make, seeds=300):
+    for seed in range(seeds):
+        try:
+            run_roles(make().roles(), random.Random(seed))
+        except ProtocolError:
+            return True
+    return False
 
 
 @pytest.mark.parametrize("mutation,ncta,nkt,nkt0", [("release_without_fill", 1, 6, 3),
                                                     ("release_without_fill", 2, 6, 2),
-                                                    ("single_cta_counts", 2, 3, 3)])
-def test_planted_protocol_mistakes_are_caught(mutation, ncta, nkt, nkt0):
+                                                    ("single_cta_counts", 2, 3, 3),
+                                                    ("no_p_free_wait", 1, 4, 4),
+                                                    ("no_p_free_wait", 2, 4, 4)])
+def test_planted_forward_protocol_mistakes_are_caught(mutation, ncta, nkt, nkt0):
     """Releasing ring stages without waiting for their fill lets the issuer that skips tiles
     run a phase ahead; counting one CTA's warps on the pair's barriers completes a phase
-    early.  Some schedule must expose each."""
-    caught = False
-    for seed in range(200):
-        try:
-            Model(ncta, 6 if ncta == 2 else 3, nkt, (nkt0, nkt), set(), random.Random(seed), mutation).run()
-        except ProtocolError:
-            caught = True
-            break
-    assert caught
+    early; skipping the P-free wait rewrites P under a running product."""
+    assert _caught(lambda: ForwardModel(ncta, 6 if ncta == 2 else 3, nkt, (nkt0, nkt), set(), mutation))
+
+
+# ---------------------------------------------------------------------------- dK/dV kernel
+
+class DkdvModel:
+    """One key tile of the dK/dV kernel over nq query tiles: a producer (Q and dO tiles in
+    rings of NQS and NDS slots, the per-query constants X and Y as bulk copies), issuer 0
+    (S^T = K Q^T and dP^T = V dO^T), issuer 1 (dV += P^T dO, P^T read from tensor memory over
+    the S^T columns, then dK += dS^T Q) and the softmax warps (P^T into tensor memory, dS^T
+    into a shared tile)."""
+
+    def __init__(self, nq, nqs, nds, warps=4, mutation=None):
+        self.nq, self.nqs, self.nds, self.W, self.mutation = nq, nqs, nds, warps, mutation
+        W = warps
+        self.kv_full = Bar("kv_full", 1)
+        self.q_full = [Bar(f"q_full[{i}]", 1) for i in range(nqs)]
+        self.q_empty = [Bar(f"q_empty[{i}]", 2) for i in range(nqs)]
+        self.do_full = [Bar(f"do_full[{i}]", 1) for i in range(nds)]
+        self.do_empty = [Bar(f"do_empty[{i}]", 2) for i in range(nds)]
+        self.st_full = Bar("st_full", 2)      # issuer 0's commit + the producer's arming for X
+        self.dpt_full = Bar("dpt_full", 2)    # issuer 0's commit + the producer's arming for Y
+        self.dpt_free = Bar("dpt_free", W)
+        self.p_full = Bar("p_full", W)
+        self.p_free = Bar("p_free", 1)
+        self.acc_full = Bar("acc_full", 1)
+        self.cx_empty = Bar("cx_empty", W)
+        self.cy_empty = Bar("cy_empty", W)
+        self.ds_full = Bar("ds_full", W)
+        self.ds_free = Bar("ds_free", 1)
+        # data state
+        self.q_slot = [-1] * nqs          # tile whose Q has landed in each slot
+        self.do_slot = [-1] * nds
+        self.q_readers = defaultdict(int)  # tile -> products reading its Q
+        self.do_readers = defaultdict(int)
+        self.x_tile = self.y_tile = -1     # constants that have landed
+        self.x_readers = defaultdict(int)
+        self.y_readers = defaultdict(int)
+        self.st_state = ("empty", -1)      # tensor-memory S^T columns: ("S", it) or ("P", it)
+        self.st_readers = 0
+        self.pt_written = defaultdict(set)
+        self.dpt_tile, self.dpt_readers = -1, 0
+        self.ds_written = defaultdict(set)
+        self.ds_reading = -1               # tile whose dS^T the running dK product reads
+        self.outstanding = 0
+
+    def producer(self):
+        nq, nqs, nds = self.nq, self.nqs, self.nds
+        yield ("do", lambda: self.kv_full.arrive(0, tx=1))
+        yield ("copy", self.kv_full, 0, None)
+        for it in range(nq):
+            qs, ds = it % nqs, it % nds
+            yield ("wait", self.q_empty[qs], it // nqs - 1)
+            require(not any(v for t, v in self.q_readers.items() if t < it and t % nqs == qs),
+                    f"Q slot {qs} refilled (tile {it}) while read")
+            yield ("do", lambda qs=qs, it=it: self.q_full[qs].arrive(it // nqs, tx=1))
+            yield ("copy", self.q_full[qs], it // nqs, lambda qs=qs, it=it: self.q_slot.__setitem__(qs, it))
+            yield ("wait", self.cx_empty, it - 1)
+            require(not any(v for t, v in self.x_readers.items() if t < it), f"X rewritten (tile {it}) while read")
+            yield ("do", lambda it=it: self.st_full.arrive(it, tx=1))
+            yield ("copy", self.st_full, it, lambda it=it: setattr(self, "x_tile", it))
+            yield ("wait", self.do_empty[ds], it // nds - 1)
+            require(not any(v for t, v in self.do_readers.items() if t < it and t % nds == ds),
+                    f"dO slot {ds} refilled (tile {it}) while read")
+            yield ("do", lambda ds=ds, it=it: self.do_full[ds].arrive(it // nds, tx=1))
+            yield ("copy", self.do_full[ds], it // nds, lambda ds=ds, it=it: self.do_slot.__setitem__(ds, it))
+            yield ("wait", self.cy_empty, it - 1)
+            if self.mutation != "y_before_dk":
+                yield ("wait", self.ds_free, it - 1)
+            require(not any(v for t, v in self.y_readers.items() if t < it), f"Y rewritten (tile {it}) while read")
+            yield ("do", lambda it=it: self.dpt_full.arrive(it, tx=1))
+            yield ("copy", self.dpt_full, it, lambda it=it: setattr(self, "y_tile", it))
+
+    def _product(self, who, done):
+        self.outstanding += 1
+
+        def complete():
+            self.outstanding -= 1
+            done()
+        return ("mma", who, complete)
+
+    def issuer0(self):
+        nqs, nds = self.nqs, self.nds
+        yield ("wait", self.kv_full, 0)
+        for it in range(self.nq):
+            qs, ds = it % nqs, it % nds
+            yield ("wait", self.q_full[qs], it // nqs)
+            yield ("wait", self.p_free, it - 1)
+            require(self.q_slot[qs] == it, f"S^T of tile {it} issued before its Q landed")
+            require(self.st_readers == 0 and (it == 0 or self.st_state == ("P", it - 1) and self.pt_read_done),
+                    f"S^T of tile {it} overwrites the S^T/P^T columns while in use")
+            self.q_readers[it] += 1
+
+            def s_done(it=it):
+                self.q_readers[it] -= 1
+                self.st_state = ("S", it)
+                self.pt_read_done = False
+            yield self._product(0, s_done)
+            yield ("commit", 0, [(self.st_full, it), (self.q_empty[qs], it // nqs)])
+            yield ("wait", self.do_full[ds], it // nds)
+            yield ("wait", self.dpt_free, it - 1)
+            require(self.do_slot[ds] == it, f"dP^T of tile {it} issued before its dO landed")
+            require(self.dpt_readers == 0, f"dP^T of tile {it} overwrites the dP^T columns while read")
+            self.do_readers[it] += 1
+
+            def dp_done(it=it):
+                self.do_readers[it] -= 1
+                self.dpt_tile = it
+            yield self._product(0, dp_done)
+            yield ("commit", 0, [(self.dpt_full, it), (self.do_empty[ds], it // nds)])
+
+    def issuer1(self):
+        nqs, nds = self.nqs, self.nds
+        yield ("wait", self.kv_full, 0)
+        for it in range(self.nq):
+            qs, ds = it % nqs, it % nds
+            yield ("wait", self.q_full[qs], it // nqs)
+            yield ("wait", self.do_full[ds], it // nds)
+            yield ("wait", self.p_full, it)
+            require(len(self.pt_written[it]) == self.W and self.st_state == ("P", it),
+                    f"dV of tile {it} issued before every warp wrote P^T")
+            self.do_readers[it] += 1
+
+            def dv_done(it=it):
+                self.do_readers[it] -= 1
+                self.pt_read_done = True
+            yield self._product(1, dv_done)
+            yield ("commit", 1, [(self.do_empty[ds], it // nds), (self.p_free, it)])
+            yield ("wait", self.ds_full, it)
+            require(len(self.ds_written[it]) == self.W, f"dK of tile {it} issued before every warp wrote dS^T")
+            self.q_readers[it] += 1
+            self.ds_reading = it
+
+            def dk_done(it=it):
+                self.q_readers[it] -= 1
+                self.ds_reading = -1
+            yield self._product(1, dk_done)
+            yield ("commit", 1, [(self.q_empty[qs], it // nqs), (self.ds_free, it)])
+        yield ("commit", 1, [(self.acc_full, 0)])
+
+    def softmax(self, w):
+        for it in range(self.nq):
+            yield ("wait", self.st_full, it)
+            require(self.st_state == ("S", it) and self.x_tile == it, f"warp reads S^T/X of tile {it} before they are in")
+            self.st_readers += 1
+            self.x_readers[it] += 1
+            yield ("do", lambda: None)
+            self.st_readers -= 1
+            self.x_readers[it] -= 1
+            self.pt_written[it].add(w)
+            if len(self.pt_written[it]) == self.W:
+                self.st_state = ("P", it)
+            yield ("do", lambda it=it: (self.cx_empty.arrive(it), self.p_full.arrive(it)))
+            yield ("wait", self.dpt_full, it)
+            require(self.dpt_tile == it and self.y_tile == it, f"warp reads dP^T/Y of tile {it} before they are in")
+            self.dpt_readers += 1
+            yield ("do", lambda: None)
+            self.dpt_readers -= 1
+            yield ("do", lambda it=it: self.dpt_free.arrive(it))
+            self.y_readers[it] += 1
+            require(self.ds_reading < 0, f"dS^T tile rewritten (tile {it}) while dK of tile {self.ds_reading} reads it")
+            self.ds_written[it].add(w)
+            yield ("do", lambda: None)
+            self.y_readers[it] -= 1
+            yield ("do", lambda it=it: (self.cy_empty.arrive(it), self.ds_full.arrive(it)))
+        if self.nq > 0:
+            yield ("wait", self.acc_full, 0)
+            require(self.outstanding == 0, "dK/dV accumulators read while products are outstanding")
+
+    def roles(self):
+        self.pt_read_done = False
+        return [self.producer(), self.issuer0(), self.issuer1()] + [self.softmax(w) for w in range(self.W)]
+
+
+@pytest.mark.parametrize("nq,nqs,nds", [(1, 2, 2), (2, 2, 2), (5, 2, 2), (6, 3, 2), (7, 2, 3)])
+def test_dkdv_protocol_holds_on_random_schedules(nq, nqs, nds):
+    for seed in range(80):
+        run_roles(DkdvModel(nq, nqs, nds).roles(), random.Random(seed * 100 + nq))
+
+
+def test_planted_dkdv_protocol_mistake_is_caught():
+    """Issuing Y (and with it the dP^T-complete phase) before dK has read the previous dS^T
+    tile lets a warp overwrite that tile under the running dK product."""
+    assert _caught(lambda: DkdvModel(5, 2, 2, mutation="y_before_dk"))
