@@ -94,8 +94,8 @@ struct DqCfg {
   static constexpr int OFF_V = OFF_K + NKS * TILE;
   static constexpr int OFF_BAR = OFF_V + NVS * TILE;
   // qdo_full, k_full[NKS], k_empty[NKS], v_full[NVS], v_empty[NVS], s_full[2], e_free[2],
-  // dp_full, dp_free, e_full, dq_full, drain[2]
-  static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 10;
+  // dp_full, dp_free, e_full[2], dq_full, drain[2]
+  static constexpr int NUM_BARS = 1 + 2 * NKS + 2 * NVS + 11;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_XCH = OFF_MISC + 16;   // [4][128] floats: per-part partials of D_i, then R_i
   static constexpr int USED = OFF_XCH + 4 * BM * 4;
@@ -151,8 +151,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint64_t* e_free = s_full + 2;
   uint64_t* dp_full = e_free + 2;
   uint64_t* dp_free = dp_full + 1;
+  // e_full[b]: every softmax warp has written E into score buffer b.  One barrier per
+  // buffer: a warp that has finished tile j may finish tile j + 1 (dP_{j+1} waits only for
+  // dp_free) before a slower warp's arrival for tile j, but never tile j + 2 (S_{j+2} waits
+  // for the dQ product of tile j), so arrivals for consecutive tiles never share a phase.
   uint64_t* e_full = dp_free + 1;
-  uint64_t* dq_full = e_full + 1;
+  uint64_t* dq_full = e_full + 2;
   uint64_t* drain = dq_full + 1;   // [2], one per issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -184,7 +188,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
     mbar_init(dp_full, 1);
     mbar_init(dp_free, DQ_SOFTMAX_WARPS);
-    mbar_init(e_full, DQ_SOFTMAX_WARPS);
+    mbar_init(&e_full[0], DQ_SOFTMAX_WARPS);
+    mbar_init(&e_full[1], DQ_SOFTMAX_WARPS);
     mbar_init(dq_full, 1);
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       } else {
         for (int t = 0; t < nkt && ok; ++t) {   // dQ += E_t K_t
           const int ks = t % C::NKS;
-          ok = mbar_wait(e_full, t & 1u, abort_flag, ctx) &&
+          ok = mbar_wait(&e_full[t & 1], (t >> 1) & 1u, abort_flag, ctx) &&
                mbar_wait(&k_full[ks], (t / C::NKS) & 1u, abort_flag, ctx);
           if (!ok) break;
           tc_fence_after();
@@ -436,7 +441,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(e_full);
+      if (lane == 0) mbar_arrive(&e_full[sb]);
     }
 #undef SV
     // R_i over the parts (reached by every softmax warp, also after a wait gave up)

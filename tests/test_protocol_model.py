@@ -14,8 +14,8 @@ wait sees exactly the phase it means, and that every arrival and copy lands in t
 is meant for; each model adds checks that no buffer is rewritten while a reader still needs
 it.  Planted protocol mistakes must be caught.
 
-Models: the forward (attn_fwd_tc.cu), as one CTA and as a CTA pair, and the dK/dV kernel
-of the backward (attn_bwd_tc.cu).
+Models: the forward (attn_fwd_tc.cu), as one CTA and as a CTA pair, and both kernels of
+the backward (attn_bwd_tc.cu).
 """
 import random
 from collections import defaultdict
@@ -501,3 +501,150 @@ def test_planted_dkdv_protocol_mistake_is_caught():
     """Issuing Y (and with it the dP^T-complete phase) before dK has read the previous dS^T
     tile lets a warp overwrite that tile under the running dK product."""
     assert _caught(lambda: DkdvModel(5, 2, 2, mutation="y_before_dk"))
+
+
+# ---------------------------------------------------------------------------- dQ kernel
+
+class DqModel:
+    """One query tile of the dQ kernel over nkt key tiles: a producer (K and V tiles in rings
+    of NKS and NVS slots), issuer 0 (S_j = Q K_j^T into score buffer j & 1, dP_j = dO V_j^T),
+    issuer 1 (dQ += E_t K_t, E read from tensor memory) and the softmax warps (E_j written
+    over the S_j columns they have read)."""
+
+    def __init__(self, nkt, nks, nvs, warps=4, mutation=None):
+        self.nkt, self.nks, self.nvs, self.W, self.mutation = nkt, nks, nvs, warps, mutation
+        W = warps
+        self.qdo_full = Bar("qdo_full", 1)
+        self.k_full = [Bar(f"k_full[{i}]", 1) for i in range(nks)]
+        self.k_empty = [Bar(f"k_empty[{i}]", 2) for i in range(nks)]   # S_j and dQ_j read K_j
+        self.v_full = [Bar(f"v_full[{i}]", 1) for i in range(nvs)]
+        self.v_empty = [Bar(f"v_empty[{i}]", 1) for i in range(nvs)]
+        self.s_full = [Bar(f"s_full[{b}]", 1) for b in range(2)]
+        self.e_free = [Bar(f"e_free[{b}]", 1) for b in range(2)]
+        self.dp_full = Bar("dp_full", 1)
+        self.dp_free = Bar("dp_free", W)
+        # one barrier per score buffer; "single_e_full" plants the earlier form that shared one
+        self.e_full = [Bar("e_full", W)] * 2 if mutation == "single_e_full" else [Bar(f"e_full[{b}]", W) for b in range(2)]
+        self.dq_full = Bar("dq_full", 1)
+        self.k_slot = [-1] * nks
+        self.v_slot = [-1] * nvs
+        self.k_readers = defaultdict(int)
+        self.v_readers = defaultdict(int)
+        self.buf = [("empty", -1), ("empty", -1)]   # score buffer b: ("S", j) or ("E", j)
+        self.buf_readers = [0, 0]                   # warps reading S, or the dQ product reading E
+        self.e_written = defaultdict(set)
+        self.dp_tile, self.dp_readers = -1, 0
+        self.outstanding = 0
+
+    def producer(self):
+        yield ("do", lambda: self.qdo_full.arrive(0, tx=1))
+        yield ("copy", self.qdo_full, 0, None)
+        for j in range(self.nkt):
+            ks, vs = j % self.nks, j % self.nvs
+            yield ("wait", self.k_empty[ks], j // self.nks - 1)
+            require(not any(v for t, v in self.k_readers.items() if t < j and t % self.nks == ks),
+                    f"K slot {ks} refilled (tile {j}) while read")
+            yield ("do", lambda ks=ks, j=j: self.k_full[ks].arrive(j // self.nks, tx=1))
+            yield ("copy", self.k_full[ks], j // self.nks, lambda ks=ks, j=j: self.k_slot.__setitem__(ks, j))
+            yield ("wait", self.v_empty[vs], j // self.nvs - 1)
+            require(not any(v for t, v in self.v_readers.items() if t < j and t % self.nvs == vs),
+                    f"V slot {vs} refilled (tile {j}) while read")
+            yield ("do", lambda vs=vs, j=j: self.v_full[vs].arrive(j // self.nvs, tx=1))
+            yield ("copy", self.v_full[vs], j // self.nvs, lambda vs=vs, j=j: self.v_slot.__setitem__(vs, j))
+
+    def _product(self, who, done):
+        self.outstanding += 1
+
+        def complete():
+            self.outstanding -= 1
+            done()
+        return ("mma", who, complete)
+
+    def issuer0(self):
+        yield ("wait", self.qdo_full, 0)
+        for j in range(self.nkt):
+            ks, vs, sb = j % self.nks, j % self.nvs, j & 1
+            yield ("wait", self.k_full[ks], j // self.nks)
+            if self.mutation != "no_e_free_wait":
+                yield ("wait", self.e_free[sb], (j >> 1) - 1)
+            require(self.k_slot[ks] == j, f"S_{j} issued before K_{j} landed")
+            require(self.buf_readers[sb] == 0 and (j < 2 or self.buf[sb] == ("E", j - 2) and self.e_read[j - 2]),
+                    f"S_{j} overwrites score buffer {sb} while in use")
+            self.k_readers[j] += 1
+
+            def s_done(j=j, sb=sb):
+                self.k_readers[j] -= 1
+                self.buf[sb] = ("S", j)
+            yield self._product(0, s_done)
+            yield ("commit", 0, [(self.s_full[sb], j >> 1), (self.k_empty[ks], j // self.nks)])
+            yield ("wait", self.v_full[vs], j // self.nvs)
+            yield ("wait", self.dp_free, j - 1)
+            require(self.v_slot[vs] == j, f"dP_{j} issued before V_{j} landed")
+            require(self.dp_readers == 0, f"dP_{j} overwrites the dP columns while read")
+            self.v_readers[j] += 1
+
+            def dp_done(j=j):
+                self.v_readers[j] -= 1
+                self.dp_tile = j
+            yield self._product(0, dp_done)
+            yield ("commit", 0, [(self.v_empty[vs], j // self.nvs), (self.dp_full, j)])
+
+    def issuer1(self):
+        yield ("wait", self.qdo_full, 0)
+        for t in range(self.nkt):
+            ks, sb = t % self.nks, t & 1
+            yield ("wait", self.e_full[sb], t if self.mutation == "single_e_full" else t >> 1)
+            yield ("wait", self.k_full[ks], t // self.nks)
+            require(len(self.e_written[t]) == self.W and self.buf[sb] == ("E", t), f"dQ_{t} issued before every warp wrote E")
+            require(self.k_slot[ks] == t, f"dQ_{t} issued before K_{t} landed")
+            self.k_readers[t] += 1
+            self.buf_readers[sb] += 1
+
+            def dq_done(t=t, sb=sb):
+                self.k_readers[t] -= 1
+                self.buf_readers[sb] -= 1
+                self.e_read[t] = True
+            yield self._product(1, dq_done)
+            yield ("commit", 1, [(self.k_empty[ks], t // self.nks), (self.e_free[sb], t >> 1)])
+        yield ("commit", 1, [(self.dq_full, 0)])
+
+    def softmax(self, w):
+        for j in range(self.nkt):
+            sb = j & 1
+            yield ("wait", self.s_full[sb], j >> 1)
+            require(self.buf[sb] == ("S", j), f"warp reads S_{j} before its product completed")
+            self.buf_readers[sb] += 1
+            yield ("do", lambda: None)
+            self.buf_readers[sb] -= 1
+            yield ("wait", self.dp_full, j)
+            require(self.dp_tile == j, f"warp reads dP_{j} before its product completed")
+            self.dp_readers += 1
+            yield ("do", lambda: None)
+            self.dp_readers -= 1
+            yield ("do", lambda j=j: self.dp_free.arrive(j))
+            self.e_written[j].add(w)
+            if len(self.e_written[j]) == self.W:
+                self.buf[sb] = ("E", j)
+            yield ("do", lambda j=j, sb=sb: self.e_full[sb].arrive(j if self.mutation == "single_e_full" else j >> 1))
+        yield ("wait", self.dq_full, 0)
+        require(self.outstanding == 0, "dQ accumulator read while products are outstanding")
+
+    def roles(self):
+        self.e_read = defaultdict(bool)
+        return [self.producer(), self.issuer0(), self.issuer1()] + [self.softmax(w) for w in range(self.W)]
+
+
+@pytest.mark.parametrize("nkt,nks,nvs", [(1, 2, 2), (2, 2, 2), (5, 2, 2), (6, 3, 2), (7, 2, 3)])
+def test_dq_protocol_holds_on_random_schedules(nkt, nks, nvs):
+    for seed in range(80):
+        run_roles(DqModel(nkt, nks, nvs).roles(), random.Random(seed * 100 + nkt))
+
+
+@pytest.mark.parametrize("mutation", ["no_e_free_wait", "single_e_full"])
+def test_planted_dq_protocol_mistakes_are_caught(mutation):
+    """Issuing S_{j+2} without waiting for the dQ product that reads E_j from the same
+    buffer overwrites E_j under that product.  One E-complete barrier for both buffers (the
+    kernel's earlier form) lets a warp that has finished tile j + 1 arrive while a slower
+    warp's arrival for tile j is still missing: the phase of tile j would complete early."""
+    # three K stages, as in the kernel: with two, refilling K_{j+2} already waits for dQ_j
+    assert _caught(lambda: DqModel(5, 3, 2, mutation=mutation))
