@@ -3,9 +3,10 @@
 fp32 inputs (CUDA-core path): max-abs 2e-5 on dq, dk, dv.
 bf16 inputs (tensor-core path): max-abs 1e-2 and mean-abs 1e-3 on dq, dk, dv
 (fp32 gradients), on the same bf16-rounded inputs.  Where the GPU's argmax
-differs from the oracle's, the two candidates must be a near-tie (top-2 gap
-below 1e-3 max(1, |m|)); the oracle then follows the GPU's branch of the
-(non-differentiable at a tie) max.
+differs from the oracle's lowest-index one, the two keys' float64 scores must
+lie within twice the fp32 score-error bound (parity.check_argmax); the oracle
+then follows the GPU's branch of the (non-differentiable at a tie) max.
+Exact ties, with no exemption at all, are tested in test_gpu_argmax_ties.py.
 """
 import numpy as np
 import pytest
@@ -86,14 +87,13 @@ def check_bf16_heads(q, k, v, do, scale, causal, heads=None):
         S = scale * (qd @ kd.T)
         if causal:
             S = np.where(np.arange(nk)[None, :] <= np.arange(nq)[:, None], S, -np.inf)
-        a_or = np.argmax(S, axis=-1)
         a_gpu = ra_[b, h].cpu().numpy().astype(np.int64)
-        diff = np.nonzero(a_gpu != a_or)[0]
-        for i in diff:
-            m = S[i, a_or[i]]
-            assert S[i, a_gpu[i]] >= m - 1e-3 * max(1.0, abs(m)), f"row {i}: argmax differs beyond a near-tie"
-        ties += len(diff)
-        gq, gk, gv = oracle.ra_attention_head_bwd(qd, kd, vd, dod, scale, causal, argmax=a_gpu)
+        nd = parity.check_argmax(S, a_gpu, parity.score_error_bound(qd, kd, scale),
+                                 f"backward [{b},{h}] {tuple(q.shape)} x {nk}")
+        ties += nd
+        # the oracle's own (lowest-index) branch, unless a near tie made the GPU take the other
+        # key: then the oracle follows the GPU's branch of the max (either is a valid gradient)
+        gq, gk, gv = oracle.ra_attention_head_bwd(qd, kd, vd, dod, scale, causal, argmax=a_gpu if nd else None)
         parity.assert_close_bf16(parity.f64(dq[b, h]), gq, f"dq[{b},{h}]")
         parity.assert_close_bf16(parity.f64(dk[b, h]), gk, f"dk[{b},{h}]")
         parity.assert_close_bf16(parity.f64(dv[b, h]), gv, f"dv[{b},{h}]")
@@ -146,8 +146,8 @@ def test_bf16_autograd_function_bf16_gradients():
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp32_backward_at_scale(causal):
     """fp32 inputs at N = 2048, D = 128: dq, dk, dv of a whole head against the oracle within
-    2e-5.  The oracle follows the GPU's argmax, which must be a near-maximum where the two
-    differ."""
+    2e-5.  Where the GPU's argmax differs from the oracle's, it must be a near tie within the
+    fp32 score-error bound, and the oracle follows it."""
     scale = 128 ** -0.5
     q, k, v, do = attention_inputs(1, 1, 2048, 2048, 128, seed=31 + int(causal), dtype=torch.float32)
     qg, kg, vg, dog = q.cuda(), k.cuda(), v.cuda(), do.cuda()
@@ -160,9 +160,8 @@ def test_fp32_backward_at_scale(causal):
     S = scale * (qd @ kd.T)
     if causal:
         S = np.where(np.tril(np.ones_like(S, dtype=bool)), S, -np.inf)
-    m = S.max(axis=1)
-    assert np.all(S[np.arange(2048), a_gpu] >= m - 1e-3 * np.maximum(1.0, np.abs(m)))
-    rq, rk, rv = oracle.ra_attention_head_bwd(qd, kd, vd, dod, scale, causal, argmax=a_gpu)
+    nd = parity.check_argmax(S, a_gpu, parity.score_error_bound(qd, kd, scale), f"fp32 backward N2048 causal={causal}")
+    rq, rk, rv = oracle.ra_attention_head_bwd(qd, kd, vd, dod, scale, causal, argmax=a_gpu if nd else None)
     parity.assert_close_fp32(parity.f64(dq[0, 0]), rq, "dq")
     parity.assert_close_fp32(parity.f64(dk[0, 0]), rk, "dk")
     parity.assert_close_fp32(parity.f64(dv[0, 0]), rv, "dv")

@@ -28,35 +28,24 @@ def gpu_fwd(q, k, v, scale, causal, out_dtype=torch.float32):
     return o, rm, rs, ra_, counts
 
 
-def near_tie_rows(S_rows, m, causal_rows=None):
-    """Rows whose top-2 scaled score gap is below 1e-3 max(1, |m|): the argmax may legitimately differ."""
-    srt = np.sort(S_rows, axis=-1)
-    if srt.shape[-1] < 2:
-        return np.zeros(srt.shape[0], dtype=bool)
-    gap = srt[:, -1] - srt[:, -2]
-    return gap < 1e-3 * np.maximum(1.0, np.abs(m))
-
-
 def check_head(o, rm, rs, ra_, q, k, v, scale, causal, rows, bf16, b, h):
     """Compare one head's outputs at the given rows with the oracle's row-by-row forward."""
     qh, kh, vh = (t[b, h].double().numpy() for t in (q, k, v))
-    O, m, s, a = oracle.ra_attention_rows_fwd(qh, kh, vh, rows, scale, causal)
+    O, _, s, _ = oracle.ra_attention_rows_fwd(qh, kh, vh, rows, scale, causal)
     got = parity.f64(o[b, h])[rows]
     if bf16:
         parity.assert_close_bf16(got, O, f"O[{b},{h}]")
     else:
         parity.assert_close_fp32(got, O, f"O[{b},{h}]")
-    np.testing.assert_allclose(parity.f64(rm[b, h])[rows], m, rtol=1e-5, atol=1e-4)
     np.testing.assert_allclose(parity.f64(rs[b, h])[rows], s, rtol=2e-3 if bf16 else 1e-5)
     S = scale * (qh[rows] @ kh.T)
     if causal:
         S = np.where(np.arange(kh.shape[0])[None, :] <= rows[:, None], S, -np.inf)
-    ties = near_tie_rows(S, m)
-    ga = ra_[b, h].cpu().numpy()[rows]
-    assert np.array_equal(ga[~ties], a[~ties]), "argmax differs away from near-ties"
-    # near-tie rows: the GPU's argmax must still be a (near-)maximal allowed key
-    for r in np.nonzero(ties)[0]:
-        assert S[r, ga[r]] >= m[r] - 1e-3 * max(1.0, abs(m[r]))
+    # the row max within the fp32 score-error bound; the argmax equal to the oracle's except
+    # at near ties within twice that bound
+    err = parity.score_error_bound(qh[rows], kh, scale)
+    parity.check_argmax(S, ra_[b, h].cpu().numpy()[rows], err, f"forward O[{b},{h}] {tuple(q.shape)}",
+                        m_gpu=parity.f64(rm[b, h])[rows])
 
 
 def check_all(q, k, v, scale, causal, out_dtype=torch.float32):
