@@ -35,7 +35,7 @@
 //               whether the tile is live.  Epilogue: O = acc / sum(phi) and the row
 //               statistics for the backward.
 //   V arrives as the fp16 copy the C-ABI layer made once per call (exact for bf16
-//   values up to 65504), so the P V product runs in fp16 and P is rounded to 2^-11
+//   values from 2^-14 to 65504), so the P V product runs in fp16 and P is rounded to 2^-11
 //   rather than 2^-8.  Q K^T stays in bf16.
 //
 // CTA pairs (D = 128, N_Q > 256): a cluster of two CTAs runs the same roles on four query
@@ -97,7 +97,8 @@ struct FwdCfg {
   // o_full[2], drain[2]
   static constexpr int NUM_BARS = 1 + 2 * NSTAGE + 8 * NGROUP;
   static constexpr int OFF_MISC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;
-  static constexpr int MISC_BYTES = 16 + SOFTMAX_WARPS * 4;   // tmem base, abort flag, live votes (16-byte aligned)
+  // tmem base, abort flag, the odd CTA producer's fill count (pair), pad; live votes (16-byte aligned)
+  static constexpr int MISC_BYTES = 16 + SOFTMAX_WARPS * 4;
   static constexpr int USED = OFF_MISC + MISC_BYTES;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
   // 1024-byte aligned dynamic shared-memory base
@@ -220,6 +221,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = o_full + NGROUP;     // [NGROUP]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  // pair: ring fills the odd CTA's producer issued, stored into the even CTA's slot
+  volatile uint32_t* odd_fills = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 8);
   // [NGROUP][GROUP_WARPS] votes of this CTA's softmax warps: whether the last P tile has a
   // nonzero entry, tagged with its key tile (2 j + live)
   volatile int* live = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
@@ -295,6 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&drain[g], 1);
     }
     *abort_flag = 0;
+    *odd_fills = 0;
     for (int i = 0; i < SOFTMAX_WARPS; ++i) live[i] = -1;   // no key tile's tag
     fence_mbarrier_init();
   }
@@ -313,6 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  uint32_t prod_fills = 0;   // ring fills this CTA's producer issued (pair form, producer thread)
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -367,9 +372,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (ok) ok = issue(true, j - 1);
       }
       if (ok) ok = issue(true, nkt - 1);                                     //   V_{n-1}
-      // the barriers that count this CTA's copies are the even CTA's: it drains them for
-      // both, and the pair's closing cluster barrier keeps the odd CTA alive until then
-      if (arms) {
+      if constexpr (PAIR) {
+        // Both CTAs' copies complete on the even CTA's barriers, so the even producer drains
+        // them for both, after the first closing cluster barrier.  The two producers may have
+        // stopped after different numbers of fills (each gives up on its own CTA's abort flag
+        // or wait limit), so the odd one publishes its count for the even one to settle.
+        prod_fills = it;
+        if (rank != 0) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(odd_fills)), 0), it);
+      } else {
         drain_wait(q_full, 0, ctx);
         for (int i = 0; i < NST; ++i)
           if (issued[i]) drain_wait(&ring_full[i], last_par[i], ctx);
@@ -702,9 +712,28 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   __syncthreads();
-  // a pair's products read both CTAs' shared memory and write both tensor memories: neither
-  // CTA frees them before the even CTA has drained its products
-  if constexpr (PAIR) cluster_sync();
+  if constexpr (PAIR) {
+    // Every role of both CTAs has stopped issuing, and the odd producer's fill count is
+    // visible.  The even producer settles the fills only one CTA issued -- it arms those only
+    // the odd CTA issued for the odd CTA's bytes alone, and counts the bytes of the odd CTA's
+    // copies that never came for those only it issued -- then drains every fill, so no copy
+    // is still landing in either CTA when the memory is freed.  The second barrier keeps both
+    // CTAs (their shared memory, barriers and tensor memory) alive until then: a pair's
+    // products read both CTAs' shared memory and write both tensor memories.
+    cluster_sync();
+    if (warp == PRODUCER_WARP && lane == 0 && rank == 0) {
+      const uint32_t it_e = prod_fills, it_o = *odd_fills;
+      const uint32_t lo = min(it_e, it_o), hi = max(it_e, it_o);
+      for (uint32_t f = lo; f < hi; ++f) {
+        if (f >= it_e) mbar_arrive_expect_tx(&ring_full[f % NST], C::STAGE_BYTES);
+        else mbar_complete_tx(&ring_full[f % NST], C::STAGE_BYTES);
+      }
+      drain_wait(q_full, 0, ctx);
+      for (uint32_t st = 0; st < static_cast<uint32_t>(NST) && st < hi; ++st)
+        drain_wait(&ring_full[st], ((hi - 1 - st) / NST) & 1u, ctx);
+    }
+    cluster_sync();
+  }
   if (warp == MMA_WARP) {
     __syncwarp();
     tc_fence_after();

@@ -16,8 +16,8 @@ constexpr unsigned int kStatusTimeout = 1u;
 // A kernel whose shared-memory layout needs a 1024-byte aligned dynamic base found
 // another base and returned before doing anything.
 constexpr unsigned int kStatusBadSmem = 2u;
-// An input of the tensor-core backward lies outside the fp16 range (|x| > 65504) that
-// its internal operand format covers; the gradients of that call are not valid.
+// An operand of a tensor-core call lies outside the fp16 range (|x| > 65504, or NaN) that
+// its internal operand format covers; the outputs of that call are not valid.
 constexpr unsigned int kStatusRange = 4u;
 
 // Passed by value to every kernel: where to report a timeout and how long a wait may last.
@@ -128,6 +128,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// Count `bytes` of transaction bytes as arrived on an mbarrier of this CTA, as a copy landing
+// would (used to settle a phase whose copy was never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 // Contiguous global -> shared copy (cp.async.bulk): both addresses 16-byte aligned and
 // `bytes` a multiple of 16; completes on the mbarrier as transaction bytes.
 __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -164,6 +171,9 @@ __device__ __forceinline__ void cluster_sync() {
 // the default CTA-scope release.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr_cluster, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
 }
 __device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr_cluster) {
   uint4 v;

@@ -62,3 +62,29 @@ def test_backward_wait_timeout_is_reported_and_the_context_survives():
     parity.assert_close_bf16(parity.f64(dq[0, 0]), gq, "dq after a timed-out call")
     parity.assert_close_bf16(parity.f64(dk[0, 0]), gk, "dk after a timed-out call")
     parity.assert_close_bf16(parity.f64(dv[0, 0]), gv, "dv after a timed-out call")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_cta_pair_forward_timeout_is_reported_and_the_context_survives(causal):
+    """The D = 128 forward as CTA pairs (the layout of every long D = 128 call): the even
+    CTA's issuers give up at the forced wait, each CTA's other roles give up on their own
+    CTA's abort flag or wait limit, the even producer settles and drains both CTAs' copies,
+    and both CTAs pass the two closing cluster barriers.  The CPU model of this wind-down is
+    tests/test_protocol_abort.py."""
+    q, k, v = attention_inputs(1, 2, 512, 640, 128, seed=13 + int(causal), dtype=torch.bfloat16, with_dout=False)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    assert ra.device_status() == "RA_OK"
+    ra.debug_fwd_pair(2)
+    try:
+        with forced_timeout():
+            ra.ra_attention_forward(qg, kg, vg, causal=causal, out_dtype=torch.float32)
+            torch.cuda.synchronize()
+            status = ra.device_status()
+        assert status == "RA_ERR_TIMEOUT"
+        o, *_ = ra.ra_attention_forward(qg, kg, vg, causal=causal, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert ra.device_status() == "RA_OK"
+    finally:
+        ra.debug_fwd_pair(0)
+    O, *_ = oracle.ra_attention_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), causal=causal)
+    parity.assert_close_bf16(parity.f64(o), O, "O after a timed-out CTA-pair call")
