@@ -204,17 +204,19 @@ class HotPath:
             int(self.w.causal), 1, 0, 0, st))
 
     def step(self, st, events=None, b=0):
+        """One step.  events (optional): {"sm": e, "fwd": [3 events], "bwd": [4 events]}; the
+        library records the call's events at its kernel boundaries (ra_debug_kernel_events)."""
         if events:
-            events[0].record()
+            events["sm"].record()
         self.softmax(st, b)
         if events:
-            events[1].record()
+            self.ra.debug_kernel_events(events["fwd"])
         self.fwd(st, None, b)
         if events:
-            events[2].record()
+            self.ra.debug_kernel_events(events["bwd"])
         self.bwd(st, b)
         if events:
-            events[3].record()
+            self.ra.debug_kernel_events(None)
 
     def run_e2e(self, stream, steps):
         """`steps` end-to-end steps, timed with events on `stream`, returned in ms.
@@ -282,26 +284,28 @@ def traffic_from_profiles(kernel_tag):
     return None
 
 
-def cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=1024, softmax_rows=64):
-    """Bounded sample of the same workload through the float64 oracle (head 0, the first
-    `query_rows` queries against all keys, forward + backward; `softmax_rows` logit rows).
-    Returns (seconds, counted attention FLOPs, description)."""
-    import numpy as np
-
+def cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=8192, softmax_rows=1024, heads=2):
+    """Bounded sample of the same workload through the float64 oracle as it stands: the first
+    `heads` heads of batch 0, the first `query_rows` queries of each against all keys, forward
+    + backward; `softmax_rows` logit rows.  Returns (seconds, counted attention FLOPs,
+    description)."""
     import oracle
-    qd = q[0, 0, :query_rows].double().numpy()
-    dod = do[0, 0, :query_rows].double().numpy()
-    kd, vd = k[0, 0].double().numpy(), v[0, 0].double().numpy()
     xd = x[:softmax_rows].double().numpy()
+    dt = 0.0
+    for h in range(heads):
+        qd = q[0, h, :query_rows].double().numpy()
+        dod = do[0, h, :query_rows].double().numpy()
+        kd, vd = k[0, h].double().numpy(), v[0, h].double().numpy()
+        t0 = time.perf_counter()
+        oracle.ra_attention_head_fwd(qd, kd, vd, w.scale, w.causal)
+        oracle.ra_attention_head_bwd(qd, kd, vd, dod, w.scale, w.causal)
+        dt += time.perf_counter() - t0
     t0 = time.perf_counter()
-    oracle.ra_attention_head_fwd(qd, kd, vd, w.scale, w.causal)
-    oracle.ra_attention_head_bwd(qd, kd, vd, dod, w.scale, w.causal)
     oracle.ra_softmax(xd)
-    dt = time.perf_counter() - t0
-    flops = attn_flops(1, 1, query_rows, kd.shape[0], kd.shape[1], w.causal, True)
-    desc = (f"head (0,0), queries 0..{query_rows - 1} against all {kd.shape[0]} keys, forward+backward "
-            f"in float64, plus ra_softmax of {softmax_rows} logit rows")
-    del np
+    dt += time.perf_counter() - t0
+    flops = heads * attn_flops(1, 1, query_rows, k.shape[2], k.shape[3], w.causal, True)
+    desc = (f"heads (0,0)..(0,{heads - 1}), queries 0..{query_rows - 1} of each against all {k.shape[2]} keys, "
+            f"forward+backward in float64, plus ra_softmax of {softmax_rows} logit rows")
     return dt, flops, desc
 
 
@@ -319,8 +323,9 @@ def cpu_threads():
 def run_ours(args):
     import torch
 
-    from rational_softmax_attention_gb300.inputs import (ATTN_LONG_CAUSAL, ATTN_LONG_WIDE, RA_SOFTMAX_LONG_ROWS,
-                                                         attention_inputs, softmax_inputs, workload_inputs)
+    from rational_softmax_attention_gb300.inputs import (ATTN_LONG_CAUSAL, ATTN_LONG_WIDE, ATTN_MODULE_SHAPE,
+                                                         ATTN_TINY_FP32, RA_SOFTMAX_LONG_ROWS, attention_inputs,
+                                                         softmax_inputs, workload_inputs)
     world, rank, local = dist_env()
     dist = None
     if world > 1:
@@ -347,8 +352,15 @@ def run_ours(args):
     for _ in range(args.warmup):
         hp.step(st)
     barrier()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def new_ev():
+        return torch.cuda.Event(enable_timing=True)
+    ev = [{"sm": new_ev(), "fwd": [new_ev() for _ in range(3)], "bwd": [new_ev() for _ in range(4)]}
+          for _ in range(args.steps)]
+    for e in ev:                      # create every CUDA event before the timed region
+        for x in [e["sm"]] + e["fwd"] + e["bwd"]:
+            x.record(stream)
+    torch.cuda.synchronize(dev)
+    t_start, t_end = new_ev(), new_ev()
     with ClockSampler(local) as clocks:
         t_start.record(stream)
         for i in range(args.steps):
@@ -359,12 +371,20 @@ def run_ours(args):
     if status != "RA_OK":
         raise RuntimeError(f"device status after the timed region: {status}")
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
-    per_call = {"ra_softmax_ms": [], "ra_attention_fwd_ms": [], "ra_attention_bwd_ms": []}
-    for e in ev:
-        per_call["ra_softmax_ms"].append(e[0].elapsed_time(e[1]))
-        per_call["ra_attention_fwd_ms"].append(e[1].elapsed_time(e[2]))
-        per_call["ra_attention_bwd_ms"].append(e[2].elapsed_time(e[3]))
-    med = {kk: statistics.median(vv) for kk, vv in per_call.items()}
+    # per call and per kernel, from events on the launching stream (the library records the
+    # calls' events between its own launches)
+    spans = {
+        "ra_softmax_ms": lambda e: e["sm"].elapsed_time(e["fwd"][0]),
+        "ra_attention_fwd_ms": lambda e: e["fwd"][0].elapsed_time(e["fwd"][2]),
+        "ra_attention_bwd_ms": lambda e: e["bwd"][0].elapsed_time(e["bwd"][3]),
+        "bf16_to_f16_kernel (fwd)": lambda e: e["fwd"][0].elapsed_time(e["fwd"][1]),
+        "attn_fwd_tc_kernel": lambda e: e["fwd"][1].elapsed_time(e["fwd"][2]),
+        "bf16_to_f16_kernel (bwd)": lambda e: e["bwd"][0].elapsed_time(e["bwd"][1]),
+        "attn_bwd_dq_tc_kernel": lambda e: e["bwd"][1].elapsed_time(e["bwd"][2]),
+        "attn_bwd_dkdv_tc_kernel": lambda e: e["bwd"][2].elapsed_time(e["bwd"][3]),
+    }
+    med = {kk: statistics.median(fn(e) for e in ev) for kk, fn in spans.items()}
+    med["ra_softmax_fwd_vec_kernel"] = med["ra_softmax_ms"]
 
     B, H, N, D = hp.shape
     flops_step = attn_flops(B, H, N, N, D, w.causal, True)
@@ -513,35 +533,85 @@ def run_ours(args):
     ffma_peak = 152 * 128 * 2 * 2.07e9 / 1e12
     del qf, kf, vf, dof, of, rmf, rsf, raf
 
+    # the two small configurations: the fp32 forward B1 H2 N128 D64 (scale 1/8) and the bf16
+    # forward + backward B2 H12 N128 D64 causal (scale 1/8); latency-bound, times per call
+    # through the binding (each call launches one or two tiny grids)
+    w1 = ATTN_TINY_FP32
+    q1, k1, v1 = (t.to(dev) for t in workload_inputs(w1))
+
+    def tiny_fwd():
+        return hp.ra.ra_attention_forward(q1, k1, v1, scale=w1.scale, causal=w1.causal, out_dtype=torch.float32)
+    w3 = ATTN_MODULE_SHAPE
+    q3, k3, v3, do3 = (t.to(dev) for t in workload_inputs(w3))
+
+    def small_fwd_bwd():
+        o3, rm3, rs3, ra3, _ = hp.ra.ra_attention_forward(q3, k3, v3, scale=w3.scale, causal=w3.causal,
+                                                          out_dtype=torch.float32)
+        hp.ra.ra_attention_backward(q3, k3, v3, o3, do3, rm3, rs3, ra3, scale=w3.scale, causal=w3.causal)
+
+    def per_call_ms(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        m0.record(torch.cuda.current_stream(dev))
+        for _ in range(n):
+            fn()
+        m1.record(torch.cuda.current_stream(dev))
+        torch.cuda.synchronize(dev)
+        return m0.elapsed_time(m1) / n
+    tiny_ms = per_call_ms(tiny_fwd, max(args.steps, 20))
+    small_ms = per_call_ms(small_fwd_bwd, max(args.steps, 20))
+    if hp.ra.device_status() != "RA_OK":
+        raise RuntimeError("small-configuration components failed")
+    tiny_fl = attn_flops(w1.B, w1.H, w1.N, w1.N, w1.D, w1.causal, False)
+    small_fl = attn_flops(w3.B, w3.H, w3.N, w3.N, w3.D, w3.causal, True)
+    del q1, k1, v1, q3, k3, v3, do3
+
     peaks, peak_src = load_peaks()
-    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # every kernel here is timed in a loop of well under a second at the maximum SM clock
+    # (the clocks entry of this line), so the burst figures are the denominators
     tc_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tc_sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bwd_tflops = bwd_fl / (med["ra_attention_bwd_ms"] * 1e-3) / 1e12
     fwd_tflops = fwd_fl / (med["ra_attention_fwd_ms"] * 1e-3) / 1e12
     sm_gbs = sm_bytes / (med["ra_softmax_ms"] * 1e-3) / 1e9
-    dominant = max(("ra_attention_bwd", med["ra_attention_bwd_ms"]), ("ra_attention_fwd", med["ra_attention_fwd_ms"]),
-                   ("ra_softmax", med["ra_softmax_ms"]), key=lambda t: t[1])[0]
-    rl = {
-        "ra_attention_bwd": {"bound": "tensor", "achieved": bwd_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                             "traffic": traffic_from_profiles("ra_attention_bwd"),
-                             "kernel": "ra_attention_bwd call: bf16_to_f16 + attn_bwd_dq_tc + attn_bwd_dkdv_tc",
-                             "algorithmic": f"{bwd_fl:.4e} FLOP per call (2.5 x 4 B H N^2 D)"},
-        "ra_attention_fwd": {"bound": "tensor", "achieved": fwd_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                             "traffic": traffic_from_profiles("ra_attention_fwd"), "kernel": "attn_fwd_tc_kernel",
-                             "algorithmic": f"{fwd_fl:.4e} FLOP per launch (4 B H N^2 D)"},
-        "ra_softmax": {"bound": "hbm", "achieved": sm_gbs, "peak": hbm_peak, "unit": "GB/s",
-                       "traffic": traffic_from_profiles("ra_softmax"), "kernel": "ra_softmax_fwd_vec_kernel",
-                       "algorithmic": f"{sm_bytes:.4e} B per launch (4 B read + 4 B written per element)"},
-    }[dominant]
-    rl["frac"] = rl["achieved"] / rl["peak"]
-    rl["peak_source"] = f"{peak_src} ({'bf16 sustained' if rl['unit'] == 'TFLOP/s' else 'HBM copy'})"
+    n_qkvo = B * H * N * D
+    # Algorithmic work per launch of each kernel of the step.  The backward's standard count
+    # is five products (S recomputed, dP, dV, dK, dQ); the dK/dV kernel forms four of them
+    # and the dQ kernel the fifth (its own recomputation of S and dP is counted nowhere).
+    kern = {
+        "ra_softmax_fwd_vec_kernel": ("hbm", sm_bytes, "4 B read + 4 B written per element"),
+        "bf16_to_f16_kernel (fwd)": ("hbm", 4.0 * n_qkvo, "V: 2 B read + 2 B written per element"),
+        "attn_fwd_tc_kernel": ("tensor", fwd_fl, "4 B H N^2 D FLOP (Q K^T and P V)"),
+        "bf16_to_f16_kernel (bwd)": ("hbm", 16.0 * n_qkvo, "Q, K, V, dO: 2 B read + 2 B written per element"),
+        "attn_bwd_dq_tc_kernel": ("tensor", 0.2 * bwd_fl, "2 B H N^2 D FLOP (dQ = dS K; its S and dP "
+                                                         "recomputation is not counted)"),
+        "attn_bwd_dkdv_tc_kernel": ("tensor", 0.8 * bwd_fl, "8 B H N^2 D FLOP (S^T, dP^T, dV, dK)"),
+    }
+    kernels = {}
+    for name, (bound, work, what) in kern.items():
+        ms = med[name]
+        achieved = work / (ms * 1e-3) / (1e12 if bound == "tensor" else 1e9)
+        peak = tc_burst if bound == "tensor" else hbm_peak
+        kernels[name] = {"ms": ms, "bound": bound, "achieved": achieved, "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                         "frac": achieved / peak, "algorithmic": what}
+    dominant = max(kernels, key=lambda k: kernels[k]["ms"])
+    dk = kernels[dominant]
+    traffic = traffic_from_profiles(dominant.replace(" (", "_").replace(")", ""))
+    rl = {"bound": dk["bound"], "achieved": dk["achieved"], "peak": tc_burst if dk["bound"] == "tensor" else hbm_peak,
+          "unit": dk["unit"], "frac": dk["frac"], "traffic": traffic, "kernel": dominant,
+          "algorithmic": f"{kern[dominant][1]:.4e} {'FLOP' if dk['bound'] == 'tensor' else 'B'} per launch: "
+                         f"{kern[dominant][2]}",
+          "peak_source": f"{peak_src} ({'bf16 burst' if dk['bound'] == 'tensor' else 'HBM copy'}): the kernel runs "
+                         f"{dk['ms']:.2f} ms per launch inside a {elapsed_ms / 1e3:.2f} s timed region"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded torch.randn (CPU generator), no dataset",
         "config": step_config(w, sw),
+        "kernels": kernels,
         "components": {
             "ra_softmax": {"ms": med["ra_softmax_ms"], "GB_per_s": sm_gbs, "frac_hbm": sm_gbs / hbm_peak,
                            "frac_hbm_8000": sm_gbs / 8000.0},
@@ -550,10 +620,18 @@ def run_ours(args):
                                  "tiles_visited": visited, "tiles_skipped": skipped,
                                  "skipped_fraction": (skipped / visited) if visited else None},
             "ra_attention_bwd": {"ms": med["ra_attention_bwd_ms"], "TFLOP_per_s": bwd_tflops,
-                                 "frac_bf16_burst": bwd_tflops / tc_burst},
+                                 "frac_bf16_burst": bwd_tflops / tc_burst,
+                                 "frac_bf16_sustained": bwd_tflops / tc_sustained},
             "ra_attention_fwd_causal_b4h16n8192d128": {"ms": causal_ms,
                                                        "TFLOP_per_s": causal_fl / (causal_ms * 1e-3) / 1e12,
                                                        "frac_bf16_burst": causal_fl / (causal_ms * 1e-3) / 1e12 / tc_burst},
+            "ra_attention_fwd_fp32_b1h2n128d64": {
+                "ms": tiny_ms, "TFLOP_per_s": tiny_fl / (tiny_ms * 1e-3) / 1e12,
+                "note": "one tiny fp32 forward per call through the binding; latency-bound, no roofline claim"},
+            "ra_attention_fwdbwd_bf16_b2h12n128d64_causal": {
+                "ms": small_ms, "TFLOP_per_s": small_fl / (small_ms * 1e-3) / 1e12,
+                "note": "forward + backward per call through the binding (24 heads of one 128-row tile); "
+                        "latency-bound, no roofline claim"},
             "ra_softmax_bf16": {"ms": sm16_ms, "GB_per_s": sm16_bytes / (sm16_ms * 1e-3) / 1e9,
                                 "frac_hbm": sm16_bytes / (sm16_ms * 1e-3) / 1e9 / hbm_peak,
                                 "algorithmic": "4 B per element (bf16 read and written)"},
@@ -600,10 +678,10 @@ def run_reference(args):
     q, k, v, do = workload_inputs(w)
     x = softmax_inputs(sw.rows, sw.cols, seed=sw.seed, sigma=sw.sigma)
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=256, softmax_rows=16)
+        cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=256, softmax_rows=16, heads=1)
     total, flops, desc = 0.0, 0.0, ""
     for _ in range(args.steps):
-        dt, fl, desc = cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=256, softmax_rows=16)
+        dt, fl, desc = cpu_oracle_sample(w, sw, q, k, v, do, x, query_rows=256, softmax_rows=16, heads=1)
         total += dt
         flops += fl
     value = flops / total / 1e12
@@ -618,6 +696,53 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                if ln.lower().startswith(("model name", "cpu part", "hardware")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def run_oracle_configs(max_heads):
+    """The float64 oracle timed on this host's cores for each of the five workloads (inputs
+    drawn before the clock starts).  Attention workloads time up to `max_heads` heads and
+    scale linearly to all heads (the work is exactly linear in heads); ra_softmax times 2048
+    of its 16384 rows and scales by rows.  One JSON line per workload."""
+    import oracle
+    from rational_softmax_attention_gb300.inputs import (ATTN_LONG_CAUSAL, ATTN_LONG_WIDE, ATTN_MODULE_SHAPE,
+                                                         ATTN_TINY_FP32, RA_SOFTMAX_LONG_ROWS, softmax_inputs,
+                                                         workload_inputs)
+    base = {"cores": cpu_threads(), "cpu": cpu_model(), "kind": "oracle (float64 NumPy, materialised per head)"}
+    for w in (ATTN_TINY_FP32, RA_SOFTMAX_LONG_ROWS, ATTN_MODULE_SHAPE, ATTN_LONG_CAUSAL, ATTN_LONG_WIDE):
+        if w is RA_SOFTMAX_LONG_ROWS:
+            rows = 2048
+            xd = softmax_inputs(w.rows, w.cols, seed=w.seed, sigma=w.sigma)[:rows].double().numpy()
+            t0 = time.perf_counter()
+            oracle.ra_softmax(xd)
+            dt = time.perf_counter() - t0
+            print(json.dumps({"workload": w.name, "seconds_timed": dt, "timed": f"{rows} of {w.rows} rows",
+                              "seconds_all": dt * w.rows / rows, **base}), flush=True)
+            continue
+        ts = workload_inputs(w)
+        heads = [(b, h) for b in range(w.B) for h in range(w.H)][:max_heads]
+        dt = 0.0
+        for b, h in heads:
+            qd, kd, vd = (t[b, h].double().numpy() for t in ts[:3])
+            t0 = time.perf_counter()
+            oracle.ra_attention_head_fwd(qd, kd, vd, w.scale, w.causal)
+            if w.backward:
+                oracle.ra_attention_head_bwd(qd, kd, vd, ts[3][b, h].double().numpy(), w.scale, w.causal)
+            dt += time.perf_counter() - t0
+        nh = w.B * w.H
+        print(json.dumps({"workload": w.name, "seconds_timed": dt, "timed": f"{len(heads)} of {nh} heads",
+                          "seconds_all": dt * nh / len(heads), "backward": w.backward, **base}), flush=True)
 
 
 def run_profile_case():
@@ -650,9 +775,14 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing on the host")
     ap.add_argument("--profile-case", action="store_true",
                     help="run only the small fixed case used for ncu captures, then exit")
+    ap.add_argument("--oracle-configs", type=int, metavar="MAX_HEADS", default=0,
+                    help="time the float64 oracle on the host for each workload (up to MAX_HEADS heads), then exit")
     args = ap.parse_args(argv)
     if args.profile_case:
         run_profile_case()
+        return
+    if args.oracle_configs:
+        run_oracle_configs(args.oracle_configs)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -110,9 +110,12 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
  *   workspace    device memory of ra_attention_fwd_workspace_size() bytes, 16-byte
  *                aligned, contents on entry irrelevant; required for RA_BF16 inputs
  *                (NULL allowed for RA_F32).  The call writes an fp16 copy of v there
- *                and forms P V in fp16: exact for bf16 values up to 65504, and P is
- *                rounded to 2^-11 instead of 2^-8.  Larger |v| (or NaN) saturates and
- *                is reported as RA_ERR_UNSUPPORTED by ra_device_status().
+ *                and forms P V in fp16, with P rounded to 2^-11 instead of 2^-8.  The
+ *                copy is exact for 2^-14 <= |v| <= 65504 (normal fp16); smaller
+ *                magnitudes become fp16 subnormals, rounded to a multiple of 2^-24
+ *                (below 2^-25 to 0), an absolute error of at most 2^-25 per value.
+ *                |v| > 65504 (or NaN) saturates and is reported as RA_ERR_UNSUPPORTED
+ *                by ra_device_status().
  *   scale        score scale; <= 0 means 1/sqrt(D).
  *   causal       0: every key visible; nonzero: key j visible to query i iff j <= i
  *                (top-left alignment, as scaled_dot_product_attention's is_causal).
@@ -143,9 +146,11 @@ size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
  * of five 128-entry arrays (two constants of the recomputed weights, D_i = dO_i . O_i,
  * the argmax correction R_i and the argmax index), at least two float arrays of
  * B*H*N_Q entries, then fp16 copies of q, dout, k and v, which the tensor-core path
- * multiplies in fp16 (exact for bf16 values up to 65504; P, E and dS are then rounded
- * to fp16 rather than bf16 before their products).  Each piece is padded to 256
- * bytes.  Returns 0 for invalid sizes.
+ * multiplies in fp16 (P, E and dS are then rounded to fp16 rather than bf16 before
+ * their products).  The copies are exact for 2^-14 <= |x| <= 65504; smaller values are
+ * rounded to a multiple of 2^-24 (fp16 subnormals; below 2^-25 to 0), and |x| > 65504
+ * or NaN saturates and is reported as RA_ERR_UNSUPPORTED by ra_device_status().  Each
+ * piece is padded to 256 bytes.  Returns 0 for invalid sizes.
  */
 size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 
@@ -183,12 +188,20 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
  * status word of the current device, for everything launched since the last call:
  *   RA_OK               nothing to report;
  *   RA_ERR_TIMEOUT      a kernel gave up a bounded wait (its outputs are undefined);
- *   RA_ERR_UNSUPPORTED  a tensor-core backward met an input beyond the fp16 range
- *                       (|x| > 65504 or NaN); its gradients are undefined;
+ *   RA_ERR_UNSUPPORTED  a bf16 (tensor-core) call met an operand beyond the fp16 range
+ *                       of its internal copies (|x| > 65504 or NaN: v in the forward;
+ *                       q, k, v or dout in the backward); its outputs are undefined;
  *   RA_ERR_LAUNCH       the synchronisation failed, or a kernel found its shared
  *                       memory misaligned and returned without doing anything.
  */
 ra_status_t ra_device_status(void* stream);
+/*
+ * The library looks up the device addresses of its own device variables (this status
+ * word, and the scratch array of ra_attention_bwd_noalloc) once per device ordinal and
+ * keeps them for the life of the process.  They belong to the device's primary context:
+ * after cudaDeviceReset() on a device (or any other destruction of its primary context)
+ * they are stale, and the library must not be used on that device again in the process.
+ */
 
 /*
  * ra_set_wait_limit_ns -- limit, in nanoseconds of %globaltimer, on every
@@ -215,6 +228,20 @@ void ra_debug_force_timeout(int on);
  * time both layouts.
  */
 void ra_debug_fwd_pair(int mode);
+
+/*
+ * ra_debug_kernel_events -- measurement knob (n = 0 or events = NULL: off, the default).
+ * When on, every later bf16 (tensor-core) ra_attention_fwd / ra_attention_bwd call, masked
+ * or not, records the caller's CUDA events (cudaEvent_t handles passed as void*) on its
+ * stream at its kernel boundaries, so that each kernel can be timed on the launching
+ * stream:
+ *   forward:  events[0] before the V conversion, [1] before the attention kernel, [2] after;
+ *   backward: events[0] before the operand conversion, [1] before the dQ kernel, [2]
+ *             before the dK/dV kernel, [3] after it.
+ * At most four events are used; a NULL entry or an index >= n is skipped.  The handles must
+ * stay valid while the knob is on.  A failed record makes the call return RA_ERR_LAUNCH.
+ */
+void ra_debug_kernel_events(void* const* events, int n);
 
 /* Size of the device array behind ra_attention_bwd_noalloc (32 MiB). */
 #define RA_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -280,10 +307,14 @@ ra_status_t ra_attention_bwd_masked(const void* q, const void* k, const void* v,
  * RA_NOALLOC_SCRATCH_BYTES inside the library: every GPU that loads the library holds
  * that memory until the process exits, and nothing is allocated per call.
  *   Arguments, results and errors are those of ra_attention_bwd without `workspace`.
- *   Sizes whose ra_attention_bwd_workspace_size() exceeds RA_NOALLOC_SCRATCH_BYTES are
- *   rejected with RA_ERR_UNSUPPORTED before anything runs (use ra_attention_bwd then).
- *   The first call on a device looks up the array's device address (once per device);
- *   make that first call before any stream capture.
+ *   Sizes whose workspace exceeds RA_NOALLOC_SCRATCH_BYTES are rejected with
+ *   RA_ERR_UNSUPPORTED before anything runs (use ra_attention_bwd then).  The workspace
+ *   counted is the one this call's path uses: ra_attention_bwd_workspace_size() for
+ *   RA_BF16 inputs, and for RA_F32 inputs only two float arrays of B*H*N_Q entries (each
+ *   padded to 256 bytes).  Device ordinals of 64 and above also give RA_ERR_UNSUPPORTED.
+ *   The first call on a device looks up the array's device address (once per device)
+ *   and keeps it, like the status word's (see ra_device_status); make that first call
+ *   before any stream capture.
  *   All calls share the one array and it keeps the previous call's contents (nothing in
  *   it needs to start at zero).  Calls that overlap on the GPU -- on different streams,
  *   or from different host threads without ordering -- race on it: serialise them.

@@ -22,6 +22,7 @@ import torch
 __all__ = [
     "RaError", "lib", "ra_softmax", "ra_softmax_backward", "ra_attention", "ra_attention_forward", "RaAttention",
     "ra_attention_backward", "pack_attn_mask", "device_status", "set_wait_limit_ns", "exported_symbols", "LIB_PATH",
+    "debug_kernel_events",
 ]
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
@@ -62,6 +63,7 @@ _SIGNATURES = {
     "ra_set_wait_limit_ns": ([_u64], None),
     "ra_debug_force_timeout": ([_i32], None),
     "ra_debug_fwd_pair": ([_i32], None),
+    "ra_debug_kernel_events": ([ctypes.POINTER(ctypes.c_void_p), _i32], None),
 }
 
 
@@ -302,7 +304,7 @@ class RaAttention(torch.nn.Module):
 
 
 def device_status(stream=None):
-    """Synchronise and return the device-side status ('RA_OK' or 'RA_ERR_TIMEOUT'), clearing it."""
+    """Synchronise and return the device-side status name ('RA_OK', 'RA_ERR_TIMEOUT', ...), clearing it."""
     s = stream if stream is not None else torch.cuda.current_stream()
     return _STATUS.get(lib().ra_device_status(ctypes.c_void_p(s.cuda_stream)), "unknown")
 
@@ -321,3 +323,21 @@ def debug_fwd_pair(mode):
     """Layout of later bf16 D = 128 forward calls: 0 automatic (CTA pairs when N_Q > 256),
     1 single CTAs, 2 CTA pairs."""
     lib().ra_debug_fwd_pair(int(mode))
+
+
+def debug_kernel_events(events):
+    """Measurement knob: later bf16 attention calls record these torch.cuda.Event objects
+    (up to four, created with enable_timing=True) at their kernel boundaries; None turns it
+    off.  Forward: [before the V conversion, before the attention kernel, after it];
+    backward: [before the conversion, before dQ, before dK/dV, after dK/dV]."""
+    if not events:
+        lib().ra_debug_kernel_events(None, 0)
+        return
+    stream = torch.cuda.current_stream()
+    handles = []
+    for e in events:
+        if e.cuda_event == 0:      # torch creates the CUDA event on its first record
+            e.record(stream)
+        handles.append(e.cuda_event)
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    lib().ra_debug_kernel_events(arr, len(handles))

@@ -21,6 +21,13 @@ std::mutex g_status_mu;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_force_timeout{0};
 std::atomic<int> g_fwd_pair{0};
+KernelEvents g_events = {{nullptr, nullptr, nullptr, nullptr}, 0};
+std::mutex g_events_mu;
+
+KernelEvents current_events() {
+  std::lock_guard<std::mutex> lock(g_events_mu);
+  return g_events;
+}
 
 ra_status_t status_ptr_for_current_device(unsigned int** out) {
   int dev = 0;
@@ -116,6 +123,13 @@ ra_status_t check_attn_sizes(int B, int H, int NQ, int NK, int D) {
 }
 
 }  // namespace
+
+size_t bwd_workspace_bytes(int B, int H, int NQ, int NK, int D, bool f32_inputs) {
+  if (check_attn_sizes(B, H, NQ, NK, D) != RA_OK) return 0;
+  const BwdLayout lay(B, H, NQ, NK, D);
+  return f32_inputs ? lay.total_f32 : lay.total_tc;
+}
+
 }  // namespace raattn
 
 using namespace raattn;
@@ -140,6 +154,12 @@ void ra_set_wait_limit_ns(uint64_t limit_ns) {
 void ra_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
 
 void ra_debug_fwd_pair(int mode) { g_fwd_pair.store(mode == 1 || mode == 2 ? mode : 0); }
+
+void ra_debug_kernel_events(void* const* events, int n) {
+  std::lock_guard<std::mutex> lock(g_events_mu);
+  g_events.n = (events && n > 0) ? std::min(n, 4) : 0;
+  for (int i = 0; i < 4; ++i) g_events.e[i] = i < g_events.n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+}
 
 ra_status_t ra_device_status(void* stream) {
   unsigned int* p = nullptr;
@@ -249,9 +269,13 @@ ra_status_t attn_fwd_impl(const void* q, const void* k, const void* v, void* o, 
   a.out_bf16 = out_dtype == RA_BF16 ? 1 : 0;
   a.mask = mask;
   if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
+  const KernelEvents ev = current_events();
+  if (ev.rec(0, st) != cudaSuccess) return RA_ERR_LAUNCH;
   if (launch_bf16_to_f16(job, ctx.status, st) != cudaSuccess) return RA_ERR_LAUNCH;
+  if (ev.rec(1, st) != cudaSuccess) return RA_ERR_LAUNCH;
   const cudaError_t e = launch_attn_fwd_tc(s, a, ctx, st);
-  return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+  if (e != cudaSuccess || ev.rec(2, st) != cudaSuccess) return RA_ERR_LAUNCH;
+  return RA_OK;
 }
 
 }  // namespace
@@ -363,7 +387,7 @@ ra_status_t attn_bwd_impl(const void* q, const void* k, const void* v, const voi
   a.ws_consts = reinterpret_cast<float*>(ws);
   a.mask_q = mask_q;
   a.mask_k = mask_k;
-  const cudaError_t e = launch_attn_bwd_tc(s, a, ctx, st);
+  const cudaError_t e = launch_attn_bwd_tc(s, a, ctx, st, current_events());
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
 

@@ -27,9 +27,11 @@ void* g_scratch_ptr[kMaxScratchDevices] = {};
 std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device (looked up on first use).
+// Device ordinals from kMaxScratchDevices on are beyond what the cache holds.
 ra_status_t scratch_for_current_device(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return RA_ERR_LAUNCH;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return RA_ERR_LAUNCH;
+  if (dev >= kMaxScratchDevices) return RA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
@@ -49,11 +51,13 @@ extern "C" ra_status_t ra_attention_bwd_noalloc(const void* q, const void* k, co
                                                 int H, int N_Q, int N_K, int D, float scale, int causal,
                                                 ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype,
                                                 void* stream) {
-  const size_t need = ra_attention_bwd_workspace_size(B, H, N_Q, N_K, D);
+  // the workspace this call's path uses: fp32 inputs need far less than bf16 ones
+  const size_t need = raattn::bwd_workspace_bytes(B, H, N_Q, N_K, D, in_dtype == RA_F32);
   if (need == 0) return RA_ERR_ARG;
   if (need > RA_NOALLOC_SCRATCH_BYTES) return RA_ERR_UNSUPPORTED;   // use ra_attention_bwd with a workspace
   void* scratch = nullptr;
-  if (raattn::scratch_for_current_device(&scratch) != RA_OK) return RA_ERR_LAUNCH;
+  const ra_status_t got = raattn::scratch_for_current_device(&scratch);
+  if (got != RA_OK) return got;
   // Nothing in the workspace has to start at zero: every entry the kernels read is
   // written earlier in the same call, so the previous call's contents do no harm.
   return ra_attention_bwd(q, k, v, o, dout, row_m, row_s, row_arg, dq, dk, dv, scratch, B, H, N_Q, N_K, D, scale,

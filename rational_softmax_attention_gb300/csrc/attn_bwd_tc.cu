@@ -28,8 +28,9 @@
 //
 // Operand format: the MMAs of the backward take fp16 operands (fp32 accumulation).
 // A prologue converts Q, K, V and dO from bf16 to fp16 into the workspace; that is
-// exact for |x| <= 65504 (bf16 has 8 significant bits, fp16 11), so the recomputed
-// scores equal the forward's, while P, E and dS -- formed in fp32 -- are rounded to
+// exact for 2^-14 <= |x| <= 65504 (bf16 has 8 significant bits, fp16 11), so for such
+// operands the recomputed scores equal the forward's (smaller ones are rounded to the fp16
+// subnormal spacing 2^-24), while P, E and dS -- formed in fp32 -- are rounded to
 // fp16 (unit roundoff 2^-11) instead of bf16 (2^-8) before their products.  With
 // |E| up to ~10 at wide score spreads, bf16 rounding alone costs ~2e-2 in dQ.
 #include "kernels.cuh"
@@ -614,6 +615,14 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     mbar_init(st_full, 2);   // issuer 0's commit + the producer's arrival for X
     mbar_init(dpt_full, 2);   // issuer 0's commit + the producer's arrival for Y
     mbar_init(dpt_free, KV_SOFTMAX_WARPS);
+    // p_full and ds_full: one counted barrier each for all query tiles.  A warp that has
+    // finished tile i cannot arrive for tile i + 1 while another warp's arrival for tile i is
+    // missing: its next P^T needs S^T_{i+1} (st_full), which issuer 0 issues only after
+    // p_free, i.e. after the dV_i product that p_full's phase i started; its next dS^T needs
+    // Y_{i+1} (dpt_full), which the producer issues only after ds_free, i.e. after the dK_i
+    // product that ds_full's phase i started.  Those two waits keep every arrival in its own
+    // tile's phase; a reordering that drops either needs one barrier per buffer, as e_full in
+    // the dQ kernel.
     mbar_init(p_full, KV_SOFTMAX_WARPS);
     mbar_init(p_free, 1);
     mbar_init(acc_full, 1);
@@ -976,7 +985,8 @@ cudaError_t set_smem(KernelFn fn, int bytes) {
 }
 
 template <int D, bool MASK>
-cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
+cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st,
+                         const KernelEvents& ev) {
   cudaError_t e = set_smem(attn_bwd_dq_tc_kernel<D, MASK>, DqCfg<D>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   e = set_smem(attn_bwd_dkdv_tc_kernel<D, MASK>, DkvCfg<D>::SMEM_BYTES);
@@ -995,21 +1005,29 @@ cudaError_t launch_bwd_d(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx
     job.n8[i] = ns[i];
   }
   job.count = 4;
+  if ((e = ev.rec(0, st)) != cudaSuccess) return e;
   e = launch_bf16_to_f16(job, ctx.status, st);
   if (e != cudaSuccess) return e;
+  if ((e = ev.rec(1, st)) != cudaSuccess) return e;
   attn_bwd_dq_tc_kernel<D, MASK><<<nqt * BH, DQ_THREADS, DqCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if ((e = ev.rec(2, st)) != cudaSuccess) return e;
   attn_bwd_dkdv_tc_kernel<D, MASK><<<nkt * BH, KV_THREADS, DkvCfg<D>::SMEM_BYTES, st>>>(s, a, ctx);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return ev.rec(3, st);
 }
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st) {
+cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st,
+                               const KernelEvents& ev) {
   const bool mask = a.mask_q.bits != nullptr;
-  if (s.D == 128) return mask ? launch_bwd_d<128, true>(s, a, ctx, st) : launch_bwd_d<128, false>(s, a, ctx, st);
-  if (s.D == 64) return mask ? launch_bwd_d<64, true>(s, a, ctx, st) : launch_bwd_d<64, false>(s, a, ctx, st);
+  if (s.D == 128)
+    return mask ? launch_bwd_d<128, true>(s, a, ctx, st, ev) : launch_bwd_d<128, false>(s, a, ctx, st, ev);
+  if (s.D == 64)
+    return mask ? launch_bwd_d<64, true>(s, a, ctx, st, ev) : launch_bwd_d<64, false>(s, a, ctx, st, ev);
   return cudaErrorInvalidValue;
 }
 

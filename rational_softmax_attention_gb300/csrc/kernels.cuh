@@ -26,6 +26,17 @@ struct MaskBits {
 cudaError_t launch_mask_pack(const uint8_t* mask, int G, int NQ, int NK, uint32_t* bits_q, int wq, uint32_t* bits_k,
                              int wk, cudaStream_t st);
 
+// Caller-supplied CUDA events recorded at an attention call's kernel boundaries (a
+// measurement knob, ra_debug_kernel_events): e[i] is recorded before kernel i of the call
+// and e[k] after its last kernel k - 1; null entries and i >= n are skipped.
+struct KernelEvents {
+  cudaEvent_t e[4];
+  int n;
+  cudaError_t rec(int i, cudaStream_t st) const {
+    return (i < n && e[i]) ? cudaEventRecord(e[i], st) : cudaSuccess;
+  }
+};
+
 // Problem description shared by the attention launchers.
 struct AttnShape {
   int B, H, NQ, NK, D;
@@ -96,6 +107,12 @@ struct BwdTcArgs {
   MaskBits mask_k;   // the same mask transposed, rows = keys (dK/dV kernel)
 };
 constexpr int kConstBlockFloats = 5 * 128;
-cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st);
+// Workspace bytes the backward uses for these sizes and input dtype (api.cu): the CUDA-core
+// fp32 path needs only two per-row float arrays; the tensor-core path the constant blocks and
+// the fp16 operand copies.  0 for invalid sizes.
+size_t bwd_workspace_bytes(int B, int H, int NQ, int NK, int D, bool f32_inputs);
+// Kernels in launch order: bf16 -> fp16 operand copies, dQ kernel, dK/dV kernel.
+cudaError_t launch_attn_bwd_tc(const AttnShape& s, const BwdTcArgs& a, const LaunchCtx& ctx, cudaStream_t st,
+                               const KernelEvents& ev);
 
 }  // namespace raattn
