@@ -357,8 +357,8 @@ def run_ours(args):
     ev = [{"sm": new_ev(), "fwd": [new_ev() for _ in range(3)], "bwd": [new_ev() for _ in range(4)]}
           for _ in range(args.steps)]
     for e in ev:                      # create every CUDA event before the timed region
-        for x in [e["sm"]] + e["fwd"] + e["bwd"]:
-            x.record(stream)
+        for one in [e["sm"]] + e["fwd"] + e["bwd"]:
+            one.record(stream)
     torch.cuda.synchronize(dev)
     t_start, t_end = new_ev(), new_ev()
     with ClockSampler(local) as clocks:
