@@ -55,6 +55,7 @@
 // as packed f32x2 operations.  At w = 1 the computed q is below 3e-7, so phi rounds to
 // exactly 0.0.
 #include "kernels.cuh"
+#include "phi.cuh"
 
 namespace raattn {
 namespace {
@@ -107,29 +108,6 @@ struct FwdCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
-// phi for four scores of a row (columns c .. c+3): w = sat(base - c2 s) = (1+u)/2.  The
-// reciprocals come from one packed product of the pairs A = (w0, w1), B = (w2, w3):
-// R = 1/(A B) = (1/(w0 w2), 1/(w1 w3)), so R B = (1/w0, 1/w1) and R A = (1/w2, 1/w3);
-// q = 1/w - 1 is one packed FMA per pair and phi = ((q^2)^2)^2 three packed products.
-__device__ __forceinline__ void phi_quad(float s0, float s1, float s2, float s3, float c2, float base,
-                                         float2& pa, float2& pb) {
-  const float2 A = make_float2(fma_sat(s0, -c2, base), fma_sat(s1, -c2, base));
-  const float2 B = make_float2(fma_sat(s2, -c2, base), fma_sat(s3, -c2, base));
-  const float2 P = __fmul2_rn(A, B);
-  const float2 R = make_float2(rcp_approx(P.x), rcp_approx(P.y));
-  const float2 minus1 = make_float2(-1.0f, -1.0f);
-  float2 qa = __ffma2_rn(R, B, minus1);
-  float2 qb = __ffma2_rn(R, A, minus1);
-  qa = __fmul2_rn(qa, qa);
-  qb = __fmul2_rn(qb, qb);
-  qa = __fmul2_rn(qa, qa);
-  qb = __fmul2_rn(qb, qb);
-  pa = __fmul2_rn(qa, qa);
-  pb = __fmul2_rn(qb, qb);
-}
-
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-
 // Pass-2 arithmetic of one 64-key half of a row, held in h (two 32-column chunks): phi
 // as packed fp16 pairs in pk (four per 16-byte chunk of P) and the partial row sum.
 // MASKED: columns past `lim` (causal diagonal, ragged tail) get s = -inf, hence w = 1
@@ -177,15 +155,6 @@ __device__ __forceinline__ float2 phi_store_half(const uint32_t (&h)[2][32], uin
   const float2 t = phi_half<MASKED, BITS>(h, pk, col0, lim, c2, base, mw0, mw1);
   store_p_half(pk, phalf_row, row_local);
   return t;
-}
-
-// Lowest column of a 32-column chunk whose score equals m (visible columns only: at most
-// `lim`, attention-mask bit set in mword), or 32.
-__device__ __forceinline__ int find_in_chunk(const uint32_t (&v)[32], float m, int col0, int lim, uint32_t mword) {
-  int idx = 32;
-#pragma unroll
-  for (int c = 31; c >= 0; --c) idx = (u2f(v[c]) == m && col0 + c <= lim && ((mword >> c) & 1u)) ? c : idx;
-  return idx;
 }
 
 // MASK: a boolean attention mask (args.mask) applies on top of `causal`.  PAIR: the CTA
