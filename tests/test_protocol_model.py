@@ -285,18 +285,22 @@ class ForwardModel:
 
 
 FWD_CONFIGS = [
-    # (CTAs, ring stages, key tiles, key tiles of product 0, dead fraction)
-    (1, 3, 1, 1, 0.0), (1, 3, 4, 4, 0.0), (1, 3, 5, 4, 0.3), (1, 6, 3, 3, 0.5), (1, 6, 7, 6, 0.0),
-    (2, 6, 1, 1, 0.0), (2, 6, 4, 4, 0.0), (2, 6, 5, 3, 0.3), (2, 6, 9, 7, 0.2), (2, 6, 2, 1, 0.0),
+    # (CTAs, ring stages, key tiles, key tiles of the shorter product, which product is shorter,
+    # dead fraction).  Under a causal mask product 0 ends earlier (the kernel's order); the
+    # configurations with product 1 shorter check that the protocol does not depend on which.
+    (1, 3, 1, 1, 0, 0.0), (1, 3, 4, 4, 0, 0.0), (1, 3, 5, 4, 0, 0.3), (1, 6, 3, 3, 0, 0.5), (1, 6, 7, 6, 0, 0.0),
+    (2, 6, 1, 1, 1, 0.0), (2, 6, 4, 4, 1, 0.0), (2, 6, 5, 4, 1, 0.3), (2, 6, 9, 8, 1, 0.2), (2, 6, 2, 1, 1, 0.0),
+    (2, 6, 5, 3, 0, 0.3), (2, 6, 6, 5, 1, 0.0),
 ]
 
 
-@pytest.mark.parametrize("ncta,nst,nkt,nkt0,dead_frac", FWD_CONFIGS)
-def test_forward_protocol_holds_on_random_schedules(ncta, nst, nkt, nkt0, dead_frac):
+@pytest.mark.parametrize("ncta,nst,nkt,nshort,short,dead_frac", FWD_CONFIGS)
+def test_forward_protocol_holds_on_random_schedules(ncta, nst, nkt, nshort, short, dead_frac):
+    nkt_g = (nshort, nkt) if short == 0 else (nkt, nshort)
     for seed in range(60):
         rng = random.Random(seed * 1000 + nkt * 10 + ncta)
         dead = {(g, j) for g in range(2) for j in range(nkt) if rng.random() < dead_frac}
-        run_roles(ForwardModel(ncta, nst, nkt, (nkt0, nkt), dead).roles(), rng)
+        run_roles(ForwardModel(ncta, nst, nkt, nkt_g, dead).roles(), rng)
 
 
 def _caught(make, seeds=300):
@@ -310,6 +314,7 @@ def _caught(make, seeds=300):
 
 @pytest.mark.parametrize("mutation,ncta,nkt,nkt0", [("release_without_fill", 1, 6, 3),
                                                     ("release_without_fill", 2, 6, 2),
+                                                    ("release_without_fill", 2, 6, -2),
                                                     ("single_cta_counts", 2, 3, 3),
                                                     ("no_p_free_wait", 1, 4, 4),
                                                     ("no_p_free_wait", 2, 4, 4)])
@@ -317,7 +322,8 @@ def test_planted_forward_protocol_mistakes_are_caught(mutation, ncta, nkt, nkt0)
     """Releasing ring stages without waiting for their fill lets the issuer that skips tiles
     run a phase ahead; counting one CTA's warps on the pair's barriers completes a phase
     early; skipping the P-free wait rewrites P under a running product."""
-    assert _caught(lambda: ForwardModel(ncta, 6 if ncta == 2 else 3, nkt, (nkt0, nkt), set(), mutation))
+    nkt_g = (nkt0, nkt) if nkt0 > 0 else (nkt, -nkt0)   # negative: product 1 is the shorter one
+    assert _caught(lambda: ForwardModel(ncta, 6 if ncta == 2 else 3, nkt, nkt_g, set(), mutation))
 
 
 # ---------------------------------------------------------------------------- dK/dV kernel
