@@ -148,13 +148,38 @@ __device__ __forceinline__ void store_p_half(const uint32_t (&pk)[32], uint8_t* 
         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
-template <bool MASKED, bool BITS>
-__device__ __forceinline__ float2 phi_store_half(const uint32_t (&h)[2][32], uint8_t* phalf_row, int row_local,
-                                                 int col0, int lim, float c2, float base, uint32_t mw0, uint32_t mw1) {
-  uint32_t pk[32];
-  const float2 t = phi_half<MASKED, BITS>(h, pk, col0, lim, c2, base, mw0, mw1);
-  store_p_half(pk, phalf_row, row_local);
-  return t;
+// How the 32-column chunk starting at key col0 is masked for this row (attention-mask word w,
+// last visible key lim), voted over the warp: every row sees all 32 columns, none sees any, or
+// mixed.  Key padding and block masks make the first two the rule away from their edges.  A
+// warp vote: call it only where all 32 lanes of the warp execute it together.
+constexpr int kChunkAll = 0, kChunkNone = 1, kChunkMixed = 2;
+__device__ __forceinline__ int chunk_kind(uint32_t w, int col0, int lim) {
+  if (__all_sync(0xffffffffu, w == ~0u && col0 + 31 <= lim)) return kChunkAll;
+  if (__all_sync(0xffffffffu, w == 0u || col0 > lim)) return kChunkNone;
+  return kChunkMixed;
+}
+
+// phi of one 64-key half (phi_half) through the cheapest path the warp's rows allow: with an
+// attention mask, a half every row sees whole runs unmasked, a half no row sees gives zeros
+// without the arithmetic, anything else the per-entry masked path; without one, the causal
+// `masked` flag decides as before.
+// With MASK it votes over the warp (chunk_kind): called by all lanes together.
+template <bool MASK>
+__device__ __forceinline__ float2 phi_half_any(bool masked, const uint32_t (&h)[2][32], uint32_t (&pk)[32], int col0,
+                                               int lim, float c2, float base, uint32_t mw0, uint32_t mw1) {
+  if constexpr (MASK) {
+    const int k0 = chunk_kind(mw0, col0, lim), k1 = chunk_kind(mw1, col0 + 32, lim);
+    if (k0 == kChunkNone && k1 == kChunkNone) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = 0u;
+      return make_float2(0.0f, 0.0f);
+    }
+    if (k0 == kChunkAll && k1 == kChunkAll) return phi_half<false, false>(h, pk, col0, lim, c2, base, ~0u, ~0u);
+    return phi_half<true, true>(h, pk, col0, lim, c2, base, mw0, mw1);
+  } else {
+    return masked ? phi_half<true, false>(h, pk, col0, lim, c2, base, ~0u, ~0u)
+                  : phi_half<false, false>(h, pk, col0, lim, c2, base, ~0u, ~0u);
+  }
 }
 
 // MASK: a boolean attention mask (args.mask) applies on top of `causal`.  PAIR: the CTA
@@ -570,11 +595,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int k = 0; k < BN / 32; ++k) {
           float u0 = -INFINITY, u1 = -INFINITY;
+          // With an attention mask this branch is taken by the whole warp (the condition above
+          // is false for every lane), so the chunk vote is safe: a chunk every row of the warp
+          // may see whole takes the plain max, a chunk none of them may see is skipped (key
+          // padding and block masks are uniform per chunk).  Without one, the branch is taken
+          // per lane on causal diagonal tiles and must hold no warp vote: every chunk is mixed.
+          int kind = kChunkMixed;
+          if constexpr (MASK) kind = chunk_kind(mw[k], col0 + 32 * k, lim);
+          if (kind == kChunkAll) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            u0 = fmaxf(u0, (col0 + 32 * k + c <= lim && ((mw[k] >> c) & 1u)) ? u2f(sv[k][c]) : -INFINITY);
-            u1 = fmaxf(u1, (col0 + 32 * k + c + 1 <= lim && ((mw[k] >> (c + 1)) & 1u)) ? u2f(sv[k][c + 1])
-                                                                                       : -INFINITY);
+            for (int c = 0; c < 32; c += 4) {
+              u0 = max3f(u0, u2f(sv[k][c]), u2f(sv[k][c + 1]));
+              u1 = max3f(u1, u2f(sv[k][c + 2]), u2f(sv[k][c + 3]));
+            }
+          } else if (kind == kChunkMixed) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              u0 = fmaxf(u0, (col0 + 32 * k + c <= lim && ((mw[k] >> c) & 1u)) ? u2f(sv[k][c]) : -INFINITY);
+              u1 = fmaxf(u1, (col0 + 32 * k + c + 1 <= lim && ((mw[k] >> (c + 1)) & 1u)) ? u2f(sv[k][c + 1])
+                                                                                         : -INFINITY);
+            }
           }
           cm[k] = fmaxf(u0, u1);
         }
@@ -615,8 +655,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         a = col0 + ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 32, lim, mw[1])
                              : find_in_chunk(h[0], m, col0, lim, mw[0]));
       uint32_t pk[32];
-      float2 tsum2 = masked ? phi_half<true, MASK>(h, pk, col0, lim, c2, base, mw[0], mw[1])
-                            : phi_half<false, false>(h, pk, col0, lim, c2, base, ~0u, ~0u);
+      float2 tsum2 = phi_half_any<MASK>(masked, h, pk, col0, lim, c2, base, mw[0], mw[1]);
       tmem_ld32(scol + 64, h[0]);
       tmem_ld32(scol + 96, h[1]);
       tc_wait_ld();
@@ -631,9 +670,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = warp_wait(&p_empty[g], (j & 1u) ^ 1u);
       if (!ok) break;
       store_p_half(pk, prow, row_local);
-      const float2 t2 =
-          masked ? phi_store_half<true, MASK>(h, prow + BOX_BYTES, row_local, col0 + 64, lim, c2, base, mw[2], mw[3])
-                 : phi_store_half<false, false>(h, prow + BOX_BYTES, row_local, col0 + 64, lim, c2, base, ~0u, ~0u);
+      float2 t2;
+      {
+        uint32_t pk2[32];
+        t2 = phi_half_any<MASK>(masked, h, pk2, col0 + 64, lim, c2, base, mw[2], mw[3]);
+        store_p_half(pk2, prow + BOX_BYTES, row_local);
+      }
       tsum2 = __fadd2_rn(tsum2, t2);
       fence_proxy_async_smem();
       const float tsum = tsum2.x + tsum2.y;
