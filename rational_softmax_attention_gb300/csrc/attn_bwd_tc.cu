@@ -34,6 +34,7 @@
 // fp16 (unit roundoff 2^-11) instead of bf16 (2^-8) before their products.  With
 // |E| up to ~10 at wide score spreads, bf16 rounding alone costs ~2e-2 in dQ.
 #include "kernels.cuh"
+#include "phi.cuh"
 
 namespace raattn {
 namespace {
@@ -43,7 +44,6 @@ constexpr int BN = 128;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BOX_BYTES = 128 * 64 * 2;
 
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
 // 16-byte chunk `chunk` (0..15) of row r of a 128 x 128 bf16 K-major operand tile,
 // stored as two 64-column halves in the 128-byte-swizzled layout TMA and tcgen05 use.
@@ -389,12 +389,22 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         tc_wait_ld();
       }
       const int col0 = j * BN + cbase;   // key index of local column 0
-      const bool need_mask = MASK || col0 + DQ_COLS - 1 > lim;
       const uint32_t mw = MASK ? mrow[4 * j + part] : ~0u;
+      // With an attention mask, a chunk every row of the warp sees whole needs no per-entry
+      // test, and a chunk no row sees has zero coefficients and E (no arithmetic).  The vote
+      // runs in the masked instance only, where the whole warp is here together.
+      int kind = kChunkMixed;
+      if constexpr (MASK) kind = chunk_kind(mw, col0, lim);
+      const bool need_mask = MASK ? kind == kChunkMixed : col0 + DQ_COLS - 1 > lim;
+      const bool dead = MASK && kind == kChunkNone;
       // coefficient q^7 (1/w)^2 per entry, in place; the factor 1/(4 s_i) is applied with
       // dP - D_i below.  Four entries share two reciprocals (coef_quad).
+      if (dead) {
 #pragma unroll
-      for (int c = 0; c < DQ_COLS; c += 4) {
+        for (int c = 0; c < DQ_COLS; ++c) SV(c) = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < DQ_COLS && !dead; c += 4) {
         float x[4] = {u2f(SV(c)), u2f(SV(c + 1)), u2f(SV(c + 2)), u2f(SV(c + 3))};
         if (need_mask) {
 #pragma unroll
@@ -431,6 +441,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         uint32_t e16[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
+          if (dead) {
+            e16[t] = 0u;
+            continue;
+          }
           const int c = cc * 32 + 2 * t;
           const float2 dpp = make_float2(u2f(dv[2 * t]), u2f(dv[2 * t + 1]));
           const float2 ee = __fmul2_rn(make_float2(u2f(SV(c)), u2f(SV(c + 1))), __ffma2_rn(dpp, cE2, mcED2));
@@ -823,9 +837,16 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       for (int h = 0; h < KV_COLS / 32; ++h) tmem_ld32(lane_addr + KV_TM_ST + cbase + 32 * h, sv[h]);
       tc_wait_ld();
       // masked: key past N_K, or (causal) query i0 + c < j
-      const bool need_mask = MASK || !j_ok || (s.causal && i0 + cbase < j);
       const uint32_t mw = MASK ? mkey[4 * (qt0 + it) + part] : ~0u;
       const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
+      // With an attention mask, a chunk every key row of the warp sees whole needs no per-entry
+      // test, and a chunk none of them sees has zero P^T and dS^T (no constants read, no
+      // arithmetic).  The vote runs in the masked instance only, where the whole warp is here
+      // together.
+      int kind = kChunkMixed;
+      if constexpr (MASK) kind = chunk_vote(mw == ~0u && first_vis <= cbase, mw == 0u || first_vis >= cbase + KV_COLS);
+      const bool need_mask = MASK ? kind == kChunkMixed : (!j_ok || (s.causal && i0 + cbase < j));
+      const bool dead = MASK && kind == kChunkNone;
       // P^T = q^8 / s_i and the dS coefficient q^7 (1/w)^2 / s_i = q^7 (1 + q)^2 / s_i (in
       // place): with t = q^7 / s_i, P = t q and the coefficient is t + P (2 + q).  The factor
       // 1/4 comes with dP^T - D_i below.  Four entries share two reciprocals (as in coef_quad).
@@ -839,6 +860,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         for (int h = 0; h < 2; ++h) {
           const int cb = c + 4 * h;        // local column
           const int cg = cbase + cb;       // column in the tile
+          if (dead) {
+            SV(cb) = SV(cb + 1) = SV(cb + 2) = SV(cb + 3) = 0u;
+            pk[2 * h] = pk[2 * h + 1] = 0u;
+            continue;
+          }
           const float4 b4 = *reinterpret_cast<const float4*>(st_base + cg);
           const float4 i4 = *reinterpret_cast<const float4*>(st_invs + cg);
           float x[4] = {u2f(SV(cb)), u2f(SV(cb + 1)), u2f(SV(cb + 2)), u2f(SV(cb + 3))};
@@ -898,6 +924,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           uint32_t pk[4];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
+            if (dead) {
+              pk[2 * h] = pk[2 * h + 1] = 0u;
+              continue;
+            }
             const float4 d4 = *reinterpret_cast<const float4*>(st_d + cg + 4 * h);   // D_i / 4
             const int c = cb + 4 * h;
             const float2 q4 = make_float2(0.25f, 0.25f);

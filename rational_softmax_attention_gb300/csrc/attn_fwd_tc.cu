@@ -148,17 +148,6 @@ __device__ __forceinline__ void store_p_half(const uint32_t (&pk)[32], uint8_t* 
         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
-// How the 32-column chunk starting at key col0 is masked for this row (attention-mask word w,
-// last visible key lim), voted over the warp: every row sees all 32 columns, none sees any, or
-// mixed.  Key padding and block masks make the first two the rule away from their edges.  A
-// warp vote: call it only where all 32 lanes of the warp execute it together.
-constexpr int kChunkAll = 0, kChunkNone = 1, kChunkMixed = 2;
-__device__ __forceinline__ int chunk_kind(uint32_t w, int col0, int lim) {
-  if (__all_sync(0xffffffffu, w == ~0u && col0 + 31 <= lim)) return kChunkAll;
-  if (__all_sync(0xffffffffu, w == 0u || col0 > lim)) return kChunkNone;
-  return kChunkMixed;
-}
-
 // phi of one 64-key half (phi_half) through the cheapest path the warp's rows allow: with an
 // attention mask, a half every row sees whole runs unmasked, a half no row sees gives zeros
 // without the arithmetic, anything else the per-entry masked path; without one, the causal

@@ -1,4 +1,5 @@
-// phi of the rational soft-argmax on the FMA pipe, shared by the forward kernels.
+// phi of the rational soft-argmax on the FMA pipe, shared by the forward kernels, and the
+// attention-mask chunk vote shared by every masked tensor-core kernel.
 //
 // Page "Ra-Family: Rational Neural Architecture", section 3, ra_softmax: u = (x_max - x)/16,
 // q = (1-u)/(1+u), phi = q^8 for u < 1 and exactly 0 otherwise.  With w = (1+u)/2 computed
@@ -41,6 +42,22 @@ __device__ __forceinline__ int find_in_chunk(const uint32_t (&v)[32], float m, i
 #pragma unroll
   for (int c = 31; c >= 0; --c) idx = (u2f(v[c]) == m && col0 + c <= lim && ((mword >> c) & 1u)) ? c : idx;
   return idx;
+}
+
+// How a warp's 32-entry chunk of an attention-mask row is masked, voted over the warp: every
+// lane may see all 32 entries, none may see any, or mixed.  `all_vis` / `none_vis` are this
+// lane's answers (its mask word all ones / zero, and the causal or ragged limit).  Key padding
+// and block masks make the first two the rule away from their edges.  A warp vote: call it
+// only where all 32 lanes of the warp execute it together.
+constexpr int kChunkAll = 0, kChunkNone = 1, kChunkMixed = 2;
+__device__ __forceinline__ int chunk_vote(bool all_vis, bool none_vis) {
+  if (__all_sync(0xffffffffu, all_vis)) return kChunkAll;
+  if (__all_sync(0xffffffffu, none_vis)) return kChunkNone;
+  return kChunkMixed;
+}
+// The chunk of keys col0 .. col0 + 31 of a query row: mask word w, last visible key lim.
+__device__ __forceinline__ int chunk_kind(uint32_t w, int col0, int lim) {
+  return chunk_vote(w == ~0u && col0 + 31 <= lim, w == 0u || col0 > lim);
 }
 
 }  // namespace raattn
