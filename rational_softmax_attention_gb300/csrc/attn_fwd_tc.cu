@@ -696,7 +696,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_wait_ld();
         float o[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = u2f(ov[e]) * inv;
+        // a row with no visible key writes exact zeros: when every P V product of the query
+        // tile was skipped, the accumulator was never written and holds stale bits
+        for (int e = 0; e < 32; ++e) o[e] = rowsum > 0.0f ? u2f(ov[e]) * inv : 0.0f;
         if (args.out_bf16)
           warp_store_block32<true>(stage, o, args.o, row0, D, c0, n_ok, lane);
         else

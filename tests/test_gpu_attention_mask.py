@@ -148,3 +148,21 @@ def test_autograd_with_attn_mask():
             for name, got, want in (("O", out, wo), ("dq", qg.grad, gq), ("dk", kg.grad, gk), ("dv", vg.grad, gv)):
                 g = parity.f64(got[b, h])
                 assert np.all(np.abs(g - want) <= 1e-2 + 2.0 ** -8 * np.abs(want)), name
+
+
+@pytest.mark.parametrize("D,nq,empty", [(64, 300, (0, 128)), (128, 600, (0, 256)), (128, 600, (256, 512))])
+def test_query_tiles_with_no_allowed_key_give_zeros(D, nq, empty):
+    """A mask that leaves whole query tiles (D = 64: one 128-row tile; D = 128 CTA pairs: the 256
+    rows of one product) with no allowed key: every P V product of those rows is skipped, so
+    their accumulator is never written, and O must still be exactly 0 there, with the rest of
+    the head matching the oracle."""
+    B, H, nk = 1, 2, 384
+    q, k, v, do = attention_inputs(B, H, nq, nk, D, seed=D + nq, dtype=torch.bfloat16)
+    rng = np.random.default_rng(D + nq)
+    mask = rng.random((nq, nk)) < 0.5
+    mask[:, 0] = True
+    mask[empty[0]:empty[1]] = False
+    o, rs, ra_, dq, dk, dv = _check(q, k, v, do, D ** -0.5, False, mask)
+    lo, hi = empty
+    assert torch.all(o[:, :, lo:hi] == 0) and torch.all(rs[:, :, lo:hi] == 0) and torch.all(ra_[:, :, lo:hi] == -1)
+    assert torch.all(dq[:, :, lo:hi] == 0)
