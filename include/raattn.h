@@ -100,16 +100,20 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
  *                row_m, row_s and row_arg are what ra_attention_bwd needs; each may
  *                be NULL when no backward follows.
  *   tile_counts  optional (NULL allowed) int64[2] in device memory, zeroed then written:
- *                [0] = (query tile, key tile) pairs visited by the second pass,
- *                [1] = pairs whose P*V product was skipped because every entry of
- *                      the pair lies outside the compact support (the V tile is still
- *                      loaded: the decision is taken while it is in flight).
+ *                [0] = (query tile, key tile) pairs in range (for causal calls, the key
+ *                      tiles up to the query tile's diagonal),
+ *                [1] = pairs whose P*V product did not run: every entry of the pair lies
+ *                      outside the compact support (the V tile is still loaded: the
+ *                      decision is taken while it is in flight), or, in masked calls, the
+ *                      mask allows no pair of the tile (such tiles are not loaded, and
+ *                      take no part in either pass).
  *                Tiles are 128 x 128 on the tensor-core path; at D = 128 with N_Q > 256
  *                two query tiles share each product (CTA pairs), which is skipped
  *                only when both are.
  *   workspace    device memory of ra_attention_fwd_workspace_size() bytes, 16-byte
  *                aligned, contents on entry irrelevant; required for RA_BF16 inputs
  *                (NULL allowed for RA_F32).  The call writes an fp16 copy of v there
+ *                (masked calls also a map of the 128 x 128 tiles the mask allows a pair in)
  *                and forms P V in fp16, with P rounded to 2^-11 instead of 2^-8.  The
  *                copy is exact for 2^-14 <= |v| <= 65504 (normal fp16); smaller
  *                magnitudes become fp16 subnormals, rounded to a multiple of 2^-24
@@ -134,9 +138,10 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
                              ra_dtype_t in_dtype, ra_dtype_t out_dtype, void* stream);
 
 /*
- * ra_attention_fwd_workspace_size -- bytes of device workspace ra_attention_fwd needs
- * for these sizes: the fp16 copy of v (B*H*N_K*D*2 bytes, padded to 256).  Returns 0
- * for invalid sizes.
+ * ra_attention_fwd_workspace_size -- bytes of device workspace ra_attention_fwd (and
+ * ra_attention_fwd_masked) needs for these sizes: the fp16 copy of v (B*H*N_K*D*2 bytes,
+ * padded to 256), then the tile map a masked call builds (B*H*ceil(N_Q/128) rows of
+ * ceil(ceil(N_K/128)/32) uint32 words, padded to 256).  Returns 0 for invalid sizes.
  */
 size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 

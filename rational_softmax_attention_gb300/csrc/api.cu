@@ -53,6 +53,10 @@ ra_status_t make_ctx(LaunchCtx* ctx) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Forward workspace: the fp16 copy of V, then (masked calls) the tile live map of up to B * H
+// mask heads, 128-row query tiles by ceil(N_K / 128 / 32) words.  Each piece 256-byte padded.
+int live_words_for(int NK) { return ((NK + 127) / 128 + 31) / 32; }
 bool dtype_ok(ra_dtype_t t) { return t == RA_F32 || t == RA_BF16; }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
@@ -123,6 +127,14 @@ ra_status_t check_attn_sizes(int B, int H, int NQ, int NK, int D) {
 }
 
 }  // namespace
+
+size_t fwd_workspace_v_bytes(int B, int H, int NK, int D) {
+  return (static_cast<size_t>(B) * H * NK * D * 2 + 255) & ~static_cast<size_t>(255);
+}
+size_t fwd_workspace_live_bytes(int B, int H, int NQ, int NK) {
+  const size_t nqt = (static_cast<size_t>(NQ) + 127) / 128;
+  return (static_cast<size_t>(B) * H * nqt * live_words_for(NK) * 4 + 255) & ~static_cast<size_t>(255);
+}
 
 size_t bwd_workspace_bytes(int B, int H, int NQ, int NK, int D, bool f32_inputs) {
   if (check_attn_sizes(B, H, NQ, NK, D) != RA_OK) return 0;
@@ -200,7 +212,7 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
 
 size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D) {
   if (check_attn_sizes(B, H, N_Q, N_K, D) != RA_OK) return 0;
-  return (static_cast<size_t>(B) * H * N_K * D * 2 + 255) & ~static_cast<size_t>(255);   // fp16 copy of V
+  return raattn::fwd_workspace_v_bytes(B, H, N_K, D) + raattn::fwd_workspace_live_bytes(B, H, N_Q, N_K);
 }
 
 }  // extern "C"
@@ -214,6 +226,8 @@ ra_status_t mask_args(const uint32_t* bits, int MB, int MH, int B, int H, int co
   m->words = ra_attention_mask_words(cols);
   m->mb = MB;
   m->mh = MH;
+  m->live = nullptr;
+  m->live_words = 0;
   if (!bits) return RA_OK;
   if (!aligned16(bits) || !(MB == 1 || MB == B) || !(MH == 1 || MH == H)) return RA_ERR_ARG;
   return RA_OK;
@@ -268,6 +282,14 @@ ra_status_t attn_fwd_impl(const void* q, const void* k, const void* v, void* o, 
   a.tile_counts = reinterpret_cast<unsigned long long*>(tile_counts);
   a.out_bf16 = out_dtype == RA_BF16 ? 1 : 0;
   a.mask = mask;
+  if (mask.bits) {   // tile live map after the V copy: fully masked tiles are left out of both passes
+    uint32_t* live = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + fwd_workspace_v_bytes(B, H, N_K, D));
+    a.mask.live = live;
+    a.mask.live_words = live_words_for(N_K);
+    if (launch_mask_tile_live(mask.bits, mask.mb * mask.mh, N_Q, N_K, mask.words, live, a.mask.live_words, st) !=
+        cudaSuccess)
+      return RA_ERR_LAUNCH;
+  }
   if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
   const KernelEvents ev = current_events();
   if (ev.rec(0, st) != cudaSuccess) return RA_ERR_LAUNCH;
@@ -287,7 +309,7 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
                              int32_t* row_arg, int64_t* tile_counts, void* workspace, int B, int H, int N_Q,
                              int N_K, int D, float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t out_dtype,
                              void* stream) {
-  const MaskBits none{nullptr, 0, 1, 1};
+  const MaskBits none{nullptr, 0, 1, 1, nullptr, 0};
   return attn_fwd_impl(q, k, v, o, row_m, row_s, row_arg, tile_counts, workspace, B, H, N_Q, N_K, D, scale, causal,
                        in_dtype, out_dtype, stream, none);
 }
@@ -401,7 +423,7 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
                              void* dv, void* workspace, int B, int H, int N_Q, int N_K, int D, float scale,
                              int causal, ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype,
                              void* stream) {
-  const MaskBits none{nullptr, 0, 1, 1};
+  const MaskBits none{nullptr, 0, 1, 1, nullptr, 0};
   return attn_bwd_impl(q, k, v, o, dout, row_m, row_s, row_arg, dq, dk, dv, workspace, B, H, N_Q, N_K, D, scale,
                        causal, in_dtype, o_dtype, grad_dtype, stream, none, none);
 }

@@ -173,6 +173,13 @@ __device__ __forceinline__ float2 phi_half_any(bool masked, const uint32_t (&h)[
 
 // MASK: a boolean attention mask (args.mask) applies on top of `causal`.  PAIR: the CTA
 // pair form (FwdCfg).
+// One word of the key-tile walk: bit t of bits[g] is whether product g takes key tile 32 w + t
+template <int NG>
+struct TileWalk {
+  int w = -1;
+  uint32_t bits[NG];
+};
+
 template <int D, bool MASK, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_tc_kernel(const AttnShape s, const __grid_constant__ FwdTcArgs args, const LaunchCtx ctx) {
@@ -246,6 +253,61 @@ __global__ void __launch_bounds__(THREADS, 1)
   // producer streams all nkt for the last product, and the other issuer releases the
   // stages it does not use
   auto group_keys = [&](int g) { return last_key_of(tile_row0(g, NCTA - 1) + BM) / BN + 1; };
+  // The mask head of this (batch, head), and the key tiles product g takes part in: its causal
+  // range and, with a tile live map, the tiles holding an allowed pair for one of its query
+  // tiles.  Every role walks the same tiles: the producer streams those either product takes
+  // (a tile neither takes is left out of both passes: no copy, no product, no softmax work),
+  // each issuer issues only its own product's and waits on and releases the others.
+  const int gm = MASK ? (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0) : 0;
+  // tiles 32 w .. 32 w + 31 that product g takes, as bits
+  auto take_word = [&](int g, int w) -> uint32_t {
+    const int n = group_keys(g) - 32 * w;
+    uint32_t bits = n >= 32 ? ~0u : (n > 0 ? (1u << n) - 1u : 0u);
+    if constexpr (MASK) {
+      if (args.mask.live && bits) {
+        uint32_t any = 0;
+#pragma unroll
+        for (int r = 0; r < NCTA; ++r) {
+          const int qt = tile_row0(g, r) / BM;
+          if (qt < nqt) any |= args.mask.live[(static_cast<size_t>(gm) * nqt + qt) * args.mask.live_words + w];
+        }
+        bits &= any;
+      }
+    }
+    return bits;
+  };
+  // Each role walks the tiles in increasing order and keeps the current word of both products
+  TileWalk<NGROUP> walk;
+  auto walk_word = [&](int w) {
+    if (walk.w != w) {
+      walk.w = w;
+#pragma unroll
+      for (int g = 0; g < NGROUP; ++g) walk.bits[g] = take_word(g, w);
+    }
+  };
+  auto takes = [&](int g, int j) -> bool {   // product g takes key tile j
+    if constexpr (!MASK) return j < group_keys(g);   // no map: the whole range
+    walk_word(j >> 5);
+    uint32_t b = 0;
+#pragma unroll
+    for (int h = 0; h < NGROUP; ++h)   // g is not a compile-time index: select, keep bits in registers
+      if (h == g) b = walk.bits[h];
+    return (b >> (j & 31)) & 1u;
+  };
+  // first tile after j that product g (g < 0: either product) takes, or -1
+  auto next_tile = [&](int g, int j) -> int {
+    if constexpr (!MASK) return j + 1 < (g < 0 ? nkt : group_keys(g)) ? j + 1 : -1;
+    for (int t = j + 1; t < nkt; t = (t | 31) + 1) {
+      walk_word(t >> 5);
+      uint32_t u = 0;
+#pragma unroll
+      for (int h = 0; h < NGROUP; ++h)
+        if (g < 0 || g == h) u |= walk.bits[h];
+      u >>= (t & 31);
+      if (u) return t + __ffs(static_cast<int>(u)) - 1;
+    }
+    return -1;
+  };
   // Barrier operations of the pair form: arrivals go to the even CTA's barrier, products and
   // commits span both CTAs.  Arrivals release, and waits acquire, at CTA scope: what they
   // order is this SM's own shared and tensor memory (a P tile, the scores a warp has read)
@@ -348,13 +410,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         return true;
       };
       bool ok = true;
-      for (int j = 0; j < nkt && ok; ++j) ok = issue(false, j);              // pass 1: K_0 .. K_{n-1}
-      if (ok) ok = issue(false, 0);                                          // pass 2: K_0, then
-      for (int j = 1; j < nkt && ok; ++j) {                                  //   K_j, V_{j-1}
+      // pass 1: K of every tile either product takes; pass 2 over those tiles t0 < t1 < ...:
+      // K_t0, then K_ti and V_t(i-1) interleaved, then the last V
+      for (int j = next_tile(-1, -1); j >= 0 && ok; j = next_tile(-1, j)) ok = issue(false, j);
+      int prev = -1;
+      for (int j = next_tile(-1, -1); j >= 0 && ok; j = next_tile(-1, j)) {
         ok = issue(false, j);
-        if (ok) ok = issue(true, j - 1);
+        if (ok && prev >= 0) ok = issue(true, prev);
+        prev = j;
       }
-      if (ok) ok = issue(true, nkt - 1);                                     //   V_{n-1}
+      if (ok && prev >= 0) ok = issue(true, prev);
       if constexpr (PAIR) {
         // Both CTAs' copies complete on the even CTA's barriers, so the even producer drains
         // them for both, after the first closing cluster barrier.  The two producers may have
@@ -401,7 +466,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int nkt_b = PAIR ? tile_keys(1) : 0;
       uint32_t pos = 0;   // ring position (K and V tiles in producer order)
       uint32_t uc0 = 0, uc1 = 0;   // S products issued into score buffer 0 and 1
-      unsigned long long visited = 0, skipped = 0;
+      // pairs in the product's range (its query tiles' key ranges), and those whose P V product ran
+      const unsigned long long visited = static_cast<unsigned long long>(nkt_a + nkt_b);
+      unsigned long long ran = 0;
       bool o_started = false;
       auto ring_wait = [&](uint32_t p, uint32_t& addr) -> bool {
         const int st = p % NST;
@@ -428,8 +495,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (b) ++uc1; else ++uc0;
         return true;
       };
-      auto mma_pv = [&](int j, uint32_t vaddr) -> bool {   // O_g += P_g V_j
-        if (!wait_bar(&p_full[g], j & 1u)) return false;   // P tiles and votes of both CTAs
+      // O_g += P_g V_j, the product's c-th P tile (p_full's phase c)
+      auto mma_pv = [&](int j, uint32_t c, uint32_t vaddr) -> bool {
+        if (!wait_bar(&p_full[g], c & 1u)) return false;   // P tiles and votes of both CTAs
         tc_fence_after();
         // votes of the warps of product g (the odd CTA's read from its shared memory), each
         // tagged with its key tile: a vote that is not this tile's counts as live, so the
@@ -447,10 +515,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int any = 0;
 #pragma unroll
         for (int w = 0; w < NCTA * GROUP_WARPS; ++w) any |= (v[w] >> 1) != j || (v[w] & 1);
-        const int vis = (j < nkt_a ? 1 : 0) + (j < nkt_b ? 1 : 0);
-        visited += vis;
-        if (any == 0) skipped += vis;
         if (any != 0) {
+          ran += (j < nkt_a ? 1 : 0) + (j < nkt_b ? 1 : 0);   // (query tile, key tile) pairs of the product
           const uint32_t vlo = sdesc_lo(vaddr, BOX_BYTES);
           const uint32_t acc0 = o_started ? 1u : 0u;
 #pragma unroll
@@ -468,41 +534,47 @@ __global__ void __launch_bounds__(THREADS, 1)
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
       if (ok && ctx.force_timeout) ok = wait_bar(&drain[g], 0);
       uint32_t ka = 0, va = 0;
-      // pass 1: S_g(j) for every key tile; a ring stage is free once both issuers commit.
-      // Tiles from nkt_g on are only waited for and released: waiting for the fill keeps
-      // this issuer from releasing a stage's next use before the other issuer has read it.
-      const int nkt_g = group_keys(g);
-      for (int j = 0; j < nkt && ok; ++j) {
+      // pass 1: S_g(j) for every key tile the product takes, into score buffer c & 1 for its
+      // c-th; a ring stage is free once both issuers commit.  Tiles only the other product
+      // takes are waited for and released: waiting for the fill keeps this issuer from
+      // releasing a stage's next use before the other issuer has read it.
+      uint32_t c = 0;
+      for (int j = next_tile(-1, -1); j >= 0 && ok; j = next_tile(-1, j)) {
         ok = ring_wait(pos, ka);
-        if (ok && j < nkt_g) ok = mma_s(ka, j & 1);
+        if (ok && takes(g, j)) ok = mma_s(ka, static_cast<int>(c++ & 1u));
         if (ok) commit(&ring_empty[pos % NST]);
         ++pos;
       }
-      // pass 2: S_g(0); then per j: S_g(j+1), O_g(j)
-      if (ok) ok = ring_wait(pos, ka);
-      if (ok) ok = mma_s(ka, 0);
-      if (ok) commit(&ring_empty[pos % NST]);
-      ++pos;
-      for (int j = 0; j < nkt && ok; ++j) {
-        const bool more = j + 1 < nkt;
-        uint32_t kpos = 0;
-        if (more) {
-          kpos = pos++;
+      // pass 2 over the same tiles t0 < t1 < ...: S_g(t0); then per ti: S_g(t(i+1)), O_g(ti),
+      // every S product into buffer 0 and the c-th O product after the c-th P tile
+      c = 0;
+      int j = next_tile(-1, -1);
+      if (ok && j >= 0) {
+        ok = ring_wait(pos, ka);
+        if (ok && takes(g, j)) ok = mma_s(ka, 0);
+        if (ok) commit(&ring_empty[pos % NST]);
+        ++pos;
+      }
+      for (; j >= 0 && ok;) {
+        const int jn = next_tile(-1, j);
+        if (jn >= 0) {
+          const uint32_t kpos = pos++;
           ok = ring_wait(kpos, ka);
-          if (ok && j + 1 < nkt_g) ok = mma_s(ka, 0);
+          if (ok && takes(g, jn)) ok = mma_s(ka, 0);
           if (ok) commit(&ring_empty[kpos % NST]);
         }
         const uint32_t vpos = pos++;
         if (ok) ok = ring_wait(vpos, va);
-        if (ok && j < nkt_g) ok = mma_pv(j, va);
+        if (ok && takes(g, j)) ok = mma_pv(j, c++, va);
         if (ok) commit(&ring_empty[vpos % NST]);
+        j = jn;
       }
       if (ok) commit(&o_full[g]);
       commit(&drain[g]);
       drain_wait(&drain[g], 0, ctx);
       if (ok && args.tile_counts) {
         atomicAdd(&args.tile_counts[0], visited);
-        atomicAdd(&args.tile_counts[1], skipped);
+        atomicAdd(&args.tile_counts[1], visited - ran);
       }
     }
   } else {
@@ -523,7 +595,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // this row's attention-mask words: four per key tile (rows past N_Q read the last row)
     const uint32_t* mrow = nullptr;
     if (MASK) {
-      const int gm = (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0);
       mrow = args.mask.bits + (static_cast<size_t>(gm) * s.NQ + min(row, s.NQ - 1)) * args.mask.words;
     }
     auto mask_words = [&](int j, uint32_t (&mw)[4]) {
@@ -539,7 +610,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     uint32_t sv[BN / 32][32];
     // S_g into registers, then hand the buffer back to the MMA thread
-    // pass-1 tile j sits in score buffer j & 1, as that buffer's use j >> 1
     auto take_s = [&](int b, uint32_t use) -> bool {
       if (!warp_wait(&s_full[2 * g + b], use & 1u)) return false;
       tc_fence_after();
@@ -558,10 +628,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m = -INFINITY;
     int a = -1;
     int jm = 0;   // 32-column chunk (tile * 4 + chunk) holding the first occurrence of the maximum
-    // pass 1: running maximum of the raw scores q.k (scale > 0 keeps the argmax)
-    const int nkt_g = group_keys(g);
-    for (int j = 0; j < nkt_g && ok; ++j) {
-      ok = take_s(j & 1, static_cast<uint32_t>(j) >> 1);
+    // pass 1: running maximum of the raw scores q.k (scale > 0 keeps the argmax), over the
+    // key tiles the product takes; its c-th sits in score buffer c & 1, as that buffer's use c >> 1
+    uint32_t c = 0;
+    for (int j = next_tile(g, -1); j >= 0 && ok; j = next_tile(g, j)) {
+      ok = take_s(static_cast<int>(c & 1u), c >> 1);
+      ++c;
       if (!ok) break;
       const int col0 = j * BN;   // key index of column 0
       uint32_t mw[4];
@@ -625,8 +697,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float base = (m > -INFINITY) ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
     uint8_t* prow = sP + g * C::P_BYTES + row_local * 128;
     float rowsum = 0.0f;
-    sidx = static_cast<uint32_t>(nkt_g + 1) >> 1;   // pass 1 used buffer 0 for tiles 0, 2, 4, ...
-    for (int j = 0; j < nkt_g && ok; ++j) {
+    sidx = (c + 1) >> 1;   // pass 1 used buffer 0 for its tiles 0, 2, 4, ...
+    c = 0;                 // P tiles written
+    for (int j = next_tile(g, -1); j >= 0 && ok; j = next_tile(g, j)) {
       ok = warp_wait(&s_full[2 * g], sidx & 1u);   // buffer 0
       if (!ok) break;
       ++sidx;
@@ -656,7 +729,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 96, lim, mw[3])
                       : find_in_chunk(h[0], m, col0 + 64, lim, mw[2]));
       // the P tile is free once the previous O_g += P_g V product has completed
-      ok = warp_wait(&p_empty[g], (j & 1u) ^ 1u);
+      ok = warp_wait(&p_empty[g], (c & 1u) ^ 1u);
       if (!ok) break;
       store_p_half(pk, prow, row_local);
       float2 t2;
@@ -674,6 +747,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       __syncwarp();
       if (lane == 0) arrive_even(&p_full[g]);
+      ++c;
       rowsum += tsum;
     }
 #undef SV

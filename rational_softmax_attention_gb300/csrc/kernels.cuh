@@ -20,11 +20,18 @@ struct MaskBits {
   const uint32_t* bits;   // null: no mask
   int words;
   int mb, mh;
+  const uint32_t* live;   // optional tile live map of the same mask heads (null: every tile may be live)
+  int live_words;         // words per query tile row of the map
 };
 // Packs a [G, NQ, NK] byte mask (nonzero = may attend) into bits_q [G, NQ, wq] (rows = queries)
 // and bits_k [G, NK, wk] (rows = keys); either may be null (mask.cu).
 cudaError_t launch_mask_pack(const uint8_t* mask, int G, int NQ, int NK, uint32_t* bits_q, int wq, uint32_t* bits_k,
                              int wk, cudaStream_t st);
+// Tile live map from packed query rows (bits_q, `words` per row): for mask head g and 128-row
+// query tile qt, bit kt of live[(g * nqt + qt) * live_words + kt / 32] is set when any pair of
+// the 128 x 128 block (query tile qt, key tile kt) may attend (mask.cu).
+cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live,
+                                  int live_words, cudaStream_t st);
 
 // Caller-supplied CUDA events recorded at an attention call's kernel boundaries (a
 // measurement knob, ra_debug_kernel_events): e[i] is recorded before kernel i of the call
@@ -107,6 +114,9 @@ struct BwdTcArgs {
   MaskBits mask_k;   // the same mask transposed, rows = keys (dK/dV kernel)
 };
 constexpr int kConstBlockFloats = 5 * 128;
+// Forward workspace pieces (api.cu): the fp16 copy of V, and the tile live map of a masked call.
+size_t fwd_workspace_v_bytes(int B, int H, int NK, int D);
+size_t fwd_workspace_live_bytes(int B, int H, int NQ, int NK);
 // Workspace bytes the backward uses for these sizes and input dtype (api.cu): the CUDA-core
 // fp32 path needs only two per-row float arrays; the tensor-core path the constant blocks and
 // the fp16 operand copies.  0 for invalid sizes.

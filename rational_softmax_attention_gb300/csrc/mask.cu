@@ -4,7 +4,8 @@
 // scaled_dot_product_attention, whose boolean attn_mask marks with True the (query, key)
 // pairs that take part.  The kernels read the mask one 32-column word per row and tile
 // chunk: bits_q with a row per query (forward, dQ kernel) and bits_k with a row per key
-// (dK/dV kernel, whose threads own key rows).
+// (dK/dV kernel, whose threads own key rows).  A tile live map (one bit per 128 x 128 block
+// with any allowed pair) lets a kernel leave fully masked tiles out altogether.
 #include "kernels.cuh"
 
 namespace raattn {
@@ -47,7 +48,43 @@ __global__ void __launch_bounds__(32 * WARPS) mask_pack_cols_kernel(const uint8_
   if (j < NK) bits[(g * NK + j) * words + w] = word;
 }
 
+// One warp per (mask head, query tile, key tile): bit kt of the tile's live words is set when
+// any of the query tile's rows may attend to any key of the tile, read from the packed rows
+// (four words per key tile).  Lane l scans rows l, l + 32, l + 64, l + 96 of the query tile.
+__global__ void __launch_bounds__(32 * WARPS) mask_tile_live_kernel(const uint32_t* bits_q, int NQ, int words,
+                                                                    int nqt, int nkt, uint32_t* live, int live_words,
+                                                                    long long total) {
+  const long long wid = static_cast<long long>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= total) return;   // uniform across the warp
+  const int kt = static_cast<int>(wid % nkt);
+  const long long rest = wid / nkt;   // g * nqt + qt
+  const int qt = static_cast<int>(rest % nqt);
+  const long long g = rest / nqt;
+  uint32_t any = 0;
+  for (int r = lane; r < 128; r += 32) {
+    const int i = qt * 128 + r;
+    if (i < NQ) {
+      const uint4 u = *reinterpret_cast<const uint4*>(bits_q + (g * NQ + i) * words + 4 * kt);
+      any |= u.x | u.y | u.z | u.w;
+    }
+  }
+  const bool on = __any_sync(0xffffffffu, any != 0);
+  if (lane == 0 && on) atomicOr(&live[rest * live_words + kt / 32], 1u << (kt % 32));
+}
+
 }  // namespace
+
+cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live,
+                                  int live_words, cudaStream_t st) {
+  const int nqt = (NQ + 127) / 128, nkt = (NK + 127) / 128;
+  cudaError_t e = cudaMemsetAsync(live, 0, static_cast<size_t>(G) * nqt * live_words * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  const long long total = static_cast<long long>(G) * nqt * nkt;
+  const unsigned grid = static_cast<unsigned>((total + WARPS - 1) / WARPS);
+  mask_tile_live_kernel<<<grid, 32 * WARPS, 0, st>>>(bits_q, NQ, words, nqt, nkt, live, live_words, total);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mask_pack(const uint8_t* mask, int G, int NQ, int NK, uint32_t* bits_q, int wq, uint32_t* bits_k,
                              int wk, cudaStream_t st) {

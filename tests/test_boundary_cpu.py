@@ -84,8 +84,11 @@ def test_attention_fwd_validation(lib):
     assert _fwd(lib, D=48, in_dt=0) == 2                              # fp32 path: D in {16, 32, 64, 128}
     assert _fwd(lib, ws=NULL) == 1                                    # bf16 needs the fp16 V workspace
     assert _fwd(lib, ws=MISALIGNED) == 1
-    assert lib.ra_attention_fwd_workspace_size(4, 16, 8192, 8192, 128) == 4 * 16 * 8192 * 128 * 2
-    assert lib.ra_attention_fwd_workspace_size(1, 1, 3, 3, 64) == 512
+    # the fp16 V copy, then the masked calls' tile map (ceil(N_Q / 128) rows of
+    # ceil(ceil(N_K / 128) / 32) words per head), each padded to 256 bytes
+    assert lib.ra_attention_fwd_workspace_size(4, 16, 8192, 8192, 128) == 4 * 16 * 8192 * 128 * 2 + 4 * 16 * 64 * 2 * 4
+    assert lib.ra_attention_fwd_workspace_size(1, 3, 300, 5000, 64) == (3 * 5000 * 64 * 2 + 255) // 256 * 256 + 256
+    assert lib.ra_attention_fwd_workspace_size(1, 1, 3, 3, 64) == 512 + 256   # 384 V bytes, 4 map bytes
     assert lib.ra_attention_fwd_workspace_size(1, 1, 3, 0, 64) == 0
 
 

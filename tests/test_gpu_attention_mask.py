@@ -166,3 +166,61 @@ def test_query_tiles_with_no_allowed_key_give_zeros(D, nq, empty):
     lo, hi = empty
     assert torch.all(o[:, :, lo:hi] == 0) and torch.all(rs[:, :, lo:hi] == 0) and torch.all(ra_[:, :, lo:hi] == -1)
     assert torch.all(dq[:, :, lo:hi] == 0)
+
+
+def _expected_tile_counts(blocks, nq, nk, causal, span):
+    """(pairs in range, pairs whose P V product does not run) for a block mask: blocks[qt, kt]
+    says whether query tile qt may attend to anything in key tile kt (random fill inside a live
+    block, so every live block in causal range holds an allowed pair).  A product covers `span`
+    consecutive query tiles and runs on key tile kt when any of them has a live block there in
+    range; its pairs (one per query tile with kt in range) all count as run then."""
+    nqt, nkt = -(-nq // 128), -(-nk // 128)
+
+    def keys(qt):
+        last = min(nk - 1, min(nq - 1, qt * 128 + 127)) if causal else nk - 1
+        return last // 128 + 1
+    visited = sum(keys(qt) for qt in range(nqt))
+    ran = 0
+    for p0 in range(0, nqt, span):
+        tiles = range(p0, min(p0 + span, nqt))
+        for kt in range(nkt):
+            if any(kt < keys(qt) and blocks[qt, kt] for qt in tiles):
+                ran += sum(kt < keys(qt) for qt in tiles)
+    return visited, visited - ran
+
+
+@pytest.mark.parametrize("D,nq,nk", [(64, 520, 700), (128, 520, 700), (128, 1024, 896)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("layout", ["per_head", "per_batch"])
+def test_block_sparse_masks_leave_dead_tiles_out(D, nq, nk, causal, layout):
+    """Block-sparse masks (each 128 x 128 block either fully masked or randomly half filled,
+    a different block pattern per mask head): fully masked tiles are left out of both passes
+    (no copy, no product), the results match the oracle, and the tile counters show exactly
+    the pairs no product ran on.  With D = 128 and N_Q > 256 two query tiles share each
+    product (CTA pairs), so a key tile is left out only when it is dead for both."""
+    B, H = 2, 2
+    q, k, v, do = attention_inputs(B, H, nq, nk, D, seed=nq + nk + D, sigma_qk=1.0, dtype=torch.bfloat16)
+    rng = np.random.default_rng(nq * 7 + nk + D + int(causal))
+    nqt, nkt = -(-nq // 128), -(-nk // 128)
+    G = H if layout == "per_head" else B
+    blocks = rng.random((G, nqt, nkt)) < 0.45
+    blocks[:, :, 0] = True   # every row keeps some key
+    fine = rng.random((G, nqt * 128, nkt * 128)) < 0.5
+    dense = np.repeat(np.repeat(blocks, 128, axis=1), 128, axis=2) & fine
+    dense = dense[:, :nq, :nk]
+    dense[:, :, 0] = True
+    mask = dense[None] if layout == "per_head" else dense[:, None]
+    _check(q, k, v, do, D ** -0.5, causal, mask, heads=[(0, 0), (1, 1)])
+    pm = ra.pack_attn_mask(torch.from_numpy(np.ascontiguousarray(mask)).cuda(), B, H, nq, nk)
+    _, _, _, _, counts = ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), causal=causal, tile_counts=True,
+                                                 mask=pm)
+    torch.cuda.synchronize()
+    got = tuple(int(c) for c in counts.tolist())
+    span = 2 if D == 128 and nq > 256 else 1
+    want = [0, 0]
+    for b in range(B):
+        for h in range(H):
+            vis, skip = _expected_tile_counts(blocks[h if layout == "per_head" else b], nq, nk, causal, span)
+            want[0] += vis
+            want[1] += skip
+    assert got == tuple(want)

@@ -129,12 +129,16 @@ def run_roles(roles, rng, max_steps=400000):
 
 class ForwardModel:
     """One work item of the forward: NCTA CTAs (1, or a pair), two products (query tiles, or
-    pairs of them), NST ring stages, nkt key tiles (nkt_g[g] of them needed by product g)."""
+    pairs of them), NST ring stages, and the key tiles each product takes (takes[g]: its causal
+    range, less the tiles a tile live map shows fully masked).  The producer streams the tiles
+    either product takes; a tile neither takes is in no pass."""
 
     NGROUP, WARPS = 2, 4
 
-    def __init__(self, ncta, nst, nkt, nkt_g, dead, mutation=None):
-        self.ncta, self.nst, self.nkt, self.nkt_g, self.dead, self.mutation = ncta, nst, nkt, nkt_g, dead, mutation
+    def __init__(self, ncta, nst, takes, dead, mutation=None):
+        self.ncta, self.nst, self.dead, self.mutation = ncta, nst, dead, mutation
+        self.takes = [sorted(t) for t in takes]
+        self.tiles = sorted(set(takes[0]) | set(takes[1]))   # the walk: tiles either product takes
         n, G, W = ncta, self.NGROUP, self.WARPS
         sw = W if mutation == "single_cta_counts" else n * W
         self.q_full = Bar("q_full", 1)
@@ -149,21 +153,25 @@ class ForwardModel:
         self.stage_readers = [defaultdict(int) for _ in range(nst)]
         self.s_written = defaultdict(set)    # (g, b) -> uses whose product completed
         self.s_readers = defaultdict(int)    # (g, b, use) -> warps reading
-        self.p_written = defaultdict(set)    # (g, j) -> warps that wrote P
-        self.pv_done = set()
+        self.s_tile = {}                     # (g, b, use) -> key tile whose scores the use holds
+        self.p_written = defaultdict(set)    # (g, c) -> warps that wrote the c-th P tile
+        self.p_tile = {}                     # (g, c) -> key tile of the c-th P tile
+        self.pv_done = set()                 # (g, c): the c-th P V product completed (or was skipped)
         self.pv_issued = defaultdict(int)
         self.outstanding = defaultdict(int)
 
     def producer(self, r):
-        n, nst = self.ncta, self.nst
+        n, nst, t = self.ncta, self.nst, self.tiles
         arms = r == 0
         if arms:
             yield ("do", lambda: self.q_full.arrive(0, tx=n))
         yield ("copy", self.q_full, 0, None)
-        fills = [("K", j) for j in range(self.nkt)] + [("K", 0)]
-        for j in range(1, self.nkt):
-            fills += [("K", j), ("V", j - 1)]
-        fills.append(("V", self.nkt - 1))
+        fills = [("K", j) for j in t]
+        if t:
+            fills.append(("K", t[0]))
+            for i in range(1, len(t)):
+                fills += [("K", t[i]), ("V", t[i - 1])]
+            fills.append(("V", t[-1]))
         for it, _ in enumerate(fills):
             st, use = it % nst, it // nst
             yield ("wait", self.ring_empty[r][st], use - 1)
@@ -177,8 +185,8 @@ class ForwardModel:
             yield ("copy", self.ring_full[st], use, land)
 
     def issuer(self, g):
-        n, nst = self.ncta, self.nst
-        nkt, nkt_g = self.nkt, self.nkt_g[g]
+        n, nst, t = self.ncta, self.nst, self.tiles
+        mine = set(self.takes[g])
         yield ("wait", self.q_full, 0)
         uses = [0, 0]
 
@@ -202,79 +210,94 @@ class ForwardModel:
                 done()
             return ("mma", g, complete)
 
-        def mma_s(p, b):
+        def mma_s(p, b, j):
             use = uses[b]
             yield ("wait", self.s_empty[g][b], use - 1)
             require(not any(self.s_readers[(g, b, u)] for u in range(use)),
                     f"S[{g}][{b}] use {use} written while an earlier use is being read")
             require(not (b == 1 and self.pv_issued[g]), f"pass-1 S into O[{g}]'s columns after a P V product")
+            self.s_tile[(g, b, use)] = j
             yield product((p % nst, p // nst), lambda: self.s_written[(g, b)].add(use))
             yield ("commit", g, [(self.s_full[r][g][b], use) for r in range(n)])
             uses[b] += 1
 
-        def mma_pv(j, p):
-            yield ("wait", self.p_full[g], j)
-            require(len(self.p_written[(g, j)]) == n * self.WARPS, f"P V product {j} issued before every warp wrote P[{g}]")
+        def mma_pv(j, c, p):
+            yield ("wait", self.p_full[g], c)
+            require(len(self.p_written[(g, c)]) == n * self.WARPS, f"P V product {c} issued before every warp wrote P[{g}]")
+            require(self.p_tile[(g, c)] == j, f"P V product of tile {j} reads the P tile of tile {self.p_tile[(g, c)]}")
             require(not any(self.s_readers[(g, 1, u)] for u in range(uses[1])),
                     f"P V product into O[{g}] while pass-1 scores in its columns are read")
             if (g, j) in self.dead:
-                self.pv_done.add((g, j))
+                self.pv_done.add((g, c))
             else:
                 self.pv_issued[g] += 1
-                yield product((p % nst, p // nst), lambda: self.pv_done.add((g, j)))
-            yield ("commit", g, [(self.p_empty[r][g], j) for r in range(n)])
+                yield product((p % nst, p // nst), lambda: self.pv_done.add((g, c)))
+            yield ("commit", g, [(self.p_empty[r][g], c) for r in range(n)])
 
         skip_wait = self.mutation == "release_without_fill"
         pos = 0
-        for j in range(nkt):                                   # pass 1
-            if not (skip_wait and j >= nkt_g):
+        c = 0
+        for j in t:                                            # pass 1
+            if not (skip_wait and j not in mine):
                 yield from ring_wait(pos)
-                if j < nkt_g:
-                    yield from mma_s(pos, j & 1)
+                if j in mine:
+                    yield from mma_s(pos, c & 1, j)
+                    c += 1
             yield from release(pos)
             pos += 1
-        yield from ring_wait(pos)                              # pass 2: S(0)
-        yield from mma_s(pos, 0)
-        yield from release(pos)
-        pos += 1
-        for j in range(nkt):
-            if j + 1 < nkt:
-                if not (skip_wait and j + 1 >= nkt_g):
+        if t:                                                  # pass 2: S(t0)
+            yield from ring_wait(pos)
+            if t[0] in mine:
+                yield from mma_s(pos, 0, t[0])
+            yield from release(pos)
+            pos += 1
+        c = 0
+        for i, j in enumerate(t):
+            if i + 1 < len(t):
+                jn = t[i + 1]
+                if not (skip_wait and jn not in mine):
                     yield from ring_wait(pos)
-                    if j + 1 < nkt_g:
-                        yield from mma_s(pos, 0)
+                    if jn in mine:
+                        yield from mma_s(pos, 0, jn)
                 yield from release(pos)
                 pos += 1
-            if not (skip_wait and j >= nkt_g):
+            if not (skip_wait and j not in mine):
                 yield from ring_wait(pos)
-                if j < nkt_g:
-                    yield from mma_pv(j, pos)
+                if j in mine:
+                    yield from mma_pv(j, c, pos)
+                    c += 1
             yield from release(pos)
             pos += 1
         yield ("commit", g, [(self.o_full[r][g], 0) for r in range(n)])
 
     def softmax(self, r, g, w):
-        nkt_g = self.nkt_g[g]
+        mine = self.takes[g]
 
-        def take(b, use):
+        def take(b, use, j):
             yield ("wait", self.s_full[r][g][b], use)
             require(use in self.s_written[(g, b)], f"S[{g}][{b}] use {use} read before its product completed")
+            require(self.s_tile[(g, b, use)] == j, f"S[{g}][{b}] use {use} holds tile {self.s_tile[(g, b, use)]}, "
+                                                   f"read as tile {j}")
             self.s_readers[(g, b, use)] += 1
             yield ("do", lambda: None)
             self.s_readers[(g, b, use)] -= 1
             yield ("do", lambda: self.s_empty[g][b].arrive(use))
 
-        for j in range(nkt_g):                                 # pass 1
-            yield from take(j & 1, j >> 1)
-        sidx = (nkt_g + 1) >> 1
-        for j in range(nkt_g):                                 # pass 2
-            yield from take(0, sidx)
+        for c, j in enumerate(mine):                           # pass 1
+            if self.mutation == "tile_index_buffers":          # buffer and use by key tile, not by count
+                yield from take(j & 1, j >> 1, j)
+            else:
+                yield from take(c & 1, c >> 1, j)
+        sidx = (len(mine) + 1) >> 1
+        for c, j in enumerate(mine):                           # pass 2
+            yield from take(0, sidx, j)
             sidx += 1
             if self.mutation != "no_p_free_wait":
-                yield ("wait", self.p_empty[r][g], j - 1)
-            require(j == 0 or (g, j - 1) in self.pv_done, f"P[{g}] rewritten (tile {j}) before P V product {j - 1} completed")
-            self.p_written[(g, j)].add((r, w))
-            yield ("do", lambda j=j: self.p_full[g].arrive(j))
+                yield ("wait", self.p_empty[r][g], c - 1)
+            require(c == 0 or (g, c - 1) in self.pv_done, f"P[{g}] rewritten (tile {j}) before the previous P V product completed")
+            self.p_written[(g, c)].add((r, w))
+            self.p_tile[(g, c)] = j
+            yield ("do", lambda c=c: self.p_full[g].arrive(c))
         yield ("wait", self.o_full[r][g], 0)
         require(self.outstanding[g] == 0, f"O[{g}] read while products are outstanding")
 
@@ -296,11 +319,28 @@ FWD_CONFIGS = [
 
 @pytest.mark.parametrize("ncta,nst,nkt,nshort,short,dead_frac", FWD_CONFIGS)
 def test_forward_protocol_holds_on_random_schedules(ncta, nst, nkt, nshort, short, dead_frac):
-    nkt_g = (nshort, nkt) if short == 0 else (nkt, nshort)
+    takes = (range(nshort), range(nkt)) if short == 0 else (range(nkt), range(nshort))
     for seed in range(60):
         rng = random.Random(seed * 1000 + nkt * 10 + ncta)
         dead = {(g, j) for g in range(2) for j in range(nkt) if rng.random() < dead_frac}
-        run_roles(ForwardModel(ncta, nst, nkt, nkt_g, dead).roles(), rng)
+        run_roles(ForwardModel(ncta, nst, takes, dead).roles(), rng)
+
+
+@pytest.mark.parametrize("ncta,nst,nkt", [(1, 3, 6), (1, 6, 9), (2, 6, 6), (2, 6, 11)])
+def test_forward_protocol_holds_with_tile_live_maps(ncta, nst, nkt):
+    """Under an attention mask each product takes a subset of its range (the tiles the live map
+    shows an allowed pair in): random subsets, often different for the two products, sometimes
+    one or both empty."""
+    for seed in range(80):
+        rng = random.Random(seed * 7919 + nkt * 31 + ncta)
+        hi = (rng.randint(0, nkt), nkt) if rng.random() < 0.5 else (nkt, rng.randint(0, nkt))
+        takes = [{j for j in range(hi[g]) if rng.random() < 0.6} for g in range(2)]
+        if seed % 9 == 0:
+            takes[seed % 2] = set()
+        if seed % 27 == 0:
+            takes = [set(), set()]
+        dead = {(g, j) for g in range(2) for j in range(nkt) if rng.random() < 0.2}
+        run_roles(ForwardModel(ncta, nst, takes, dead).roles(), rng)
 
 
 def _caught(make, seeds=300):
@@ -312,18 +352,21 @@ def _caught(make, seeds=300):
     return False
 
 
-@pytest.mark.parametrize("mutation,ncta,nkt,nkt0", [("release_without_fill", 1, 6, 3),
-                                                    ("release_without_fill", 2, 6, 2),
-                                                    ("release_without_fill", 2, 6, -2),
-                                                    ("single_cta_counts", 2, 3, 3),
-                                                    ("no_p_free_wait", 1, 4, 4),
-                                                    ("no_p_free_wait", 2, 4, 4)])
-def test_planted_forward_protocol_mistakes_are_caught(mutation, ncta, nkt, nkt0):
+@pytest.mark.parametrize("mutation,ncta,takes0,takes1", [("release_without_fill", 1, range(3), range(6)),
+                                                         ("release_without_fill", 2, range(2), range(6)),
+                                                         ("release_without_fill", 2, range(6), range(2)),
+                                                         ("release_without_fill", 2, {0, 2, 5}, {1, 2, 3, 4}),
+                                                         ("single_cta_counts", 2, range(3), range(3)),
+                                                         ("no_p_free_wait", 1, range(4), range(4)),
+                                                         ("no_p_free_wait", 2, {1, 3}, {0, 1, 3, 4}),
+                                                         ("tile_index_buffers", 1, {0, 2, 3, 5}, {0, 2, 3, 5}),
+                                                         ("tile_index_buffers", 2, {1, 2}, {0, 1, 2, 4})])
+def test_planted_forward_protocol_mistakes_are_caught(mutation, ncta, takes0, takes1):
     """Releasing ring stages without waiting for their fill lets the issuer that skips tiles
     run a phase ahead; counting one CTA's warps on the pair's barriers completes a phase
-    early; skipping the P-free wait rewrites P under a running product."""
-    nkt_g = (nkt0, nkt) if nkt0 > 0 else (nkt, -nkt0)   # negative: product 1 is the shorter one
-    assert _caught(lambda: ForwardModel(ncta, 6 if ncta == 2 else 3, nkt, nkt_g, set(), mutation))
+    early; skipping the P-free wait rewrites P under a running product; picking a score buffer
+    by key tile instead of by the product's own tile count breaks once the walk has holes."""
+    assert _caught(lambda: ForwardModel(ncta, 6 if ncta == 2 else 3, (takes0, takes1), set(), mutation))
 
 
 # ---------------------------------------------------------------------------- dK/dV kernel
