@@ -173,13 +173,6 @@ __device__ __forceinline__ float2 phi_half_any(bool masked, const uint32_t (&h)[
 
 // MASK: a boolean attention mask (args.mask) applies on top of `causal`.  PAIR: the CTA
 // pair form (FwdCfg).
-// One word of the key-tile walk: bit t of bits[g] is whether product g takes key tile 32 w + t
-template <int NG>
-struct TileWalk {
-  int w = -1;
-  uint32_t bits[NG];
-};
-
 template <int D, bool MASK, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_tc_kernel(const AttnShape s, const __grid_constant__ FwdTcArgs args, const LaunchCtx ctx) {
@@ -253,18 +246,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   // producer streams all nkt for the last product, and the other issuer releases the
   // stages it does not use
   auto group_keys = [&](int g) { return last_key_of(tile_row0(g, NCTA - 1) + BM) / BN + 1; };
-  // The mask head of this (batch, head), and the key tiles product g takes part in: its causal
-  // range and, with a tile live map, the tiles holding an allowed pair for one of its query
-  // tiles.  Every role walks the same tiles: the producer streams those either product takes
-  // (a tile neither takes is left out of both passes: no copy, no product, no softmax work),
-  // each issuer issues only its own product's and waits on and releases the others.
-  const int gm = MASK ? (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0) : 0;
-  // tiles 32 w .. 32 w + 31 that product g takes, as bits
+  // Key tiles 32 w .. 32 w + 31 that product g takes, as bits: its causal range and, with a
+  // tile live map, the tiles holding an allowed pair for one of its query tiles.  Every role
+  // walks the same tiles in key order, refreshing its word every 32: the producer streams
+  // those either product takes (a tile neither takes is left out of both passes: no copy, no
+  // product, no softmax work); each issuer issues only its own product's and waits on and
+  // releases the others.  Unmasked instances take the whole range.
   auto take_word = [&](int g, int w) -> uint32_t {
     const int n = group_keys(g) - 32 * w;
     uint32_t bits = n >= 32 ? ~0u : (n > 0 ? (1u << n) - 1u : 0u);
     if constexpr (MASK) {
       if (args.mask.live && bits) {
+        const int gm = (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0);
         uint32_t any = 0;
 #pragma unroll
         for (int r = 0; r < NCTA; ++r) {
@@ -276,38 +269,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     return bits;
   };
-  // Each role walks the tiles in increasing order and keeps the current word of both products
-  TileWalk<NGROUP> walk;
-  auto walk_word = [&](int w) {
-    if (walk.w != w) {
-      walk.w = w;
+  auto union_word = [&](int w) {
+    uint32_t u = 0;
 #pragma unroll
-      for (int g = 0; g < NGROUP; ++g) walk.bits[g] = take_word(g, w);
-    }
+    for (int h = 0; h < NGROUP; ++h) u |= take_word(h, w);
+    return u;
   };
-  auto takes = [&](int g, int j) -> bool {   // product g takes key tile j
-    if constexpr (!MASK) return j < group_keys(g);   // no map: the whole range
-    walk_word(j >> 5);
-    uint32_t b = 0;
-#pragma unroll
-    for (int h = 0; h < NGROUP; ++h)   // g is not a compile-time index: select, keep bits in registers
-      if (h == g) b = walk.bits[h];
-    return (b >> (j & 31)) & 1u;
-  };
-  // first tile after j that product g (g < 0: either product) takes, or -1
-  auto next_tile = [&](int g, int j) -> int {
-    if constexpr (!MASK) return j + 1 < (g < 0 ? nkt : group_keys(g)) ? j + 1 : -1;
-    for (int t = j + 1; t < nkt; t = (t | 31) + 1) {
-      walk_word(t >> 5);
-      uint32_t u = 0;
-#pragma unroll
-      for (int h = 0; h < NGROUP; ++h)
-        if (g < 0 || g == h) u |= walk.bits[h];
-      u >>= (t & 31);
-      if (u) return t + __ffs(static_cast<int>(u)) - 1;
-    }
-    return -1;
-  };
+  auto bit = [](uint32_t word, int j) { return ((word >> (j & 31)) & 1u) != 0u; };
   // Barrier operations of the pair form: arrivals go to the even CTA's barrier, products and
   // commits span both CTAs.  Arrivals release, and waits acquire, at CTA scope: what they
   // order is this SM's own shared and tensor memory (a P tile, the scores a warp has read)
@@ -412,9 +380,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       // pass 1: K of every tile either product takes; pass 2 over those tiles t0 < t1 < ...:
       // K_t0, then K_ti and V_t(i-1) interleaved, then the last V
-      for (int j = next_tile(-1, -1); j >= 0 && ok; j = next_tile(-1, j)) ok = issue(false, j);
+      uint32_t uw = ~0u;   // tiles either product takes (unmasked: all nkt)
+      for (int j = 0; j < nkt && ok; ++j) {
+        if constexpr (MASK) {
+          if ((j & 31) == 0) uw = union_word(j >> 5);
+          if (!bit(uw, j)) continue;
+        }
+        ok = issue(false, j);
+      }
       int prev = -1;
-      for (int j = next_tile(-1, -1); j >= 0 && ok; j = next_tile(-1, j)) {
+      for (int j = 0; j < nkt && ok; ++j) {
+        if constexpr (MASK) {
+          if ((j & 31) == 0) uw = union_word(j >> 5);
+          if (!bit(uw, j)) continue;
+        }
         ok = issue(false, j);
         if (ok && prev >= 0) ok = issue(true, prev);
         prev = j;
@@ -538,36 +517,61 @@ __global__ void __launch_bounds__(THREADS, 1)
       // c-th; a ring stage is free once both issuers commit.  Tiles only the other product
       // takes are waited for and released: waiting for the fill keeps this issuer from
       // releasing a stage's next use before the other issuer has read it.
-      uint32_t c = 0;
-      for (int j = next_tile(-1, -1); j >= 0 && ok; j = next_tile(-1, j)) {
-        ok = ring_wait(pos, ka);
-        if (ok && takes(g, j)) ok = mma_s(ka, static_cast<int>(c++ & 1u));
-        if (ok) commit(&ring_empty[pos % NST]);
-        ++pos;
-      }
-      // pass 2 over the same tiles t0 < t1 < ...: S_g(t0); then per ti: S_g(t(i+1)), O_g(ti),
-      // every S product into buffer 0 and the c-th O product after the c-th P tile
-      c = 0;
-      int j = next_tile(-1, -1);
-      if (ok && j >= 0) {
-        ok = ring_wait(pos, ka);
-        if (ok && takes(g, j)) ok = mma_s(ka, 0);
-        if (ok) commit(&ring_empty[pos % NST]);
-        ++pos;
-      }
-      for (; j >= 0 && ok;) {
-        const int jn = next_tile(-1, j);
-        if (jn >= 0) {
-          const uint32_t kpos = pos++;
-          ok = ring_wait(kpos, ka);
-          if (ok && takes(g, jn)) ok = mma_s(ka, 0);
-          if (ok) commit(&ring_empty[kpos % NST]);
+      const int nkt_g = group_keys(g);
+      uint32_t uw = ~0u, ow = ~0u;   // tiles either product takes, and this one
+      auto refresh = [&](int j) {
+        if ((j & 31) == 0) {
+          uw = 0;
+#pragma unroll
+          for (int h = 0; h < NGROUP; ++h) {
+            const uint32_t t = take_word(h, j >> 5);
+            uw |= t;
+            if (h == g) ow = t;
+          }
         }
+      };
+      uint32_t c = 0;
+      for (int j = 0; j < nkt && ok; ++j) {
+        if constexpr (MASK) {
+          refresh(j);
+          if (!bit(uw, j)) continue;
+        }
+        const bool mine = MASK ? bit(ow, j) : j < nkt_g;
+        ok = ring_wait(pos, ka);
+        if (ok && mine) ok = mma_s(ka, static_cast<int>(c++ & 1u));
+        if (ok) commit(&ring_empty[pos % NST]);
+        ++pos;
+      }
+      // pass 2 over the same tiles t0 < t1 < ...: S_g(t0); then per ti, i >= 1: S_g(ti),
+      // O_g(t(i-1)); then O_g of the last.  Every S product into buffer 0; the c-th O product
+      // after the c-th P tile
+      c = 0;
+      int prev = -1;
+      bool prev_mine = false;
+      for (int j = 0; j < nkt && ok; ++j) {
+        if constexpr (MASK) {
+          refresh(j);
+          if (!bit(uw, j)) continue;
+        }
+        const bool mine = MASK ? bit(ow, j) : j < nkt_g;
+        const uint32_t kpos = pos++;
+        ok = ring_wait(kpos, ka);
+        if (ok && mine) ok = mma_s(ka, 0);
+        if (ok) commit(&ring_empty[kpos % NST]);
+        if (ok && prev >= 0) {
+          const uint32_t vpos = pos++;
+          ok = ring_wait(vpos, va);
+          if (ok && prev_mine) ok = mma_pv(prev, c++, va);
+          if (ok) commit(&ring_empty[vpos % NST]);
+        }
+        prev = j;
+        prev_mine = mine;
+      }
+      if (ok && prev >= 0) {
         const uint32_t vpos = pos++;
-        if (ok) ok = ring_wait(vpos, va);
-        if (ok && takes(g, j)) ok = mma_pv(j, c++, va);
+        ok = ring_wait(vpos, va);
+        if (ok && prev_mine) ok = mma_pv(prev, c++, va);
         if (ok) commit(&ring_empty[vpos % NST]);
-        j = jn;
       }
       if (ok) commit(&o_full[g]);
       commit(&drain[g]);
@@ -595,6 +599,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // this row's attention-mask words: four per key tile (rows past N_Q read the last row)
     const uint32_t* mrow = nullptr;
     if (MASK) {
+      const int gm = (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0);
       mrow = args.mask.bits + (static_cast<size_t>(gm) * s.NQ + min(row, s.NQ - 1)) * args.mask.words;
     }
     auto mask_words = [&](int j, uint32_t (&mw)[4]) {
@@ -631,13 +636,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     // pass 1: running maximum of the raw scores q.k (scale > 0 keeps the argmax), over the
     // key tiles the product takes; its c-th sits in score buffer c & 1, as that buffer's use c >> 1
     uint32_t c = 0;
-    for (int j = next_tile(g, -1); j >= 0 && ok; j = next_tile(g, j)) {
+    const int nkt_g = group_keys(g);
+    uint32_t tw = 0;   // tiles this product takes (masked instances), refreshed every 32
+    for (int j = 0; j < nkt_g && ok; ++j) {
+      if constexpr (MASK) {
+        if ((j & 31) == 0) tw = take_word(g, j >> 5);
+        if (!bit(tw, j)) continue;
+      }
+      uint32_t mw[4];
+      mask_words(j, mw);   // issued before the wait below: its latency hides behind it
       ok = take_s(static_cast<int>(c & 1u), c >> 1);
       ++c;
       if (!ok) break;
       const int col0 = j * BN;   // key index of column 0
-      uint32_t mw[4];
-      mask_words(j, mw);
       // maximum of each 32-column chunk; the first chunk (in key order) that raises the
       // running maximum strictly is remembered, so ties keep the lowest index
       float cm[BN / 32];
@@ -699,7 +710,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     float rowsum = 0.0f;
     sidx = (c + 1) >> 1;   // pass 1 used buffer 0 for its tiles 0, 2, 4, ...
     c = 0;                 // P tiles written
-    for (int j = next_tile(g, -1); j >= 0 && ok; j = next_tile(g, j)) {
+    for (int j = 0; j < nkt_g && ok; ++j) {
+      if constexpr (MASK) {
+        if ((j & 31) == 0) tw = take_word(g, j >> 5);
+        if (!bit(tw, j)) continue;
+      }
+      uint32_t mw[4];
+      mask_words(j, mw);   // in flight during the wait
       ok = warp_wait(&s_full[2 * g], sidx & 1u);   // buffer 0
       if (!ok) break;
       ++sidx;
@@ -707,8 +724,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int col0 = j * BN;
       const bool masked = MASK || col0 + BN - 1 > lim;
       const bool arg_tile = j == (jm >> 2) && m > -INFINITY;
-      uint32_t mw[4];
-      mask_words(j, mw);
       uint32_t h[2][32];
       tmem_ld32(scol, h[0]);
       tmem_ld32(scol + 32, h[1]);
