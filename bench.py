@@ -475,7 +475,26 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     sm16_ms = b0.elapsed_time(b1) / args.steps
     sm16_bytes = 2.0 * x.numel() * 2
-    del xs16, ys16
+
+    # bf16 ra_softmax backward: the bf16 x, its bf16 p, a bf16 dy; 8 B per element
+    dy16 = softmax_inputs(sw.rows, sw.cols, seed=sw.seed + 1, sigma=1.0).to(dev).to(torch.bfloat16)
+    dx16 = torch.empty_like(dy16)
+
+    def softmax_bwd_bf16():
+        code = hp.L.ra_softmax_bwd(_ptr(xs16), _ptr(ys16), _ptr(dy16), _ptr(dx16), sw.rows, sw.cols, 1, st)
+        if code != 0:
+            raise RuntimeError("ra_softmax_bwd (bf16) failed")
+    for _ in range(3):
+        softmax_bwd_bf16()
+    torch.cuda.synchronize(dev)
+    b0.record(stream)
+    for _ in range(args.steps):
+        softmax_bwd_bf16()
+    b1.record(stream)
+    torch.cuda.synchronize(dev)
+    smb16_ms = b0.elapsed_time(b1) / args.steps
+    smb16_bytes = 4.0 * x.numel() * 2
+    del xs16, ys16, dy16, dx16
 
     # the RaAttention module at the page's example shape (dim 768, 12 heads, causal,
     # x [2, 128, 768], bf16): forward + backward through the module, seeded weights
@@ -638,6 +657,9 @@ def run_ours(args):
             "ra_softmax_bwd": {"ms": smb_ms, "GB_per_s": smb_bytes / (smb_ms * 1e-3) / 1e9,
                                "frac_hbm": smb_bytes / (smb_ms * 1e-3) / 1e9 / hbm_peak,
                                "algorithmic": "16 B per element (x, p, dy read; dx written)"},
+            "ra_softmax_bwd_bf16": {"ms": smb16_ms, "GB_per_s": smb16_bytes / (smb16_ms * 1e-3) / 1e9,
+                                    "frac_hbm": smb16_bytes / (smb16_ms * 1e-3) / 1e9 / hbm_peak,
+                                    "algorithmic": "8 B per element (bf16 x, p, dy read; dx written)"},
             "ra_attention_module_b2n128d768h12_causal": {
                 "ms_fwd_bwd": mod_ms, "tokens_per_s": 2 * 128 / (mod_ms * 1e-3),
                 "note": "latency-bound (24 heads of one 128-row tile); no roofline claim"},

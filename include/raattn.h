@@ -80,7 +80,9 @@ ra_status_t ra_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols,
  *   dx_j = 0                                           for u_j >= 1
  *   dx_argmax = -(sum of the other dx_j)               (lowest index among ties)
  *   x, p, dy, dx   device pointers to rows*cols elements of `dtype`; dx may equal dy.
- *   dtype          RA_F32.
+ *   dtype          RA_F32, or RA_BF16: all four arrays bf16, widened exactly to fp32, the
+ *                  arithmetic in fp32 and dx rounded once to bf16 (dx_argmax is minus the
+ *                  fp32 sum of the others, then rounded).
  * Errors as ra_softmax_fwd.
  */
 ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* dx,

@@ -133,6 +133,8 @@ def ra_softmax_backward(x, p, dy, out=None):
 
     out: optional tensor for dx, shaped like x; it may be dy itself (gradient in place)."""
     _require_cuda(x, p, dy)
+    if p.dtype != x.dtype or dy.dtype != x.dtype or p.shape != x.shape or dy.shape != x.shape:
+        raise ValueError("x, p and dy must share one shape and dtype (float32 or bfloat16)")
     if out is not None:
         _require_cuda(out)
         if out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():

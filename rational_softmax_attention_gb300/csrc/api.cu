@@ -202,11 +202,12 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
                            ra_dtype_t dtype, void* stream) {
   if (!x || !p || !dy || !dx || rows < 1 || cols < 1 || !dtype_ok(dtype)) return RA_ERR_ARG;
   if (rows > INT_MAX || cols > (INT64_MAX / rows)) return RA_ERR_ARG;
-  if (dtype != RA_F32) return RA_ERR_UNSUPPORTED;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t e =
-      launch_ra_softmax_bwd_f32(static_cast<const float*>(x), static_cast<const float*>(p),
-                                static_cast<const float*>(dy), static_cast<float*>(dx), rows, cols,
-                                static_cast<cudaStream_t>(stream));
+      dtype == RA_F32 ? launch_ra_softmax_bwd_f32(static_cast<const float*>(x), static_cast<const float*>(p),
+                                                  static_cast<const float*>(dy), static_cast<float*>(dx), rows, cols,
+                                                  st)
+                      : launch_ra_softmax_bwd_bf16(x, p, dy, dx, rows, cols, st);
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
 

@@ -11,6 +11,8 @@ cudaError_t launch_ra_softmax_fwd_f32(const float* x, float* y, int64_t rows, in
 cudaError_t launch_ra_softmax_fwd_bf16(const void* x, void* y, int64_t rows, int64_t cols, cudaStream_t st);
 cudaError_t launch_ra_softmax_bwd_f32(const float* x, const float* p, const float* dy, float* dx, int64_t rows,
                                       int64_t cols, cudaStream_t st);
+cudaError_t launch_ra_softmax_bwd_bf16(const void* x, const void* p, const void* dy, void* dx, int64_t rows,
+                                       int64_t cols, cudaStream_t st);
 
 // Boolean attention mask, bit-packed: bit (c % 32) of word c / 32 of a row is set when that
 // column may be attended.  Rows of `words` uint32 (a multiple of 4: whole 128-column tiles,

@@ -195,25 +195,37 @@ __global__ void __launch_bounds__(THREADS) ra_softmax_fwd_bf16_generic_kernel(co
     yr[c] = static_cast<uint16_t>(pack_bf16x2(ra_phi_fast(m - ld(c)) * inv, 0.0f) & 0xffffu);
 }
 
+// Element access for the backward kernels: fp32 as is; bf16 (raw uint16_t) widened exactly
+// to fp32 on load and rounded to nearest on store.  The arithmetic is fp32 either way.
+__device__ __forceinline__ float ld_elem(const float* a, int64_t i) { return a[i]; }
+__device__ __forceinline__ float ld_elem(const uint16_t* a, int64_t i) {
+  return __uint_as_float(static_cast<uint32_t>(a[i]) << 16);
+}
+__device__ __forceinline__ void st_elem(float* a, int64_t i, float v) { a[i] = v; }
+__device__ __forceinline__ void st_elem(uint16_t* a, int64_t i, float v) {
+  a[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xffffu);
+}
+
 // Backward: dx_j = p_j (dy_j - D) / (1 - u_j^2) for j != a with u_j < 1, 0 for u_j >= 1,
 // dx_a = -(sum of the others); D = sum_k p_k dy_k, a = lowest index of the row max of x.
-// 1/(1-u^2) is written as 256 / ((16 - Delta)(16 + Delta)).
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS) ra_softmax_bwd_kernel(const float* x, const float* p,
-                                                                 const float* dy, float* dx, int64_t cols) {
+// 1/(1-u^2) is written as 256 / ((16 - Delta)(16 + Delta)).  T: float or bf16 (uint16_t);
+// any cols and alignment (three sweeps over the row in global memory).
+template <int THREADS, typename T>
+__global__ void __launch_bounds__(THREADS) ra_softmax_bwd_kernel(const T* x, const T* p, const T* dy, T* dx,
+                                                                 int64_t cols) {
   __shared__ float red[THREADS / 32];
   __shared__ long long red_idx[THREADS / 32];
   const size_t row = blockIdx.x;
   const size_t off = row * static_cast<size_t>(cols);
-  const float* xr = x + off;
-  const float* pr = p + off;
-  const float* gr = dy + off;
-  float* dr = dx + off;
+  const T* xr = x + off;
+  const T* pr = p + off;
+  const T* gr = dy + off;
+  T* dr = dx + off;
   // row max and its lowest index
   float m = -INFINITY;
   long long a = -1;
   for (int64_t c = threadIdx.x; c < cols; c += THREADS) {
-    const float xv = xr[c];
+    const float xv = ld_elem(xr, c);
     if (xv > m) { m = xv; a = c; }
   }
   const float mall = block_max<THREADS>(m, red);
@@ -231,19 +243,20 @@ __global__ void __launch_bounds__(THREADS) ra_softmax_bwd_kernel(const float* x,
   __syncthreads();
   // D = sum p dy
   float d = 0.0f;
-  for (int64_t c = threadIdx.x; c < cols; c += THREADS) d = fmaf(pr[c], gr[c], d);
+  for (int64_t c = threadIdx.x; c < cols; c += THREADS) d = fmaf(ld_elem(pr, c), ld_elem(gr, c), d);
   d = block_sum<THREADS>(d, red);
   // e_j and their sum (excluding the argmax)
   float rsum = 0.0f;
   for (int64_t c = threadIdx.x; c < cols; c += THREADS) {
-    const float delta = mall - xr[c];
+    const float delta = mall - ld_elem(xr, c);
     float e = 0.0f;
-    if (c != amin && delta < 16.0f) e = 256.0f * pr[c] * (gr[c] - d) / ((16.0f - delta) * (16.0f + delta));
-    rsum += e;
-    if (c != amin) dr[c] = e;
+    if (c != amin && delta < 16.0f)
+      e = 256.0f * ld_elem(pr, c) * (ld_elem(gr, c) - d) / ((16.0f - delta) * (16.0f + delta));
+    rsum += e;   // the unrounded values: dx_a is minus their sum, rounded once
+    if (c != amin) st_elem(dr, c, e);
   }
   rsum = block_sum<THREADS>(rsum, red);
-  if (threadIdx.x == 0 && amin >= 0 && amin < cols) dr[amin] = -rsum;
+  if (threadIdx.x == 0 && amin >= 0 && amin < cols) st_elem(dr, amin, -rsum);
 }
 
 // The same backward with the row held in registers (cols % 4 == 0, cols <= THREADS*4*VPT,
@@ -321,6 +334,83 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) ra_softmax_bwd_ve
   if (amin < cols && threadIdx.x == (amin >> 2) % THREADS) dx[off + amin] = -rsum;
 }
 
+// The bf16 backward with the row held in registers, still packed (8 elements per 16-byte
+// vector; cols % 8 == 0, cols <= THREADS*8*VPT, 16-byte aligned rows): 8 bytes per element
+// in all.  Each packed vector is widened to fp32 where it is used; dx is rounded once.
+template <int THREADS, int VPT>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2)
+    ra_softmax_bwd_bf16_vec_kernel(const uint16_t* x, const uint16_t* p, const uint16_t* dy, uint16_t* dx,
+                                   int cols) {
+  __shared__ float red[THREADS / 32];
+  __shared__ int red_idx[THREADS / 32];
+  const size_t off = blockIdx.x * static_cast<size_t>(cols);
+  const uint4* xr = reinterpret_cast<const uint4*>(x + off);
+  const uint4* pr = reinterpret_cast<const uint4*>(p + off);
+  const uint4* gr = reinterpret_cast<const uint4*>(dy + off);
+  uint4* dr = reinterpret_cast<uint4*>(dx + off);
+  const int n8 = cols >> 3;
+  uint4 xv[VPT], pv[VPT], gv[VPT];
+  float m = -INFINITY, d = 0.0f;
+  int a = cols;   // lowest column of this thread's maximum (columns are visited in increasing order)
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < n8) {
+      xv[i] = __ldcs(xr + idx);
+      pv[i] = __ldcs(pr + idx);
+      gv[i] = __ldcs(gr + idx);
+      float xs[8], ps[8], gs[8];
+      unpack_bf16x8(xv[i], xs);
+      unpack_bf16x8(pv[i], ps);
+      unpack_bf16x8(gv[i], gs);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (xs[k] > m) {
+          m = xs[k];
+          a = 8 * idx + k;
+        }
+        d = fmaf(ps[k], gs[k], d);
+      }
+    }
+  }
+  const float mall = block_max<THREADS>(m, red);
+  int cand = (m == mall) ? a : cols;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red_idx[warp] = cand;
+  __syncthreads();
+  int amin = red_idx[0];
+#pragma unroll
+  for (int w = 1; w < THREADS / 32; ++w) amin = min(amin, red_idx[w]);
+  d = block_sum<THREADS>(d, red);   // D = sum_k p_k dy_k
+  float rsum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < n8) {
+      float xs[8], ps[8], gs[8], es[8];
+      unpack_bf16x8(xv[i], xs);
+      unpack_bf16x8(pv[i], ps);
+      unpack_bf16x8(gv[i], gs);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float delta = mall - xs[k];
+        es[k] = (8 * idx + k != amin && delta < 16.0f)
+                    ? __fdividef(256.0f * ps[k] * (gs[k] - d), (16.0f - delta) * (16.0f + delta))
+                    : 0.0f;
+        rsum += es[k];
+      }
+      __stcs(dr + idx, make_uint4(pack_bf16x2(es[0], es[1]), pack_bf16x2(es[2], es[3]), pack_bf16x2(es[4], es[5]),
+                                  pack_bf16x2(es[6], es[7])));
+    }
+  }
+  rsum = block_sum<THREADS>(rsum, red);
+  // the thread that stored the argmax's eight columns overwrites that column
+  if (amin < cols && threadIdx.x == (amin >> 3) % THREADS)
+    dx[off + amin] = static_cast<uint16_t>(pack_bf16x2(-rsum, 0.0f) & 0xffffu);
+}
+
 // ----------------------------------------------------------------------------
 // launchers
 // ----------------------------------------------------------------------------
@@ -383,7 +473,33 @@ cudaError_t launch_ra_softmax_bwd_f32(const float* x, const float* p, const floa
       ra_softmax_bwd_vec_kernel<512, 4><<<grid, 512, 0, st>>>(x, p, dy, dx, c);
     return cudaGetLastError();
   }
-  ra_softmax_bwd_kernel<256><<<static_cast<unsigned>(rows), 256, 0, st>>>(x, p, dy, dx, cols);
+  ra_softmax_bwd_kernel<256, float><<<static_cast<unsigned>(rows), 256, 0, st>>>(x, p, dy, dx, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ra_softmax_bwd_bf16(const void* x, const void* p, const void* dy, void* dx, int64_t rows,
+                                       int64_t cols, cudaStream_t st) {
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  const uint16_t* ps = static_cast<const uint16_t*>(p);
+  const uint16_t* gs = static_cast<const uint16_t*>(dy);
+  uint16_t* ds = static_cast<uint16_t*>(dx);
+  const bool vec_ok = (cols % 8 == 0) && cols <= 16384 && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
+                      ((reinterpret_cast<uintptr_t>(p) & 15u) == 0) && ((reinterpret_cast<uintptr_t>(dy) & 15u) == 0) &&
+                      ((reinterpret_cast<uintptr_t>(dx) & 15u) == 0);
+  const unsigned grid = static_cast<unsigned>(rows);
+  if (vec_ok) {
+    const int c = static_cast<int>(cols);
+    if (cols <= 2048)
+      ra_softmax_bwd_bf16_vec_kernel<256, 1><<<grid, 256, 0, st>>>(xs, ps, gs, ds, c);
+    else if (cols <= 4096)
+      ra_softmax_bwd_bf16_vec_kernel<256, 2><<<grid, 256, 0, st>>>(xs, ps, gs, ds, c);
+    else if (cols <= 8192)
+      ra_softmax_bwd_bf16_vec_kernel<512, 2><<<grid, 512, 0, st>>>(xs, ps, gs, ds, c);
+    else
+      ra_softmax_bwd_bf16_vec_kernel<512, 4><<<grid, 512, 0, st>>>(xs, ps, gs, ds, c);
+    return cudaGetLastError();
+  }
+  ra_softmax_bwd_kernel<256, uint16_t><<<grid, 256, 0, st>>>(xs, ps, gs, ds, cols);
   return cudaGetLastError();
 }
 

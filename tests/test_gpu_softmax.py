@@ -162,3 +162,83 @@ def test_ra_softmax_bf16_full_workload_sampled_rows():
     rows = np.random.default_rng(0).choice(w.rows, size=64, replace=False)
     want, *_ = oracle.ra_softmax(x[rows].double().numpy())
     _assert_bf16_rounding_of(parity.f64(got[rows]), want, "ra_softmax bf16 full workload")
+
+
+def _bwd_bf16_bound(x, p, dy, want):
+    """Error bound for the bf16 backward fed p_hat = bf16(p), p the float64 probabilities.
+
+    With |p_hat - p| <= 2^-9 p (round to nearest, 8 significant bits), D_hat = sum p_hat dy
+    is within eD = 2^-9 sum_k p_k |dy_k| of D, and an entry e_j = r_j (dy_j - D) with
+    r_j = p_j / (1 - u_j^2) (live entries, u_j < 1) moves by at most
+      b_j = 2^-9 r_j |dy_j - D| + (1 + 2^-9) r_j eD;
+    the argmax entry (minus the sum of the others) by the sum of the others' b_j.  On top: the
+    fp32 arithmetic (2e-5, the fp32 backward's bound) and half a bf16 ulp of the result."""
+    m = x.max(axis=-1, keepdims=True)
+    u = (m - x) / 16.0
+    live = u < 1.0
+    r = np.where(live, p / np.where(live, 1.0 - u * u, 1.0), 0.0)
+    D = (p * dy).sum(axis=-1, keepdims=True)
+    eD = 2.0 ** -9 * (p * np.abs(dy)).sum(axis=-1, keepdims=True)
+    b = 2.0 ** -9 * r * np.abs(dy - D) + (1 + 2.0 ** -9) * r * eD
+    a = x.argmax(axis=-1)   # lowest index of the maximum
+    rows = np.arange(x.shape[0])
+    b[rows, a] = b.sum(axis=-1) - b[rows, a]
+    mag = np.abs(want) + b
+    half_ulp = np.where(mag > 0, 2.0 ** (np.floor(np.log2(np.where(mag > 0, mag, 1.0))) - 8), 0.0)
+    return b + half_ulp + 2e-5
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (3, 5), (4, 512), (5, 1000), (3, 2048), (2, 4096), (3, 8192),
+                                       (2, 16384), (2, 8200)])
+def test_ra_softmax_backward_bf16_matches_oracle(rows, cols):
+    """bf16 x, p and dy (p the float64 probabilities rounded once to bf16, as a bf16 forward
+    would save them), fp32 arithmetic, dx rounded once: within the propagated bound of the
+    float64 gradient.  Rows of up to 16384 columns in multiples of 8 take the register-held
+    kernel; 5 columns (and the misaligned rows of the next test) the generic one."""
+    g = torch.Generator().manual_seed(cols + 7)
+    x = (torch.randn(rows, cols, generator=g) * 4.0).to(torch.bfloat16)
+    dy = torch.randn(rows, cols, generator=g).to(torch.bfloat16)
+    xd, dyd = x.double().numpy(), dy.double().numpy()
+    p64, *_ = oracle.ra_softmax(xd)
+    p = torch.from_numpy(p64).to(torch.bfloat16)
+    dx = ra.ra_softmax_backward(x.cuda(), p.cuda(), dy.cuda())
+    torch.cuda.synchronize()
+    assert dx.dtype == torch.bfloat16 and ra.device_status() == "RA_OK"
+    want = oracle.ra_softmax_bwd(xd, dyd)
+    bound = _bwd_bf16_bound(xd, p64, dyd, want)
+    err = np.abs(parity.f64(dx) - want)
+    assert np.all(err <= bound), f"bf16 ra_softmax_bwd [{rows}x{cols}]: {int((err > bound).sum())} beyond the bound"
+
+
+def test_ra_softmax_backward_bf16_ties_in_place_and_misaligned():
+    """Exact maxima twice in a row (the gradient of the maximum goes to the lowest column),
+    dx written over dy, and rows 2 bytes off a 16-byte boundary (the generic kernel)."""
+    g = torch.Generator().manual_seed(12)
+    rows, cols = 4, 8192
+    x = (torch.randn(rows, cols, generator=g) * 4.0).to(torch.bfloat16)
+    for r, (c1, c2) in enumerate([(5, 4000), (4000, 5), (1023, 1024), (8190, 8191)]):
+        top = float(x[r].float().max()) + 1.0
+        x[r, c1] = top
+        x[r, c2] = top
+    dy = torch.randn(rows, cols, generator=g).to(torch.bfloat16)
+    xd, dyd = x.double().numpy(), dy.double().numpy()
+    p64, *_ = oracle.ra_softmax(xd)
+    dyg = dy.cuda()
+    dx = ra.ra_softmax_backward(x.cuda(), torch.from_numpy(p64).to(torch.bfloat16).cuda(), dyg, out=dyg)
+    torch.cuda.synchronize()
+    assert dx.data_ptr() == dyg.data_ptr()
+    want = oracle.ra_softmax_bwd(xd, dyd)
+    assert np.all(np.abs(parity.f64(dx) - want) <= _bwd_bf16_bound(xd, p64, dyd, want))
+    # misaligned rows: a view one element into a flat buffer
+    n = 3 * 64
+    buf = [(torch.randn(n + 1, generator=g) * s).to(torch.bfloat16) for s in (4.0, 1.0)]
+    xv, dyv = (b[1:].reshape(3, 64) for b in buf)
+    xd, dyd = xv.double().numpy(), dyv.double().numpy()
+    p64, *_ = oracle.ra_softmax(xd)
+    pbuf = torch.zeros(n + 1, dtype=torch.bfloat16)
+    pbuf[1:] = torch.from_numpy(p64.reshape(-1)).to(torch.bfloat16)
+    xg, dyg, pg = (b.cuda()[1:].reshape(3, 64) for b in (buf[0], buf[1], pbuf))
+    dx = ra.ra_softmax_backward(xg, pg, dyg)
+    torch.cuda.synchronize()
+    want = oracle.ra_softmax_bwd(xd, dyd)
+    assert np.all(np.abs(parity.f64(dx) - want) <= _bwd_bf16_bound(xd, p64, dyd, want))
