@@ -156,8 +156,10 @@ size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
  * multiplies in fp16 (P, E and dS are then rounded to fp16 rather than bf16 before
  * their products).  The copies are exact for 2^-14 <= |x| <= 65504; smaller values are
  * rounded to a multiple of 2^-24 (fp16 subnormals; below 2^-25 to 0), and |x| > 65504
- * or NaN saturates and is reported as RA_ERR_UNSUPPORTED by ra_device_status().  Each
- * piece is padded to 256 bytes.  Returns 0 for invalid sizes.
+ * or NaN saturates and is reported as RA_ERR_UNSUPPORTED by ra_device_status().  Last,
+ * the tile map a masked call builds, both ways: B*H*ceil(N_Q/128) rows of
+ * ceil(ceil(N_K/128)/32) uint32 words and B*H*ceil(N_K/128) rows of ceil(ceil(N_Q/128)/32).
+ * Each piece is padded to 256 bytes.  Returns 0 for invalid sizes.
  */
 size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 

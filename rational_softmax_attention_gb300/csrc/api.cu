@@ -101,7 +101,7 @@ bool make_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int D) {
 // per-query-tile constant blocks, then the fp16 copies of Q, dO, K and V.  Every piece
 // starts on a 256-byte boundary.
 struct BwdLayout {
-  size_t per_row, consts, head, q16, kv16, total_f32, total_tc;
+  size_t per_row, consts, head, q16, kv16, live_q, live_k, total_f32, total_tc;
   BwdLayout(int B, int H, int NQ, int NK, int D) {
     auto pad = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t bh = static_cast<size_t>(B) * H;
@@ -112,7 +112,11 @@ struct BwdLayout {
     head = std::max(total_f32, consts);
     q16 = pad(bh * NQ * D * 2);
     kv16 = pad(bh * NK * D * 2);
-    total_tc = head + 2 * q16 + 2 * kv16;
+    // masked calls: the tile live map by query tile (key-tile bits) and by key tile
+    const size_t nkt = (static_cast<size_t>(NK) + 127) / 128;
+    live_q = pad(bh * nqt * live_words_for(NK) * 4);
+    live_k = pad(bh * nkt * live_words_for(NQ) * 4);
+    total_tc = head + 2 * q16 + 2 * kv16 + live_q + live_k;
   }
 };
 
@@ -287,8 +291,8 @@ ra_status_t attn_fwd_impl(const void* q, const void* k, const void* v, void* o, 
     uint32_t* live = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + fwd_workspace_v_bytes(B, H, N_K, D));
     a.mask.live = live;
     a.mask.live_words = live_words_for(N_K);
-    if (launch_mask_tile_live(mask.bits, mask.mb * mask.mh, N_Q, N_K, mask.words, live, a.mask.live_words, st) !=
-        cudaSuccess)
+    if (launch_mask_tile_live(mask.bits, mask.mb * mask.mh, N_Q, N_K, mask.words, live, a.mask.live_words, nullptr,
+                              0, st) != cudaSuccess)
       return RA_ERR_LAUNCH;
   }
   if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
@@ -410,6 +414,17 @@ ra_status_t attn_bwd_impl(const void* q, const void* k, const void* v, const voi
   a.ws_consts = reinterpret_cast<float*>(ws);
   a.mask_q = mask_q;
   a.mask_k = mask_k;
+  if (mask_q.bits) {   // the tile live map, both ways: fully masked tiles are left out of both kernels
+    char* lq = ws + lay.head + 2 * lay.q16 + 2 * lay.kv16;
+    a.mask_q.live = reinterpret_cast<uint32_t*>(lq);
+    a.mask_q.live_words = live_words_for(N_K);
+    a.mask_k.live = reinterpret_cast<uint32_t*>(lq + lay.live_q);
+    a.mask_k.live_words = live_words_for(N_Q);
+    if (launch_mask_tile_live(mask_q.bits, mask_q.mb * mask_q.mh, N_Q, N_K, mask_q.words,
+                              const_cast<uint32_t*>(a.mask_q.live), a.mask_q.live_words,
+                              const_cast<uint32_t*>(a.mask_k.live), a.mask_k.live_words, st) != cudaSuccess)
+      return RA_ERR_LAUNCH;
+  }
   const cudaError_t e = launch_attn_bwd_tc(s, a, ctx, st, current_events());
   return e == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }

@@ -172,6 +172,21 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   const int q0 = qt * BM;
   const int last_key = s.causal ? min(s.NK - 1, min(s.NQ - 1, q0 + BM - 1)) : s.NK - 1;
   const int nkt = last_key / BN + 1;
+  // Key tiles 32 w .. 32 w + 31 this query tile takes, as bits: its range and, with a tile
+  // live map, the tiles holding an allowed pair.  Every role walks them in key order and
+  // counts them: ring slots, score buffers and barrier phases follow that count, so a fully
+  // masked tile costs nothing (no copy, no product, no arithmetic).  Unmasked: every tile.
+  auto take_word = [&](int w) -> uint32_t {
+    const int n = nkt - 32 * w;
+    uint32_t bits = n >= 32 ? ~0u : (n > 0 ? (1u << n) - 1u : 0u);
+    if constexpr (MASK) {
+      if (args.mask_q.live && bits) {
+        const int gm = (args.mask_q.mb > 1 ? bh / s.H : 0) * args.mask_q.mh + (args.mask_q.mh > 1 ? bh % s.H : 0);
+        bits &= args.mask_q.live[(static_cast<size_t>(gm) * nqt + qt) * args.mask_q.live_words + w];
+      }
+    }
+    return bits;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(qdo_full, 1);
@@ -220,23 +235,29 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
       bool ok = true;
       int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < nkt && ok; ++j) {
-        const int ks = j % C::NKS;
-        ok = mbar_wait(&k_empty[ks], ((j / C::NKS) & 1u) ^ 1u, abort_flag, ctx);
+      uint32_t tw = 0;
+      for (int j = 0, c = 0; j < nkt && ok; ++j) {
+        if constexpr (MASK) {
+          if ((j & 31) == 0) tw = take_word(j >> 5);
+          if (!((tw >> (j & 31)) & 1u)) continue;
+        }
+        const int ks = c % C::NKS;
+        ok = mbar_wait(&k_empty[ks], ((c / C::NKS) & 1u) ^ 1u, abort_flag, ctx);
         if (!ok) break;
         mbar_arrive_expect_tx(&k_full[ks], C::TILE);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sK + ks * C::TILE + c * BOX_BYTES, &args.tm_k, &k_full[ks], c * 64, j * BN, bh);
-        k_issued = j + 1;
-        const int vs = j % C::NVS;
-        ok = mbar_wait(&v_empty[vs], ((j / C::NVS) & 1u) ^ 1u, abort_flag, ctx);
+        for (int cc = 0; cc < D / 64; ++cc)
+          tma_load_3d(sK + ks * C::TILE + cc * BOX_BYTES, &args.tm_k, &k_full[ks], cc * 64, j * BN, bh);
+        k_issued = c + 1;
+        const int vs = c % C::NVS;
+        ok = mbar_wait(&v_empty[vs], ((c / C::NVS) & 1u) ^ 1u, abort_flag, ctx);
         if (!ok) break;
         mbar_arrive_expect_tx(&v_full[vs], C::TILE);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sV + vs * C::TILE + c * BOX_BYTES, &args.tm_v, &v_full[vs], c * 64, j * BN, bh);
-        v_issued = j + 1;
+        for (int cc = 0; cc < D / 64; ++cc)
+          tma_load_3d(sV + vs * C::TILE + cc * BOX_BYTES, &args.tm_v, &v_full[vs], cc * 64, j * BN, bh);
+        v_issued = c + 1;
+        ++c;
       }
       // drain every copy issued (the last fill of each stage)
       drain_wait(qdo_full, 0, ctx);
@@ -256,14 +277,19 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       bool ok = mbar_wait(qdo_full, 0, abort_flag, ctx);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
       if (ok && ctx.force_timeout) ok = mbar_wait(&drain[who], 0, abort_flag, ctx);
+      uint32_t tw = 0;
       if (who == 0) {
-        for (int j = 0; j < nkt && ok; ++j) {
-          // S_j = Q K_j^T
-          const int ks = j % C::NKS, sb = j & 1;
-          // buffer sb is free once the dQ product of tile j - 2 has read E_{j-2} from it
-          // (the softmax warps loaded S_{j-2} before writing E_{j-2})
-          ok = mbar_wait(&k_full[ks], (j / C::NKS) & 1u, abort_flag, ctx) &&
-               mbar_wait(&e_free[sb], ((j >> 1) & 1u) ^ 1u, abort_flag, ctx);
+        for (int j = 0, c = 0; j < nkt && ok; ++j) {
+          if constexpr (MASK) {
+            if ((j & 31) == 0) tw = take_word(j >> 5);
+            if (!((tw >> (j & 31)) & 1u)) continue;
+          }
+          // S_j = Q K_j^T, the c-th tile taken
+          const int ks = c % C::NKS, sb = c & 1;
+          // buffer sb is free once the dQ product of tile c - 2 has read E_{c-2} from it
+          // (the softmax warps loaded S_{c-2} before writing E_{c-2})
+          ok = mbar_wait(&k_full[ks], (c / C::NKS) & 1u, abort_flag, ctx) &&
+               mbar_wait(&e_free[sb], ((c >> 1) & 1u) ^ 1u, abort_flag, ctx);
           if (!ok) break;
           tc_fence_after();
           const uint32_t klo = sdesc_lo(aK + ks * C::TILE, 16);
@@ -276,9 +302,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           tc_commit(&s_full[sb]);
           tc_commit(&k_empty[ks]);
           // dP_j = dO V_j^T
-          const int vs = j % C::NVS;
-          ok = mbar_wait(&v_full[vs], (j / C::NVS) & 1u, abort_flag, ctx) &&
-               mbar_wait(dp_free, (j & 1u) ^ 1u, abort_flag, ctx);
+          const int vs = c % C::NVS;
+          ok = mbar_wait(&v_full[vs], (c / C::NVS) & 1u, abort_flag, ctx) &&
+               mbar_wait(dp_free, (c & 1u) ^ 1u, abort_flag, ctx);
           if (!ok) break;
           tc_fence_after();
           const uint32_t vlo = sdesc_lo(aV + vs * C::TILE, 16);
@@ -289,9 +315,14 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           }
           tc_commit(&v_empty[vs]);
           tc_commit(dp_full);
+          ++c;
         }
       } else {
-        for (int t = 0; t < nkt && ok; ++t) {   // dQ += E_t K_t
+        for (int j = 0, t = 0; j < nkt && ok; ++j) {   // dQ += E_t K_t, t counting the tiles taken
+          if constexpr (MASK) {
+            if ((j & 31) == 0) tw = take_word(j >> 5);
+            if (!((tw >> (j & 31)) & 1u)) continue;
+          }
           const int ks = t % C::NKS;
           ok = mbar_wait(&e_full[t & 1], (t >> 1) & 1u, abort_flag, ctx) &&
                mbar_wait(&k_full[ks], (t / C::NKS) & 1u, abort_flag, ctx);
@@ -307,6 +338,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
                           sdesc(klo + ((kk * 2048) >> 4), HI), idesc_kmn, (t > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&k_empty[ks]);
           tc_commit(&e_free[t & 1]);
+          ++t;
         }
         if (ok) tc_commit(dq_full);
       }
@@ -378,9 +410,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     bool ok = true;
     uint32_t sv[32];
 #define SV(c) sv[c]
+    uint32_t tw = 0;
+    int ntaken = 0;   // key tiles taken (their E written); 0 leaves the dQ accumulator unwritten
     for (int j = 0; j < nkt && ok; ++j) {
-      const int sb = j & 1;
-      ok = warp_wait(&s_full[sb], (j >> 1) & 1u);
+      if constexpr (MASK) {
+        if ((j & 31) == 0) tw = take_word(j >> 5);
+        if (!((tw >> (j & 31)) & 1u)) continue;
+      }
+      const int cnt = ntaken++;
+      const int sb = cnt & 1;
+      ok = warp_wait(&s_full[sb], (cnt >> 1) & 1u);
       if (!ok) break;
       tc_fence_after();
       {
@@ -423,7 +462,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         for (int c = 0; c < DQ_COLS; ++c)
           if (col0 + c == a) SV(c) = 0u;
       }
-      ok = warp_wait(dp_full, j & 1u);
+      ok = warp_wait(dp_full, cnt & 1u);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -494,7 +533,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           float kv[8];
           load8_bf16(krow + (c0 + e) * 2, kv);
 #pragma unroll
-          for (int t = 0; t < 8; ++t) out[e + t] = s.scale * fmaf(-R, kv[t], u2f(acc[e + t]));
+          for (int t = 0; t < 8; ++t) out[e + t] = s.scale * fmaf(-R, kv[t], ntaken > 0 ? u2f(acc[e + t]) : 0.0f);
         }
         if (args.grad_bf16)
           warp_store_block32<true>(stage, out, args.dq, row0, D, c0, n_ok, lane);
@@ -615,6 +654,20 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   const int k0 = kt * BN;
   const int qt0 = s.causal ? k0 / BM : 0;   // first query tile that can see key k0 (j <= i)
   const int nq = max(0, nqt - qt0);
+  // Query tiles 32 w .. 32 w + 31 this key tile takes, as bits (the loops run over qt0 ..
+  // nqt - 1): with a tile live map, the tiles holding an allowed pair.  Every role walks
+  // them in order and counts them (it): ring slots and barrier phases follow that count, so
+  // a fully masked tile costs nothing.  Unmasked: every tile of the range.
+  auto take_word = [&](int w) -> uint32_t {
+    uint32_t bits = ~0u;
+    if constexpr (MASK) {
+      if (args.mask_k.live) {
+        const int gm = (args.mask_k.mb > 1 ? bh / s.H : 0) * args.mask_k.mh + (args.mask_k.mh > 1 ? bh % s.H : 0);
+        bits = args.mask_k.live[(static_cast<size_t>(gm) * nkt_all + kt) * args.mask_k.live_words + w];
+      }
+    }
+    return bits;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -672,11 +725,17 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       }
       bool ok = true;
       int q_issued = 0, d_issued = 0, cx_issued = 0, cy_issued = 0;
-      for (int it = 0; it < nq && ok; ++it) {
-        const int i0 = (qt0 + it) * BM;
+      uint32_t tw = ~0u;
+      for (int qa = qt0, cnt = 0; qa < nqt && ok; ++qa) {
+        if constexpr (MASK) {
+          if (qa == qt0 || (qa & 31) == 0) tw = take_word(qa >> 5);
+          if (!((tw >> (qa & 31)) & 1u)) continue;
+        }
+        const int it = cnt++;
+        const int i0 = qa * BM;
         const int qs = it % C::NQS;
         const uint32_t cpar = (it & 1u) ^ 1u;
-        const float* blk = args.ws_consts + (static_cast<size_t>(bh) * nqt + qt0 + it) * kConstBlockFloats;
+        const float* blk = args.ws_consts + (static_cast<size_t>(bh) * nqt + qa) * kConstBlockFloats;
         ok = mbar_wait(&q_empty[qs], ((it / C::NQS) & 1u) ^ 1u, abort_flag, ctx);
         if (!ok) break;
         mbar_arrive_expect_tx(&q_full[qs], C::TILE);
@@ -729,7 +788,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       bool ok = mbar_wait(kv_full, 0, abort_flag, ctx);
       // test knob: nothing is committed to `drain` yet, so this wait can only time out
       if (ok && ctx.force_timeout) ok = mbar_wait(&drain[who], 0, abort_flag, ctx);
-      for (int it = 0; it < nq && ok; ++it) {
+      uint32_t tw = ~0u;
+      for (int qa = qt0, cnt = 0; qa < nqt && ok; ++qa) {
+        if constexpr (MASK) {
+          if (qa == qt0 || (qa & 31) == 0) tw = take_word(qa >> 5);
+          if (!((tw >> (qa & 31)) & 1u)) continue;
+        }
+        const int it = cnt++;
         const int qs = it % C::NQS, ds = it % C::NDS;
         const uint32_t par = it & 1u;
         if (who == 0) {
@@ -827,8 +892,15 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     }
     uint32_t sv[KV_COLS / 32][32];
 #define SV(c) sv[(c) >> 5][(c) & 31]
-    for (int it = 0; it < nq; ++it) {
-      const int i0 = (qt0 + it) * BM;
+    uint32_t tw = ~0u;
+    int ntaken = 0;   // query tiles taken; 0 leaves the dK and dV accumulators unwritten
+    for (int qa = qt0; qa < nqt; ++qa) {
+      if constexpr (MASK) {
+        if (qa == qt0 || (qa & 31) == 0) tw = take_word(qa >> 5);
+        if (!((tw >> (qa & 31)) & 1u)) continue;
+      }
+      const int it = ntaken++;
+      const int i0 = qa * BM;
       const uint32_t par = it & 1u;
       // S^T and this tile's per-query constants X (queries past N_Q carry base 2: zero weight)
       warp_wait(st_full, par);
@@ -837,7 +909,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       for (int h = 0; h < KV_COLS / 32; ++h) tmem_ld32(lane_addr + KV_TM_ST + cbase + 32 * h, sv[h]);
       tc_wait_ld();
       // masked: key past N_K, or (causal) query i0 + c < j
-      const uint32_t mw = MASK ? mkey[4 * (qt0 + it) + part] : ~0u;
+      const uint32_t mw = MASK ? mkey[4 * qa + part] : ~0u;
       const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
       // With an attention mask, a chunk every key row of the warp sees whole needs no per-entry
       // test, and a chunk none of them sees has zero P^T and dS^T (no constants read, no
@@ -968,7 +1040,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       }
     }
 #undef SV
-    if (nq > 0) warp_wait(acc_full, 0);
+    if (ntaken > 0) warp_wait(acc_full, 0);
     if (ok) {
       tc_fence_after();
       // the warps of a row quarter store 32-column chunks of its key rows in turn, through
@@ -986,8 +1058,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         float ov[32], okv[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          ov[e] = nq > 0 ? u2f(av[e]) : 0.0f;
-          okv[e] = nq > 0 ? s.scale * u2f(kv[e]) : 0.0f;
+          ov[e] = ntaken > 0 ? u2f(av[e]) : 0.0f;
+          okv[e] = ntaken > 0 ? s.scale * u2f(kv[e]) : 0.0f;
         }
         if (args.grad_bf16) {
           warp_store_block32<true>(stage, ov, args.dv, row0, D, c0, n_ok, lane);

@@ -29,11 +29,12 @@ struct MaskBits {
 // and bits_k [G, NK, wk] (rows = keys); either may be null (mask.cu).
 cudaError_t launch_mask_pack(const uint8_t* mask, int G, int NQ, int NK, uint32_t* bits_q, int wq, uint32_t* bits_k,
                              int wk, cudaStream_t st);
-// Tile live map from packed query rows (bits_q, `words` per row): for mask head g and 128-row
-// query tile qt, bit kt of live[(g * nqt + qt) * live_words + kt / 32] is set when any pair of
-// the 128 x 128 block (query tile qt, key tile kt) may attend (mask.cu).
-cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live,
-                                  int live_words, cudaStream_t st);
+// Tile live map from packed query rows (bits_q, `words` per row): for mask head g, bit kt of
+// live_q[(g * nqt + qt) * wq + kt / 32] is set when any pair of the 128 x 128 block (query tile
+// qt, key tile kt) may attend; live_k (optional) holds the transpose, bit qt of
+// live_k[(g * nkt + kt) * wk + qt / 32] (mask.cu).
+cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live_q,
+                                  int wq, uint32_t* live_k, int wk, cudaStream_t st);
 
 // Caller-supplied CUDA events recorded at an attention call's kernel boundaries (a
 // measurement knob, ra_debug_kernel_events): e[i] is recorded before kernel i of the call

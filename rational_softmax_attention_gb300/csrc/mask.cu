@@ -48,12 +48,14 @@ __global__ void __launch_bounds__(32 * WARPS) mask_pack_cols_kernel(const uint8_
   if (j < NK) bits[(g * NK + j) * words + w] = word;
 }
 
-// One warp per (mask head, query tile, key tile): bit kt of the tile's live words is set when
-// any of the query tile's rows may attend to any key of the tile, read from the packed rows
-// (four words per key tile).  Lane l scans rows l, l + 32, l + 64, l + 96 of the query tile.
+// One warp per (mask head, query tile, key tile): the block is live when any of the query
+// tile's rows may attend to any key of the tile, read from the packed rows (four words per
+// key tile).  Lane l scans rows l, l + 32, l + 64, l + 96 of the query tile.  A live block
+// sets bit kt of its query tile's row of live_q (key tiles along the row) and, when live_k
+// is given, bit qt of its key tile's row of live_k (the same map transposed).
 __global__ void __launch_bounds__(32 * WARPS) mask_tile_live_kernel(const uint32_t* bits_q, int NQ, int words,
-                                                                    int nqt, int nkt, uint32_t* live, int live_words,
-                                                                    long long total) {
+                                                                    int nqt, int nkt, uint32_t* live_q, int wq,
+                                                                    uint32_t* live_k, int wk, long long total) {
   const long long wid = static_cast<long long>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= total) return;   // uniform across the warp
@@ -70,19 +72,24 @@ __global__ void __launch_bounds__(32 * WARPS) mask_tile_live_kernel(const uint32
     }
   }
   const bool on = __any_sync(0xffffffffu, any != 0);
-  if (lane == 0 && on) atomicOr(&live[rest * live_words + kt / 32], 1u << (kt % 32));
+  if (lane == 0 && on) {
+    atomicOr(&live_q[rest * wq + kt / 32], 1u << (kt % 32));
+    if (live_k) atomicOr(&live_k[(g * nkt + kt) * wk + qt / 32], 1u << (qt % 32));
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live,
-                                  int live_words, cudaStream_t st) {
+cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live_q,
+                                  int wq, uint32_t* live_k, int wk, cudaStream_t st) {
   const int nqt = (NQ + 127) / 128, nkt = (NK + 127) / 128;
-  cudaError_t e = cudaMemsetAsync(live, 0, static_cast<size_t>(G) * nqt * live_words * sizeof(uint32_t), st);
+  cudaError_t e = cudaMemsetAsync(live_q, 0, static_cast<size_t>(G) * nqt * wq * sizeof(uint32_t), st);
+  if (e == cudaSuccess && live_k)
+    e = cudaMemsetAsync(live_k, 0, static_cast<size_t>(G) * nkt * wk * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   const long long total = static_cast<long long>(G) * nqt * nkt;
   const unsigned grid = static_cast<unsigned>((total + WARPS - 1) / WARPS);
-  mask_tile_live_kernel<<<grid, 32 * WARPS, 0, st>>>(bits_q, NQ, words, nqt, nkt, live, live_words, total);
+  mask_tile_live_kernel<<<grid, 32 * WARPS, 0, st>>>(bits_q, NQ, words, nqt, nkt, live_q, wq, live_k, wk, total);
   return cudaGetLastError();
 }
 

@@ -540,7 +540,10 @@ class DkdvModel:
         return [self.producer(), self.issuer0(), self.issuer1()] + [self.softmax(w) for w in range(self.W)]
 
 
-@pytest.mark.parametrize("nq,nqs,nds", [(1, 2, 2), (2, 2, 2), (5, 2, 2), (6, 3, 2), (7, 2, 3)])
+# With an attention mask's tile live map the backward kernels walk only the tiles their tile
+# takes and index every slot and phase by that count, so the protocol is this one over the
+# count of taken tiles; 0 (a tile with nothing to take) is included.
+@pytest.mark.parametrize("nq,nqs,nds", [(0, 2, 2), (1, 2, 2), (2, 2, 2), (5, 2, 2), (6, 3, 2), (7, 2, 3)])
 def test_dkdv_protocol_holds_on_random_schedules(nq, nqs, nds):
     for seed in range(80):
         run_roles(DkdvModel(nq, nqs, nds).roles(), random.Random(seed * 100 + nq))
@@ -683,7 +686,7 @@ class DqModel:
         return [self.producer(), self.issuer0(), self.issuer1()] + [self.softmax(w) for w in range(self.W)]
 
 
-@pytest.mark.parametrize("nkt,nks,nvs", [(1, 2, 2), (2, 2, 2), (5, 2, 2), (6, 3, 2), (7, 2, 3)])
+@pytest.mark.parametrize("nkt,nks,nvs", [(0, 2, 2), (1, 2, 2), (2, 2, 2), (5, 2, 2), (6, 3, 2), (7, 2, 3)])
 def test_dq_protocol_holds_on_random_schedules(nkt, nks, nvs):
     for seed in range(80):
         run_roles(DqModel(nkt, nks, nvs).roles(), random.Random(seed * 100 + nkt))
