@@ -576,9 +576,9 @@ struct DkvCfg {
   static constexpr int CY_BYTES = 3 * BM * 4;
   static constexpr int OFF_BAR = OFF_CY + CY_BYTES;
   // kv_full, q_full[NQS], q_empty[NQS], do_full[NDS], do_empty[NDS],
-  // st_full, dpt_full, dpt_free, p_full, p_free, acc_full, drain[2],
+  // st_full, dpt_full, dpt_free, p_full[2], p_free, acc_full, drain[2],
   // cx_empty, cy_empty, ds_full, ds_free
-  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 12;
+  static constexpr int NUM_BARS = 1 + 2 * NQS + 2 * NDS + 13;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int USED = OFF_MISC + 16;
   // alignment slack only where it fits; otherwise the kernel requires (and checks) a
@@ -598,7 +598,7 @@ constexpr int KV_PRODUCER_WARP = KV_SOFTMAX_WARPS;
 // two MMA-issuing threads: the first issues S^T and dP^T, the second dV and dK
 constexpr int KV_MMA_WARP = KV_SOFTMAX_WARPS + 1;
 constexpr int KV_THREADS = 32 * (KV_SOFTMAX_WARPS + 3);
-static_assert(KV_COLS % 32 == 0, "whole 32-column TMEM loads per softmax warp");
+static_assert(KV_COLS == 32, "one 32-column TMEM load per softmax warp; P^T handed over in two 16-query halves");
 
 // MASK: a boolean attention mask (args.mask_k, rows = keys) applies on top of `causal`.
 template <int D, bool MASK>
@@ -631,8 +631,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* st_full = do_empty + C::NDS;   // S^T committed and constants X landed
   uint64_t* dpt_full = st_full + 1;   // dP^T committed and constants Y landed (after dK read dS^T)
   uint64_t* dpt_free = dpt_full + 1;
+  // p_full[h]: every softmax warp has written half h of its P^T (query columns 16 h .. 16 h + 15
+  // of its 32): dV takes each half as it lands
   uint64_t* p_full = dpt_free + 1;
-  uint64_t* p_free = p_full + 1;
+  uint64_t* p_free = p_full + 2;
   uint64_t* acc_full = p_free + 1;
   uint64_t* drain = acc_full + 1;   // [2], one per issuer
   uint64_t* cx_empty = drain + 2;
@@ -682,15 +684,17 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     mbar_init(st_full, 2);   // issuer 0's commit + the producer's arrival for X
     mbar_init(dpt_full, 2);   // issuer 0's commit + the producer's arrival for Y
     mbar_init(dpt_free, KV_SOFTMAX_WARPS);
-    // p_full and ds_full: one counted barrier each for all query tiles.  A warp that has
-    // finished tile i cannot arrive for tile i + 1 while another warp's arrival for tile i is
-    // missing: its next P^T needs S^T_{i+1} (st_full), which issuer 0 issues only after
-    // p_free, i.e. after the dV_i product that p_full's phase i started; its next dS^T needs
+    // p_full[0], p_full[1] and ds_full: one counted barrier each for all query tiles.  A warp
+    // that has finished tile i cannot arrive for tile i + 1 while another warp's arrival for
+    // tile i is missing: its next P^T needs S^T_{i+1} (st_full), which issuer 0 issues only
+    // after p_free, i.e. after the dV_i products that p_full's phases i started (the second
+    // half's arrivals come after the first's in every warp); its next dS^T needs
     // Y_{i+1} (dpt_full), which the producer issues only after ds_free, i.e. after the dK_i
     // product that ds_full's phase i started.  Those two waits keep every arrival in its own
     // tile's phase; a reordering that drops either needs one barrier per buffer, as e_full in
     // the dQ kernel.
-    mbar_init(p_full, KV_SOFTMAX_WARPS);
+    mbar_init(&p_full[0], KV_SOFTMAX_WARPS);
+    mbar_init(&p_full[1], KV_SOFTMAX_WARPS);
     mbar_init(p_free, 1);
     mbar_init(acc_full, 1);
     mbar_init(&drain[0], 1);
@@ -830,19 +834,26 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           // Q_i and dO_i arrived long before: waiting on them first leaves a single wait
           // between the softmax warps' arrival and the first product.
           ok = mbar_wait(&q_full[qs], (it / C::NQS) & 1u, abort_flag, ctx) &&
-               mbar_wait(&do_full[ds], (it / C::NDS) & 1u, abort_flag, ctx) &&
-               mbar_wait(p_full, par, abort_flag, ctx);
+               mbar_wait(&do_full[ds], (it / C::NDS) & 1u, abort_flag, ctx);
           if (!ok) break;
-          tc_fence_after();
           const uint32_t qmn = sdesc_lo(aQ + qs * C::TILE, BOX_BYTES), domn = sdesc_lo(aDO + ds * C::TILE, BOX_BYTES);
+          // two halves: the first 16 query columns of every softmax warp (16-query steps kk =
+          // 0, 2, 4, 6), issued while the warps form the second 16 (kk = 1, 3, 5, 7)
+          for (int h = 0; h < 2 && ok; ++h) {
+            ok = mbar_wait(&p_full[h], par, abort_flag, ctx);
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk) {
-            // P^T from tensor memory: the softmax warps of queries 16 kk .. 16 kk + 15 wrote
-            // it over the first half of their S^T columns, 8 columns per 16 queries
-            tc_mma_f16_ts(tmem + KV_TM_DV,
-                          tmem + KV_TM_ST + (16 * kk / KV_COLS) * KV_COLS + (16 * kk % KV_COLS) / 2,
-                          sdesc(domn + ((kk * 2048) >> 4), HI), idesc_kmn, (it > 0 || kk > 0) ? 1u : 0u);
+            for (int kq = 0; kq < BM / 32; ++kq) {
+              const int kk = 2 * kq + h;
+              // P^T from tensor memory: the softmax warps of queries 16 kk .. 16 kk + 15 wrote
+              // it over the first half of their S^T columns, 8 columns per 16 queries
+              tc_mma_f16_ts(tmem + KV_TM_DV,
+                            tmem + KV_TM_ST + (16 * kk / KV_COLS) * KV_COLS + (16 * kk % KV_COLS) / 2,
+                            sdesc(domn + ((kk * 2048) >> 4), HI), idesc_kmn, (it > 0 || kk > 0) ? 1u : 0u);
+            }
           }
+          if (!ok) break;
           tc_commit(&do_empty[ds]);
           tc_commit(p_free);
           ok = mbar_wait(ds_full, par, abort_flag, ctx);
@@ -965,14 +976,21 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           pk[2 * h] = pack_f16x2_sat(pa.x, pa.y);
           pk[2 * h + 1] = pack_f16x2_sat(pb.x, pb.y);
         }
-        if ((c & 31) == 24) tmem_st16(lane_addr + KV_TM_ST + cbase + ((c & 32) >> 1), pt);
+        if (c == 8) {   // the first 16 queries' P^T: dV starts on it while the rest is formed
+          tmem_st8(lane_addr + KV_TM_ST + cbase, pt);
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_full[0]);
+        }
       }
+      tmem_st8(lane_addr + KV_TM_ST + cbase + 8, pt + 8);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(cx_empty);   // this warp's reads of X are done
-        mbar_arrive(p_full);
+        mbar_arrive(&p_full[1]);
       }
       // dS^T = coef (dP^T - D_i); the entries (a_i, i) where this key is the query's argmax
       // take -R_i afterwards

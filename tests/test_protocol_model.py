@@ -376,7 +376,8 @@ class DkdvModel:
     rings of NQS and NDS slots, the per-query constants X and Y as bulk copies), issuer 0
     (S^T = K Q^T and dP^T = V dO^T), issuer 1 (dV += P^T dO, P^T read from tensor memory over
     the S^T columns, then dK += dS^T Q) and the softmax warps (P^T into tensor memory, dS^T
-    into a shared tile)."""
+    into a shared tile).  P^T is handed over in two halves (the first and second 16 query
+    columns of every warp, p_full[0] and p_full[1]); dV takes each half as it lands."""
 
     def __init__(self, nq, nqs, nds, warps=4, mutation=None):
         self.nq, self.nqs, self.nds, self.W, self.mutation = nq, nqs, nds, warps, mutation
@@ -389,7 +390,7 @@ class DkdvModel:
         self.st_full = Bar("st_full", 2)      # issuer 0's commit + the producer's arming for X
         self.dpt_full = Bar("dpt_full", 2)    # issuer 0's commit + the producer's arming for Y
         self.dpt_free = Bar("dpt_free", W)
-        self.p_full = Bar("p_full", W)
+        self.p_full = [Bar(f"p_full[{h}]", W) for h in range(2)]
         self.p_free = Bar("p_free", 1)
         self.acc_full = Bar("acc_full", 1)
         self.cx_empty = Bar("cx_empty", W)
@@ -404,9 +405,9 @@ class DkdvModel:
         self.x_tile = self.y_tile = -1     # constants that have landed
         self.x_readers = defaultdict(int)
         self.y_readers = defaultdict(int)
-        self.st_state = ("empty", -1)      # tensor-memory S^T columns: ("S", it) or ("P", it)
+        self.st_tile = -1                  # tile whose S^T product has completed (P^T then goes over it)
         self.st_readers = 0
-        self.pt_written = defaultdict(set)
+        self.pt_written = defaultdict(set)   # (tile, half) -> warps that wrote that half of P^T
         self.dpt_tile, self.dpt_readers = -1, 0
         self.ds_written = defaultdict(set)
         self.ds_reading = -1               # tile whose dS^T the running dK product reads
@@ -455,13 +456,13 @@ class DkdvModel:
             yield ("wait", self.q_full[qs], it // nqs)
             yield ("wait", self.p_free, it - 1)
             require(self.q_slot[qs] == it, f"S^T of tile {it} issued before its Q landed")
-            require(self.st_readers == 0 and (it == 0 or self.st_state == ("P", it - 1) and self.pt_read_done),
+            require(self.st_readers == 0 and (it == 0 or self.pt_read_done),
                     f"S^T of tile {it} overwrites the S^T/P^T columns while in use")
             self.q_readers[it] += 1
 
             def s_done(it=it):
                 self.q_readers[it] -= 1
-                self.st_state = ("S", it)
+                self.st_tile = it
                 self.pt_read_done = False
             yield self._product(0, s_done)
             yield ("commit", 0, [(self.st_full, it), (self.q_empty[qs], it // nqs)])
@@ -484,15 +485,18 @@ class DkdvModel:
             qs, ds = it % nqs, it % nds
             yield ("wait", self.q_full[qs], it // nqs)
             yield ("wait", self.do_full[ds], it // nds)
-            yield ("wait", self.p_full, it)
-            require(len(self.pt_written[it]) == self.W and self.st_state == ("P", it),
-                    f"dV of tile {it} issued before every warp wrote P^T")
             self.do_readers[it] += 1
+            for h in range(2):
+                if not (h == 1 and self.mutation == "dv_half_without_wait"):
+                    yield ("wait", self.p_full[h], it)
+                require(len(self.pt_written[(it, h)]) == self.W and self.st_tile == it,
+                        f"dV (half {h}) of tile {it} issued before every warp wrote that half of P^T")
 
-            def dv_done(it=it):
-                self.do_readers[it] -= 1
-                self.pt_read_done = True
-            yield self._product(1, dv_done)
+                def dv_done(it=it, h=h):
+                    if h == 1:
+                        self.do_readers[it] -= 1
+                        self.pt_read_done = True
+                yield self._product(1, dv_done)
             yield ("commit", 1, [(self.do_empty[ds], it // nds), (self.p_free, it)])
             yield ("wait", self.ds_full, it)
             require(len(self.ds_written[it]) == self.W, f"dK of tile {it} issued before every warp wrote dS^T")
@@ -509,16 +513,17 @@ class DkdvModel:
     def softmax(self, w):
         for it in range(self.nq):
             yield ("wait", self.st_full, it)
-            require(self.st_state == ("S", it) and self.x_tile == it, f"warp reads S^T/X of tile {it} before they are in")
+            require(self.st_tile == it and self.x_tile == it, f"warp reads S^T/X of tile {it} before they are in")
             self.st_readers += 1
             self.x_readers[it] += 1
             yield ("do", lambda: None)
-            self.st_readers -= 1
+            self.st_readers -= 1   # this warp's S^T columns are read: its P^T goes over them
+            self.pt_written[(it, 0)].add(w)
+            yield ("do", lambda it=it: self.p_full[0].arrive(it))
+            yield ("do", lambda: None)
             self.x_readers[it] -= 1
-            self.pt_written[it].add(w)
-            if len(self.pt_written[it]) == self.W:
-                self.st_state = ("P", it)
-            yield ("do", lambda it=it: (self.cx_empty.arrive(it), self.p_full.arrive(it)))
+            self.pt_written[(it, 1)].add(w)
+            yield ("do", lambda it=it: (self.cx_empty.arrive(it), self.p_full[1].arrive(it)))
             yield ("wait", self.dpt_full, it)
             require(self.dpt_tile == it and self.y_tile == it, f"warp reads dP^T/Y of tile {it} before they are in")
             self.dpt_readers += 1
@@ -553,6 +558,12 @@ def test_planted_dkdv_protocol_mistake_is_caught():
     """Issuing Y (and with it the dP^T-complete phase) before dK has read the previous dS^T
     tile lets a warp overwrite that tile under the running dK product."""
     assert _caught(lambda: DkdvModel(5, 2, 2, mutation="y_before_dk"))
+
+
+def test_planted_dkdv_half_hand_off_mistake_is_caught():
+    """Issuing the second half of dV on the first half's arrival reads P^T columns a slow
+    warp has not written yet."""
+    assert _caught(lambda: DkdvModel(4, 2, 2, mutation="dv_half_without_wait"))
 
 
 # ---------------------------------------------------------------------------- dQ kernel
