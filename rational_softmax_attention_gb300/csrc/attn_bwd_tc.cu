@@ -419,6 +419,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
       const int cnt = ntaken++;
       const int sb = cnt & 1;
+      const uint32_t mw = MASK ? mrow[4 * j + part] : ~0u;   // in flight during the wait
       ok = warp_wait(&s_full[sb], (cnt >> 1) & 1u);
       if (!ok) break;
       tc_fence_after();
@@ -428,7 +429,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         tc_wait_ld();
       }
       const int col0 = j * BN + cbase;   // key index of local column 0
-      const uint32_t mw = MASK ? mrow[4 * j + part] : ~0u;
       // With an attention mask, a chunk every row of the warp sees whole needs no per-entry
       // test, and a chunk no row sees has zero coefficients and E (no arithmetic).  The vote
       // runs in the masked instance only, where the whole warp is here together.
@@ -914,13 +914,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       const int i0 = qa * BM;
       const uint32_t par = it & 1u;
       // S^T and this tile's per-query constants X (queries past N_Q carry base 2: zero weight)
+      const uint32_t mw = MASK ? mkey[4 * qa + part] : ~0u;   // in flight during the wait
       warp_wait(st_full, par);
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < KV_COLS / 32; ++h) tmem_ld32(lane_addr + KV_TM_ST + cbase + 32 * h, sv[h]);
       tc_wait_ld();
       // masked: key past N_K, or (causal) query i0 + c < j
-      const uint32_t mw = MASK ? mkey[4 * qa + part] : ~0u;
       const int first_vis = !j_ok ? BM : (s.causal ? min(BM, max(0, j - i0)) : 0);   // first visible column
       // With an attention mask, a chunk every key row of the warp sees whole needs no per-entry
       // test, and a chunk none of them sees has zero P^T and dS^T (no constants read, no

@@ -224,3 +224,19 @@ def test_block_sparse_masks_leave_dead_tiles_out(D, nq, nk, causal, layout):
             want[0] += vis
             want[1] += skip
     assert got == tuple(want)
+
+
+@pytest.mark.parametrize("D,nq,nk,causal", [(64, 520, 700, False), (128, 640, 700, True), (128, 1024, 896, False)])
+def test_block_masks_with_full_dead_and_mixed_tiles(D, nq, nk, causal):
+    """Blocks fully allowed (they take the unmasked code), fully masked (left out) and half
+    filled (per-row mask words), ragged at both ends: forward and backward against the oracle."""
+    B, H = 1, 2
+    q, k, v, do = attention_inputs(B, H, nq, nk, D, seed=nq + 2 * nk + D, sigma_qk=1.0, dtype=torch.bfloat16)
+    rng = np.random.default_rng(nq + nk + D)
+    nqt, nkt = -(-nq // 128), -(-nk // 128)
+    kind = rng.integers(0, 3, size=(H, nqt, nkt))   # 0 masked, 1 full, 2 half filled
+    kind[:, :, 0] = 1
+    fine = rng.random((H, nqt * 128, nkt * 128)) < 0.5
+    blocks = np.repeat(np.repeat(kind, 128, axis=1), 128, axis=2)
+    dense = ((blocks == 1) | ((blocks == 2) & fine))[:, :nq, :nk]
+    _check(q, k, v, do, D ** -0.5, causal, dense[None])
