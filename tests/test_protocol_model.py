@@ -66,13 +66,15 @@ def require(cond, msg):
         raise ProtocolError(msg)
 
 
-def run_roles(roles, rng, max_steps=400000):
+def run_roles(roles, rng, max_steps=400000, slow=()):
     """Run role generators to completion on a random schedule.  Actions:
       ("wait", bar, k)            block until phase k of bar has completed
       ("do", fn)                  run fn now (an arrival, a state change, a check)
       ("copy", bar, k, fn)        start a copy whose bytes complete phase k of bar; fn on landing
       ("mma", issuer, fn)         issue a product; fn when it completes (in issue order)
       ("commit", issuer, arrivals) arrive on each (bar, phase) once the issuer's earlier products completed
+    Roles listed in `slow` are scheduled only one time in fifty while anything else can move:
+    a thread that falls far behind the others.
     """
     state = [None] * len(roles)
     alive = set(range(len(roles)))
@@ -98,6 +100,10 @@ def run_roles(roles, rng, max_steps=400000):
         if not choices:
             raise ProtocolError("deadlock: " + ", ".join(
                 f"{state[i][1].name} phase {state[i][2]}" for i in alive if state[i][0] == "wait"))
+        if slow:
+            fast = [c for c in choices if not (c[0] == "role" and c[1] in slow)]
+            if fast and len(fast) < len(choices) and rng.random() < 0.98:
+                choices = fast
         kind, i = rng.choice(choices)
         if kind == "copy":
             bar, phase, fn = copies.pop(rng.randrange(len(copies)))
@@ -324,6 +330,12 @@ def test_forward_protocol_holds_on_random_schedules(ncta, nst, nkt, nshort, shor
         rng = random.Random(seed * 1000 + nkt * 10 + ncta)
         dead = {(g, j) for g in range(2) for j in range(nkt) if rng.random() < dead_frac}
         run_roles(ForwardModel(ncta, nst, takes, dead).roles(), rng)
+    # one role far behind the others: a producer, either issuer, a softmax warp
+    for slow in (0, ncta, ncta + 1, ncta + 2):
+        for seed in range(20):
+            rng = random.Random(seed * 31 + slow)
+            dead = {(g, j) for g in range(2) for j in range(nkt) if rng.random() < dead_frac}
+            run_roles(ForwardModel(ncta, nst, takes, dead).roles(), rng, slow={slow})
 
 
 @pytest.mark.parametrize("ncta,nst,nkt", [(1, 3, 6), (1, 6, 9), (2, 6, 6), (2, 6, 11)])
@@ -552,6 +564,10 @@ class DkdvModel:
 def test_dkdv_protocol_holds_on_random_schedules(nq, nqs, nds):
     for seed in range(80):
         run_roles(DkdvModel(nq, nqs, nds).roles(), random.Random(seed * 100 + nq))
+    # one role far behind the others: the producer, either issuer, a softmax warp
+    for slow in (0, 1, 2, 3):
+        for seed in range(40):
+            run_roles(DkdvModel(nq, nqs, nds).roles(), random.Random(seed * 7 + slow), slow={slow})
 
 
 def test_planted_dkdv_protocol_mistake_is_caught():
@@ -701,6 +717,9 @@ class DqModel:
 def test_dq_protocol_holds_on_random_schedules(nkt, nks, nvs):
     for seed in range(80):
         run_roles(DqModel(nkt, nks, nvs).roles(), random.Random(seed * 100 + nkt))
+    for slow in (0, 1, 2, 3):
+        for seed in range(40):
+            run_roles(DqModel(nkt, nks, nvs).roles(), random.Random(seed * 7 + slow), slow={slow})
 
 
 @pytest.mark.parametrize("mutation", ["no_e_free_wait", "single_e_full"])
