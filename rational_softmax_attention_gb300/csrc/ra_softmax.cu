@@ -493,8 +493,8 @@ cudaError_t launch_ra_softmax_bwd_bf16(const void* x, const void* p, const void*
       ra_softmax_bwd_bf16_vec_kernel<256, 1><<<grid, 256, 0, st>>>(xs, ps, gs, ds, c);
     else if (cols <= 4096)
       ra_softmax_bwd_bf16_vec_kernel<256, 2><<<grid, 256, 0, st>>>(xs, ps, gs, ds, c);
-    else if (cols <= 8192)
-      ra_softmax_bwd_bf16_vec_kernel<512, 2><<<grid, 512, 0, st>>>(xs, ps, gs, ds, c);
+    else if (cols <= 8192)   // 256 threads x 4 vectors: 0.228 ms at 16384 x 8192 against 0.260 for 512 x 2
+      ra_softmax_bwd_bf16_vec_kernel<256, 4><<<grid, 256, 0, st>>>(xs, ps, gs, ds, c);
     else
       ra_softmax_bwd_bf16_vec_kernel<512, 4><<<grid, 512, 0, st>>>(xs, ps, gs, ds, c);
     return cudaGetLastError();
