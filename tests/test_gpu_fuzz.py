@@ -105,3 +105,38 @@ def test_random_configuration_matches_oracle(i):
             close(parity.f64(dq[b, h]), gq, f"{what} dq[{b},{h}]")
             close(parity.f64(dk[b, h]), gk, f"{what} dk[{b},{h}]")
             close(parity.f64(dv[b, h]), gv, f"{what} dv[{b},{h}]")
+
+
+@pytest.mark.parametrize("i", range(48))
+def test_random_softmax_rows_match_oracle(i):
+    """ra_softmax forward and backward on seeded random shapes (both the register-held and
+    the generic kernels: columns in and out of multiples of 4 and 8, up to 20000), fp32 and
+    bf16, spread 0.5 to 8: fp32 within 2e-5; bf16 forward within half a bf16 ulp (+1e-6) and
+    bf16 backward within the bound of test_gpu_softmax (p the float64 probabilities rounded
+    to bf16)."""
+    from test_gpu_softmax import _assert_bf16_rounding_of, _bwd_bf16_bound
+    rng = np.random.default_rng(11000 + i)
+    bf16 = bool(rng.random() < 0.5)
+    rows = int(rng.integers(1, 7))
+    cols = int(rng.choice([1, 2, 3, 7, 8, 31, 64, 100, 1000, 1024, 2050, 4096, 4100, 8192, 8200, 12288, 16384, 20000]))
+    sigma = float(rng.choice([0.5, 2.0, 8.0]))
+    x = torch.from_numpy(rng.standard_normal((rows, cols)) * sigma).float()
+    dy = torch.from_numpy(rng.standard_normal((rows, cols))).float()
+    if bf16:
+        x, dy = x.to(torch.bfloat16), dy.to(torch.bfloat16)
+    xd, dyd = x.double().numpy(), dy.double().numpy()
+    want_p, *_ = oracle.ra_softmax(xd)
+    want_dx = oracle.ra_softmax_bwd(xd, dyd)
+    p = ra.ra_softmax(x.cuda())
+    p_in = torch.from_numpy(want_p).to(x.dtype).cuda() if bf16 else p
+    dx = ra.ra_softmax_backward(x.cuda(), p_in, dy.cuda())
+    torch.cuda.synchronize()
+    assert ra.device_status() == "RA_OK"
+    what = f"softmax case {i}: {'bf16' if bf16 else 'fp32'} [{rows}x{cols}] sigma {sigma}"
+    if bf16:
+        _assert_bf16_rounding_of(parity.f64(p), want_p, what)
+        err = np.abs(parity.f64(dx) - want_dx)
+        assert np.all(err <= _bwd_bf16_bound(xd, want_p, dyd, want_dx)), what
+    else:
+        parity.assert_close_fp32(parity.f64(p), want_p, what)
+        parity.assert_close_fp32(parity.f64(dx), want_dx, what + " bwd")
