@@ -240,3 +240,28 @@ def test_block_masks_with_full_dead_and_mixed_tiles(D, nq, nk, causal):
     blocks = np.repeat(np.repeat(kind, 128, axis=1), 128, axis=2)
     dense = ((blocks == 1) | ((blocks == 2) & fine))[:, :nq, :nk]
     _check(q, k, v, do, D ** -0.5, causal, dense[None])
+
+
+@pytest.mark.parametrize("D,causal", [(64, False), (128, True), (128, False)])
+def test_tile_maps_span_several_words(D, causal):
+    """More than 32 tiles each way (4264 rows and keys: 34 tiles), so every role's walk over
+    the tile maps crosses a 32-tile word, and (causal) the dK/dV kernel's walk starts inside a
+    word: a block mask, forward and backward of one whole head against the oracle, and the
+    exact count of tiles no product ran on."""
+    B, H, n = 1, 1, 34 * 128 - 88
+    q, k, v, do = attention_inputs(B, H, n, n, D, seed=4000 + D + int(causal), sigma_qk=1.0, dtype=torch.bfloat16)
+    rng = np.random.default_rng(4000 + D)
+    nt = -(-n // 128)
+    blocks = rng.random((nt, nt)) < 0.35
+    blocks[:, 0] = True
+    blocks[:, 33] = rng.random(nt) < 0.5    # the second word's tiles
+    fine = rng.random((nt * 128, nt * 128)) < 0.6
+    dense = (np.repeat(np.repeat(blocks, 128, axis=0), 128, axis=1) & fine)[:n, :n]
+    dense[:, 0] = True
+    _check(q, k, v, do, D ** -0.5, causal, dense)
+    pm = ra.pack_attn_mask(torch.from_numpy(dense).cuda(), B, H, n, n)
+    _, _, _, _, counts = ra.ra_attention_forward(q.cuda(), k.cuda(), v.cuda(), causal=causal, tile_counts=True,
+                                                 mask=pm)
+    torch.cuda.synchronize()
+    span = 2 if D == 128 and n > 256 else 1
+    assert tuple(int(c) for c in counts.tolist()) == _expected_tile_counts(blocks, n, n, causal, span)
