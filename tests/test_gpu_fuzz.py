@@ -55,7 +55,9 @@ def _case(i):
     sigma = float(rng.choice([0.5, 1.0])) if fp32 else float(rng.choice([0.5, 1.0, 3.0]))
     kind = None if fp32 or rng.random() < 0.3 else str(rng.choice(["random", "blocks", "keypad", "rows"]))
     mask = _mask(rng, kind, B, H, nq, nk) if kind else None
-    return dict(fp32=fp32, D=D, nq=nq, nk=nk, B=B, H=H, causal=causal, sigma=sigma, kind=kind, mask=mask)
+    bf16_out = (not fp32) and rng.random() < 0.3   # O and the gradients rounded to bf16 once
+    return dict(fp32=fp32, D=D, nq=nq, nk=nk, B=B, H=H, causal=causal, sigma=sigma, kind=kind, mask=mask,
+                bf16_out=bf16_out)
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
@@ -64,7 +66,9 @@ def test_random_configuration_matches_oracle(i):
     dtype = torch.float32 if c["fp32"] else torch.bfloat16
     B, H, nq, nk, D, causal = c["B"], c["H"], c["nq"], c["nk"], c["D"], c["causal"]
     scale = D ** -0.5
-    what = f"case {i}: {'fp32' if c['fp32'] else 'bf16'} B{B} H{H} {nq}x{nk} D{D} causal={causal} mask={c['kind']}"
+    what = (f"case {i}: {'fp32' if c['fp32'] else 'bf16'} B{B} H{H} {nq}x{nk} D{D} causal={causal} "
+            f"mask={c['kind']} bf16_out={c['bf16_out']}")
+    out_dt = torch.bfloat16 if c["bf16_out"] else torch.float32
     q, k, v, do = attention_inputs(B, H, nq, nk, D, seed=9000 + i, sigma_qk=c["sigma"], dtype=dtype)
     qg, kg, vg, dog = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     pm = None
@@ -75,15 +79,25 @@ def test_random_configuration_matches_oracle(i):
         while m.ndim < 4:
             m = m[None]
         full = np.broadcast_to(m, (B, H, nq, nk))
-    o, rm, rs, ra_, _ = ra.ra_attention_forward(qg, kg, vg, scale=scale, causal=causal, out_dtype=torch.float32,
+    o, rm, rs, ra_, _ = ra.ra_attention_forward(qg, kg, vg, scale=scale, causal=causal, out_dtype=out_dt,
                                                 mask=pm)
-    dq, dk, dv = ra.ra_attention_backward(qg, kg, vg, o, dog, rm, rs, ra_, scale=scale, causal=causal,
-                                          grad_dtype=torch.float32, mask=pm)
+    # the backward reads O for D_i = dO . O; it takes the fp32 O here, so that bf16 gradients
+    # differ from the oracle's only by their own rounding (a bf16 O in D_i is covered by
+    # test_bf16_autograd_function_bf16_gradients)
+    o32 = o if out_dt == torch.float32 else ra.ra_attention_forward(qg, kg, vg, scale=scale, causal=causal,
+                                                                     out_dtype=torch.float32, mask=pm)[0]
+    dq, dk, dv = ra.ra_attention_backward(qg, kg, vg, o32, dog, rm, rs, ra_, scale=scale, causal=causal,
+                                          grad_dtype=out_dt, mask=pm)
     torch.cuda.synchronize()
     assert ra.device_status() == "RA_OK", what
     def close(got, want, msg):
         sc = max(1.0, float(np.sqrt(np.mean(np.square(want)))) if want.size else 1.0)
-        if c["fp32"]:
+        if c["bf16_out"]:   # the bounds plus one bf16 rounding of each value (half an ulp: 2^-9 relative)
+            err = np.abs(np.asarray(got) - want)
+            assert np.all(np.isfinite(got)), msg
+            assert np.all(err <= parity.BF16_MAX_ABS * sc + 2.0 ** -8 * np.abs(want)), msg
+            assert err.mean() <= parity.BF16_MEAN_ABS * sc + 2.0 ** -9 * np.abs(want).mean(), msg
+        elif c["fp32"]:
             parity.assert_close_fp32(got, want, msg, max_abs=parity.FP32_MAX_ABS * sc)
         else:
             parity.assert_close_bf16(got, want, msg, max_abs=parity.BF16_MAX_ABS * sc, mean_abs=parity.BF16_MEAN_ABS * sc)
