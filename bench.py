@@ -433,6 +433,30 @@ def run_ours(args):
     causal_fl = attn_flops(wc.B, wc.H, wc.N, wc.N, wc.D, True, False)
     del qc, kc, vc, oc, rmc, rsc, rac
 
+    # the step's attention with a key-padding mask (the second half of the keys masked for
+    # every query): the tile maps leave the padded key tiles out of every kernel
+    qm, km, vm, dom = hp.dev_in[:4]
+    Bm, Hm, Nm, _ = qm.shape
+    kpm = hp.ra.pack_attn_mask((torch.arange(Nm, device=dev) < Nm // 2)[None, :].expand(Nm, Nm), Bm, Hm, Nm, Nm)
+    om, rmm, rsm, ram, _ = hp.ra.ra_attention_forward(qm, km, vm, scale=w.scale, out_dtype=torch.float32, mask=kpm)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1) / args.steps
+    kp_fwd_ms = timed(lambda: hp.ra.ra_attention_forward(qm, km, vm, scale=w.scale, out_dtype=torch.float32, mask=kpm))
+    kp_bwd_ms = timed(lambda: hp.ra.ra_attention_backward(qm, km, vm, om, dom, rmm, rsm, ram, scale=w.scale, mask=kpm))
+    if hp.ra.device_status() != "RA_OK":
+        raise RuntimeError("masked attention: device status " + hp.ra.device_status())
+    del kpm, om, rmm, rsm, ram
+
     # ra_softmax backward on the step's softmax workload (reported beside the step): x, the
     # forward's p, and a seeded dy; 16 B per element (x, p, dy read, dx written)
     xs, ps = hp.dev_in[4], hp.outs[4]
@@ -641,6 +665,10 @@ def run_ours(args):
             "ra_attention_bwd": {"ms": med["ra_attention_bwd_ms"], "TFLOP_per_s": bwd_tflops,
                                  "frac_bf16_burst": bwd_tflops / tc_burst,
                                  "frac_bf16_sustained": bwd_tflops / tc_sustained},
+            "ra_attention_keypad_half_b4h16n8192d128": {
+                "fwd_ms": kp_fwd_ms, "bwd_ms": kp_bwd_ms,
+                "note": "the step's attention with the second half of the keys masked for every query "
+                        "(through the binding); fully masked tiles are left out, so about half the work"},
             "ra_attention_fwd_causal_b4h16n8192d128": {"ms": causal_ms,
                                                        "TFLOP_per_s": causal_fl / (causal_ms * 1e-3) / 1e12,
                                                        "frac_bf16_burst": causal_fl / (causal_ms * 1e-3) / 1e12 / tc_burst},
