@@ -115,7 +115,8 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
  *   workspace    device memory of ra_attention_fwd_workspace_size() bytes, 16-byte
  *                aligned, contents on entry irrelevant; required for RA_BF16 inputs
  *                (NULL allowed for RA_F32).  The call writes an fp16 copy of v there
- *                (masked calls also a map of the 128 x 128 tiles the mask allows a pair in)
+ *                (masked calls also two maps of the 128 x 128 tiles: those the mask allows
+ *                a pair in, and those it allows every pair of)
  *                and forms P V in fp16, with P rounded to 2^-11 instead of 2^-8.  The
  *                copy is exact for 2^-14 <= |v| <= 65504 (normal fp16); smaller
  *                magnitudes become fp16 subnormals, rounded to a multiple of 2^-24
@@ -142,8 +143,9 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
 /*
  * ra_attention_fwd_workspace_size -- bytes of device workspace ra_attention_fwd (and
  * ra_attention_fwd_masked) needs for these sizes: the fp16 copy of v (B*H*N_K*D*2 bytes,
- * padded to 256), then the tile map a masked call builds (B*H*ceil(N_Q/128) rows of
- * ceil(ceil(N_K/128)/32) uint32 words, padded to 256).  Returns 0 for invalid sizes.
+ * padded to 256), then the two tile maps a masked call builds (each B*H*ceil(N_Q/128)
+ * rows of ceil(ceil(N_K/128)/32) uint32 words, padded to 256).  Returns 0 for invalid
+ * sizes.
  */
 size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 
@@ -157,9 +159,10 @@ size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
  * their products).  The copies are exact for 2^-14 <= |x| <= 65504; smaller values are
  * rounded to a multiple of 2^-24 (fp16 subnormals; below 2^-25 to 0), and |x| > 65504
  * or NaN saturates and is reported as RA_ERR_UNSUPPORTED by ra_device_status().  Last,
- * the tile map a masked call builds, both ways: B*H*ceil(N_Q/128) rows of
- * ceil(ceil(N_K/128)/32) uint32 words and B*H*ceil(N_K/128) rows of ceil(ceil(N_Q/128)/32).
- * Each piece is padded to 256 bytes.  Returns 0 for invalid sizes.
+ * the two tile maps a masked call builds (tiles with an allowed pair, tiles with every pair
+ * allowed), each both ways: B*H*ceil(N_Q/128) rows of ceil(ceil(N_K/128)/32) uint32 words
+ * and B*H*ceil(N_K/128) rows of ceil(ceil(N_Q/128)/32).  Each piece is padded to 256
+ * bytes.  Returns 0 for invalid sizes.
  */
 size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 
@@ -260,7 +263,8 @@ void ra_debug_kernel_events(void* const* events, int n);
  * query may attend to the key), applied together with `causal`.  Page "Ra-Family: Rational
  * Neural Architecture", section 3, ra_attention (a drop-in for scaled_dot_product_attention).
  * The masked calls take the mask bit-packed: bit (c % 32) of word c / 32 of a row is set when
- * column c may be attended; rows of ra_attention_mask_words(columns) uint32 words.  A mask has
+ * column c may be attended; rows of ra_attention_mask_words(columns) uint32 words (bits of
+ * columns past the last are ignored; ra_attention_mask_pack leaves them clear).  A mask has
  * MB x MH heads (MB = 1 or B, MH = 1 or H: shared across the batch and/or the heads); head
  * (b, h) uses mask head (MB > 1 ? b : 0) * MH + (MH > 1 ? h : 0).  A query row with no
  * attendable key gives O = 0, row_s = 0, row_arg = -1 and zero gradients.

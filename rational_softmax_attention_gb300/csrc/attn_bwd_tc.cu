@@ -126,9 +126,10 @@ __device__ __forceinline__ void softmax_sync() {
 }
 
 // MASK: a boolean attention mask (args.mask_q, rows = queries) applies on top of `causal`.
+// nk: the keys taken, N_K, or fewer for a query tile run as an unmasked one over the keys its
+// mask leaves (the masked kernel's plain_run test).
 template <int D, bool MASK>
-__global__ void __launch_bounds__(DQ_THREADS, 1)
-    attn_bwd_dq_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
+__device__ __forceinline__ void dq_body(const AttnShape& s, const BwdTcArgs& args, const LaunchCtx& ctx, int nk) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t mis = smem_u32(smem_raw) & 1023u;
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   const int bh = item / nqt;
   const int qt = s.causal ? (nqt - 1 - item % nqt) : (item % nqt);
   const int q0 = qt * BM;
-  const int last_key = s.causal ? min(s.NK - 1, min(s.NQ - 1, q0 + BM - 1)) : s.NK - 1;
+  const int last_key = s.causal ? min(nk - 1, min(s.NQ - 1, q0 + BM - 1)) : nk - 1;
   const int nkt = last_key / BN + 1;
   // Key tiles 32 w .. 32 w + 31 this query tile takes, as bits: its range and, with a tile
   // live map, the tiles holding an allowed pair.  Every role walks them in key order and
@@ -186,6 +187,17 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
     }
     return bits;
+  };
+  // Key tiles 32 w .. 32 w + 31 the mask allows whole to every row of this query tile: their
+  // mask words are all ones and are not read.
+  auto full_word = [&](int w) -> uint32_t {
+    if constexpr (MASK) {
+      if (args.mask_q.full) {
+        const int gm = (args.mask_q.mb > 1 ? bh / s.H : 0) * args.mask_q.mh + (args.mask_q.mh > 1 ? bh % s.H : 0);
+        return args.mask_q.full[(static_cast<size_t>(gm) * nqt + qt) * args.mask_q.live_words + w];
+      }
+    }
+    return 0u;
   };
 
   if (threadIdx.x == 0) {
@@ -404,22 +416,26 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const float base = (i_ok && m_sc > -INFINITY) ? fmaf(m_sc, 1.0f / 32.0f, 0.5f) : 2.0f;
     const float c2 = s.scale * (1.0f / 32.0f);
     const float cE = 0.25f * inv_s;
-    const int lim = s.causal ? min(i, s.NK - 1) : s.NK - 1;
+    const int lim = s.causal ? min(i, nk - 1) : nk - 1;
     const float2 cE2 = make_float2(cE, cE), mcED2 = make_float2(-cE * Di, -cE * Di);
     float2 R2 = make_float2(0.0f, 0.0f);
     bool ok = true;
     uint32_t sv[32];
 #define SV(c) sv[c]
-    uint32_t tw = 0;
+    uint32_t tw = 0, fw = 0;
     int ntaken = 0;   // key tiles taken (their E written); 0 leaves the dQ accumulator unwritten
     for (int j = 0; j < nkt && ok; ++j) {
       if constexpr (MASK) {
-        if ((j & 31) == 0) tw = take_word(j >> 5);
+        if ((j & 31) == 0) {
+          tw = take_word(j >> 5);
+          fw = full_word(j >> 5);
+        }
         if (!((tw >> (j & 31)) & 1u)) continue;
       }
       const int cnt = ntaken++;
       const int sb = cnt & 1;
-      const uint32_t mw = MASK ? mrow[4 * j + part] : ~0u;   // in flight during the wait
+      // in flight during the wait; a tile the mask allows whole reads none
+      const uint32_t mw = (MASK && !((fw >> (j & 31)) & 1u)) ? mrow[4 * j + part] : ~0u;
       ok = warp_wait(&s_full[sb], (cnt >> 1) & 1u);
       if (!ok) break;
       tc_fence_after();
@@ -600,10 +616,34 @@ constexpr int KV_MMA_WARP = KV_SOFTMAX_WARPS + 1;
 constexpr int KV_THREADS = 32 * (KV_SOFTMAX_WARPS + 3);
 static_assert(KV_COLS == 32, "one 32-column TMEM load per softmax warp; P^T handed over in two 16-query halves");
 
+// The masked dQ kernel runs a query tile whose row of the tile maps is a plain run of key
+// tiles 0 .. n - 1 (plain_run: a key-padding mask, or an all-true one) as an unmasked one
+// over the first min(N_K, 128 n) keys: its rows see exactly those keys, so the results are
+// the same without the per-row mask words, the chunk votes or the tile walk.
+template <int D, bool MASK>
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+    attn_bwd_dq_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
+  if constexpr (MASK) {
+    if (args.mask_q.live && args.mask_q.full) {
+      const int nqt = (s.NQ + BM - 1) / BM;
+      const int item = blockIdx.x;
+      const int bh = item / nqt;
+      const int qt = s.causal ? (nqt - 1 - item % nqt) : (item % nqt);
+      const int gm = (args.mask_q.mb > 1 ? bh / s.H : 0) * args.mask_q.mh + (args.mask_q.mh > 1 ? bh % s.H : 0);
+      const size_t o = (static_cast<size_t>(gm) * nqt + qt) * args.mask_q.live_words;
+      const int n = plain_run(args.mask_q.live + o, args.mask_q.full + o, args.mask_q.live_words);
+      if (n > 0) {
+        dq_body<D, false>(s, args, ctx, min(s.NK, n * BN));
+        return;
+      }
+    }
+  }
+  dq_body<D, MASK>(s, args, ctx, s.NK);
+}
+
 // MASK: a boolean attention mask (args.mask_k, rows = keys) applies on top of `causal`.
 template <int D, bool MASK>
-__global__ void __launch_bounds__(KV_THREADS, 1)
-    attn_bwd_dkdv_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
+__device__ __forceinline__ void dkdv_body(const AttnShape& s, const BwdTcArgs& args, const LaunchCtx& ctx) {
   using C = DkvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t mis = smem_u32(smem_raw) & 1023u;
@@ -669,6 +709,17 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       }
     }
     return bits;
+  };
+  // Query tiles 32 w .. 32 w + 31 the mask allows whole to every key of this tile: their mask
+  // words are all ones and are not read.
+  auto full_word = [&](int w) -> uint32_t {
+    if constexpr (MASK) {
+      if (args.mask_k.full) {
+        const int gm = (args.mask_k.mb > 1 ? bh / s.H : 0) * args.mask_k.mh + (args.mask_k.mh > 1 ? bh % s.H : 0);
+        return args.mask_k.full[(static_cast<size_t>(gm) * nkt_all + kt) * args.mask_k.live_words + w];
+      }
+    }
+    return 0u;
   };
 
   if (threadIdx.x == 0) {
@@ -903,18 +954,22 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     }
     uint32_t sv[KV_COLS / 32][32];
 #define SV(c) sv[(c) >> 5][(c) & 31]
-    uint32_t tw = ~0u;
+    uint32_t tw = ~0u, fw = 0;
     int ntaken = 0;   // query tiles taken; 0 leaves the dK and dV accumulators unwritten
     for (int qa = qt0; qa < nqt; ++qa) {
       if constexpr (MASK) {
-        if (qa == qt0 || (qa & 31) == 0) tw = take_word(qa >> 5);
+        if (qa == qt0 || (qa & 31) == 0) {
+          tw = take_word(qa >> 5);
+          fw = full_word(qa >> 5);
+        }
         if (!((tw >> (qa & 31)) & 1u)) continue;
       }
       const int it = ntaken++;
       const int i0 = qa * BM;
       const uint32_t par = it & 1u;
       // S^T and this tile's per-query constants X (queries past N_Q carry base 2: zero weight)
-      const uint32_t mw = MASK ? mkey[4 * qa + part] : ~0u;   // in flight during the wait
+      // in flight during the wait; a tile the mask allows whole reads none
+      const uint32_t mw = (MASK && !((fw >> (qa & 31)) & 1u)) ? mkey[4 * qa + part] : ~0u;
       warp_wait(st_full, par);
       tc_fence_after();
 #pragma unroll
@@ -1097,6 +1152,38 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+// The masked dK/dV kernel runs a key tile whose every query tile in range the mask allows
+// whole (its rows of both tile maps cover the range) as an unmasked one: the same results
+// without the per-key mask words, the chunk votes or the tile walk.
+template <int D, bool MASK>
+__global__ void __launch_bounds__(KV_THREADS, 1)
+    attn_bwd_dkdv_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
+  if constexpr (MASK) {
+    if (args.mask_k.live && args.mask_k.full) {
+      const int nqt = (s.NQ + BM - 1) / BM;
+      const int nkt_all = (s.NK + BN - 1) / BN;
+      const int item = blockIdx.x;
+      const int bh = item / nkt_all;
+      const int kt = item % nkt_all;
+      const int qt0 = s.causal ? kt * BN / BM : 0;
+      const int gm = (args.mask_k.mb > 1 ? bh / s.H : 0) * args.mask_k.mh + (args.mask_k.mh > 1 ? bh % s.H : 0);
+      const size_t o = (static_cast<size_t>(gm) * nkt_all + kt) * args.mask_k.live_words;
+      bool whole = true;
+      for (int w = qt0 / 32; w < (nqt + 31) / 32 && whole; ++w) {
+        // query tiles qt0 .. nqt - 1 that fall in word w
+        const int lo = max(qt0 - 32 * w, 0), hi = min(nqt - 32 * w, 32);
+        const uint32_t range = (hi >= 32 ? ~0u : (1u << hi) - 1u) & ~((1u << lo) - 1u);
+        whole = (args.mask_k.full[o + w] & range) == range;   // full implies live
+      }
+      if (whole) {
+        dkdv_body<D, false>(s, args, ctx);
+        return;
+      }
+    }
+  }
+  dkdv_body<D, MASK>(s, args, ctx);
 }
 
 template <typename KernelFn>

@@ -152,12 +152,17 @@ __device__ __forceinline__ void store_p_half(const uint32_t (&pk)[32], uint8_t* 
 // attention mask, a half every row sees whole runs unmasked, a half no row sees gives zeros
 // without the arithmetic, anything else the per-entry masked path; without one, the causal
 // `masked` flag decides as before.
-// With MASK it votes over the warp (chunk_kind): called by all lanes together.
+// With MASK it votes over the warp (chunk_kind), unless `whole` (the same for every lane of
+// the warp) says every row sees the whole tile: called by all lanes together.
 template <bool MASK>
-__device__ __forceinline__ float2 phi_half_any(bool masked, const uint32_t (&h)[2][32], uint32_t (&pk)[32], int col0,
-                                               int lim, float c2, float base, uint32_t mw0, uint32_t mw1) {
+__device__ __forceinline__ float2 phi_half_any(bool masked, bool whole, const uint32_t (&h)[2][32], uint32_t (&pk)[32],
+                                               int col0, int lim, float c2, float base, uint32_t mw0, uint32_t mw1) {
   if constexpr (MASK) {
-    const int k0 = chunk_kind(mw0, col0, lim), k1 = chunk_kind(mw1, col0 + 32, lim);
+    int k0 = kChunkAll, k1 = kChunkAll;
+    if (!whole) {
+      k0 = chunk_kind(mw0, col0, lim);
+      k1 = chunk_kind(mw1, col0 + 32, lim);
+    }
     if (k0 == kChunkNone && k1 == kChunkNone) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) pk[i] = 0u;
@@ -171,11 +176,66 @@ __device__ __forceinline__ float2 phi_half_any(bool masked, const uint32_t (&h)[
   }
 }
 
+// The work item of this CTA (pair): its (batch, head) bh and first query row q0; the item
+// spans NCTA * NGROUP query tiles.
+// Head-major order: the ~150 resident CTAs share a few heads, so each head's K and V
+// stay in L2 across its query tiles.  Causal: CTA lengths differ, so heads are taken in
+// groups of CAUSAL_HEADS and within a group the longest CTAs of all its heads go first;
+// only the last group's short CTAs are left for the tail.  With 64 heads per group the
+// resident CTAs still come two or three to a head, of nearly equal length, so they walk
+// that head's keys together and L2 serves the repeated reads.
+template <bool PAIR>
+__device__ __forceinline__ void fwd_item(const AttnShape& s, int& bh, int& q0) {
+  constexpr int NCTA = PAIR ? 2 : 1;
+  const int nqt = (s.NQ + BM - 1) / BM;
+  const int nct = (nqt + NCTA * NGROUP - 1) / (NCTA * NGROUP);   // work items (CTAs or pairs) per (batch, head)
+  const int item = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  int ct;
+  if (s.causal) {
+    const int grp = item / (CAUSAL_HEADS * nct);
+    const int gsize = min(CAUSAL_HEADS, s.B * s.H - grp * CAUSAL_HEADS);
+    const int i = item - grp * CAUSAL_HEADS * nct;
+    ct = nct - 1 - i / gsize;
+    bh = grp * CAUSAL_HEADS + i % gsize;
+  } else {
+    bh = item / nct;
+    ct = item % nct;
+  }
+  q0 = ct * (NCTA * NGROUP * BM);
+}
+
+// Masked calls: the number of leading keys nk > 0 over which an item may run as an unmasked
+// one, or 0.  It may when every query tile of the item (below N_Q) has the same row in the
+// tile live map as in the tile full map, and that row is the same run of key tiles 0 .. n - 1
+// for all of them (a key-padding mask, or an all-true one): each of its rows then may see
+// exactly the keys before nk = min(N_K, 128 n) (and the causal limit), as in an unmasked call
+// on those keys alone, and the unmasked code gives the same results without the per-row mask
+// words, the chunk votes or the tile walk.  Every thread of both CTAs of a pair reads the same
+// map words and takes the same decision.
+template <bool PAIR>
+__device__ __forceinline__ int fwd_plain_keys(const AttnShape& s, const FwdTcArgs& args, int bh, int q0) {
+  constexpr int NCTA = PAIR ? 2 : 1;
+  if (!args.mask.live || !args.mask.full) return 0;
+  const int nqt = (s.NQ + BM - 1) / BM;
+  const int lw = args.mask.live_words;
+  const int gm = (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0);
+  int n = 0;
+  for (int r = 0; r < NCTA * NGROUP; ++r) {
+    const int qt = q0 / BM + r;
+    if (qt >= nqt) break;
+    const size_t o = (static_cast<size_t>(gm) * nqt + qt) * lw;
+    const int m = plain_run(args.mask.live + o, args.mask.full + o, lw);
+    if (m == 0 || (r > 0 && m != n)) return 0;
+    n = m;
+  }
+  return min(s.NK, n * BN);
+}
+
 // MASK: a boolean attention mask (args.mask) applies on top of `causal`.  PAIR: the CTA
-// pair form (FwdCfg).
+// pair form (FwdCfg).  nk: the keys taken, N_K, or fewer for an item run as an unmasked one
+// over the keys its mask leaves (fwd_plain_keys).
 template <int D, bool MASK, bool PAIR>
-__global__ void __launch_bounds__(THREADS, 1)
-    attn_fwd_tc_kernel(const AttnShape s, const __grid_constant__ FwdTcArgs args, const LaunchCtx ctx) {
+__device__ __forceinline__ void fwd_body(const AttnShape& s, const FwdTcArgs& args, const LaunchCtx& ctx, int nk) {
   using C = FwdCfg<D, PAIR>;
   constexpr int NST = C::NSTAGE;
   constexpr int NCTA = C::NCTA;
@@ -214,32 +274,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // CTA of the pair; 0 issues the products
   const int nqt = (s.NQ + BM - 1) / BM;
-  const int nct = (nqt + NCTA * NGROUP - 1) / (NCTA * NGROUP);   // work items (CTAs or pairs) per (batch, head)
-  const int item = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  // Head-major order: the ~150 resident CTAs share a few heads, so each head's K and V
-  // stay in L2 across its query tiles.  Causal: CTA lengths differ, so heads are taken in
-  // groups of CAUSAL_HEADS and within a group the longest CTAs of all its heads go first;
-  // only the last group's short CTAs are left for the tail.  With 64 heads per group the
-  // resident CTAs still come two or three to a head, of nearly equal length, so they walk
-  // that head's keys together and L2 serves the repeated reads.
-  int bh, ct;
-  if (s.causal) {
-    const int grp = item / (CAUSAL_HEADS * nct);
-    const int gsize = min(CAUSAL_HEADS, s.B * s.H - grp * CAUSAL_HEADS);
-    const int i = item - grp * CAUSAL_HEADS * nct;
-    ct = nct - 1 - i / gsize;
-    bh = grp * CAUSAL_HEADS + i % gsize;
-  } else {
-    bh = item / nct;
-    ct = item % nct;
-  }
-  const int q0 = ct * (NCTA * NGROUP * BM);
+  int bh, q0;
+  fwd_item<PAIR>(s, bh, q0);
   // first row of query tile g of CTA r: product g spans rows q0 + NCTA BM g .. + NCTA BM - 1,
   // the even CTA's tile first
   auto tile_row0 = [&](int g, int r) { return q0 + (g * NCTA + r) * BM; };
   // last key any row of the CTA (pair) may see, and per query tile
   auto last_key_of = [&](int rows_end) {   // rows_end: one past the last row of the range
-    return s.causal ? min(s.NK - 1, min(s.NQ - 1, rows_end - 1)) : s.NK - 1;
+    return s.causal ? min(nk - 1, min(s.NQ - 1, rows_end - 1)) : nk - 1;
   };
   const int nkt = last_key_of(q0 + NCTA * NGROUP * BM) / BN + 1;
   // key tiles product g needs (causal: fewer for g = 0, whose rows end earlier); the
@@ -437,16 +479,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t ocol = tmem + TMEM_O + g * 128;
       // key tiles each query tile of product g can see (0 for a tile wholly past N_Q):
       // only those count as visited (query tile, key tile) pairs
-      auto tile_keys = [&](int r) {
+      auto tile_keys = [&](int r, int n) {
         const int r0 = tile_row0(g, r);
-        return r0 < s.NQ ? last_key_of(r0 + BM) / BN + 1 : 0;
+        return r0 < s.NQ ? (s.causal ? min(n - 1, min(s.NQ - 1, r0 + BM - 1)) : n - 1) / BN + 1 : 0;
       };
-      const int nkt_a = tile_keys(0);
-      const int nkt_b = PAIR ? tile_keys(1) : 0;
+      const int nkt_a = tile_keys(0, nk);
+      const int nkt_b = PAIR ? tile_keys(1, nk) : 0;
       uint32_t pos = 0;   // ring position (K and V tiles in producer order)
       uint32_t uc0 = 0, uc1 = 0;   // S products issued into score buffer 0 and 1
-      // pairs in the product's range (its query tiles' key ranges), and those whose P V product ran
-      const unsigned long long visited = static_cast<unsigned long long>(nkt_a + nkt_b);
+      // pairs in the product's range (its query tiles' key ranges over all N_K keys: those
+      // past nk, of an item run over fewer keys, count as skipped), and those whose P V
+      // product ran
+      const unsigned long long visited =
+          static_cast<unsigned long long>(tile_keys(0, s.NK) + (PAIR ? tile_keys(1, s.NK) : 0));
       unsigned long long ran = 0;
       bool o_started = false;
       auto ring_wait = [&](uint32_t p, uint32_t& addr) -> bool {
@@ -588,7 +633,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp % GROUP_WARPS;
     const int row_local = quarter * 32 + lane;   // TMEM lane
     const int row = tile_row0(g, static_cast<int>(rank)) + row_local;
-    const int lim = s.causal ? min(row, s.NK - 1) : s.NK - 1;   // last key this row may see
+    const int lim = s.causal ? min(row, nk - 1) : nk - 1;   // last key this row may see
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t scol = lane_addr + TMEM_S + g * 128;
     auto warp_wait = [&](uint64_t* bar, uint32_t par) -> bool {
@@ -598,10 +643,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     // this row's attention-mask words: four per key tile (rows past N_Q read the last row)
     const uint32_t* mrow = nullptr;
+    const uint32_t* frow = nullptr;   // this query tile's row of the tile full map
     if (MASK) {
       const int gm = (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0);
       mrow = args.mask.bits + (static_cast<size_t>(gm) * s.NQ + min(row, s.NQ - 1)) * args.mask.words;
+      const int qt_own = tile_row0(g, static_cast<int>(rank)) / BM;
+      if (args.mask.full && qt_own < nqt)
+        frow = args.mask.full + (static_cast<size_t>(gm) * nqt + qt_own) * args.mask.live_words;
     }
+    // Key tiles 32 w .. 32 w + 31 the mask allows whole to every row of this query tile: their
+    // words are all ones and are not read
+    auto full_word = [&](int w) -> uint32_t { return (MASK && frow) ? frow[w] : 0u; };
+    // the lowest `lim` of the warp's rows (lane 0's): a tile wholly at or below it, and whole
+    // under the mask, is unmasked for every row of the warp
+    const int lim_lo = s.causal ? min(tile_row0(g, static_cast<int>(rank)) + quarter * 32, nk - 1) : nk - 1;
     auto mask_words = [&](int j, uint32_t (&mw)[4]) {
       if (MASK) {
         const uint4 u = *reinterpret_cast<const uint4*>(mrow + 4 * j);
@@ -638,21 +693,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t c = 0;
     const int nkt_g = group_keys(g);
     uint32_t tw = 0;   // tiles this product takes (masked instances), refreshed every 32
+    uint32_t fw = 0;   // tiles the mask allows whole to this query tile, likewise
     for (int j = 0; j < nkt_g && ok; ++j) {
       if constexpr (MASK) {
-        if ((j & 31) == 0) tw = take_word(g, j >> 5);
+        if ((j & 31) == 0) {
+          tw = take_word(g, j >> 5);
+          fw = full_word(j >> 5);
+        }
         if (!bit(tw, j)) continue;
       }
+      const bool full = MASK && bit(fw, j);
+      const int col0 = j * BN;   // key index of column 0
+      // masked instances: the same for the whole warp
+      const bool whole = full && col0 + BN - 1 <= lim_lo;
       uint32_t mw[4];
-      mask_words(j, mw);   // issued before the wait below: its latency hides behind it
+      if (full) mw[0] = mw[1] = mw[2] = mw[3] = ~0u;
+      else mask_words(j, mw);   // issued before the wait below: its latency hides behind it
       ok = take_s(static_cast<int>(c & 1u), c >> 1);
       ++c;
       if (!ok) break;
-      const int col0 = j * BN;   // key index of column 0
       // maximum of each 32-column chunk; the first chunk (in key order) that raises the
       // running maximum strictly is remembered, so ties keep the lowest index
       float cm[BN / 32];
-      if (!MASK && col0 + BN - 1 <= lim) {
+      if (MASK ? whole : col0 + BN - 1 <= lim) {
 #pragma unroll
         for (int k = 0; k < BN / 32; ++k) {
           float u0 = -INFINITY, u1 = -INFINITY;
@@ -668,7 +731,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int k = 0; k < BN / 32; ++k) {
           float u0 = -INFINITY, u1 = -INFINITY;
           // With an attention mask this branch is taken by the whole warp (the condition above
-          // is false for every lane), so the chunk vote is safe: a chunk every row of the warp
+          // is the same for every lane), so the chunk vote is safe: a chunk every row of the warp
           // may see whole takes the plain max, a chunk none of them may see is skipped (key
           // padding and block masks are uniform per chunk).  Without one, the branch is taken
           // per lane on causal diagonal tiles and must hold no warp vote: every chunk is mixed.
@@ -712,16 +775,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     c = 0;                 // P tiles written
     for (int j = 0; j < nkt_g && ok; ++j) {
       if constexpr (MASK) {
-        if ((j & 31) == 0) tw = take_word(g, j >> 5);
+        if ((j & 31) == 0) {
+          tw = take_word(g, j >> 5);
+          fw = full_word(j >> 5);
+        }
         if (!bit(tw, j)) continue;
       }
+      const bool full = MASK && bit(fw, j);
+      const int col0 = j * BN;
+      const bool whole = full && col0 + BN - 1 <= lim_lo;
       uint32_t mw[4];
-      mask_words(j, mw);   // in flight during the wait
+      if (full) mw[0] = mw[1] = mw[2] = mw[3] = ~0u;
+      else mask_words(j, mw);   // in flight during the wait
       ok = warp_wait(&s_full[2 * g], sidx & 1u);   // buffer 0
       if (!ok) break;
       ++sidx;
       tc_fence_after();
-      const int col0 = j * BN;
       const bool masked = MASK || col0 + BN - 1 > lim;
       const bool arg_tile = j == (jm >> 2) && m > -INFINITY;
       uint32_t h[2][32];
@@ -732,7 +801,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         a = col0 + ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 32, lim, mw[1])
                              : find_in_chunk(h[0], m, col0, lim, mw[0]));
       uint32_t pk[32];
-      float2 tsum2 = phi_half_any<MASK>(masked, h, pk, col0, lim, c2, base, mw[0], mw[1]);
+      float2 tsum2 = phi_half_any<MASK>(masked, whole, h, pk, col0, lim, c2, base, mw[0], mw[1]);
       tmem_ld32(scol + 64, h[0]);
       tmem_ld32(scol + 96, h[1]);
       tc_wait_ld();
@@ -750,7 +819,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       float2 t2;
       {
         uint32_t pk2[32];
-        t2 = phi_half_any<MASK>(masked, h, pk2, col0 + 64, lim, c2, base, mw[2], mw[3]);
+        t2 = phi_half_any<MASK>(masked, whole, h, pk2, col0 + 64, lim, c2, base, mw[2], mw[3]);
         store_p_half(pk2, prow + BOX_BYTES, row_local);
       }
       tsum2 = __fadd2_rn(tsum2, t2);
@@ -831,6 +900,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     if constexpr (PAIR) tmem_dealloc_pair(tmem, TMEM_COLS);
     else tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+// The masked instances run an item whose mask is a plain key range (fwd_plain_keys) as an
+// unmasked one: same protocol, none of the mask's per-tile work.
+template <int D, bool MASK, bool PAIR>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fwd_tc_kernel(const AttnShape s, const __grid_constant__ FwdTcArgs args, const LaunchCtx ctx) {
+  if constexpr (MASK) {
+    int bh, q0;
+    fwd_item<PAIR>(s, bh, q0);
+    const int nk = fwd_plain_keys<PAIR>(s, args, bh, q0);
+    if (nk > 0) {
+      fwd_body<D, false, PAIR>(s, args, ctx, nk);
+      return;
+    }
+  }
+  fwd_body<D, MASK, PAIR>(s, args, ctx, s.NK);
 }
 
 template <int D, bool MASK, bool PAIR>

@@ -5,7 +5,9 @@
 // pairs that take part.  The kernels read the mask one 32-column word per row and tile
 // chunk: bits_q with a row per query (forward, dQ kernel) and bits_k with a row per key
 // (dK/dV kernel, whose threads own key rows).  A tile live map (one bit per 128 x 128 block
-// with any allowed pair) lets a kernel leave fully masked tiles out altogether.
+// with any allowed pair) lets a kernel leave fully masked tiles out altogether, and a tile
+// full map (every pair below N_Q and N_K allowed) lets it treat such a block as unmasked,
+// reading no mask words.
 #include "kernels.cuh"
 
 namespace raattn {
@@ -49,13 +51,17 @@ __global__ void __launch_bounds__(32 * WARPS) mask_pack_cols_kernel(const uint8_
 }
 
 // One warp per (mask head, query tile, key tile): the block is live when any of the query
-// tile's rows may attend to any key of the tile, read from the packed rows (four words per
-// key tile).  Lane l scans rows l, l + 32, l + 64, l + 96 of the query tile.  A live block
-// sets bit kt of its query tile's row of live_q (key tiles along the row) and, when live_k
-// is given, bit qt of its key tile's row of live_k (the same map transposed).
-__global__ void __launch_bounds__(32 * WARPS) mask_tile_live_kernel(const uint32_t* bits_q, int NQ, int words,
-                                                                    int nqt, int nkt, uint32_t* live_q, int wq,
-                                                                    uint32_t* live_k, int wk, long long total) {
+// tile's rows may attend to any key of the tile, and full when every row may attend to every
+// key of it below N_K, read from the packed rows (four words per key tile).  Lane l scans
+// rows l, l + 32, l + 64, l + 96 of the query tile (those below N_Q).  A live block sets bit
+// kt of its query tile's row of live_q (key tiles along the row) and, when live_k is given,
+// bit qt of its key tile's row of live_k (the same map transposed); a full one the same bits
+// of full_q and full_k.  The kernels check N_K and N_Q themselves, so a full block past
+// either edge is treated as unmasked there.
+__global__ void __launch_bounds__(32 * WARPS) mask_tile_live_kernel(const uint32_t* bits_q, int NQ, int NK,
+                                                                    int words, int nqt, int nkt, uint32_t* live_q,
+                                                                    uint32_t* full_q, int wq, uint32_t* live_k,
+                                                                    uint32_t* full_k, int wk, long long total) {
   const long long wid = static_cast<long long>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= total) return;   // uniform across the warp
@@ -63,33 +69,52 @@ __global__ void __launch_bounds__(32 * WARPS) mask_tile_live_kernel(const uint32
   const long long rest = wid / nkt;   // g * nqt + qt
   const int qt = static_cast<int>(rest % nqt);
   const long long g = rest / nqt;
-  uint32_t any = 0;
+  // bits of the columns past N_K, which count as allowed for the full test
+  uint32_t pad[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int c0 = kt * 128 + 32 * w;   // first column of word w
+    const int n_in = min(max(NK - c0, 0), 32);
+    pad[w] = n_in >= 32 ? 0u : ~((1u << n_in) - 1u);
+  }
+  uint32_t any = 0, all = ~0u;
   for (int r = lane; r < 128; r += 32) {
     const int i = qt * 128 + r;
     if (i < NQ) {
       const uint4 u = *reinterpret_cast<const uint4*>(bits_q + (g * NQ + i) * words + 4 * kt);
       any |= u.x | u.y | u.z | u.w;
+      all &= (u.x | pad[0]) & (u.y | pad[1]) & (u.z | pad[2]) & (u.w | pad[3]);
     }
   }
   const bool on = __any_sync(0xffffffffu, any != 0);
+  const bool whole = __all_sync(0xffffffffu, all == ~0u);   // row qt * 128 < N_Q: whole implies on
   if (lane == 0 && on) {
     atomicOr(&live_q[rest * wq + kt / 32], 1u << (kt % 32));
     if (live_k) atomicOr(&live_k[(g * nkt + kt) * wk + qt / 32], 1u << (qt % 32));
+  }
+  if (lane == 0 && whole) {
+    if (full_q) atomicOr(&full_q[rest * wq + kt / 32], 1u << (kt % 32));
+    if (full_k) atomicOr(&full_k[(g * nkt + kt) * wk + qt / 32], 1u << (qt % 32));
   }
 }
 
 }  // namespace
 
 cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live_q,
-                                  int wq, uint32_t* live_k, int wk, cudaStream_t st) {
+                                  uint32_t* full_q, int wq, uint32_t* live_k, uint32_t* full_k, int wk,
+                                  cudaStream_t st) {
   const int nqt = (NQ + 127) / 128, nkt = (NK + 127) / 128;
-  cudaError_t e = cudaMemsetAsync(live_q, 0, static_cast<size_t>(G) * nqt * wq * sizeof(uint32_t), st);
-  if (e == cudaSuccess && live_k)
-    e = cudaMemsetAsync(live_k, 0, static_cast<size_t>(G) * nkt * wk * sizeof(uint32_t), st);
+  const size_t bytes_q = static_cast<size_t>(G) * nqt * wq * sizeof(uint32_t);
+  const size_t bytes_k = static_cast<size_t>(G) * nkt * wk * sizeof(uint32_t);
+  cudaError_t e = cudaMemsetAsync(live_q, 0, bytes_q, st);
+  if (e == cudaSuccess && full_q) e = cudaMemsetAsync(full_q, 0, bytes_q, st);
+  if (e == cudaSuccess && live_k) e = cudaMemsetAsync(live_k, 0, bytes_k, st);
+  if (e == cudaSuccess && full_k) e = cudaMemsetAsync(full_k, 0, bytes_k, st);
   if (e != cudaSuccess) return e;
   const long long total = static_cast<long long>(G) * nqt * nkt;
   const unsigned grid = static_cast<unsigned>((total + WARPS - 1) / WARPS);
-  mask_tile_live_kernel<<<grid, 32 * WARPS, 0, st>>>(bits_q, NQ, words, nqt, nkt, live_q, wq, live_k, wk, total);
+  mask_tile_live_kernel<<<grid, 32 * WARPS, 0, st>>>(bits_q, NQ, NK, words, nqt, nkt, live_q, full_q, wq, live_k,
+                                                     full_k, wk, total);
   return cudaGetLastError();
 }
 

@@ -89,14 +89,19 @@ def test_masked_attention_matches_oracle(D, nq, nk, causal, layout):
     _check(q, k, v, do, D ** -0.5, causal, mask)
 
 
-def test_all_true_mask_equals_unmasked():
-    q, k, v, _ = attention_inputs(1, 2, 257, 300, 128, seed=5, dtype=torch.bfloat16)
-    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
-    pm = ra.pack_attn_mask(torch.ones(257, 300, dtype=torch.bool, device="cuda"), 1, 2, 257, 300)
-    a = ra.ra_attention_forward(qg, kg, vg, causal=True, out_dtype=torch.float32, mask=pm)
-    b = ra.ra_attention_forward(qg, kg, vg, causal=True, out_dtype=torch.float32)
+@pytest.mark.parametrize("D,nq,nk,causal", [(128, 257, 300, True), (64, 300, 520, False), (128, 640, 700, False)])
+def test_all_true_mask_equals_unmasked(D, nq, nk, causal):
+    """An all-true mask (ragged at both ends) gives the unmasked results bit for bit, forward
+    and backward: every item runs as an unmasked one over all N_K keys."""
+    q, k, v, do = (t.cuda() for t in attention_inputs(1, 2, nq, nk, D, seed=5 + D + nq, dtype=torch.bfloat16))
+    pm = ra.pack_attn_mask(torch.ones(nq, nk, dtype=torch.bool, device="cuda"), 1, 2, nq, nk)
+    a = ra.ra_attention_forward(q, k, v, causal=causal, out_dtype=torch.float32, mask=pm, tile_counts=True)
+    b = ra.ra_attention_forward(q, k, v, causal=causal, out_dtype=torch.float32, tile_counts=True)
+    ga = ra.ra_attention_backward(q, k, v, a[0], do, *a[1:4], causal=causal, mask=pm)
+    gb = ra.ra_attention_backward(q, k, v, b[0], do, *b[1:4], causal=causal)
     torch.cuda.synchronize()
-    for x, y in zip(a[:4], b[:4]):
+    assert ra.device_status() == "RA_OK"
+    for x, y in zip(list(a) + list(ga), list(b) + list(gb)):
         assert torch.equal(x, y)
 
 
@@ -265,3 +270,37 @@ def test_tile_maps_span_several_words(D, causal):
     torch.cuda.synchronize()
     span = 2 if D == 128 and n > 256 else 1
     assert tuple(int(c) for c in counts.tolist()) == _expected_tile_counts(blocks, n, n, causal, span)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L", [256, 200])
+def test_key_padding_equals_truncated_keys(D, causal, L):
+    """Keys from L on masked for every query give, bit for bit, the results of the same call
+    on the first L keys alone (and zero dK, dV past L): the key tiles wholly below L are
+    allowed whole (no mask words read: the unmasked arithmetic), the tiles wholly past L are
+    left out, and a tile L falls inside takes the per-row mask words, whose clear bits give
+    the exact zeros a ragged N_K gives.  640 query rows: D = 128 runs as CTA pairs."""
+    B, H, n = 1, 2, 640
+    q, k, v, do = (t.cuda() for t in attention_inputs(B, H, n, n, D, seed=6000 + D + L + int(causal), sigma_qk=1.0,
+                                                      dtype=torch.bfloat16))
+    pm = ra.pack_attn_mask((torch.arange(n, device="cuda") < L)[None, :].expand(n, n), B, H, n, n)
+    kt, vt = k[:, :, :L].contiguous(), v[:, :, :L].contiguous()
+    om, rmm, rsm, ram, _ = ra.ra_attention_forward(q, k, v, causal=causal, out_dtype=torch.float32, mask=pm)
+    ot, rmt, rst, rat, _ = ra.ra_attention_forward(q, kt, vt, causal=causal, out_dtype=torch.float32)
+    gm = ra.ra_attention_backward(q, k, v, om, do, rmm, rsm, ram, causal=causal, mask=pm)
+    gt = ra.ra_attention_backward(q, kt, vt, ot, do, rmt, rst, rat, causal=causal)
+    torch.cuda.synchronize()
+    assert ra.device_status() == "RA_OK"
+    for name, a, b in (("o", om, ot), ("row_m", rmm, rmt), ("row_s", rsm, rst), ("row_arg", ram, rat),
+                       ("dq", gm[0], gt[0]), ("dk", gm[1][:, :, :L], gt[1]), ("dv", gm[2][:, :, :L], gt[2])):
+        assert torch.equal(a, b), name
+    assert torch.all(gm[1][:, :, L:] == 0) and torch.all(gm[2][:, :, L:] == 0)
+    # the key tiles past L count as pairs no product ran on, as in any masked call
+    _, _, _, _, counts = ra.ra_attention_forward(q, k, v, causal=causal, mask=pm, tile_counts=True)
+    torch.cuda.synchronize()
+    nt = -(-n // 128)
+    blocks = np.array([[kt * 128 < L for kt in range(nt)] for _ in range(nt)])
+    span = 2 if D == 128 and n > 256 else 1
+    vis, skip = _expected_tile_counts(blocks, n, n, causal, span)   # per head
+    assert tuple(int(c) for c in counts.tolist()) == (B * H * vis, B * H * skip)
