@@ -116,7 +116,8 @@ ra_status_t ra_softmax_bwd(const void* x, const void* p, const void* dy, void* d
  *                aligned, contents on entry irrelevant; required for RA_BF16 inputs
  *                (NULL allowed for RA_F32).  The call writes an fp16 copy of v there
  *                (masked calls also two maps of the 128 x 128 tiles: those the mask allows
- *                a pair in, and those it allows every pair of)
+ *                a pair in, and those it allows every pair of; and per query tile whether
+ *                its rows may see exactly a run of leading keys)
  *                and forms P V in fp16, with P rounded to 2^-11 instead of 2^-8.  The
  *                copy is exact for 2^-14 <= |v| <= 65504 (normal fp16); smaller
  *                magnitudes become fp16 subnormals, rounded to a multiple of 2^-24
@@ -144,8 +145,8 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
  * ra_attention_fwd_workspace_size -- bytes of device workspace ra_attention_fwd (and
  * ra_attention_fwd_masked) needs for these sizes: the fp16 copy of v (B*H*N_K*D*2 bytes,
  * padded to 256), then the two tile maps a masked call builds (each B*H*ceil(N_Q/128)
- * rows of ceil(ceil(N_K/128)/32) uint32 words, padded to 256).  Returns 0 for invalid
- * sizes.
+ * rows of ceil(ceil(N_K/128)/32) uint32 words, padded to 256) and one int32 per row of them
+ * (padded to 256).  Returns 0 for invalid sizes.
  */
 size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 
@@ -161,8 +162,8 @@ size_t ra_attention_fwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
  * or NaN saturates and is reported as RA_ERR_UNSUPPORTED by ra_device_status().  Last,
  * the two tile maps a masked call builds (tiles with an allowed pair, tiles with every pair
  * allowed), each both ways: B*H*ceil(N_Q/128) rows of ceil(ceil(N_K/128)/32) uint32 words
- * and B*H*ceil(N_K/128) rows of ceil(ceil(N_Q/128)/32).  Each piece is padded to 256
- * bytes.  Returns 0 for invalid sizes.
+ * and B*H*ceil(N_K/128) rows of ceil(ceil(N_Q/128)/32), then one int32 per row of either
+ * layout.  Each piece is padded to 256 bytes.  Returns 0 for invalid sizes.
  */
 size_t ra_attention_bwd_workspace_size(int B, int H, int N_Q, int N_K, int D);
 

@@ -101,7 +101,7 @@ bool make_map_bf16(CUtensorMap* map, const void* base, int BH, int N, int D) {
 // per-query-tile constant blocks, then the fp16 copies of Q, dO, K and V.  Every piece
 // starts on a 256-byte boundary.
 struct BwdLayout {
-  size_t per_row, consts, head, q16, kv16, live_q, live_k, total_f32, total_tc;
+  size_t per_row, consts, head, q16, kv16, live_q, live_k, plain_q, plain_k, total_f32, total_tc;
   BwdLayout(int B, int H, int NQ, int NK, int D) {
     auto pad = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t bh = static_cast<size_t>(B) * H;
@@ -113,11 +113,13 @@ struct BwdLayout {
     q16 = pad(bh * NQ * D * 2);
     kv16 = pad(bh * NK * D * 2);
     // masked calls: the tile live map by query tile (key-tile bits) and by key tile, then
-    // the tile full map in the same two layouts
+    // the tile full map in the same two layouts, then one int per row of each layout
     const size_t nkt = (static_cast<size_t>(NK) + 127) / 128;
     live_q = pad(bh * nqt * live_words_for(NK) * 4);
     live_k = pad(bh * nkt * live_words_for(NQ) * 4);
-    total_tc = head + 2 * q16 + 2 * kv16 + 2 * (live_q + live_k);
+    plain_q = pad(bh * nqt * 4);
+    plain_k = pad(bh * nkt * 4);
+    total_tc = head + 2 * q16 + 2 * kv16 + 2 * (live_q + live_k) + plain_q + plain_k;
   }
 };
 
@@ -140,7 +142,13 @@ size_t fwd_workspace_map_bytes(int B, int H, int NQ, int NK) {
   const size_t nqt = (static_cast<size_t>(NQ) + 127) / 128;
   return (static_cast<size_t>(B) * H * nqt * live_words_for(NK) * 4 + 255) & ~static_cast<size_t>(255);
 }
-size_t fwd_workspace_live_bytes(int B, int H, int NQ, int NK) { return 2 * fwd_workspace_map_bytes(B, H, NQ, NK); }
+size_t fwd_workspace_plain_bytes(int B, int H, int NQ) {
+  const size_t nqt = (static_cast<size_t>(NQ) + 127) / 128;
+  return (static_cast<size_t>(B) * H * nqt * 4 + 255) & ~static_cast<size_t>(255);
+}
+size_t fwd_workspace_live_bytes(int B, int H, int NQ, int NK) {
+  return 2 * fwd_workspace_map_bytes(B, H, NQ, NK) + fwd_workspace_plain_bytes(B, H, NQ);
+}
 
 size_t bwd_workspace_bytes(int B, int H, int NQ, int NK, int D, bool f32_inputs) {
   if (check_attn_sizes(B, H, NQ, NK, D) != RA_OK) return 0;
@@ -235,6 +243,7 @@ ra_status_t mask_args(const uint32_t* bits, int MB, int MH, int B, int H, int co
   m->mh = MH;
   m->live = nullptr;
   m->full = nullptr;
+  m->plain = nullptr;
   m->live_words = 0;
   if (!bits) return RA_OK;
   if (!aligned16(bits) || !(MB == 1 || MB == B) || !(MH == 1 || MH == H)) return RA_ERR_ARG;
@@ -293,13 +302,16 @@ ra_status_t attn_fwd_impl(const void* q, const void* k, const void* v, void* o, 
   if (mask.bits) {   // tile maps after the V copy: fully masked tiles are left out of both passes,
                      // wholly allowed ones read no mask words
     char* maps = static_cast<char*>(workspace) + fwd_workspace_v_bytes(B, H, N_K, D);
+    const size_t map_bytes = fwd_workspace_map_bytes(B, H, N_Q, N_K);
     uint32_t* live = reinterpret_cast<uint32_t*>(maps);
-    uint32_t* full = reinterpret_cast<uint32_t*>(maps + fwd_workspace_map_bytes(B, H, N_Q, N_K));
+    uint32_t* full = reinterpret_cast<uint32_t*>(maps + map_bytes);
+    int* plain = reinterpret_cast<int*>(maps + 2 * map_bytes);
     a.mask.live = live;
     a.mask.full = full;
+    a.mask.plain = plain;
     a.mask.live_words = live_words_for(N_K);
-    if (launch_mask_tile_live(mask.bits, mask.mb * mask.mh, N_Q, N_K, mask.words, live, full, a.mask.live_words,
-                              nullptr, nullptr, 0, st) != cudaSuccess)
+    if (launch_mask_tile_live(mask.bits, mask.mb * mask.mh, N_Q, N_K, mask.words, causal ? 1 : 0, live, full, plain,
+                              a.mask.live_words, nullptr, nullptr, nullptr, 0, st) != cudaSuccess)
       return RA_ERR_LAUNCH;
   }
   if (tile_counts && cudaMemsetAsync(tile_counts, 0, 2 * sizeof(int64_t), st) != cudaSuccess) return RA_ERR_LAUNCH;
@@ -321,7 +333,7 @@ ra_status_t ra_attention_fwd(const void* q, const void* k, const void* v, void* 
                              int32_t* row_arg, int64_t* tile_counts, void* workspace, int B, int H, int N_Q,
                              int N_K, int D, float scale, int causal, ra_dtype_t in_dtype, ra_dtype_t out_dtype,
                              void* stream) {
-  const MaskBits none{nullptr, 0, 1, 1, nullptr, nullptr, 0};
+  const MaskBits none{nullptr, 0, 1, 1, nullptr, nullptr, nullptr, 0};
   return attn_fwd_impl(q, k, v, o, row_m, row_s, row_arg, tile_counts, workspace, B, H, N_Q, N_K, D, scale, causal,
                        in_dtype, out_dtype, stream, none);
 }
@@ -428,14 +440,19 @@ ra_status_t attn_bwd_impl(const void* q, const void* k, const void* v, const voi
     uint32_t* live_k = reinterpret_cast<uint32_t*>(lq + lay.live_q);
     uint32_t* full_q = reinterpret_cast<uint32_t*>(lq + lay.live_q + lay.live_k);
     uint32_t* full_k = reinterpret_cast<uint32_t*>(lq + 2 * lay.live_q + lay.live_k);
+    int* plain_q = reinterpret_cast<int*>(lq + 2 * (lay.live_q + lay.live_k));
+    int* plain_k = reinterpret_cast<int*>(lq + 2 * (lay.live_q + lay.live_k) + lay.plain_q);
     a.mask_q.live = live_q;
     a.mask_q.full = full_q;
+    a.mask_q.plain = plain_q;
     a.mask_q.live_words = live_words_for(N_K);
     a.mask_k.live = live_k;
     a.mask_k.full = full_k;
+    a.mask_k.plain = plain_k;
     a.mask_k.live_words = live_words_for(N_Q);
-    if (launch_mask_tile_live(mask_q.bits, mask_q.mb * mask_q.mh, N_Q, N_K, mask_q.words, live_q, full_q,
-                              a.mask_q.live_words, live_k, full_k, a.mask_k.live_words, st) != cudaSuccess)
+    if (launch_mask_tile_live(mask_q.bits, mask_q.mb * mask_q.mh, N_Q, N_K, mask_q.words, causal ? 1 : 0, live_q,
+                              full_q, plain_q, a.mask_q.live_words, live_k, full_k, plain_k, a.mask_k.live_words,
+                              st) != cudaSuccess)
       return RA_ERR_LAUNCH;
   }
   const cudaError_t e = launch_attn_bwd_tc(s, a, ctx, st, current_events());
@@ -452,7 +469,7 @@ ra_status_t ra_attention_bwd(const void* q, const void* k, const void* v, const 
                              void* dv, void* workspace, int B, int H, int N_Q, int N_K, int D, float scale,
                              int causal, ra_dtype_t in_dtype, ra_dtype_t o_dtype, ra_dtype_t grad_dtype,
                              void* stream) {
-  const MaskBits none{nullptr, 0, 1, 1, nullptr, nullptr, 0};
+  const MaskBits none{nullptr, 0, 1, 1, nullptr, nullptr, nullptr, 0};
   return attn_bwd_impl(q, k, v, o, dout, row_m, row_s, row_arg, dq, dk, dv, workspace, B, H, N_Q, N_K, D, scale,
                        causal, in_dtype, o_dtype, grad_dtype, stream, none, none);
 }

@@ -127,7 +127,7 @@ __device__ __forceinline__ void softmax_sync() {
 
 // MASK: a boolean attention mask (args.mask_q, rows = queries) applies on top of `causal`.
 // nk: the keys taken, N_K, or fewer for a query tile run as an unmasked one over the keys its
-// mask leaves (the masked kernel's plain_run test).
+// mask leaves (the per-row plain lengths of the tile maps).
 template <int D, bool MASK>
 __device__ __forceinline__ void dq_body(const AttnShape& s, const BwdTcArgs& args, const LaunchCtx& ctx, int nk) {
   using C = DqCfg<D>;
@@ -617,21 +617,20 @@ constexpr int KV_THREADS = 32 * (KV_SOFTMAX_WARPS + 3);
 static_assert(KV_COLS == 32, "one 32-column TMEM load per softmax warp; P^T handed over in two 16-query halves");
 
 // The masked dQ kernel runs a query tile whose row of the tile maps is a plain run of key
-// tiles 0 .. n - 1 (plain_run: a key-padding mask, or an all-true one) as an unmasked one
+// tiles 0 .. n - 1 (its plain length: a key-padding mask, or an all-true one) as an unmasked one
 // over the first min(N_K, 128 n) keys: its rows see exactly those keys, so the results are
 // the same without the per-row mask words, the chunk votes or the tile walk.
 template <int D, bool MASK>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
   if constexpr (MASK) {
-    if (args.mask_q.live && args.mask_q.full) {
+    if (args.mask_q.plain) {
       const int nqt = (s.NQ + BM - 1) / BM;
       const int item = blockIdx.x;
       const int bh = item / nqt;
       const int qt = s.causal ? (nqt - 1 - item % nqt) : (item % nqt);
       const int gm = (args.mask_q.mb > 1 ? bh / s.H : 0) * args.mask_q.mh + (args.mask_q.mh > 1 ? bh % s.H : 0);
-      const size_t o = (static_cast<size_t>(gm) * nqt + qt) * args.mask_q.live_words;
-      const int n = plain_run(args.mask_q.live + o, args.mask_q.full + o, args.mask_q.live_words);
+      const int n = args.mask_q.plain[static_cast<size_t>(gm) * nqt + qt];
       if (n > 0) {
         dq_body<D, false>(s, args, ctx, min(s.NK, n * BN));
         return;
@@ -1155,28 +1154,19 @@ __device__ __forceinline__ void dkdv_body(const AttnShape& s, const BwdTcArgs& a
 }
 
 // The masked dK/dV kernel runs a key tile whose every query tile in range the mask allows
-// whole (its rows of both tile maps cover the range) as an unmasked one: the same results
-// without the per-key mask words, the chunk votes or the tile walk.
+// whole (its plain flag: its row of the full map covers the range) as an unmasked one: the
+// same results without the per-key mask words, the chunk votes or the tile walk.
 template <int D, bool MASK>
 __global__ void __launch_bounds__(KV_THREADS, 1)
     attn_bwd_dkdv_tc_kernel(const AttnShape s, const __grid_constant__ BwdTcArgs args, const LaunchCtx ctx) {
   if constexpr (MASK) {
-    if (args.mask_k.live && args.mask_k.full) {
-      const int nqt = (s.NQ + BM - 1) / BM;
+    if (args.mask_k.plain) {
       const int nkt_all = (s.NK + BN - 1) / BN;
       const int item = blockIdx.x;
       const int bh = item / nkt_all;
       const int kt = item % nkt_all;
-      const int qt0 = s.causal ? kt * BN / BM : 0;
       const int gm = (args.mask_k.mb > 1 ? bh / s.H : 0) * args.mask_k.mh + (args.mask_k.mh > 1 ? bh % s.H : 0);
-      const size_t o = (static_cast<size_t>(gm) * nkt_all + kt) * args.mask_k.live_words;
-      bool whole = true;
-      for (int w = qt0 / 32; w < (nqt + 31) / 32 && whole; ++w) {
-        // query tiles qt0 .. nqt - 1 that fall in word w
-        const int lo = max(qt0 - 32 * w, 0), hi = min(nqt - 32 * w, 32);
-        const uint32_t range = (hi >= 32 ? ~0u : (1u << hi) - 1u) & ~((1u << lo) - 1u);
-        whole = (args.mask_k.full[o + w] & range) == range;   // full implies live
-      }
+      const bool whole = args.mask_k.plain[static_cast<size_t>(gm) * nkt_all + kt] != 0;
       if (whole) {
         dkdv_body<D, false>(s, args, ctx);
         return;

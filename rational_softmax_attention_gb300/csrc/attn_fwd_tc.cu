@@ -152,17 +152,12 @@ __device__ __forceinline__ void store_p_half(const uint32_t (&pk)[32], uint8_t* 
 // attention mask, a half every row sees whole runs unmasked, a half no row sees gives zeros
 // without the arithmetic, anything else the per-entry masked path; without one, the causal
 // `masked` flag decides as before.
-// With MASK it votes over the warp (chunk_kind), unless `whole` (the same for every lane of
-// the warp) says every row sees the whole tile: called by all lanes together.
+// With MASK it votes over the warp (chunk_kind): called by all lanes together.
 template <bool MASK>
-__device__ __forceinline__ float2 phi_half_any(bool masked, bool whole, const uint32_t (&h)[2][32], uint32_t (&pk)[32],
-                                               int col0, int lim, float c2, float base, uint32_t mw0, uint32_t mw1) {
+__device__ __forceinline__ float2 phi_half_any(bool masked, const uint32_t (&h)[2][32], uint32_t (&pk)[32], int col0,
+                                               int lim, float c2, float base, uint32_t mw0, uint32_t mw1) {
   if constexpr (MASK) {
-    int k0 = kChunkAll, k1 = kChunkAll;
-    if (!whole) {
-      k0 = chunk_kind(mw0, col0, lim);
-      k1 = chunk_kind(mw1, col0 + 32, lim);
-    }
+    const int k0 = chunk_kind(mw0, col0, lim), k1 = chunk_kind(mw1, col0 + 32, lim);
     if (k0 == kChunkNone && k1 == kChunkNone) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) pk[i] = 0u;
@@ -205,30 +200,27 @@ __device__ __forceinline__ void fwd_item(const AttnShape& s, int& bh, int& q0) {
 }
 
 // Masked calls: the number of leading keys nk > 0 over which an item may run as an unmasked
-// one, or 0.  It may when every query tile of the item (below N_Q) has the same row in the
-// tile live map as in the tile full map, and that row is the same run of key tiles 0 .. n - 1
-// for all of them (a key-padding mask, or an all-true one): each of its rows then may see
-// exactly the keys before nk = min(N_K, 128 n) (and the causal limit), as in an unmasked call
-// on those keys alone, and the unmasked code gives the same results without the per-row mask
-// words, the chunk votes or the tile walk.  Every thread of both CTAs of a pair reads the same
-// map words and takes the same decision.
+// one, or 0.  It may when every query tile of it (below N_Q) has the same plain length n > 0
+// (the mask's rows of the tile maps are key tiles 0 .. n - 1, the same in both: a key-padding
+// mask, or an all-true one): each of its rows then may see exactly the keys before
+// nk = min(N_K, 128 n) (and the causal limit), as in an unmasked call on those keys alone, and
+// the unmasked code gives the same results without the per-row mask words, the chunk votes
+// or the tile walk.  Every thread of both CTAs of a pair reads the same lengths and takes the
+// same decision.
 template <bool PAIR>
 __device__ __forceinline__ int fwd_plain_keys(const AttnShape& s, const FwdTcArgs& args, int bh, int q0) {
-  constexpr int NCTA = PAIR ? 2 : 1;
-  if (!args.mask.live || !args.mask.full) return 0;
+  constexpr int NT = (PAIR ? 2 : 1) * NGROUP;   // query tiles of the item
+  if (!args.mask.plain) return 0;
   const int nqt = (s.NQ + BM - 1) / BM;
-  const int lw = args.mask.live_words;
   const int gm = (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0);
-  int n = 0;
-  for (int r = 0; r < NCTA * NGROUP; ++r) {
-    const int qt = q0 / BM + r;
-    if (qt >= nqt) break;
-    const size_t o = (static_cast<size_t>(gm) * nqt + qt) * lw;
-    const int m = plain_run(args.mask.live + o, args.mask.full + o, lw);
-    if (m == 0 || (r > 0 && m != n)) return 0;
-    n = m;
-  }
-  return min(s.NK, n * BN);
+  const int* len = args.mask.plain + static_cast<size_t>(gm) * nqt;
+  int n[NT];
+#pragma unroll
+  for (int r = 0; r < NT; ++r) n[r] = q0 / BM + r < nqt ? len[q0 / BM + r] : -1;   // -1: past N_Q
+  bool same = n[0] > 0;
+#pragma unroll
+  for (int r = 1; r < NT; ++r) same = same && (n[r] < 0 || n[r] == n[0]);
+  return same ? min(s.NK, n[0] * BN) : 0;
 }
 
 // MASK: a boolean attention mask (args.mask) applies on top of `causal`.  PAIR: the CTA
@@ -643,20 +635,10 @@ __device__ __forceinline__ void fwd_body(const AttnShape& s, const FwdTcArgs& ar
     };
     // this row's attention-mask words: four per key tile (rows past N_Q read the last row)
     const uint32_t* mrow = nullptr;
-    const uint32_t* frow = nullptr;   // this query tile's row of the tile full map
     if (MASK) {
       const int gm = (args.mask.mb > 1 ? bh / s.H : 0) * args.mask.mh + (args.mask.mh > 1 ? bh % s.H : 0);
       mrow = args.mask.bits + (static_cast<size_t>(gm) * s.NQ + min(row, s.NQ - 1)) * args.mask.words;
-      const int qt_own = tile_row0(g, static_cast<int>(rank)) / BM;
-      if (args.mask.full && qt_own < nqt)
-        frow = args.mask.full + (static_cast<size_t>(gm) * nqt + qt_own) * args.mask.live_words;
     }
-    // Key tiles 32 w .. 32 w + 31 the mask allows whole to every row of this query tile: their
-    // words are all ones and are not read
-    auto full_word = [&](int w) -> uint32_t { return (MASK && frow) ? frow[w] : 0u; };
-    // the lowest `lim` of the warp's rows (lane 0's): a tile wholly at or below it, and whole
-    // under the mask, is unmasked for every row of the warp
-    const int lim_lo = s.causal ? min(tile_row0(g, static_cast<int>(rank)) + quarter * 32, nk - 1) : nk - 1;
     auto mask_words = [&](int j, uint32_t (&mw)[4]) {
       if (MASK) {
         const uint4 u = *reinterpret_cast<const uint4*>(mrow + 4 * j);
@@ -693,29 +675,21 @@ __device__ __forceinline__ void fwd_body(const AttnShape& s, const FwdTcArgs& ar
     uint32_t c = 0;
     const int nkt_g = group_keys(g);
     uint32_t tw = 0;   // tiles this product takes (masked instances), refreshed every 32
-    uint32_t fw = 0;   // tiles the mask allows whole to this query tile, likewise
     for (int j = 0; j < nkt_g && ok; ++j) {
       if constexpr (MASK) {
-        if ((j & 31) == 0) {
-          tw = take_word(g, j >> 5);
-          fw = full_word(j >> 5);
-        }
+        if ((j & 31) == 0) tw = take_word(g, j >> 5);
         if (!bit(tw, j)) continue;
       }
-      const bool full = MASK && bit(fw, j);
-      const int col0 = j * BN;   // key index of column 0
-      // masked instances: the same for the whole warp
-      const bool whole = full && col0 + BN - 1 <= lim_lo;
       uint32_t mw[4];
-      if (full) mw[0] = mw[1] = mw[2] = mw[3] = ~0u;
-      else mask_words(j, mw);   // issued before the wait below: its latency hides behind it
+      mask_words(j, mw);   // issued before the wait below: its latency hides behind it
       ok = take_s(static_cast<int>(c & 1u), c >> 1);
       ++c;
       if (!ok) break;
+      const int col0 = j * BN;   // key index of column 0
       // maximum of each 32-column chunk; the first chunk (in key order) that raises the
       // running maximum strictly is remembered, so ties keep the lowest index
       float cm[BN / 32];
-      if (MASK ? whole : col0 + BN - 1 <= lim) {
+      if (!MASK && col0 + BN - 1 <= lim) {
 #pragma unroll
         for (int k = 0; k < BN / 32; ++k) {
           float u0 = -INFINITY, u1 = -INFINITY;
@@ -731,7 +705,7 @@ __device__ __forceinline__ void fwd_body(const AttnShape& s, const FwdTcArgs& ar
         for (int k = 0; k < BN / 32; ++k) {
           float u0 = -INFINITY, u1 = -INFINITY;
           // With an attention mask this branch is taken by the whole warp (the condition above
-          // is the same for every lane), so the chunk vote is safe: a chunk every row of the warp
+          // is false for every lane), so the chunk vote is safe: a chunk every row of the warp
           // may see whole takes the plain max, a chunk none of them may see is skipped (key
           // padding and block masks are uniform per chunk).  Without one, the branch is taken
           // per lane on causal diagonal tiles and must hold no warp vote: every chunk is mixed.
@@ -775,22 +749,16 @@ __device__ __forceinline__ void fwd_body(const AttnShape& s, const FwdTcArgs& ar
     c = 0;                 // P tiles written
     for (int j = 0; j < nkt_g && ok; ++j) {
       if constexpr (MASK) {
-        if ((j & 31) == 0) {
-          tw = take_word(g, j >> 5);
-          fw = full_word(j >> 5);
-        }
+        if ((j & 31) == 0) tw = take_word(g, j >> 5);
         if (!bit(tw, j)) continue;
       }
-      const bool full = MASK && bit(fw, j);
-      const int col0 = j * BN;
-      const bool whole = full && col0 + BN - 1 <= lim_lo;
       uint32_t mw[4];
-      if (full) mw[0] = mw[1] = mw[2] = mw[3] = ~0u;
-      else mask_words(j, mw);   // in flight during the wait
+      mask_words(j, mw);   // in flight during the wait
       ok = warp_wait(&s_full[2 * g], sidx & 1u);   // buffer 0
       if (!ok) break;
       ++sidx;
       tc_fence_after();
+      const int col0 = j * BN;
       const bool masked = MASK || col0 + BN - 1 > lim;
       const bool arg_tile = j == (jm >> 2) && m > -INFINITY;
       uint32_t h[2][32];
@@ -801,7 +769,7 @@ __device__ __forceinline__ void fwd_body(const AttnShape& s, const FwdTcArgs& ar
         a = col0 + ((jm & 1) ? 32 + find_in_chunk(h[1], m, col0 + 32, lim, mw[1])
                              : find_in_chunk(h[0], m, col0, lim, mw[0]));
       uint32_t pk[32];
-      float2 tsum2 = phi_half_any<MASK>(masked, whole, h, pk, col0, lim, c2, base, mw[0], mw[1]);
+      float2 tsum2 = phi_half_any<MASK>(masked, h, pk, col0, lim, c2, base, mw[0], mw[1]);
       tmem_ld32(scol + 64, h[0]);
       tmem_ld32(scol + 96, h[1]);
       tc_wait_ld();
@@ -819,7 +787,7 @@ __device__ __forceinline__ void fwd_body(const AttnShape& s, const FwdTcArgs& ar
       float2 t2;
       {
         uint32_t pk2[32];
-        t2 = phi_half_any<MASK>(masked, whole, h, pk2, col0 + 64, lim, c2, base, mw[2], mw[3]);
+        t2 = phi_half_any<MASK>(masked, h, pk2, col0 + 64, lim, c2, base, mw[2], mw[3]);
         store_p_half(pk2, prow + BOX_BYTES, row_local);
       }
       tsum2 = __fadd2_rn(tsum2, t2);

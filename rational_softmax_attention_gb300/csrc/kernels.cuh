@@ -24,6 +24,7 @@ struct MaskBits {
   int mb, mh;
   const uint32_t* live;   // optional tile live map of the same mask heads (null: every tile may be live)
   const uint32_t* full;   // optional map of the tiles whose every pair is allowed, laid out like `live`
+  const int* plain;       // optional, one per row of the maps: a row an unmasked call can serve (mask.cu)
   int live_words;         // words per query tile row of the maps
 };
 // Packs a [G, NQ, NK] byte mask (nonzero = may attend) into bits_q [G, NQ, wq] (rows = queries)
@@ -34,11 +35,13 @@ cudaError_t launch_mask_pack(const uint8_t* mask, int G, int NQ, int NK, uint32_
 // live_q[(g * nqt + qt) * wq + kt / 32] is set when any pair of the 128 x 128 block (query tile
 // qt, key tile kt) may attend, and the same bit of full_q when every pair of it below N_Q
 // and N_K may;
-// live_k and full_k (optional) hold the transposes, bit qt of [(g * nkt + kt) * wk + qt / 32]
-// (mask.cu).
-cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live_q,
-                                  uint32_t* full_q, int wq, uint32_t* live_k, uint32_t* full_k, int wk,
-                                  cudaStream_t st);
+// live_k and full_k (optional) hold the transposes, bit qt of [(g * nkt + kt) * wk + qt / 32].
+// Then, per row, plain_q[g * nqt + qt] = n > 0 when query tile qt's live and full rows are
+// both key tiles 0 .. n - 1 (else 0), and (with the transposes) plain_k[g * nkt + kt] = 1 when
+// every query tile of key tile kt's range (from kt on when causal, else all) is full (mask.cu).
+cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, int causal,
+                                  uint32_t* live_q, uint32_t* full_q, int* plain_q, int wq, uint32_t* live_k,
+                                  uint32_t* full_k, int* plain_k, int wk, cudaStream_t st);
 
 // Caller-supplied CUDA events recorded at an attention call's kernel boundaries (a
 // measurement knob, ra_debug_kernel_events): e[i] is recorded before kernel i of the call
@@ -122,9 +125,11 @@ struct BwdTcArgs {
 };
 constexpr int kConstBlockFloats = 5 * 128;
 // Forward workspace pieces (api.cu): the fp16 copy of V, and the tile maps of a masked call
-// (the live map, then the full map, each fwd_workspace_map_bytes).
+// (the live map, then the full map, each fwd_workspace_map_bytes, then the per-row plain
+// lengths, fwd_workspace_plain_bytes).
 size_t fwd_workspace_v_bytes(int B, int H, int NK, int D);
 size_t fwd_workspace_map_bytes(int B, int H, int NQ, int NK);
+size_t fwd_workspace_plain_bytes(int B, int H, int NQ);
 size_t fwd_workspace_live_bytes(int B, int H, int NQ, int NK);
 // Workspace bytes the backward uses for these sizes and input dtype (api.cu): the CUDA-core
 // fp32 path needs only two per-row float arrays; the tensor-core path the constant blocks and

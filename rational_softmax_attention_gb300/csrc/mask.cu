@@ -98,11 +98,52 @@ __global__ void __launch_bounds__(32 * WARPS) mask_tile_live_kernel(const uint32
   }
 }
 
+// One thread per row of the tile maps.  Rows of query tiles: plain_q = n when the live row
+// equals the full row and is key tiles 0 .. n - 1 (a key-padding mask, or an all-true one:
+// every row of the query tile may see exactly the keys before 128 n, so an unmasked kernel
+// over those keys gives the masked results), else 0.  Rows of key tiles: plain_k = 1 when the
+// full row holds every query tile from qt0 = (causal ? kt : 0) on, the query tiles a key tile
+// of the unmasked kernels takes, else 0.
+__global__ void __launch_bounds__(256) mask_tile_plain_kernel(const uint32_t* live_q, const uint32_t* full_q, int wq,
+                                                              int nqt, int* plain_q, const uint32_t* full_k, int wk,
+                                                              int nkt, int* plain_k, int causal, long long rows_q,
+                                                              long long total) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  if (t < rows_q) {
+    const uint32_t* L = live_q + t * wq;
+    const uint32_t* F = full_q + t * wq;
+    int n = 0;
+    bool ok = true, ended = false;   // ended: a clear bit seen, every later bit must be clear
+    for (int w = 0; w < wq && ok; ++w) {
+      const uint32_t l = L[w];
+      ok = l == F[w] && (ended ? l == 0u : (l & (l + 1u)) == 0u);   // 0..01..1 before the end
+      if (!ended) n += __popc(l);
+      ended = ended || l != ~0u;
+    }
+    plain_q[t] = ok ? n : 0;
+  } else {
+    const long long r = t - rows_q;   // g * nkt + kt
+    const int kt = static_cast<int>(r % nkt);
+    const int qt0 = causal ? kt : 0;   // 128-row query tiles and 128-key tiles
+    const uint32_t* F = full_k + r * wk;
+    bool ok = true;
+    for (int w = 0; w < wk && ok; ++w) {
+      const int lo = min(max(qt0 - 32 * w, 0), 32), hi = min(max(nqt - 32 * w, 0), 32);
+      const uint32_t upto_hi = hi >= 32 ? ~0u : (1u << hi) - 1u;
+      const uint32_t from_lo = lo >= 32 ? 0u : ~((1u << lo) - 1u);
+      const uint32_t range = upto_hi & from_lo;
+      ok = (F[w] & range) == range;
+    }
+    plain_k[r] = ok ? 1 : 0;
+  }
+}
+
 }  // namespace
 
-cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, uint32_t* live_q,
-                                  uint32_t* full_q, int wq, uint32_t* live_k, uint32_t* full_k, int wk,
-                                  cudaStream_t st) {
+cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK, int words, int causal,
+                                  uint32_t* live_q, uint32_t* full_q, int* plain_q, int wq, uint32_t* live_k,
+                                  uint32_t* full_k, int* plain_k, int wk, cudaStream_t st) {
   const int nqt = (NQ + 127) / 128, nkt = (NK + 127) / 128;
   const size_t bytes_q = static_cast<size_t>(G) * nqt * wq * sizeof(uint32_t);
   const size_t bytes_k = static_cast<size_t>(G) * nkt * wk * sizeof(uint32_t);
@@ -115,6 +156,12 @@ cudaError_t launch_mask_tile_live(const uint32_t* bits_q, int G, int NQ, int NK,
   const unsigned grid = static_cast<unsigned>((total + WARPS - 1) / WARPS);
   mask_tile_live_kernel<<<grid, 32 * WARPS, 0, st>>>(bits_q, NQ, NK, words, nqt, nkt, live_q, full_q, wq, live_k,
                                                      full_k, wk, total);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !plain_q || !full_q) return e;
+  const long long rows_q = static_cast<long long>(G) * nqt;
+  const long long rows = rows_q + (plain_k && full_k ? static_cast<long long>(G) * nkt : 0);
+  mask_tile_plain_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(
+      live_q, full_q, wq, nqt, plain_q, full_k, wk, nkt, plain_k, causal, rows_q, rows);
   return cudaGetLastError();
 }
 

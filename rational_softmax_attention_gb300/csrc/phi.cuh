@@ -1,5 +1,5 @@
 // phi of the rational soft-argmax on the FMA pipe, shared by the forward kernels, and the
-// attention-mask chunk vote and tile-map test shared by every masked tensor-core kernel.
+// attention-mask chunk vote shared by every masked tensor-core kernel.
 //
 // Page "Ra-Family: Rational Neural Architecture", section 3, ra_softmax: u = (x_max - x)/16,
 // q = (1-u)/(1+u), phi = q^8 for u < 1 and exactly 0 otherwise.  With w = (1+u)/2 computed
@@ -58,28 +58,6 @@ __device__ __forceinline__ int chunk_vote(bool all_vis, bool none_vis) {
 // The chunk of keys col0 .. col0 + 31 of a query row: mask word w, last visible key lim.
 __device__ __forceinline__ int chunk_kind(uint32_t w, int col0, int lim) {
   return chunk_vote(w == ~0u && col0 + 31 <= lim, w == 0u || col0 > lim);
-}
-
-// The length n of a row of the tile maps (lw words) when its live tiles are exactly its
-// full tiles and those are tiles 0 .. n - 1 (a key-padding mask, or an all-true one); 0
-// otherwise, and for a row with no live tile.
-__device__ __forceinline__ int plain_run(const uint32_t* live, const uint32_t* full, int lw) {
-  int n = 0;
-  bool ended = false;   // a word with a clear bit seen: every later bit must be clear
-  for (int w = 0; w < lw; ++w) {
-    const uint32_t L = live[w];
-    if (L != full[w]) return 0;
-    if (ended) {
-      if (L != 0u) return 0;
-    } else if (L == ~0u) {
-      n += 32;
-    } else {
-      if ((L & (L + 1u)) != 0u) return 0;   // not of the form 0..01..1
-      n += __popc(L);
-      ended = true;
-    }
-  }
-  return n;
 }
 
 }  // namespace raattn

@@ -39,14 +39,14 @@ def test_workspace_size(lib):
     # one 5 x 128-float constant block per (head, 128-row query tile) (at least the two
     # per-row float arrays of the CUDA-core path) + fp16 copies of Q, dO (N_Q rows) and
     # K, V (N_K rows), then the masked calls' two tile maps (live and full), each both ways
-    # (per head ceil(N_Q/128) rows of ceil(ceil(N_K/128)/32) words, and the transpose), each
-    # piece padded to 256 bytes
+    # (per head ceil(N_Q/128) rows of ceil(ceil(N_K/128)/32) words, and the transpose), and
+    # one int per row of either layout; each piece padded to 256 bytes
     assert lib.ra_attention_bwd_workspace_size(4, 16, 8192, 8192, 128) == \
-        (4 * 16 * 64 * 5 * 128 * 4) + 4 * (4 * 16 * 8192 * 128 * 2) + 4 * (4 * 16 * 64 * 2 * 4)
-    assert lib.ra_attention_bwd_workspace_size(1, 1, 3, 3, 64) == 2560 + 4 * 512 + 4 * 256
+        (4 * 16 * 64 * 5 * 128 * 4) + 4 * (4 * 16 * 8192 * 128 * 2) + 4 * (4 * 16 * 64 * 2 * 4) + 2 * (4 * 16 * 64 * 4)
+    assert lib.ra_attention_bwd_workspace_size(1, 1, 3, 3, 64) == 2560 + 4 * 512 + 4 * 256 + 2 * 256
     # ragged N_Q: 1000 rows make 8 query tiles per head; 16 keys one key tile
     assert lib.ra_attention_bwd_workspace_size(8, 8, 1000, 16, 64) == \
-        (64 * 8 * 2560) + 2 * (64 * 1000 * 64 * 2) + 2 * (64 * 16 * 64 * 2) + 2 * (2048 + 256)
+        (64 * 8 * 2560) + 2 * (64 * 1000 * 64 * 2) + 2 * (64 * 16 * 64 * 2) + 2 * (2048 + 256) + 2048 + 256
     assert lib.ra_attention_bwd_workspace_size(0, 1, 3, 3, 64) == 0
     assert lib.ra_attention_bwd_workspace_size(1, 1, -3, 3, 64) == 0
 
@@ -87,11 +87,12 @@ def test_attention_fwd_validation(lib):
     assert _fwd(lib, ws=NULL) == 1                                    # bf16 needs the fp16 V workspace
     assert _fwd(lib, ws=MISALIGNED) == 1
     # the fp16 V copy, then the masked calls' two tile maps (live and full: ceil(N_Q / 128)
-    # rows of ceil(ceil(N_K / 128) / 32) words per head), each padded to 256 bytes
+    # rows of ceil(ceil(N_K / 128) / 32) words per head) and one int per row, each padded to
+    # 256 bytes
     assert lib.ra_attention_fwd_workspace_size(4, 16, 8192, 8192, 128) == \
-        4 * 16 * 8192 * 128 * 2 + 2 * (4 * 16 * 64 * 2 * 4)
-    assert lib.ra_attention_fwd_workspace_size(1, 3, 300, 5000, 64) == (3 * 5000 * 64 * 2 + 255) // 256 * 256 + 512
-    assert lib.ra_attention_fwd_workspace_size(1, 1, 3, 3, 64) == 512 + 512   # 384 V bytes, 4 bytes per map
+        4 * 16 * 8192 * 128 * 2 + 2 * (4 * 16 * 64 * 2 * 4) + 4 * 16 * 64 * 4
+    assert lib.ra_attention_fwd_workspace_size(1, 3, 300, 5000, 64) == (3 * 5000 * 64 * 2 + 255) // 256 * 256 + 768
+    assert lib.ra_attention_fwd_workspace_size(1, 1, 3, 3, 64) == 512 + 768   # 384 V bytes, 4 bytes per map and row
     assert lib.ra_attention_fwd_workspace_size(1, 1, 3, 0, 64) == 0
 
 
