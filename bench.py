@@ -668,7 +668,8 @@ def run_ours(args):
             "ra_attention_keypad_half_b4h16n8192d128": {
                 "fwd_ms": kp_fwd_ms, "bwd_ms": kp_bwd_ms,
                 "note": "the step's attention with the second half of the keys masked for every query "
-                        "(through the binding); fully masked tiles are left out, so about half the work"},
+                        "(through the binding); every query tile's mask is a run of leading keys, so the "
+                        "unmasked code runs over the first half of the keys: about half the work"},
             "ra_attention_fwd_causal_b4h16n8192d128": {"ms": causal_ms,
                                                        "TFLOP_per_s": causal_fl / (causal_ms * 1e-3) / 1e12,
                                                        "frac_bf16_burst": causal_fl / (causal_ms * 1e-3) / 1e12 / tc_burst},

@@ -304,3 +304,17 @@ def test_key_padding_equals_truncated_keys(D, causal, L):
     span = 2 if D == 128 and n > 256 else 1
     vis, skip = _expected_tile_counts(blocks, n, n, causal, span)   # per head
     assert tuple(int(c) for c in counts.tolist()) == (B * H * vis, B * H * skip)
+
+
+@pytest.mark.parametrize("D,n,causal", [(64, 600, False), (128, 640, False), (128, 600, True)])
+def test_staircase_mask_query_tiles_over_their_own_key_prefix(D, n, causal):
+    """Query tile qt may see keys 0 .. 128 (qt + 1) - 1 (a prefix per query tile, ragged at
+    the end): every query tile's map row is a plain run of its own length, so the dQ kernel
+    runs each one as an unmasked one over its own key prefix, while a forward item (two or
+    four query tiles of different lengths) and a key tile (dead for the query tiles before
+    it) keep the masked code.  Forward and backward against the oracle."""
+    B, H = 1, 2
+    q, k, v, do = attention_inputs(B, H, n, n, D, seed=7000 + D + n + int(causal), sigma_qk=1.0, dtype=torch.bfloat16)
+    rows, cols = np.arange(n)[:, None], np.arange(n)[None, :]
+    mask = cols < 128 * (rows // 128 + 1)
+    _check(q, k, v, do, D ** -0.5, causal, mask)
